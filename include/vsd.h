@@ -1,0 +1,193 @@
+/*
+ * vsd.h -- C ABI of libvsd: the data-parallel hot path of verification-guided
+ * sparse self-speculative decoding on one GB300 GPU (sm_103a).
+ *
+ * One decoding iteration of the method has three steps, each one call here:
+ *
+ *   1. vsd_verify_attn_collect -- the target model's verification pass: the gamma+1
+ *      verify rows attend the whole paged KV cache with full (causal) attention
+ *      and, in the same pass, the pre-softmax logits of two rows (the first draft
+ *      token and the bonus token) are written to memory ("Collect-2-Query").
+ *      Source: "Vegas - verification-guided sparse attention for self-speculative
+ *      decoding" (technical summary), sec. 2 (verification phase, KV selection),
+ *      sec. 2.B (Collect-2-Query), sec. 3 (kernel instrumentation).
+ *   2. vsd_select_topk -- the collected logits summed over both rows and all query
+ *      heads give one score per prefix position; the selected set keeps the
+ *      attention-sink prefix and the recent window and fills the rest of the budget
+ *      k with the highest scores.  Source: Vegas summary sec. 2.A (the selection
+ *      equation: argmax over |T| = k of the summed logits); "Dustin" (technical
+ *      summary), Methodology sec. 1 (sink and recent-window protection).
+ *   3. vsd_sparse_decode_attn -- a draft step: one query row per head attends only
+ *      the selected positions plus the tokens appended after the selection.
+ *      Source: Vegas summary sec. 2 (drafting phase) and sec. 3 (sparse execution:
+ *      paged attention with page size 1 whose page indices are the selected
+ *      token indices).
+ *
+ * Conventions shared by every call
+ *   - All pointers named as device data are CUDA device pointers; the caller owns
+ *     every buffer, including the workspace.  The library allocates no memory and
+ *     keeps no state between calls except the device status word (below).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  A non-OK return means nothing was launched.
+ *   - bf16 tensors hold IEEE bfloat16 values; fp32 tensors IEEE binary32.
+ *   - Device pointers must be 16-byte aligned; workspace 256-byte aligned.
+ *   - Geometry: G = Hq / Hkv query heads share one KV head; query head h reads KV
+ *     head h / G.  head_dim is 64 or 128; page_size is 16.
+ *   - KV cache layout: k_cache and v_cache are bf16 [num_blocks][Hkv][page_size]
+ *     [head_dim]; logical token j of sequence b is stored in physical block
+ *     block_table[b * max_blocks_per_seq + j / page_size] at row j % page_size.
+ *   - Host-side argument errors return VSD_ERR_INVALID_ARG / VSD_ERR_UNSUPPORTED /
+ *     VSD_ERR_WORKSPACE synchronously.  Data errors found on the device (a block-table
+ *     entry outside [0, num_blocks), an index outside its sequence, a length beyond
+ *     the declared maximum) never trap: the offending entry is skipped (treated as
+ *     masked) and a bit is set in the device status word, read with
+ *     vsd_read_device_status.  Every wait inside a kernel is bounded; a wait that
+ *     gives up sets VSD_DEV_TIMEOUT and the kernel returns.
+ */
+#ifndef VSD_H_
+#define VSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vsd_status {
+  VSD_OK = 0,
+  VSD_ERR_INVALID_ARG = -1, /* null pointer, bad size, inconsistent geometry */
+  VSD_ERR_UNSUPPORTED = -2, /* valid but not implemented: head_dim, page_size, rows */
+  VSD_ERR_CUDA = -3,        /* a CUDA runtime call failed (no GPU, launch failure) */
+  VSD_ERR_WORKSPACE = -4,   /* workspace missing, too small or misaligned */
+  VSD_ERR_TIMEOUT = -5      /* reserved: a bounded device wait gave up */
+} vsd_status;
+
+/* Bits of the device status word. */
+#define VSD_DEV_BAD_BLOCK 0x1u  /* block-table entry outside [0, num_blocks) */
+#define VSD_DEV_BAD_INDEX 0x2u  /* selected index outside [0, tail_start) or a bad count */
+#define VSD_DEV_BAD_LENGTH 0x4u /* a sequence length outside the declared bounds */
+#define VSD_DEV_TIMEOUT 0x8u    /* a bounded wait inside a kernel gave up */
+
+/* Shape of a batch over a paged KV cache. */
+typedef struct vsd_geom {
+  int B;                  /* sequences */
+  int Hq;                 /* query heads */
+  int Hkv;                /* KV heads; Hq % Hkv == 0 */
+  int head_dim;           /* 64 or 128 */
+  int page_size;          /* tokens per cache page; 16 */
+  int max_blocks_per_seq; /* row length of block_table */
+  int num_blocks;         /* physical blocks in k_cache / v_cache */
+} vsd_geom;
+
+/* ------------------------------------------------------------------------------
+ * Verification attention with Collect-2-Query (Vegas summary sec. 2 verification
+ * phase; sec. 2.B; sec. 3 kernel instrumentation).
+ *
+ * For sequence b with prefix length P_b (tokens before the verify block), verify
+ * row t in [0, R) sits at position P_b + t and attends keys 0 .. P_b + t; the cache
+ * must already hold the keys and values of the verify block (length P_b + R).
+ *   z[b,t,h,j] = scale * <q[b,t,h,:], K[b, j, h/G, :]>
+ *   out[b,t,h,:] = sum_j softmax_j(z[b,t,h,:]) * V[b, j, h/G, :]
+ *   logits[b,c,h,j] = z[b, row_c, h, j]        c in {0,1}, j < P_b
+ *   partial_scores[b,g,j] = sum_{c in {0,1}} sum_{h in group g} logits[b,c,h,j]
+ *
+ *   q              bf16 [B][R][Hq][head_dim]
+ *   block_table    int32 [B][max_blocks_per_seq]
+ *   prefix_len     int32 [B]; 0 <= P_b <= P_max and P_b + R <= max_blocks*page_size
+ *   collect_row0/1 verify rows whose logits are collected (0 and R-1 = gamma for
+ *                  the first draft token and the bonus token); in [0, R)
+ *   P_max          row stride of logits / partial_scores (upper bound of P_b)
+ *   scale          softmax scale (1/sqrt(head_dim) normally)
+ *   logits         fp32 [B][2][Hq][P_max] or NULL; only j < P_b are written
+ *   partial_scores fp32 [B][Hkv][P_max] or NULL; only j < P_b are written
+ *   out            bf16 [B][R][Hq][head_dim]
+ *   workspace      >= vsd_verify_workspace_size(...) bytes; contents on entry
+ *                  are ignored and on exit unspecified
+ * Supported: head_dim in {64, 128}, page_size 16, 1 <= R and R * G <= 64.
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_verify_workspace_size(const vsd_geom* geom, int R, int P_max, size_t* bytes);
+
+vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
+                                   const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, const int32_t* prefix_len,
+                                   int collect_row0, int collect_row1, int P_max, float scale,
+                                   float* logits, float* partial_scores, void* out,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * Aggregated-logit top-k with a protected sink and recent window (Vegas summary
+ * sec. 2.A selection equation; Dustin summary Methodology sec. 1).
+ *
+ * For row r (one (layer, sequence) pair) with prefix length P = prefix_len[r]:
+ *   s[j] = sum_g partial_scores[r,g,j]                  for j < P
+ *   S    = [0, min(n_sink, P)) U [max(0, P - n_recent), P)
+ *   n    = min(k, P); the n - |S| highest s outside S are added (equal scores:
+ *          the lower position first)
+ *   idx[r, 0..n) = S U added, ascending; idx[r, n..k) = -1; n_sel[r] = n
+ *
+ *   partial_scores fp32 [n_rows][Hkv][P_max]
+ *   prefix_len     int32 [n_rows], 0 <= P <= P_max
+ *   idx            int32 [n_rows][k]
+ *   n_sel          int32 [n_rows]
+ *   scores_out     fp32 [n_rows][P_max] or NULL: the aggregated s (j < P written)
+ *   workspace      >= vsd_select_workspace_size(...) bytes (may be 0)
+ * Requires n_sink + n_recent <= k.  One launch covers all rows.
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_select_workspace_size(int n_rows, int Hkv, int P_max, int k, size_t* bytes);
+
+vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
+                           const int32_t* prefix_len, int P_max, int k, int n_sink,
+                           int n_recent, int32_t* idx, int32_t* n_sel, float* scores_out,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * Sparse draft-step attention (Vegas summary sec. 2 drafting phase; sec. 3 sparse
+ * execution, page size 1 over the selected indices).
+ *
+ * For sequence b the attended positions are idx[b, 0..n_sel[b]) followed by the
+ * dense tail tail_start[b] .. seq_len[b]-1 (tokens written after the selection):
+ *   out[b,h,:] = sum_{j attended} softmax_j(scale * <q[b,h,:], K[b,j,h/G,:]>) V[b,j,h/G,:]
+ * A position listed twice is attended twice; selected indices are expected to be
+ * below tail_start[b] (the select step guarantees it).  An index outside
+ * [0, seq_len[b]) is skipped and flagged VSD_DEV_BAD_INDEX.
+ *
+ *   q          bf16 [B][Hq][head_dim]
+ *   idx        int32 [B][k_max] (may be NULL when k_max == 0)
+ *   n_sel      int32 [B] (may be NULL when k_max == 0), 0 <= n_sel[b] <= k_max
+ *   tail_start int32 [B]; seq_len int32 [B]; tail_start <= seq_len
+ *   max_tail   host-side upper bound of seq_len[b] - tail_start[b]; it only
+ *              sizes the split of the work, results do not depend on it
+ *   out        bf16 [B][Hq][head_dim]
+ *   workspace  >= vsd_sparse_workspace_size(...) bytes
+ * Supported: head_dim in {64, 128}, page_size 16, G <= 16.
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_sparse_workspace_size(const vsd_geom* geom, int k_max, int max_tail,
+                                     size_t* bytes);
+
+vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table,
+                                  const int32_t* idx, const int32_t* n_sel, int k_max,
+                                  const int32_t* tail_start, const int32_t* seq_len,
+                                  int max_tail, float scale, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * Device status word and errors.
+ * vsd_read_device_status synchronizes `stream`, returns the accumulated
+ * VSD_DEV_* bits of every kernel of this library on the current device since the
+ * last read, and clears them.
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_read_device_status(void* stream, unsigned* flags);
+
+const char* vsd_get_error_string(vsd_status status);
+
+/* The CUDA error behind the most recent VSD_ERR_CUDA of the calling thread
+ * (a cudaError_t value; 0 if none). */
+int vsd_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VSD_H_ */

@@ -167,6 +167,9 @@ def sparse_decode(q, k_cache, v_cache, block_table, idx, n_sel, tail_start, seq_
     k_cache = _u16(k_cache)
     v_cache = _u16(v_cache)
     bt = _i32(block_table)
+    if idx is None:  # no selected positions: the tail alone
+        idx = np.zeros((q.shape[0], 0), dtype=np.int32)
+        n_sel = np.zeros((q.shape[0],), dtype=np.int32)
     idx = _i32(idx)
     ns = _i32(n_sel)
     ts = _i32(tail_start)

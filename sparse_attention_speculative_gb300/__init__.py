@@ -1,0 +1,12 @@
+"""Verification-guided sparse self-speculative decoding kernels for GB300 (sm_103a).
+
+The hot path is three C-ABI calls of ``libvsd.so`` (see ``include/vsd.h``):
+verification attention with Collect-2-Query, protected top-k selection over the
+aggregated logits, and the sparse draft-step attention.  This package holds the
+CUDA sources (``csrc/``), the in-tree build (``build.py``), the ctypes binding
+(``_lib.py``), the workload table (``workloads.py``) and the seeded input generators
+(``synth.py``).
+"""
+from ._lib import (DEV_BAD_BLOCK, DEV_BAD_INDEX, DEV_BAD_LENGTH, DEV_TIMEOUT, Geom,  # noqa: F401
+                   VsdError, geom_for, load, vsd_read_device_status, vsd_select_topk,
+                   vsd_sparse_decode_attn, vsd_verify_attn_collect, vsd_verify_workspace_size)

@@ -1,0 +1,214 @@
+"""ctypes binding of libvsd (include/vsd.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  torch supplies device memory and the current stream.  If libvsd.so is
+missing the calls raise immediately; there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libvsd.so")
+
+_lock = threading.Lock()
+_lib = None
+
+VSD_OK = 0
+STATUS_NAMES = {
+    -1: "VSD_ERR_INVALID_ARG",
+    -2: "VSD_ERR_UNSUPPORTED",
+    -3: "VSD_ERR_CUDA",
+    -4: "VSD_ERR_WORKSPACE",
+    -5: "VSD_ERR_TIMEOUT",
+}
+DEV_BAD_BLOCK = 0x1
+DEV_BAD_INDEX = 0x2
+DEV_BAD_LENGTH = 0x4
+DEV_TIMEOUT = 0x8
+
+
+class VsdError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = "%s failed: %s" % (what, STATUS_NAMES.get(status, str(status)))
+        if status == -3 and _lib is not None:
+            msg += " (cudaError %d)" % _lib.vsd_last_cuda_error()
+        super().__init__(msg)
+
+
+class Geom(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int),
+                ("max_blocks_per_seq", ctypes.c_int), ("num_blocks", ctypes.c_int)]
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libvsd.so (built by ``sparse_attention_speculative_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError("libvsd.so is not built (%s); run "
+                               "`python -m sparse_attention_speculative_gb300.build`" % path)
+        lib = ctypes.CDLL(path)
+        P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        GP = ctypes.POINTER(Geom)
+        lib.vsd_verify_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
+        lib.vsd_verify_attn_collect.argtypes = [GP, I, P, P, P, P, P, I, I, I, F, P, P, P, P, SZ, P]
+        lib.vsd_select_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(SZ)]
+        lib.vsd_select_topk.argtypes = [I, I, P, P, I, I, I, I, P, P, P, P, SZ, P]
+        lib.vsd_sparse_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
+        lib.vsd_sparse_decode_attn.argtypes = [GP, P, P, P, P, P, P, I, P, P, I, F, P, P, SZ, P]
+        lib.vsd_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
+        lib.vsd_get_error_string.argtypes = [I]
+        lib.vsd_get_error_string.restype = ctypes.c_char_p
+        lib.vsd_last_cuda_error.argtypes = []
+        for name in ("vsd_verify_workspace_size", "vsd_verify_attn_collect",
+                     "vsd_select_workspace_size", "vsd_select_topk", "vsd_sparse_workspace_size",
+                     "vsd_sparse_decode_attn", "vsd_read_device_status", "vsd_last_cuda_error"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != VSD_OK:
+        raise VsdError(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str) -> None:
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def geom_for(B: int, Hq: int, k_cache: torch.Tensor, block_table: torch.Tensor) -> Geom:
+    NB, Hkv, page, d = k_cache.shape
+    return Geom(B, Hq, Hkv, d, page, int(block_table.shape[1]), NB)
+
+
+_ws_cache = {}
+
+
+def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    key = (str(device), nbytes)
+    ws = _ws_cache.get(key)
+    if ws is None:
+        ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + nbytes]
+
+
+def vsd_verify_workspace_size(geom: Geom, R: int, P_max: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().vsd_verify_workspace_size(ctypes.byref(geom), R, P_max, ctypes.byref(out)),
+           "vsd_verify_workspace_size")
+    return int(out.value)
+
+
+def vsd_verify_attn_collect(q, k_cache, v_cache, block_table, prefix_len, *, P_max: int,
+                            scale: float, row0: int = 0, row1: Optional[int] = None,
+                            logits=None, partial=None, out=None, collect: bool = True,
+                            workspace=None, stream=None):
+    """Verification attention + Collect-2-Query.  Returns (out, logits, partial)."""
+    lib = load()
+    B, R, Hq, d = q.shape
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(block_table, torch.int32, "block_table")
+    _need(prefix_len, torch.int32, "prefix_len")
+    geom = geom_for(B, Hq, k_cache, block_table)
+    if row1 is None:
+        row1 = R - 1
+    dev = q.device
+    if out is None:
+        out = torch.empty_like(q)
+    if collect:
+        if logits is None:
+            logits = torch.empty((B, 2, Hq, P_max), dtype=torch.float32, device=dev)
+        if partial is None:
+            partial = torch.empty((B, geom.Hkv, P_max), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = _workspace(vsd_verify_workspace_size(geom, R, P_max), dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.vsd_verify_attn_collect(ctypes.byref(geom), R, _ptr(q), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(block_table), _ptr(prefix_len),
+                                     int(row0), int(row1), int(P_max), float(scale),
+                                     _ptr(logits), _ptr(partial), _ptr(out), _ptr(workspace),
+                                     ws_bytes, _stream(stream))
+    _check(rc, "vsd_verify_attn_collect")
+    return out, logits, partial
+
+
+def vsd_select_topk(partial, prefix_len, *, k: int, n_sink: int, n_recent: int, idx=None,
+                    n_sel=None, scores_out=None, want_scores: bool = False,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor, Optional[torch.Tensor]]:
+    """Protected top-k over the aggregated score.  partial: fp32 [n_rows, Hkv, P_max]."""
+    lib = load()
+    _need(partial, torch.float32, "partial")
+    _need(prefix_len, torch.int32, "prefix_len")
+    n_rows, Hkv, P_max = partial.shape
+    dev = partial.device
+    if idx is None:
+        idx = torch.empty((n_rows, k), dtype=torch.int32, device=dev)
+    if n_sel is None:
+        n_sel = torch.empty((n_rows,), dtype=torch.int32, device=dev)
+    if want_scores and scores_out is None:
+        scores_out = torch.empty((n_rows, P_max), dtype=torch.float32, device=dev)
+    rc = lib.vsd_select_topk(n_rows, Hkv, _ptr(partial), _ptr(prefix_len), P_max, int(k),
+                             int(n_sink), int(n_recent), _ptr(idx), _ptr(n_sel),
+                             _ptr(scores_out), None, 0, _stream(stream))
+    _check(rc, "vsd_select_topk")
+    return idx, n_sel, scores_out
+
+
+def vsd_sparse_decode_attn(q, k_cache, v_cache, block_table, idx, n_sel, tail_start, seq_len,
+                           *, scale: float, max_tail: int, out=None, stream=None):
+    """Sparse draft-step attention.  q: bf16 [B, Hq, d]; idx: int32 [B, k_max] or None."""
+    lib = load()
+    B, Hq, d = q.shape
+    _need(q, torch.bfloat16, "q")
+    _need(tail_start, torch.int32, "tail_start")
+    _need(seq_len, torch.int32, "seq_len")
+    geom = geom_for(B, Hq, k_cache, block_table)
+    k_max = 0 if idx is None else int(idx.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib.vsd_sparse_decode_attn(ctypes.byref(geom), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(block_table), _ptr(idx), _ptr(n_sel), k_max,
+                                    _ptr(tail_start), _ptr(seq_len), int(max_tail), float(scale),
+                                    _ptr(out), None, 0, _stream(stream))
+    _check(rc, "vsd_sparse_decode_attn")
+    return out
+
+
+def vsd_read_device_status(stream=None) -> int:
+    flags = ctypes.c_uint(0)
+    _check(load().vsd_read_device_status(_stream(stream), ctypes.byref(flags)),
+           "vsd_read_device_status")
+    return int(flags.value)

@@ -1,0 +1,73 @@
+// launch.h -- internal host interface between the C-ABI layer (vsd_api.cu) and the
+// translation units that hold the kernels.  Arguments arrive here already checked.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace vsd {
+
+// ---------------------------------------------------------------- verify
+struct VerifyPlan {
+  int pairs;     // B * Hkv
+  int t_max;     // tiles of 128 keys per pair for the longest admissible sequence
+  int ctas;      // persistent grid size
+  int max_chunks;  // partial-result slots per pair
+  int nq;        // verify rows of one KV group (R * G) rounded up to 16
+};
+
+VerifyPlan plan_verify(int B, int Hkv, int R, int G, int P_max, int num_sms);
+size_t verify_workspace_bytes(const VerifyPlan& plan, int head_dim);
+
+struct VerifyArgs {
+  CUtensorMap kmap, vmap;  // 4-D maps over the caches: {d, page, Hkv, num_blocks}
+  const void* q;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  float* logits;
+  float* partial;
+  void* out;
+  float* ws;  // partial results: m, l, o per (pair, chunk) slot
+  unsigned* status;
+  int B, Hq, Hkv, G, R, d, max_blocks, num_blocks, P_max;
+  int row0, row1;
+  float scale;
+};
+
+cudaError_t launch_verify(const VerifyArgs& a, const VerifyPlan& plan, cudaStream_t stream);
+
+// ---------------------------------------------------------------- select
+struct SelectArgs {
+  const float* partial;
+  const int32_t* prefix_len;
+  int32_t* idx;
+  int32_t* n_sel;
+  float* scores_out;
+  unsigned* status;
+  int n_rows, Hkv, P_max, k, n_sink, n_recent;
+};
+
+int select_cluster_size(int P_max);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- sparse decode
+struct SparseArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* idx;
+  const int32_t* n_sel;
+  const int32_t* tail_start;
+  const int32_t* seq_len;
+  void* out;
+  unsigned* status;
+  int B, Hq, Hkv, G, d, max_blocks, num_blocks, k_max, max_tail;
+  float scale;
+};
+
+cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream);
+
+}  // namespace vsd

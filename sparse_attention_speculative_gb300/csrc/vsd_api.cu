@@ -1,0 +1,324 @@
+// vsd_api.cu -- the C ABI of libvsd (declared in include/vsd.h): argument checks,
+// launch planning, TMA descriptor encoding and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/vsd.h"
+#include "launch.h"
+
+namespace {
+
+// Accumulated VSD_DEV_* bits of every kernel of this library on a device.
+__device__ unsigned g_vsd_device_status = 0u;
+
+thread_local int t_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned* g_status_ptr[kMaxDevices] = {nullptr};
+int g_num_sms[kMaxDevices] = {0};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+vsd_status cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return VSD_ERR_CUDA;
+}
+
+// Per-device constants: the status word's device address and the SM count.
+vsd_status device_info(unsigned** status, int* num_sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return VSD_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_vsd_device_status);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+    g_num_sms[dev] = sms;
+  }
+  if (status) *status = g_status_ptr[dev];
+  if (num_sms) *num_sms = g_num_sms[dev];
+  return VSD_OK;
+}
+
+vsd_status encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &qr);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (qr != cudaDriverEntryPointSuccess || fn == nullptr) return VSD_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = g_encode;
+  return VSD_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Shared checks of a paged-cache geometry.
+vsd_status check_geom(const vsd_geom* g) {
+  if (g == nullptr) return VSD_ERR_INVALID_ARG;
+  if (g->B < 0 || g->Hq <= 0 || g->Hkv <= 0 || g->Hq % g->Hkv != 0) return VSD_ERR_INVALID_ARG;
+  if (g->max_blocks_per_seq <= 0 || g->num_blocks <= 0) return VSD_ERR_INVALID_ARG;
+  if (g->head_dim != 64 && g->head_dim != 128) return VSD_ERR_UNSUPPORTED;
+  if (g->page_size != 16) return VSD_ERR_UNSUPPORTED;
+  if (!is_pow2(g->Hq / g->Hkv)) return VSD_ERR_UNSUPPORTED;
+  return VSD_OK;
+}
+
+// 4-D tiled map over a cache [num_blocks][Hkv][page][d]: box = 64 dims x one page.
+vsd_status make_cache_map(CUtensorMap* map, const void* cache, const vsd_geom* g) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  vsd_status st = encoder(&enc);
+  if (st != VSD_OK) return st;
+  const cuuint64_t d = static_cast<cuuint64_t>(g->head_dim);
+  cuuint64_t dims[4] = {d, 16, static_cast<cuuint64_t>(g->Hkv),
+                        static_cast<cuuint64_t>(g->num_blocks)};
+  cuuint64_t strides[3] = {d * 2, 16 * d * 2, static_cast<cuuint64_t>(g->Hkv) * 16 * d * 2};
+  cuuint32_t box[4] = {64, 16, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = static_cast<int>(r);
+    return VSD_ERR_CUDA;
+  }
+  return VSD_OK;
+}
+
+vsd_status verify_checks(const vsd_geom* geom, int R, int P_max) {
+  vsd_status st = check_geom(geom);
+  if (st != VSD_OK) return st;
+  if (R < 1 || P_max < 0) return VSD_ERR_INVALID_ARG;
+  const int G = geom->Hq / geom->Hkv;
+  if (R * G > 64) return VSD_ERR_UNSUPPORTED;
+  return VSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vsd_get_error_string(vsd_status s) {
+  switch (s) {
+    case VSD_OK: return "success";
+    case VSD_ERR_INVALID_ARG: return "invalid argument";
+    case VSD_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case VSD_ERR_CUDA: return "CUDA runtime error (see vsd_last_cuda_error)";
+    case VSD_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case VSD_ERR_TIMEOUT: return "a bounded device wait gave up";
+  }
+  return "unknown status";
+}
+
+int vsd_last_cuda_error(void) { return t_last_cuda_error; }
+
+vsd_status vsd_read_device_status(void* stream, unsigned* flags) {
+  if (flags == nullptr) return VSD_ERR_INVALID_ARG;
+  unsigned* dptr = nullptr;
+  vsd_status st = device_info(&dptr, nullptr);
+  if (st != VSD_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned v = 0u;
+  e = cudaMemcpy(&v, dptr, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemset(dptr, 0, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *flags = v;
+  return VSD_OK;
+}
+
+vsd_status vsd_verify_workspace_size(const vsd_geom* geom, int R, int P_max, size_t* bytes) {
+  if (bytes == nullptr) return VSD_ERR_INVALID_ARG;
+  vsd_status st = verify_checks(geom, R, P_max);
+  if (st != VSD_OK) return st;
+  int sms = 0;
+  st = device_info(nullptr, &sms);
+  if (st != VSD_OK) return st;
+  const vsd::VerifyPlan plan =
+      vsd::plan_verify(geom->B, geom->Hkv, R, geom->Hq / geom->Hkv, P_max, sms);
+  *bytes = vsd::verify_workspace_bytes(plan, geom->head_dim);
+  return VSD_OK;
+}
+
+vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
+                                   const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, const int32_t* prefix_len,
+                                   int collect_row0, int collect_row1, int P_max, float scale,
+                                   float* logits, float* partial_scores, void* out,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  vsd_status st = verify_checks(geom, R, P_max);
+  if (st != VSD_OK) return st;
+  if (geom->B == 0) return VSD_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !prefix_len || !out)
+    return VSD_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(logits, 16) || !aligned(partial_scores, 16) || !aligned(block_table, 4) ||
+      !aligned(prefix_len, 4))
+    return VSD_ERR_INVALID_ARG;
+  if ((logits || partial_scores) &&
+      (collect_row0 < 0 || collect_row0 >= R || collect_row1 < 0 || collect_row1 >= R))
+    return VSD_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return VSD_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  int sms = 0;
+  st = device_info(&status, &sms);
+  if (st != VSD_OK) return st;
+  const int G = geom->Hq / geom->Hkv;
+  const vsd::VerifyPlan plan = vsd::plan_verify(geom->B, geom->Hkv, R, G, P_max, sms);
+  const size_t need = vsd::verify_workspace_bytes(plan, geom->head_dim);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
+    return VSD_ERR_WORKSPACE;
+  vsd::VerifyArgs va;
+  st = make_cache_map(&va.kmap, k_cache, geom);
+  if (st != VSD_OK) return st;
+  st = make_cache_map(&va.vmap, v_cache, geom);
+  if (st != VSD_OK) return st;
+  va.q = q;
+  va.block_table = block_table;
+  va.prefix_len = prefix_len;
+  va.logits = logits;
+  va.partial = partial_scores;
+  va.out = out;
+  va.ws = static_cast<float*>(workspace);
+  va.status = status;
+  va.B = geom->B;
+  va.Hq = geom->Hq;
+  va.Hkv = geom->Hkv;
+  va.G = G;
+  va.R = R;
+  va.d = geom->head_dim;
+  va.max_blocks = geom->max_blocks_per_seq;
+  va.num_blocks = geom->num_blocks;
+  va.P_max = P_max;
+  va.row0 = collect_row0;
+  va.row1 = collect_row1;
+  va.scale = scale;
+  cudaError_t e = vsd::launch_verify(va, plan, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
+vsd_status vsd_select_workspace_size(int n_rows, int Hkv, int P_max, int k, size_t* bytes) {
+  if (bytes == nullptr || n_rows < 0 || Hkv < 1 || P_max < 0 || k < 1)
+    return VSD_ERR_INVALID_ARG;
+  if (vsd::select_cluster_size(P_max) < 1) return VSD_ERR_UNSUPPORTED;
+  *bytes = 0;
+  return VSD_OK;
+}
+
+vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
+                           const int32_t* prefix_len, int P_max, int k, int n_sink,
+                           int n_recent, int32_t* idx, int32_t* n_sel, float* scores_out,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (n_rows < 0 || Hkv < 1 || P_max < 0 || k < 1 || n_sink < 0 || n_recent < 0)
+    return VSD_ERR_INVALID_ARG;
+  if (static_cast<long long>(n_sink) + n_recent > k) return VSD_ERR_INVALID_ARG;
+  if (vsd::select_cluster_size(P_max) < 1) return VSD_ERR_UNSUPPORTED;
+  if (n_rows == 0) return VSD_OK;
+  if (!partial_scores || !prefix_len || !idx || !n_sel) return VSD_ERR_INVALID_ARG;
+  if (!aligned(partial_scores, 16) || !aligned(idx, 4) || !aligned(n_sel, 4) ||
+      !aligned(prefix_len, 4) || !aligned(scores_out, 4))
+    return VSD_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  vsd_status st = device_info(&status, nullptr);
+  if (st != VSD_OK) return st;
+  vsd::SelectArgs sa;
+  sa.partial = partial_scores;
+  sa.prefix_len = prefix_len;
+  sa.idx = idx;
+  sa.n_sel = n_sel;
+  sa.scores_out = scores_out;
+  sa.status = status;
+  sa.n_rows = n_rows;
+  sa.Hkv = Hkv;
+  sa.P_max = P_max;
+  sa.k = k;
+  sa.n_sink = n_sink;
+  sa.n_recent = n_recent;
+  cudaError_t e = vsd::launch_select(sa, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
+vsd_status vsd_sparse_workspace_size(const vsd_geom* geom, int k_max, int max_tail,
+                                     size_t* bytes) {
+  if (bytes == nullptr || k_max < 0 || max_tail < 0) return VSD_ERR_INVALID_ARG;
+  vsd_status st = check_geom(geom);
+  if (st != VSD_OK) return st;
+  if (geom->Hq / geom->Hkv > 16) return VSD_ERR_UNSUPPORTED;
+  *bytes = 0;
+  return VSD_OK;
+}
+
+vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table,
+                                  const int32_t* idx, const int32_t* n_sel, int k_max,
+                                  const int32_t* tail_start, const int32_t* seq_len,
+                                  int max_tail, float scale, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  vsd_status st = check_geom(geom);
+  if (st != VSD_OK) return st;
+  if (geom->Hq / geom->Hkv > 16) return VSD_ERR_UNSUPPORTED;
+  if (k_max < 0 || max_tail < 0) return VSD_ERR_INVALID_ARG;
+  if (geom->B == 0) return VSD_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !tail_start || !seq_len || !out)
+    return VSD_ERR_INVALID_ARG;
+  if (k_max > 0 && (!idx || !n_sel)) return VSD_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(idx, 4) || !aligned(n_sel, 4) || !aligned(block_table, 4) ||
+      !aligned(tail_start, 4) || !aligned(seq_len, 4))
+    return VSD_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return VSD_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  st = device_info(&status, nullptr);
+  if (st != VSD_OK) return st;
+  vsd::SparseArgs sa;
+  sa.q = q;
+  sa.k_cache = k_cache;
+  sa.v_cache = v_cache;
+  sa.block_table = block_table;
+  sa.idx = k_max > 0 ? idx : nullptr;
+  sa.n_sel = k_max > 0 ? n_sel : nullptr;
+  sa.tail_start = tail_start;
+  sa.seq_len = seq_len;
+  sa.out = out;
+  sa.status = status;
+  sa.B = geom->B;
+  sa.Hq = geom->Hq;
+  sa.Hkv = geom->Hkv;
+  sa.G = geom->Hq / geom->Hkv;
+  sa.d = geom->head_dim;
+  sa.max_blocks = geom->max_blocks_per_seq;
+  sa.num_blocks = geom->num_blocks;
+  sa.k_max = k_max;
+  sa.max_tail = max_tail;
+  sa.scale = scale;
+  cudaError_t e = vsd::launch_sparse(sa, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
+}  // extern "C"

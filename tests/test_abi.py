@@ -1,0 +1,91 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every declared symbol,
+and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vsd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_speculative_gb300 import build
+    from sparse_attention_speculative_gb300._lib import load
+    build.build()
+    return load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vsd_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for n in ("vsd_verify_attn_collect", "vsd_select_topk", "vsd_sparse_decode_attn"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), "libvsd.so does not export %s" % name
+
+
+def test_error_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        s = lib.vsd_get_error_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+
+
+def _geom(**kw):
+    from sparse_attention_speculative_gb300._lib import Geom
+    base = dict(B=1, Hq=32, Hkv=8, head_dim=128, page_size=16, max_blocks_per_seq=64,
+                num_blocks=64)
+    base.update(kw)
+    return Geom(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=30), -1),              # Hq not a multiple of Hkv
+    (dict(head_dim=96), -2),        # unsupported head dim
+    (dict(page_size=32), -2),       # unsupported page size
+    (dict(Hq=24, Hkv=8), -2),       # G = 3 is not a power of two
+    (dict(num_blocks=0), -1),
+])
+def test_verify_rejects_bad_geometry(lib, kw, code):
+    g = _geom(**kw)
+    rc = lib.vsd_verify_attn_collect(ctypes.byref(g), 5, None, None, None, None, None, 0, 4,
+                                     1024, ctypes.c_float(0.088), None, None, None, None, 0, None)
+    assert rc == code
+
+
+def test_verify_rejects_too_many_rows(lib):
+    g = _geom(Hq=64, Hkv=8)  # G = 8: R * G = 72 > 64
+    rc = lib.vsd_verify_attn_collect(ctypes.byref(g), 9, None, None, None, None, None, 0, 8,
+                                     1024, ctypes.c_float(0.088), None, None, None, None, 0, None)
+    assert rc == -2
+
+
+def test_select_rejects_budget_below_protected(lib):
+    rc = lib.vsd_select_topk(1, 8, None, None, 1024, 10, 8, 8, None, None, None, None, 0, None)
+    assert rc == -1
+
+
+def test_select_rejects_null_outputs(lib):
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    rc = lib.vsd_select_topk(1, 8, p, p, 1024, 64, 4, 16, None, None, None, None, 0, None)
+    assert rc == -1
+
+
+def test_sparse_rejects_missing_index_arrays(lib):
+    g = _geom()
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    rc = lib.vsd_sparse_decode_attn(ctypes.byref(g), p, p, p, p, None, None, 16, p, p, 0,
+                                    ctypes.c_float(0.088), p, None, 0, None)
+    assert rc == -1

@@ -1,0 +1,285 @@
+"""GPU parity: every kernel of the hot path, called through the C ABI, against the
+fp64 oracle on the same seeded inputs (comparison rules in parity_utils)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity_utils import (assert_attn_close, assert_index_sets, assert_rel_close,
+                                fp32_row_sum)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_attention_speculative_gb300 import build
+    build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+    yield
+
+
+def _vsd():
+    import sparse_attention_speculative_gb300 as vsd
+    return vsd
+
+
+def run_verify(batch, w, row0=0, row1=None):
+    vsd = _vsd()
+    out, logits, partial = vsd.vsd_verify_attn_collect(
+        batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+        P_max=w.P_max, scale=w.scale, row0=row0, row1=row1)
+    torch.cuda.synchronize()
+    return out, logits, partial
+
+
+def check_verify(batch, w, row0=0, row1=None, status_ok=True):
+    from sparse_attention_speculative_gb300.synth import host_arrays
+    vsd = _vsd()
+    out, logits, partial = run_verify(batch, w, row0, row1)
+    status = vsd.vsd_read_device_status()
+    if status_ok:
+        assert status == 0, "device status 0x%x" % status
+    h = host_arrays(batch)
+    o_ref, l_ref, p_ref = oracle.verify(h["q"], h["k_cache"], h["v_cache"], h["block_table"],
+                                        h["prefix_len"], scale=w.scale, P_max=w.P_max,
+                                        row0=row0, row1=row1)
+    assert_attn_close(out.float().cpu().numpy(), o_ref, "verify output")
+    lg = logits.cpu().numpy()
+    pa = partial.cpu().numpy()
+    for b, P in enumerate(h["prefix_len"].tolist()):
+        assert_rel_close(lg[b, :, :, :P], l_ref[b, :, :, :P], "collected logits")
+        assert_rel_close(pa[b, :, :P], p_ref[b, :, :P], "partial scores")
+    return out, logits, partial, (o_ref, l_ref, p_ref), h
+
+
+def check_select(partial, prefix_len, w, s_ref_fp64=None):
+    vsd = _vsd()
+    idx, n_sel, scores = vsd.vsd_select_topk(partial, prefix_len, k=w.k, n_sink=w.n_sink,
+                                             n_recent=w.n_recent, want_scores=True)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    pl = prefix_len.cpu().numpy()
+    pa = partial.cpu().numpy()
+    # 1) same input, decision in the kernel's precision (fp32 sum in group order): exact
+    s32 = fp32_row_sum(pa)
+    i32, n32 = oracle.select(s32, pl, k=w.k, n_sink=w.n_sink, n_recent=w.n_recent)
+    gi, gn = idx.cpu().numpy(), n_sel.cpu().numpy()
+    for r, P in enumerate(pl.tolist()):
+        assert gn[r] == n32[r]
+        np.testing.assert_array_equal(gi[r, :gn[r]], i32[r, :n32[r]])
+        assert np.all(gi[r, gn[r]:] == -1)
+    # 2) the aggregated score itself against the oracle's fp64 aggregation
+    s64 = oracle.score_from_partials(pa, pl)
+    sc = scores.cpu().numpy()
+    for r, P in enumerate(pl.tolist()):
+        assert_rel_close(sc[r, :P], s64[r, :P], "aggregated score")
+    # 3) against the oracle's end-to-end fp64 selection, under the tolerance rule
+    if s_ref_fp64 is not None:
+        i64, n64 = oracle.select(s_ref_fp64, pl, k=w.k, n_sink=w.n_sink, n_recent=w.n_recent)
+        assert_index_sets(gi, gn, i64, n64, s_ref_fp64, pl, w.k, w.n_sink, w.n_recent)
+    return idx, n_sel
+
+
+def check_sparse(batch, w, idx, n_sel, tail_start, seq_len, q=None, max_tail=None):
+    from sparse_attention_speculative_gb300.synth import host_arrays, to_u16
+    vsd = _vsd()
+    q = batch.q_draft[0] if q is None else q
+    if max_tail is None:
+        max_tail = int((seq_len - tail_start).max().item())
+    out = vsd.vsd_sparse_decode_attn(q, batch.k_cache, batch.v_cache, batch.block_table, idx,
+                                     n_sel, tail_start, seq_len, scale=w.scale,
+                                     max_tail=max_tail)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    h = host_arrays(batch)
+    ref = oracle.sparse_decode(to_u16(q), h["k_cache"], h["v_cache"], h["block_table"],
+                               None if idx is None else idx.cpu().numpy(),
+                               None if n_sel is None else n_sel.cpu().numpy(),
+                               tail_start.cpu().numpy(), seq_len.cpu().numpy(), scale=w.scale)
+    assert_attn_close(out.float().cpu().numpy(), ref, "sparse draft output")
+    return out
+
+
+def full_path(w, device="cuda"):
+    from sparse_attention_speculative_gb300.synth import make_batch
+    batch = make_batch(w, device)
+    out, logits, partial, refs, h = check_verify(batch, w)
+    s_ref = oracle.score_from_logits(refs[1], h["prefix_len"])
+    idx, n_sel = check_select(partial, batch.prefix_len, w, s_ref)
+    # planted heavy hitters are all selected (sanity, not a tolerance)
+    for b, pos in enumerate(batch.planted):
+        sel = set(idx[b, :int(n_sel[b])].cpu().tolist())
+        missing = set(pos.cpu().tolist()) - sel
+        assert len(missing) <= 0.01 * max(1, len(pos)), "planted keys not selected: %d" % len(missing)
+    # draft steps: idx plus a dense tail after the verify block start
+    tail = batch.prefix_len.clone()
+    for step in range(min(w.gamma, 2)):
+        seq_len = batch.prefix_len + 2 + step
+        check_sparse(batch, w, idx, n_sel, tail, seq_len, q=batch.q_draft[step])
+    return batch
+
+
+def test_tiny_full_path():
+    from sparse_attention_speculative_gb300.workloads import TINY
+    full_path(TINY)
+
+
+def test_qwen3_8b_32k_full_path():
+    from sparse_attention_speculative_gb300.workloads import QWEN3_8B_32K
+    full_path(QWEN3_8B_32K)
+
+
+@pytest.mark.slow
+def test_qwen25_72b_b16_full_path():
+    from sparse_attention_speculative_gb300.workloads import QWEN25_72B_B16_32K
+    full_path(QWEN25_72B_B16_32K)
+
+
+@pytest.mark.slow
+def test_long_128k_full_path():
+    from sparse_attention_speculative_gb300.workloads import LONG_128K
+    full_path(LONG_128K)
+
+
+# ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("d,Hq,Hkv,gamma", [(128, 32, 8, 4), (64, 4, 1, 3), (128, 8, 8, 0),
+                                            (64, 16, 2, 7), (128, 64, 8, 5), (128, 16, 16, 6)])
+def test_verify_ragged_geometries(d, Hq, Hkv, gamma):
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    prefix = (0, 1, 127, 128, 129, 1000, 3001)
+    w = Workload("ragged", B=len(prefix), P=max(prefix), Hq=Hq, Hkv=Hkv, d=d, gamma=gamma,
+                 k=64, n_sink=4, n_recent=16, planted_frac=0.01, seed=9, prefix_lens=prefix)
+    batch = make_batch(w, "cuda")
+    row1 = w.R - 1
+    check_verify(batch, w, row0=0, row1=row1)
+
+
+def test_verify_collect_other_rows():
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    w = Workload("rows", B=2, P=700, Hq=8, Hkv=2, d=128, gamma=5, k=64, n_sink=4, n_recent=16,
+                 seed=3, prefix_lens=(700, 333))
+    batch = make_batch(w, "cuda")
+    check_verify(batch, w, row0=2, row1=2)
+    check_verify(batch, w, row0=4, row1=1)
+
+
+def test_verify_deterministic():
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import QWEN3_8B_32K
+    w = QWEN3_8B_32K.with_(P=8000)
+    batch = make_batch(w, "cuda")
+    a = [t.clone() for t in run_verify(batch, w)]
+    b = run_verify(batch, w)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_verify_bad_block_is_flagged_not_faulted():
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("bad", B=1, P=500, Hq=8, Hkv=2, d=128, gamma=3, k=64, n_sink=4, n_recent=16,
+                 seed=5)
+    batch = make_batch(w, "cuda")
+    batch.block_table[0, 3] = batch.num_blocks + 7  # out of range entry
+    run_verify(batch, w)
+    assert vsd.vsd_read_device_status() & vsd.DEV_BAD_BLOCK
+    assert vsd.vsd_read_device_status() == 0  # reading clears
+
+
+def test_select_ties_and_small_prefixes():
+    vsd = _vsd()
+    rng = np.random.default_rng(0)
+    prefix = np.array([0, 1, 5, 20, 64, 65, 300, 4096, 20000], np.int32)
+    P_max = int(prefix.max())
+    Hkv = 4
+    # integer-valued partials: many exact ties in the aggregated score
+    partial = rng.integers(-3, 4, size=(len(prefix), Hkv, P_max)).astype(np.float32)
+    pt = torch.tensor(partial, device="cuda")
+    pl = torch.tensor(prefix, device="cuda")
+    from sparse_attention_speculative_gb300.workloads import Workload
+    for k, ns, nr in [(64, 4, 16), (20, 20, 0), (300, 16, 256), (1, 0, 1), (5000, 4, 64)]:
+        w = Workload("sel", B=len(prefix), P=P_max, Hq=8, Hkv=Hkv, d=128, gamma=1, k=k,
+                     n_sink=ns, n_recent=nr)
+        check_select(pt, pl, w)
+
+
+def test_select_many_rows_one_launch():
+    rng = np.random.default_rng(1)
+    n_rows, Hkv, P_max = 40, 8, 65536
+    prefix = rng.integers(1000, P_max + 1, size=n_rows).astype(np.int32)
+    partial = rng.normal(size=(n_rows, Hkv, P_max)).astype(np.float32)
+    from sparse_attention_speculative_gb300.workloads import Workload
+    w = Workload("rows", B=n_rows, P=P_max, Hq=32, Hkv=Hkv, d=128, gamma=5, k=4096, n_sink=16,
+                 n_recent=256)
+    check_select(torch.tensor(partial, device="cuda"), torch.tensor(prefix, device="cuda"), w)
+
+
+def test_sparse_edge_cases():
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    w = Workload("sp", B=4, P=3000, Hq=16, Hkv=4, d=128, gamma=3, k=256, n_sink=4, n_recent=16,
+                 seed=4, prefix_lens=(3000, 17, 0, 1200))
+    batch = make_batch(w, "cuda")
+    dev = "cuda"
+    k_max = 256
+    idx = torch.full((w.B, k_max), -1, dtype=torch.int32, device=dev)
+    n_sel = torch.zeros((w.B,), dtype=torch.int32, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(0)
+    for b, P in enumerate(w.prefix()):
+        n = min(P, 200)
+        if n:
+            sel = torch.sort(torch.randperm(P, generator=g)[:n]).values
+            idx[b, :n] = sel.to(torch.int32).to(dev)
+            n_sel[b] = n
+    tail = batch.prefix_len.clone()
+    seq_len = batch.prefix_len + torch.tensor([3, 1, 2, 0], dtype=torch.int32, device=dev)
+    check_sparse(batch, w, idx, n_sel, tail, seq_len)
+    # dense decode: no indices, the whole cache as the tail
+    zero = torch.zeros_like(tail)
+    check_sparse(batch, w, None, None, zero, batch.prefix_len + 2)
+    # duplicates are attended twice
+    idx2 = idx.clone()
+    idx2[0, 1] = idx2[0, 0]
+    check_sparse(batch, w, idx2, n_sel, tail, seq_len)
+
+
+def test_sparse_bad_index_is_flagged():
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("spbad", B=1, P=100, Hq=8, Hkv=2, d=128, gamma=1, k=8, n_sink=0, n_recent=0,
+                 seed=1)
+    batch = make_batch(w, "cuda")
+    idx = torch.tensor([[0, 5, 999999]], dtype=torch.int32, device="cuda")
+    n_sel = torch.tensor([3], dtype=torch.int32, device="cuda")
+    tail = batch.prefix_len.clone()
+    vsd.vsd_sparse_decode_attn(batch.q_draft[0], batch.k_cache, batch.v_cache, batch.block_table,
+                               idx, n_sel, tail, batch.prefix_len + 1, scale=w.scale, max_tail=1)
+    assert vsd.vsd_read_device_status() & vsd.DEV_BAD_INDEX
+
+
+def test_sparse_all_prefix_equals_verify_row():
+    """k = P (all indices) sparse draft equals the full verify row it mirrors."""
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("eq", B=2, P=5000, Hq=32, Hkv=8, d=128, gamma=4, k=5000, n_sink=0, n_recent=0,
+                 seed=8, prefix_lens=(5000, 4321))
+    batch = make_batch(w, "cuda")
+    out, _, _ = run_verify(batch, w)
+    t = 2
+    idx = torch.arange(w.P_max, dtype=torch.int32, device="cuda").repeat(w.B, 1)
+    n_sel = batch.prefix_len.clone()
+    seq_len = batch.prefix_len + t + 1
+    d_out = vsd.vsd_sparse_decode_attn(batch.q[:, t].contiguous(), batch.k_cache, batch.v_cache,
+                                       batch.block_table, idx, n_sel, batch.prefix_len.clone(),
+                                       seq_len, scale=w.scale, max_tail=t + 1)
+    torch.cuda.synchronize()
+    diff = (d_out.float() - out[:, t].float()).abs().max().item()
+    assert diff <= 2e-2
