@@ -1,0 +1,500 @@
+"""Benchmark of one Vegas iteration on GB300: verify + Collect-2-Query, top-k
+selection, and gamma sparse draft steps, through the libvsd C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line.  `value` is the algorithmic bytes of the whole iteration
+(KV read by verify, logits and partial scores written, partial scores read by the
+select, gathered KV of every draft step, queries and outputs) divided by the device
+time of the iteration, summed over ranks.  L2 is flushed before every timed
+iteration (512 MB write then 512 MB read, untimed); each iteration is enqueued
+behind a GPU sleep so host launch latency never shows in the device timestamps.
+`--impl reference` times the fp64 CPU oracle on the same workload instead (a
+deliberately slow baseline).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20  # > 129 MB of L2
+METRIC = ("KV-read GB/s of one Vegas iteration (verify+collect2, top-k select, "
+          "gamma sparse draft steps)")
+
+
+def flush_l2(buf_w, buf_r):
+    """Evict L2 before a timed iteration: write a buffer larger than L2, then read
+    another one, so the lines left behind are clean and their eviction costs the
+    timed kernels no DRAM write-back."""
+    buf_w.zero_()
+    buf_r.sum(dtype=torch.int64)
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(workload: str):
+    """DRAM bytes per launch recorded by ncu for the verification kernel, if the
+    kernel sources have not changed since the counters were taken."""
+    prof = os.path.join(ROOT, "profiles", "verify_attn_collect_%s.md" % workload)
+    try:
+        text = open(prof).read()
+    except OSError:
+        return None
+    csrc = os.path.join(ROOT, "sparse_attention_speculative_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("verify_attn") or name in ("ptx.cuh", "common.cuh"):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    digest = h.hexdigest()[:16]
+    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if m_src and m_tr and m_src.group(1) == digest:
+        return int(m_tr.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+                          if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ workload bytes
+
+def iteration_bytes(w, prefix, n_sel, tail_lens):
+    """Algorithmic bytes of one iteration (per kernel), from the shapes."""
+    d, Hq, Hkv, R = w.d, w.Hq, w.Hkv, w.R
+    kv_row = d * 2  # bytes of one (token, head) K or V row
+    verify = 0
+    for P in prefix:
+        verify += 2 * Hkv * (P + R) * kv_row          # K and V of every attended key
+        verify += 2 * R * Hq * d * 2                  # q in, out
+        verify += 2 * Hq * P * 4 + Hkv * P * 4        # logits and partial scores written
+    select = sum(Hkv * P * 4 for P in prefix) + sum(4 * min(w.k, P) for P in prefix)
+    sparse = []
+    for tl in tail_lens:
+        s = 0
+        for b, P in enumerate(prefix):
+            s += 2 * Hkv * (n_sel[b] + tl[b]) * kv_row + 2 * Hq * d * 2
+        sparse.append(s)
+    return verify, select, sparse
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, world, rank, local):
+    import sparse_attention_speculative_gb300 as vsd
+    from sparse_attention_speculative_gb300 import build as pkg_build
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import ALL
+
+    if rank == 0 or not pkg_build.up_to_date():
+        pkg_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    vsd.load()
+    w = ALL[args.workload]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    batch = make_batch(w, dev)
+    B, R, Hq, d, gamma = w.B, w.R, w.Hq, w.d, w.gamma
+    prefix = list(w.prefix())
+    P_max = w.P_max
+    geom = vsd.geom_for(B, Hq, batch.k_cache, batch.block_table)
+    ws_bytes = vsd.vsd_verify_workspace_size(geom, R, P_max)
+    workspace = torch.zeros(max(ws_bytes, 1) + 256, dtype=torch.uint8, device=dev)
+    off = (-workspace.data_ptr()) % 256
+    workspace = workspace[off:off + ws_bytes] if ws_bytes else None
+    out = torch.empty_like(batch.q)
+    logits = torch.empty((B, 2, Hq, P_max), dtype=torch.float32, device=dev)
+    partial = torch.empty((B, w.Hkv, P_max), dtype=torch.float32, device=dev)
+    idx = torch.empty((B, w.k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty((B,), dtype=torch.int32, device=dev)
+    d_out = torch.empty((gamma, B, Hq, d), dtype=torch.bfloat16, device=dev)
+    tail_start = batch.prefix_len.clone()
+    seq_len = torch.empty((gamma, B), dtype=torch.int32, device=dev)
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    rng = np.random.default_rng(w.seed + 77)
+    max_tail = 2 * gamma + 1
+
+    def draw_seq_len():
+        a = rng.integers(0, gamma + 1, size=B)  # accepted drafts this iteration
+        return np.array([[prefix[b] + a[b] + 2 + i for b in range(B)] for i in range(gamma)],
+                        dtype=np.int32)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 + gamma)]
+
+    def step():
+        vsd.vsd_verify_attn_collect(batch.q, batch.k_cache, batch.v_cache, batch.block_table,
+                                    batch.prefix_len, P_max=P_max, scale=w.scale, row0=0,
+                                    row1=R - 1, logits=logits, partial=partial, out=out,
+                                    workspace=workspace)
+        ev[1].record(stream)
+        vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                            n_recent=w.n_recent, idx=idx, n_sel=n_sel)
+        ev[2].record(stream)
+        for i in range(gamma):
+            vsd.vsd_sparse_decode_attn(batch.q_draft[i], batch.k_cache, batch.v_cache,
+                                       batch.block_table, idx, n_sel, tail_start, seq_len[i],
+                                       scale=w.scale, max_tail=max_tail, out=d_out[i])
+            ev[3 + i].record(stream)
+
+    # count this library's kernel launches per step from the device-side counters is not
+    # possible without a profiler; the count follows from the launch plan instead
+    launches_per_step = 1 + (1 if ws_bytes > 0 else 0) + 1 + gamma * getattr(
+        vsd, "SPARSE_LAUNCHES_PER_CALL", 1)
+    enqueue_s = []
+    sleep_cycles = 8_000_000  # ~4 ms: the whole step is enqueued before the GPU gets to it
+
+    def timed_step(sl):
+        seq_len.copy_(torch.from_numpy(sl))
+        flush_l2(flush_w, flush_r)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(sleep_cycles)  # keep the GPU busy while the host enqueues the step
+        t_host = time.perf_counter()
+        ev[0].record(stream)
+        step()
+        enqueue_s.append(time.perf_counter() - t_host)
+
+    for _ in range(args.warmup):
+        timed_step(draw_seq_len())
+    torch.cuda.synchronize()
+    status = vsd.vsd_read_device_status()
+    if status:
+        raise RuntimeError("device status 0x%x during warm-up" % status)
+
+    per = {"verify": [], "select": [], "sparse": [], "step": []}
+    tails_seen = []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for _ in range(args.steps):
+            sl = draw_seq_len()
+            tails_seen.append([[int(sl[i, b] - prefix[b]) for b in range(B)]
+                               for i in range(gamma)])
+            timed_step(sl)
+            torch.cuda.synchronize()
+            per["verify"].append(ev[0].elapsed_time(ev[1]) * 1e-3)
+            per["select"].append(ev[1].elapsed_time(ev[2]) * 1e-3)
+            per["sparse"].append([ev[2 + i].elapsed_time(ev[3 + i]) * 1e-3 for i in range(gamma)])
+            per["step"].append(ev[0].elapsed_time(ev[2 + gamma]) * 1e-3)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    status = vsd.vsd_read_device_status()
+    if status:
+        raise RuntimeError("device status 0x%x in the timed region" % status)
+    n_sel_host = n_sel.cpu().tolist()
+
+    # algorithmic bytes (the draft tails vary with the drawn accept counts)
+    mean_tails = [[statistics.mean(t[i][b] for t in tails_seen) for b in range(B)]
+                  for i in range(gamma)]
+    vb, sb, spb = iteration_bytes(w, prefix, n_sel_host, mean_tails)
+    total_bytes = vb + sb + sum(spb)
+    t_step = sum(per["step"])
+    t_tensor = torch.tensor([t_step], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_tensor, op=torch.distributed.ReduceOp.MAX)
+    t_max = float(t_tensor.item())
+    value = world * total_bytes * args.steps / t_max / 1e9
+    peak, peak_kind = measured_peaks()
+    t_verify = statistics.mean(per["verify"])
+    t_select = statistics.mean(per["select"])
+    t_sparse = statistics.mean(statistics.mean(s) for s in per["sparse"])
+    kernels = {
+        "verify_collect": {"us": t_verify * 1e6, "bytes": vb, "GB_s": vb / t_verify / 1e9,
+                           "frac_of_%s_hbm" % peak_kind: vb / t_verify / 1e9 / peak},
+        "select_topk": {"us": t_select * 1e6, "bytes": sb, "GB_s": sb / t_select / 1e9},
+        "sparse_draft_step": {"us": t_sparse * 1e6, "bytes": statistics.mean(spb),
+                              "GB_s": statistics.mean(spb) / t_sparse / 1e9,
+                              "frac_of_%s_hbm" % peak_kind:
+                                  statistics.mean(spb) / t_sparse / 1e9 / peak},
+    }
+    achieved = vb / t_verify / 1e9
+    clk = clocks.summary()
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_max / args.steps * 1e3,
+        "us_per_iter": t_max / args.steps * 1e6,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "P": w.P, "Hq": Hq, "Hkv": w.Hkv, "d": d,
+                   "gamma": gamma, "k": w.k, "n_sink": w.n_sink, "n_recent": w.n_recent,
+                   "page": w.page,
+                   "l2": "flushed before every timed iteration (512 MB write, then 512 MB "
+                         "read so no dirty lines remain)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "kernels": kernels,
+        "select_over_verify": t_select / t_verify,
+        "roofline": {"bound": "hbm", "kernel": "vsd_verify_attn_collect",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": profile_traffic(w.name)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        # the device timestamps only measure kernels if the host finished enqueueing a
+        # step while the GPU was still asleep
+        "host_enqueue_us_median": statistics.median(enqueue_s) * 1e6,
+        "gpu_sleep_us": sleep_cycles / (clk.get("sm_max_mhz") or 2070.0),
+    }
+    if args.e2e:
+        result["e2e"] = run_e2e(args, w, batch, vsd, dev, stream, workspace, prefix, total_bytes)
+    return result, batch
+
+
+def run_e2e(args, w, batch, vsd, dev, stream, workspace, prefix, total_bytes):
+    """Same iteration through the Python API with host (pinned) inputs and outputs:
+    H2D of the step's queries and lengths, the calls, D2H of every result."""
+    B, R, Hq, d, gamma = w.B, w.R, w.Hq, w.d, w.gamma
+    h_q = batch.q.cpu().pin_memory()
+    h_qd = batch.q_draft.cpu().pin_memory()
+    h_pl = batch.prefix_len.cpu().pin_memory()
+    rng = np.random.default_rng(w.seed + 91)
+    h_sl = torch.empty((gamma, B), dtype=torch.int32).pin_memory()
+    d_q = torch.empty_like(batch.q)
+    d_qd = torch.empty_like(batch.q_draft)
+    d_pl = torch.empty_like(batch.prefix_len)
+    d_sl = torch.empty((gamma, B), dtype=torch.int32, device=dev)
+    h_out = torch.empty((B, R, Hq, d), dtype=torch.bfloat16).pin_memory()
+    h_idx = torch.empty((B, w.k), dtype=torch.int32).pin_memory()
+    h_ns = torch.empty((B,), dtype=torch.int32).pin_memory()
+    h_dout = torch.empty((gamma, B, Hq, d), dtype=torch.bfloat16).pin_memory()
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_qd, h_pl, h_sl))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_idx, h_ns, h_dout))
+    times = []
+    for it in range(args.warmup + args.steps):
+        a = rng.integers(0, gamma + 1, size=B)
+        h_sl.copy_(torch.tensor([[prefix[b] + a[b] + 2 + i for b in range(B)]
+                                 for i in range(gamma)], dtype=torch.int32))
+        flush_l2(flush_w, flush_r)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        d_q.copy_(h_q, non_blocking=True)
+        d_qd.copy_(h_qd, non_blocking=True)
+        d_pl.copy_(h_pl, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        out, _, partial = vsd.vsd_verify_attn_collect(
+            d_q, batch.k_cache, batch.v_cache, batch.block_table, d_pl, P_max=w.P_max,
+            scale=w.scale, workspace=workspace)
+        idx, n_sel, _ = vsd.vsd_select_topk(partial, d_pl, k=w.k, n_sink=w.n_sink,
+                                            n_recent=w.n_recent)
+        outs = [vsd.vsd_sparse_decode_attn(d_qd[i], batch.k_cache, batch.v_cache,
+                                           batch.block_table, idx, n_sel, d_pl, d_sl[i],
+                                           scale=w.scale, max_tail=2 * gamma + 1)
+                for i in range(gamma)]
+        h_out.copy_(out, non_blocking=True)
+        h_idx.copy_(idx, non_blocking=True)
+        h_ns.copy_(n_sel, non_blocking=True)
+        for i in range(gamma):
+            h_dout[i].copy_(outs[i], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            times.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.mean(times)
+    return {"value": total_bytes / t / 1e9, "unit": "GB/s", "us_per_iter": t * 1e6,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "Python API, eager launches, pinned host buffers"}
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+
+def cpu_oracle_iteration(w, h, prefix, steps_seed):
+    """One iteration of the fp64 oracle on the host: verify, select, gamma drafts."""
+    import oracle
+    out, logits, partial = oracle.verify(h["q"], h["k_cache"], h["v_cache"], h["block_table"],
+                                         h["prefix_len"], scale=w.scale, P_max=w.P_max)
+    score = oracle.score_from_logits(logits, h["prefix_len"])
+    idx, n_sel = oracle.select(score, h["prefix_len"], k=w.k, n_sink=w.n_sink,
+                               n_recent=w.n_recent)
+    rng = np.random.default_rng(steps_seed)
+    a = rng.integers(0, w.gamma + 1, size=w.B)
+    tails = []
+    for i in range(w.gamma):
+        sl = np.array([prefix[b] + a[b] + 2 + i for b in range(w.B)], np.int32)
+        oracle.sparse_decode(h["q_draft"][i], h["k_cache"], h["v_cache"], h["block_table"], idx,
+                             n_sel, h["prefix_len"], sl, scale=w.scale)
+        tails.append([int(sl[b] - prefix[b]) for b in range(w.B)])
+    return n_sel.tolist(), tails
+
+
+def run_cpu_baseline(w, batch, iters=3):
+    import oracle
+    from sparse_attention_speculative_gb300.synth import host_arrays
+    oracle.build()
+    h = host_arrays(batch)
+    prefix = list(w.prefix())
+    t0 = time.perf_counter()
+    for i in range(iters):
+        n_sel, tails = cpu_oracle_iteration(w, h, prefix, 1234 + i)
+    dt = (time.perf_counter() - t0) / iters
+    vb, sb, spb = iteration_bytes(w, prefix, n_sel, tails)
+    total = vb + sb + sum(spb)
+    return {"value": total / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds_per_iter": dt,
+            "sample": "%d full iteration(s) of %s (verify+collect2, select, %d draft steps), "
+                      "fp64 C oracle" % (iters, w.name, w.gamma)}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: same workload, metric and unit."""
+    if rank != 0:
+        return None
+    import oracle
+    from sparse_attention_speculative_gb300.synth import host_arrays, make_batch
+    from sparse_attention_speculative_gb300.workloads import ALL
+    oracle.build()
+    w = ALL[args.workload]
+    batch = make_batch(w, "cpu")
+    h = host_arrays(batch)
+    prefix = list(w.prefix())
+    for i in range(min(args.warmup, 1)):
+        cpu_oracle_iteration(w, h, prefix, 99 + i)
+    times = []
+    n_sel, tails = None, None
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        n_sel, tails = cpu_oracle_iteration(w, h, prefix, 1000 + i)
+        times.append(time.perf_counter() - t0)
+    vb, sb, spb = iteration_bytes(w, prefix, n_sel, tails)
+    total = vb + sb + sum(spb)
+    t = sum(times)
+    value = total * args.steps / t / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "gamma": w.gamma, "k": w.k, "n_sink": w.n_sink, "n_recent": w.n_recent},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": "each step one full iteration of %s on the host" % w.name},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="qwen3_8b_32k")
+    ap.add_argument("--impl", default="vsd", choices=["vsd", "reference"])
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res, batch = run_gpu(args, world, rank, local)
+    if rank == 0:
+        if args.cpu_baseline:
+            from sparse_attention_speculative_gb300.workloads import ALL
+            res["cpu_baseline"] = run_cpu_baseline(ALL[args.workload], batch)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
