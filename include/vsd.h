@@ -116,6 +116,36 @@ vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------
+ * Verification attention without a caller-provided workspace.  The pages have no
+ * counterpart: this is a convenience of this library.
+ *
+ * Same operation, arguments and results as vsd_verify_attn_collect, minus the
+ * workspace.  It is meant for callers that cannot allocate device memory on the
+ * decode path: an engine that has reserved all free HBM for its paged KV cache up
+ * front, or a host program that forbids cudaMalloc there because cudaMalloc can
+ * synchronize the whole device.  The scratch it needs lives instead in a fixed
+ * device array of VSD_NOALLOC_SCRATCH_BYTES that every GPU using this library holds
+ * until the process exits; this call allocates nothing.
+ *   - Returns VSD_ERR_WORKSPACE when vsd_verify_workspace_size reports more than
+ *     VSD_NOALLOC_SCRATCH_BYTES for this geometry (use the regular call then).
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array: calls whose kernels overlap on
+ *     the GPU (different streams without ordering) race and give wrong results.
+ *     Nothing in the array needs to start at zero.
+ * ------------------------------------------------------------------------------ */
+#define VSD_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
+
+vsd_status vsd_verify_attn_collect_noalloc(const vsd_geom* geom, int R, const void* q,
+                                           const void* k_cache, const void* v_cache,
+                                           const int32_t* block_table,
+                                           const int32_t* prefix_len, int collect_row0,
+                                           int collect_row1, int P_max, float scale,
+                                           float* logits, float* partial_scores, void* out,
+                                           void* stream);
+
+/* ------------------------------------------------------------------------------
  * Aggregated-logit top-k with a protected sink and recent window (Vegas summary
  * sec. 2.A selection equation; Dustin summary Methodology sec. 1).
  *

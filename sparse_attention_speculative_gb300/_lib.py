@@ -63,6 +63,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         GP = ctypes.POINTER(Geom)
         lib.vsd_verify_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
         lib.vsd_verify_attn_collect.argtypes = [GP, I, P, P, P, P, P, I, I, I, F, P, P, P, P, SZ, P]
+        lib.vsd_verify_attn_collect_noalloc.argtypes = [GP, I, P, P, P, P, P, I, I, I, F, P, P,
+                                                        P, P]
         lib.vsd_select_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(SZ)]
         lib.vsd_select_topk.argtypes = [I, I, P, P, I, I, I, I, P, P, P, P, SZ, P]
         lib.vsd_sparse_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
@@ -72,6 +74,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_get_error_string.restype = ctypes.c_char_p
         lib.vsd_last_cuda_error.argtypes = []
         for name in ("vsd_verify_workspace_size", "vsd_verify_attn_collect",
+                     "vsd_verify_attn_collect_noalloc",
                      "vsd_select_workspace_size", "vsd_select_topk", "vsd_sparse_workspace_size",
                      "vsd_sparse_decode_attn", "vsd_read_device_status", "vsd_last_cuda_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -162,6 +165,40 @@ def vsd_verify_attn_collect(q, k_cache, v_cache, block_table, prefix_len, *, P_m
                                      _ptr(logits), _ptr(partial), _ptr(out), _ptr(workspace),
                                      ws_bytes, _stream(stream))
     _check(rc, "vsd_verify_attn_collect")
+    return out, logits, partial
+
+
+def vsd_verify_attn_collect_noalloc(q, k_cache, v_cache, block_table, prefix_len, *,
+                                    P_max: int, scale: float, row0: int = 0,
+                                    row1: Optional[int] = None, logits=None, partial=None,
+                                    out=None, collect: bool = True, stream=None):
+    """vsd_verify_attn_collect with the library's fixed device scratch instead of a
+    workspace (the C call allocates nothing; outputs are allocated here when not
+    given).  Returns (out, logits, partial)."""
+    lib = load()
+    B, R, Hq, d = q.shape
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(block_table, torch.int32, "block_table")
+    _need(prefix_len, torch.int32, "prefix_len")
+    geom = geom_for(B, Hq, k_cache, block_table)
+    if row1 is None:
+        row1 = R - 1
+    dev = q.device
+    if out is None:
+        out = torch.empty_like(q)
+    if collect:
+        if logits is None:
+            logits = torch.empty((B, 2, Hq, P_max), dtype=torch.float32, device=dev)
+        if partial is None:
+            partial = torch.empty((B, geom.Hkv, P_max), dtype=torch.float32, device=dev)
+    rc = lib.vsd_verify_attn_collect_noalloc(ctypes.byref(geom), R, _ptr(q), _ptr(k_cache),
+                                             _ptr(v_cache), _ptr(block_table),
+                                             _ptr(prefix_len), int(row0), int(row1),
+                                             int(P_max), float(scale), _ptr(logits),
+                                             _ptr(partial), _ptr(out), _stream(stream))
+    _check(rc, "vsd_verify_attn_collect_noalloc")
     return out, logits, partial
 
 
