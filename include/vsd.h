@@ -104,7 +104,7 @@ typedef struct vsd_geom {
  *   out            bf16 [B][R][Hq][head_dim]
  *   workspace      >= vsd_verify_workspace_size(...) bytes; contents on entry
  *                  are ignored and on exit unspecified
- * Supported: head_dim in {64, 128}, page_size 16, 1 <= R and R * G <= 64.
+ * Supported: head_dim in {64, 128}, page_size 16, G <= 16, 1 <= R <= 16, R * G <= 64.
  * ------------------------------------------------------------------------------ */
 vsd_status vsd_verify_workspace_size(const vsd_geom* geom, int R, int P_max, size_t* bytes);
 

@@ -1,0 +1,793 @@
+// verify_attn.cuh -- verification attention with Collect-2-Query on sm_103a
+// (kernel templates; instantiated per head dimension in verify_attn_d*.cu).
+//
+// What it computes ("Vegas" technical summary, sec. 2 verification phase, sec. 2.B
+// Collect-2-Query, sec. 3 kernel instrumentation): the gamma+1 verify rows of every
+// sequence attend the whole paged KV cache (causal inside the verify block) and, in
+// the same pass over K, the scaled pre-softmax logits of two chosen rows are written
+// to HBM together with their per-KV-group sums (the first reduction of the
+// selection score of sec. 2.A).
+//
+// How (GB300 design):
+//   * One persistent CTA per SM.  The work is the list of (sequence, KV head) pairs
+//     times 128-key tiles; CTA c streams the contiguous range [c W / C, (c+1) W / C)
+//     of that list, so every SM gets the same number of tiles (split-K over the
+//     context, balanced to the tile).  A pair cut by CTA boundaries leaves one
+//     partial (m, l, o) per CTA; a small merge kernel combines them.
+//   * Warps 0 and 10 stream K and V pages with 4-D TMA loads (128-byte swizzle) into
+//     two separate shared-memory rings (3 stages of 32 KB each for head_dim 128, 5
+//     of 16 KB for 64), so a K stage is refilled as soon as its QK MMA has read it.
+//     Each 128-key tile is 8 pages; a page whose block-table entry is invalid is
+//     fetched at an out-of-range coordinate, which the TMA unit fills with zeros.
+//   * Warp 1 issues tcgen05 MMAs with the small dimension on N ("swap AB"):
+//       S^T[128 keys x NQ] = K_tile[128 x d] * Q^T        (K-major A and B)
+//       O^T[d x NQ]       += V_tile^T[d x 128] * P^T      (MN-major A and B)
+//     NQ = R*G rounded up to 16 covers all verify rows of one KV group.  It runs an
+//     event loop: QK of a tile as soon as its K tile has landed, PV of a tile as soon
+//     as its P^T is written, whichever is ready first (non-blocking polls).
+//     Accumulators live in TMEM (S double-buffered, O single).  For NQ <= 32 P^T is
+//     double-buffered in the two halves of each 128-byte swizzled row, so the
+//     softmax of tile i+1 never waits for the PV MMA of tile i.
+//   * Warps 2-9 (softmax): TMEM lane = key, and the NQ columns are split between the
+//     two warps that share a lane quarter.  Each thread reads its half row of logits,
+//     forms P against a running maximum shared by all keys of a column, and writes
+//     its P^T chunks.  The maximum is only raised when some logit exceeds it by more
+//     than 2^8 (one CTA vote per tile, bar.red.or), so the common path needs no
+//     cross-thread max; each thread keeps partial row sums l, reduced once per pair.
+//     Causal / length / bad-page masks are evaluated per key only where a key can be
+//     hidden.  The lower half also reads the two collected rows' logits with
+//     runtime-addressed TMEM loads and writes them (32 consecutive keys per warp
+//     store) with their group sum.
+#pragma once
+
+#include <cfloat>
+
+#include "common.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace vsd {
+namespace verify_detail {
+
+using namespace ptx;
+
+constexpr int kTile = 128;      // keys per tile (the MMA M dimension of S^T)
+constexpr int kPage = 16;       // tokens per cache page
+constexpr int kPagesPerTile = kTile / kPage;
+constexpr float kTau = 8.0f;    // lazy-max slack, log2 units
+constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+// warp 0: K producer, warp 1: MMA issuer, warps 2-9: softmax, warp 10: V producer
+constexpr int kThreads = 96 + kSoftmaxThreads;
+constexpr int kVWarp = 10;
+constexpr int kSoftmaxBar = 1;  // named barrier of the softmax threads
+
+template <int D>
+struct VCfg {
+  static constexpr int kStages = (D == 128) ? 3 : 5;  // depth of each of the K and V rings
+  static constexpr int kKVBytes = kTile * D * 2;      // K (or V) of one tile
+  static constexpr int kHalfBytes = kTile * 128;      // 64-column half of a tile
+  static constexpr int kQBytesMax = 64 * D * 2;
+  static constexpr int kPBytes = kTile * 128;
+  static constexpr int kOffV = kStages * kKVBytes;
+  static constexpr int kOffQ = kOffV + kStages * kKVBytes;
+  static constexpr int kOffP = kOffQ + kQBytesMax;
+  static constexpr int kOffMisc = kOffP + kPBytes;
+  static constexpr int kMiscBytes = 1920;
+  static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kOffP % 1024 == 0 && kOffQ % 1024 == 0, "swizzle atoms need 1 KB alignment");
+};
+
+struct VParams {
+  const uint16_t* q;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  float* logits;
+  float* partial;
+  uint16_t* out;
+  float* ws;
+  unsigned* status;
+  int B, Hq, Hkv, R, NV, max_blocks, num_blocks, P_max;
+  int row0, row1;
+  int pairs, t_max, max_chunks;
+  float scale;
+};
+
+// CTA whose range holds virtual tile v (ranges are [c W / C, (c+1) W / C)).
+__device__ __forceinline__ int cta_of(long long v, long long W, int C) {
+  return static_cast<int>(((v + 1) * C - 1) / W);
+}
+
+struct Seg {
+  int p, b, g;
+  bool bad_len;        // prefix length outside the declared bounds (no key is read)
+  int t_begin, t_end;  // tiles of this CTA inside the pair, clipped to the sequence
+  int P, L;            // prefix length and cache length (P + R)
+  long long next_v;
+};
+
+__device__ __forceinline__ Seg segment_at(long long v, long long v1, const VParams& a) {
+  Seg s;
+  s.p = static_cast<int>(v / a.t_max);
+  const long long pair_end = static_cast<long long>(s.p + 1) * a.t_max;
+  const long long e = v1 < pair_end ? v1 : pair_end;
+  s.next_v = e;
+  s.b = s.p / a.Hkv;
+  s.g = s.p - s.b * a.Hkv;
+  const int P = __ldg(a.prefix_len + s.b);
+  const bool ok = P >= 0 && P <= a.P_max &&
+                  static_cast<long long>(P) + a.R <= static_cast<long long>(a.max_blocks) * kPage;
+  s.bad_len = !ok;
+  s.P = ok ? P : 0;
+  s.L = ok ? P + a.R : 0;
+  const int T = ok ? (s.L + kTile - 1) / kTile : 0;
+  s.t_begin = static_cast<int>(v - static_cast<long long>(s.p) * a.t_max);
+  const int te = static_cast<int>(e - static_cast<long long>(s.p) * a.t_max);
+  s.t_end = te < T ? te : T;
+  if (s.t_end < s.t_begin) s.t_end = s.t_begin;
+  return s;
+}
+
+__device__ __forceinline__ bool softmax_vote(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "n"(kSoftmaxBar), "n"(kSoftmaxThreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void softmax_sync() {
+  named_barrier_sync(kSoftmaxBar, kSoftmaxThreads);
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+template <int D, int NQ, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    verify_attn_collect_kernel(const __grid_constant__ CUtensorMap kmap,
+                               const __grid_constant__ CUtensorMap vmap, const VParams a) {
+  using Cfg = VCfg<D>;
+  constexpr int S = Cfg::kStages;
+  constexpr int NC = NQ / 2;              // columns per softmax thread
+  constexpr int PB = (NQ <= 32) ? 2 : 1;  // P^T buffers: two halves of each 128-byte row
+  static_assert(NQ % 16 == 0 && NQ <= 64, "NQ");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* k_ring = base;
+  uint8_t* v_ring = base + Cfg::kOffV;
+  uint8_t* q_smem = base + Cfg::kOffQ;
+  uint8_t* p_smem = base + Cfg::kOffP;
+  uint8_t* misc = base + Cfg::kOffMisc;
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(misc);
+  uint64_t* k_empty = k_full + S;
+  uint64_t* v_full = k_empty + S;
+  uint64_t* v_empty = v_full + S;
+  uint64_t* s_full = v_empty + S;     // [2]
+  uint64_t* s_empty = s_full + 2;     // [2]
+  uint64_t* p_full = s_empty + 2;     // [2] (PB used)
+  uint64_t* pv_done = p_full + 2;     // [2] (PB used)
+  uint64_t* q_ready = pv_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
+  float* m2s = reinterpret_cast<float*>(misc + 320);              // [64] new running max
+  float* red = reinterpret_cast<float*>(misc + 576);              // [4][64] reductions
+  float* alphas = reinterpret_cast<float*>(misc + 1600);          // [64] rescale factors
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], kSoftmaxThreads);
+      mbar_init(&p_full[i], kSoftmaxThreads);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(q_ready, kSoftmaxThreads);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();  // the merge kernel may become resident and wait
+  const uint32_t tmem_s0 = tmem;       // S^T buffer b: columns [64 b, 64 b + NQ)
+  const uint32_t tmem_o = tmem + 128;  // O^T: columns [128, 128 + NQ)
+
+  const long long W = static_cast<long long>(a.pairs) * a.t_max;
+  const int C = gridDim.x;
+  const long long v0 = static_cast<long long>(blockIdx.x) * W / C;
+  const long long v1 = static_cast<long long>(blockIdx.x + 1) * W / C;
+
+  auto set_abort = [&]() {
+    if (!*abort_flag) {
+      *abort_flag = 1;
+      flag_status(a.status, VSD_DEV_TIMEOUT);
+    }
+  };
+
+  if (warp == 0 || warp == kVWarp) {
+    // ------------------------------------------------------------ TMA producers
+    // warp 0 streams the K tiles, warp 10 the V tiles, each through its own ring, so
+    // a K stage is refilled as soon as its QK MMA has read it.
+    const bool is_k = warp == 0;
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
+    uint8_t* ring = is_k ? k_ring : v_ring;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
+    const uint64_t pol = l2_policy_evict_first();
+    if (lane == 0) tma_prefetch_desc(map);
+    uint32_t it = 0, issued = 0;
+    for (long long v = v0; v < v1;) {
+      const Seg s = segment_at(v, v1, a);
+      v = s.next_v;
+      if (is_k && s.bad_len && lane == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
+      // block id of page `lane` of a tile (lanes 0-7); out of range -> zero fill
+      auto fetch_blk = [&](int tile, bool& bad) {
+        int blk = a.num_blocks;
+        bad = false;
+        if (lane < kPagesPerTile && tile < s.t_end) {
+          const int lp = tile * kPagesPerTile + lane;
+          if (lp * kPage < s.L) {
+            const int e = __ldg(a.block_table + static_cast<size_t>(s.b) * a.max_blocks + lp);
+            if (e < 0 || e >= a.num_blocks) bad = true;
+            else blk = e;
+          }
+        }
+        return blk;
+      };
+      bool bad_next = false;
+      int blk_next = fetch_blk(s.t_begin, bad_next);
+      for (int tile = s.t_begin; tile < s.t_end; ++tile, ++it) {
+        const int stage = it % S;
+        const uint32_t use = it / S;
+        const int blk = blk_next;
+        const bool bad = bad_next;
+        blk_next = fetch_blk(tile + 1, bad_next);  // in flight while we wait below
+        int ok = 1;
+        if (lane == 0 && use > 0) ok = mbar_wait(&empty[stage], (use - 1) & 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok && lane == 0) set_abort();
+        if (*abort_flag) continue;
+        const unsigned badbits = __ballot_sync(0xffffffffu, bad);
+        if (lane == 0) {
+          if (is_k && badbits) flag_status(a.status, VSD_DEV_BAD_BLOCK);
+          mbar_arrive_expect_tx(&full[stage], Cfg::kKVBytes);
+        }
+        __syncwarp();
+        if (lane < kPagesPerTile) {
+          uint8_t* dst = ring + stage * Cfg::kKVBytes + lane * (kPage * 128);
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_4d(dst + h * Cfg::kHalfBytes, map, &full[stage], h * 64, 0, s.g, blk, pol);
+        }
+        issued = it + 1;
+      }
+    }
+    // Never leave a copy in flight: wait (bounded) for the last stages issued.
+    if (lane == 0) {
+      const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0;
+      for (uint32_t i = first; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, NQ, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, NQ, 1, 1);
+      const uint32_t q_addr = smem_u32(q_smem);
+      const uint32_t p_addr = smem_u32(p_smem);
+      const uint32_t k_addr0 = smem_u32(k_ring);
+      const uint32_t v_addr0 = smem_u32(v_ring);
+      uint32_t total = 0;
+      for (long long v = v0; v < v1;) {
+        const Seg s = segment_at(v, v1, a);
+        v = s.next_v;
+        total += static_cast<uint32_t>(s.t_end - s.t_begin);
+      }
+      long long qv = v0;
+      Seg qs = segment_at(qv, v1, a);
+      int q_tile = qs.t_begin;
+      uint32_t nseg = 0;
+      uint32_t first_bits = 0;  // bit (i & 31): tile i is the first tile of its segment
+      uint32_t qi = 0, pi = 0;
+      const uint64_t t_start = global_timer_ns();
+      uint32_t spins = 0;
+      while (pi < total) {
+        bool progressed = false;
+        // ---- PV of tile pi (accumulates unless first of its segment)
+        if (pi < qi && mbar_test(&p_full[pi % PB], (pi / PB) & 1) &&
+            mbar_test(&v_full[pi % S], (pi / S) & 1)) {
+          tc_fence_after();
+          const int stage_i = static_cast<int>(pi % S);
+          const bool first_i = (first_bits >> (pi & 31)) & 1u;
+          const uint32_t v_addr = v_addr0 + stage_i * Cfg::kKVBytes;
+          const uint32_t pb_addr = p_addr + (pi % PB) * 64;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint64_t adesc = sdesc_sw128(v_addr + kk * 2048, Cfg::kHalfBytes, 1024);
+            const uint64_t bdesc = sdesc_sw128(pb_addr + kk * 2048, Cfg::kHalfBytes, 1024);
+            umma_bf16(tmem_o, adesc, bdesc, idesc_pv, (kk > 0 || !first_i) ? 1u : 0u);
+          }
+          umma_commit(&v_empty[stage_i]);
+          umma_commit(&pv_done[pi % PB]);
+          ++pi;
+          progressed = true;
+        }
+        // ---- QK of tile qi (needs its K tile, a free S buffer, and Q of its segment)
+        if (qi < total && qi < pi + 2) {
+          while (q_tile >= qs.t_end) {  // advance to the next non-empty segment
+            qv = qs.next_v;
+            qs = segment_at(qv, v1, a);
+            q_tile = qs.t_begin;
+          }
+          const bool first = q_tile == qs.t_begin;
+          const int stage = static_cast<int>(qi % S);
+          const int buf = qi & 1;
+          const bool ready = (!first || mbar_test(q_ready, nseg & 1)) &&
+                             mbar_test(&k_full[stage], (qi / S) & 1) &&
+                             (qi < 2 || mbar_test(&s_empty[buf], ((qi >> 1) - 1) & 1));
+          if (ready) {
+            tc_fence_after();
+            const uint32_t k_addr = k_addr0 + stage * Cfg::kKVBytes;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const int half = kk >> 2, w = kk & 3;
+              const uint64_t adesc =
+                  sdesc_sw128(k_addr + half * Cfg::kHalfBytes + w * 32, 16, 1024);
+              const uint64_t bdesc = sdesc_sw128(q_addr + half * NQ * 128 + w * 32, 16, 1024);
+              umma_bf16(tmem_s0 + buf * 64, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&k_empty[stage]);
+            umma_commit(&s_full[buf]);
+            if (first) {
+              first_bits |= 1u << (qi & 31);
+              ++nseg;
+            } else {
+              first_bits &= ~(1u << (qi & 31));
+            }
+            ++q_tile;
+            ++qi;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          spins = 0;
+        } else {
+          __nanosleep(32);
+          if ((++spins & 63u) == 0 &&
+              (*abort_flag || global_timer_ns() - t_start > VSD_WAIT_LIMIT_NS)) {
+            set_abort();
+            break;
+          }
+        }
+      }
+      // Never leave an MMA in flight: wait (bounded) for the last PV issued.
+      if (pi > 0) mbar_wait(&pv_done[(pi - 1) % PB], ((pi - 1) / PB) & 1);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int sw = warp - 2;                   // 0..7
+    const int quarter = warp & 3;              // TMEM lane quarter of this warp
+    const int half = sw >> 2;                  // which NC columns of the row
+    const int row = quarter * 32 + lane;       // key in tile (S^T) / dim (O^T)
+    const int ts = threadIdx.x - 64;           // 0..255
+    const int col0 = half * NC;                // first column of this thread
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const float scale = a.scale;
+    const float scale_log2 = a.scale * kLog2e;
+    const bool collect = a.logits != nullptr || a.partial != nullptr;
+    uint32_t it = 0;
+    for (long long v = v0; v < v1;) {
+      const Seg s = segment_at(v, v1, a);
+      v = s.next_v;
+      const long long first_v = static_cast<long long>(s.p) * a.t_max;
+      const int c_first = cta_of(first_v, W, C);
+      const int c_last = cta_of(first_v + a.t_max - 1, W, C);
+      const bool direct = c_first == c_last;
+      const int slot = s.p * a.max_chunks + (static_cast<int>(blockIdx.x) - c_first);
+      const bool has_tiles = s.t_begin < s.t_end;
+      float lacc[NC], m2[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        lacc[c] = 0.f;
+        // padded columns get +inf: their probabilities are exp2(-inf) = 0 and they
+        // never trigger a rescale
+        m2[c] = (col0 + c < a.NV) ? -INFINITY : INFINITY;
+      }
+
+      if (has_tiles) {
+        // Q rows of this (sequence, KV group): row r = t * G + hl -> q[b, t, g*G + hl, :]
+        for (int idx = ts; idx < NQ * (D / 8); idx += kSoftmaxThreads) {
+          const int r = idx / (D / 8), ch = idx % (D / 8);
+          uint4 val = make_uint4(0, 0, 0, 0);
+          if (r < a.NV) {
+            const int t = r / G, hl = r % G;
+            val = *reinterpret_cast<const uint4*>(
+                a.q + ((static_cast<size_t>(s.b) * a.R + t) * a.Hq + s.g * G + hl) * D + ch * 8);
+          }
+          const int hh = ch >> 3, w = ch & 7;
+          *reinterpret_cast<uint4*>(q_smem + hh * NQ * 128 + r * 128 + ((w ^ (r & 7)) << 4)) =
+              val;
+        }
+        if (ts < 64) m2s[ts] = (ts < a.NV) ? -INFINITY : INFINITY;
+        fence_proxy_async_smem();
+        mbar_arrive(q_ready);
+      }
+
+      // block-table entry of this thread's key page, fetched one tile ahead (a page
+      // outside [0, num_blocks) was zero-filled by the producer and is masked here)
+      auto page_entry = [&](int tile) {
+        const int jj = tile * kTile + row;
+        return (tile < s.t_end && jj < s.L)
+                   ? __ldg(a.block_table + static_cast<size_t>(s.b) * a.max_blocks + jj / kPage)
+                   : 0;
+      };
+      int entry_next = page_entry(s.t_begin);
+      for (int tile = s.t_begin; tile < s.t_end; ++tile, ++it) {
+        const int stage = it % S;
+        const int buf = it & 1;
+        const int pb = it % PB;
+        const int entry = entry_next;
+        entry_next = page_entry(tile + 1);
+        if (!mbar_wait(&s_full[buf], (it >> 1) & 1, abort_flag)) set_abort();
+        const int j = tile * kTile + row;
+        const bool want_collect = collect && half == 0 && j < s.P;
+        tc_fence_after();
+        const uint32_t s_addr = tmem_s0 + buf * 64 + lane_addr;
+        float sv[NC];
+        uint32_t c0raw[G], c1raw[G];
+        tmem_ld_cols<NC>(s_addr + col0, reinterpret_cast<uint32_t*>(sv));
+        if (collect && half == 0) {
+          // warp-uniform: the lower-half warps read the two collected rows
+          tmem_ld<G>(s_addr + a.row0 * G, c0raw);
+          tmem_ld<G>(s_addr + a.row1 * G, c1raw);
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&s_empty[buf]);
+
+        // Collect-2-Query: logits of rows row0 / row1 and their group sum, j < P_b
+        if (want_collect) {
+          float acc = 0.f;
+#pragma unroll
+          for (int hl = 0; hl < G; ++hl) {
+            const float z0 = __uint_as_float(c0raw[hl]) * scale;
+            if (a.logits)
+              __stcs(a.logits + ((static_cast<size_t>(s.b) * 2 + 0) * a.Hq + s.g * G + hl) *
+                                    a.P_max + j, z0);
+            acc += z0;
+          }
+#pragma unroll
+          for (int hl = 0; hl < G; ++hl) {
+            const float z1 = __uint_as_float(c1raw[hl]) * scale;
+            if (a.logits)
+              __stcs(a.logits + ((static_cast<size_t>(s.b) * 2 + 1) * a.Hq + s.g * G + hl) *
+                                    a.P_max + j, z1);
+            acc += z1;
+          }
+          if (a.partial) a.partial[(static_cast<size_t>(s.b) * a.Hkv + s.g) * a.P_max + j] = acc;
+        }
+
+        // d = y - m2 in log2 units (y = scaled logit); masks only where a key can be hidden
+        const bool bad = entry < 0 || entry >= a.num_blocks;
+        const bool masked = j >= s.P || bad;  // per key
+        int c_lo = 0;                         // first visible column of this key
+        if (masked) {
+          const bool valid = j < s.L && !bad;
+          c_lo = !valid ? NQ : (j - s.P) * G;
+        }
+        float dmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const float d = fmaf(sv[c], scale_log2, -m2[c]);
+          if (!masked || col0 + c >= c_lo) dmax = fmaxf(dmax, d);
+        }
+        if (softmax_vote(dmax > kTau)) {
+          // rare: some visible logit is far above its column's running max
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            const bool vis = !masked || col0 + c >= c_lo;
+            const float x = warp_max(vis ? sv[c] * scale_log2 : -INFINITY);
+            if (lane == 0) red[quarter * 64 + col0 + c] = x;
+          }
+          softmax_sync();
+          if (ts < NQ) {
+            const int c = ts;
+            const float mx = fmaxf(fmaxf(red[c], red[64 + c]), fmaxf(red[128 + c], red[192 + c]));
+            const float mo = m2s[c];
+            const float mn = fmaxf(mo, mx);
+            // -inf: nothing accumulated yet; +inf: padding column, never used
+            alphas[c] = (mo == -INFINITY) ? 0.f : (mo == INFINITY ? 1.f : exp2f(mo - mn));
+            m2s[c] = mn;
+          }
+          softmax_sync();
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            lacc[c] *= alphas[col0 + c];
+            m2[c] = m2s[col0 + c];
+          }
+          if (tile != s.t_begin) {
+            // O^T holds earlier tiles: rescale this thread's columns once the last PV is done
+            if (!mbar_wait(&pv_done[(it - 1) % PB], ((it - 1) / PB) & 1, abort_flag)) set_abort();
+            tc_fence_after();
+            uint32_t r[NC];
+            tmem_ld_cols<NC>(tmem_o + lane_addr + col0, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+              r[c] = __float_as_uint(__uint_as_float(r[c]) * alphas[col0 + c]);
+            tmem_st_cols<NC>(tmem_o + lane_addr + col0, r);
+            tmem_wait_st();
+          }
+        }
+        // probabilities relative to the shared running max
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const bool vis = !masked || col0 + c >= c_lo;
+          const float pc = vis ? exp2f(fmaf(sv[c], scale_log2, -m2[c])) : 0.f;
+          lacc[c] += pc;
+          sv[c] = pc;
+        }
+        // P^T buffer pb: the PV that last read it must be done
+        if (it >= static_cast<uint32_t>(PB) &&
+            !mbar_wait(&pv_done[pb], ((it - PB) / PB) & 1, abort_flag))
+          set_abort();
+        if (j >= s.L) {
+          // rows past the sequence end hold whatever the cache holds: zero V there once
+          // the tile has landed (each half of the pair zeroes one 64-column half)
+          if (!mbar_wait(&v_full[stage], (it / S) & 1, abort_flag)) set_abort();
+          if (half < D / 64) {
+            uint8_t* vrow = v_ring + stage * Cfg::kKVBytes + half * Cfg::kHalfBytes + row * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(vrow + ch * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        uint8_t* prow = p_smem + row * 128;
+#pragma unroll
+        for (int k = 0; k < NC / 8; ++k) {
+          const int ch = pb * 4 + col0 / 8 + k;  // buffer 1 starts 32 elements in
+          uint4 pk;
+          pk.x = pack_bf16x2(sv[k * 8 + 0], sv[k * 8 + 1]);
+          pk.y = pack_bf16x2(sv[k * 8 + 2], sv[k * 8 + 3]);
+          pk.z = pack_bf16x2(sv[k * 8 + 4], sv[k * 8 + 5]);
+          pk.w = pack_bf16x2(sv[k * 8 + 6], sv[k * 8 + 7]);
+          *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = pk;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[pb]);
+      }
+
+      // ---------------------------------------------------------- pair epilogue
+      const size_t slot_base = static_cast<size_t>(slot) * NQ * (D + 2);
+      if (has_tiles) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const float x = warp_sum(lacc[c]);
+          if (lane == 0) red[quarter * 64 + col0 + c] = x;
+        }
+        softmax_sync();
+        if (!mbar_wait(&pv_done[(it - 1) % PB], ((it - 1) / PB) & 1, abort_flag)) set_abort();
+        tc_fence_after();
+        float o[NC];
+        tmem_ld_cols<NC>(tmem_o + lane_addr + col0, reinterpret_cast<uint32_t*>(o));
+        tmem_wait_ld();
+        tc_fence_before();
+        if (row < D) {
+          const int dim = row;
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            const int cc = col0 + c;
+            if (cc < a.NV) {
+              if (direct) {
+                const float l = red[cc] + red[64 + cc] + red[128 + cc] + red[192 + cc];
+                const int t = cc / G, hl = cc % G;
+                const float val = l > 0.f ? o[c] / l : 0.f;
+                const __nv_bfloat16 bv = __float2bfloat16_rn(val);
+                a.out[((static_cast<size_t>(s.b) * a.R + t) * a.Hq + s.g * G + hl) * D + dim] =
+                    *reinterpret_cast<const uint16_t*>(&bv);
+              } else {
+                a.ws[slot_base + 2 * NQ + static_cast<size_t>(cc) * D + dim] = o[c];
+              }
+            }
+          }
+        }
+        if (!direct && quarter == 0 && lane == 0) {
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            const int cc = col0 + c;
+            a.ws[slot_base + cc] = m2[c];
+            a.ws[slot_base + NQ + cc] = red[cc] + red[64 + cc] + red[128 + cc] + red[192 + cc];
+          }
+        }
+        softmax_sync();
+      } else {
+        // no key of this pair in this CTA: an empty partial (or zeros when alone)
+        if (direct) {
+          for (int idx = ts; idx < a.NV * D; idx += kSoftmaxThreads) {
+            const int c = idx / D, dim = idx % D;
+            const int t = c / G, hl = c % G;
+            a.out[((static_cast<size_t>(s.b) * a.R + t) * a.Hq + s.g * G + hl) * D + dim] = 0;
+          }
+        } else {
+          if (ts < NQ) {
+            a.ws[slot_base + ts] = -INFINITY;
+            a.ws[slot_base + NQ + ts] = 0.f;
+          }
+          for (int idx = ts; idx < NQ * D; idx += kSoftmaxThreads) a.ws[slot_base + 2 * NQ + idx] = 0.f;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// Combine the partial (m, l, o) of the CTAs that shared a pair: block (pair, row).
+template <int D, int NQ, int G>
+__global__ void __launch_bounds__(D) verify_merge_kernel(const VParams a, int ctas) {
+  __shared__ float wgt[256];
+  __shared__ float inv_l;
+  const int p = blockIdx.x;
+  const int c = blockIdx.y;
+  pdl_wait_primary();  // partials of the verification kernel are complete
+  const long long W = static_cast<long long>(a.pairs) * a.t_max;
+  const long long first_v = static_cast<long long>(p) * a.t_max;
+  const int c_first = cta_of(first_v, W, ctas);
+  const int c_last = cta_of(first_v + a.t_max - 1, W, ctas);
+  if (c_first == c_last) return;
+  const int n = c_last - c_first + 1;
+  const size_t slot_stride = static_cast<size_t>(NQ) * (D + 2);
+  const float* ws = a.ws + static_cast<size_t>(p) * a.max_chunks * slot_stride;
+  if (threadIdx.x < 32) {
+    float M = -INFINITY;
+    for (int k = threadIdx.x; k < n; k += 32) M = fmaxf(M, ws[k * slot_stride + c]);
+    M = warp_max(M);
+    float L = 0.f;
+    for (int k = threadIdx.x; k < n; k += 32) {
+      const float mk = ws[k * slot_stride + c];
+      const float w = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
+      wgt[k] = w;
+      L += w * ws[k * slot_stride + NQ + c];
+    }
+    L = warp_sum(L);
+    if (threadIdx.x == 0) inv_l = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  const int dim = threadIdx.x;
+  float acc = 0.f;
+  for (int k0 = 0; k0 < n; k0 += 8) {
+    float x[8];  // eight partials in flight, summed in chunk order
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      x[u] = k0 + u < n ? ws[(k0 + u) * slot_stride + 2 * NQ + static_cast<size_t>(c) * D + dim]
+                        : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (k0 + u < n) acc += wgt[k0 + u] * x[u];
+  }
+  const int b = p / a.Hkv, g = p - (p / a.Hkv) * a.Hkv;
+  const int t = c / G, hl = c % G;
+  const __nv_bfloat16 bv = __float2bfloat16_rn(acc * inv_l);
+  a.out[((static_cast<size_t>(b) * a.R + t) * a.Hq + g * G + hl) * D + dim] =
+      *reinterpret_cast<const uint16_t*>(&bv);
+}
+
+template <int D, int NQ, int G>
+cudaError_t launch_dng(const VerifyArgs& va, const VerifyPlan& plan, const VParams& p,
+                       cudaStream_t stream) {
+  auto kern = verify_attn_collect_kernel<D, NQ, G>;
+  constexpr int smem = VCfg<D>::kSmemBytes;
+  // set on every call: the attribute is per device and the call costs no GPU work
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<plan.ctas, kThreads, smem, stream>>>(va.kmap, va.vmap, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (plan.max_chunks > 1) {
+    // programmatic dependent launch: resident while the verification kernel runs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.pairs, p.NV, 1);
+    cfg.blockDim = dim3(D, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G>, p, plan.ctas);
+  }
+  return e;
+}
+
+inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {
+  VParams p;
+  p.q = static_cast<const uint16_t*>(va.q);
+  p.block_table = va.block_table;
+  p.prefix_len = va.prefix_len;
+  p.logits = va.logits;
+  p.partial = va.partial;
+  p.out = static_cast<uint16_t*>(va.out);
+  p.ws = va.ws;
+  p.status = va.status;
+  p.B = va.B;
+  p.Hq = va.Hq;
+  p.Hkv = va.Hkv;
+  p.R = va.R;
+  p.NV = va.R * va.G;
+  p.max_blocks = va.max_blocks;
+  p.num_blocks = va.num_blocks;
+  p.P_max = va.P_max;
+  p.row0 = va.row0;
+  p.row1 = va.row1;
+  p.pairs = plan.pairs;
+  p.t_max = plan.t_max;
+  p.max_chunks = plan.max_chunks;
+  p.scale = va.scale;
+  return p;
+}
+
+// Dispatch over (G, NQ) for one head dimension.
+template <int D>
+cudaError_t launch_verify_d(const VerifyArgs& va, const VerifyPlan& plan, cudaStream_t stream) {
+  const VParams p = make_params(va, plan);
+#define VSD_VERIFY_CASE(GG, NN) \
+  if (va.G == GG && plan.nq == NN) return launch_dng<D, NN, GG>(va, plan, p, stream);
+  VSD_VERIFY_CASE(1, 16)
+  VSD_VERIFY_CASE(2, 16)
+  VSD_VERIFY_CASE(2, 32)
+  VSD_VERIFY_CASE(4, 16)
+  VSD_VERIFY_CASE(4, 32)
+  VSD_VERIFY_CASE(4, 48)
+  VSD_VERIFY_CASE(4, 64)
+  VSD_VERIFY_CASE(8, 16)
+  VSD_VERIFY_CASE(8, 32)
+  VSD_VERIFY_CASE(8, 48)
+  VSD_VERIFY_CASE(8, 64)
+  VSD_VERIFY_CASE(16, 16)
+  VSD_VERIFY_CASE(16, 32)
+  VSD_VERIFY_CASE(16, 48)
+  VSD_VERIFY_CASE(16, 64)
+#undef VSD_VERIFY_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace verify_detail
+}  // namespace vsd

@@ -108,7 +108,7 @@ vsd_status verify_checks(const vsd_geom* geom, int R, int P_max) {
   if (st != VSD_OK) return st;
   if (R < 1 || P_max < 0) return VSD_ERR_INVALID_ARG;
   const int G = geom->Hq / geom->Hkv;
-  if (R * G > 64) return VSD_ERR_UNSUPPORTED;
+  if (R > 16 || G > 16 || R * G > 64) return VSD_ERR_UNSUPPORTED;
   return VSD_OK;
 }
 
