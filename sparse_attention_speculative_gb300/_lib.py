@@ -114,10 +114,11 @@ def geom_for(B: int, Hq: int, k_cache: torch.Tensor, block_table: torch.Tensor) 
 _ws_cache = {}
 
 
-def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
+def _workspace(nbytes: int, device, tag: str) -> Optional[torch.Tensor]:
+    """Cached device scratch, one buffer per (call kind, device, size)."""
     if nbytes == 0:
         return None
-    key = (str(device), nbytes)
+    key = (tag, str(device), nbytes)
     ws = _ws_cache.get(key)
     if ws is None:
         ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
@@ -157,7 +158,7 @@ def vsd_verify_attn_collect(q, k_cache, v_cache, block_table, prefix_len, *, P_m
         if partial is None:
             partial = torch.empty((B, geom.Hkv, P_max), dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = _workspace(vsd_verify_workspace_size(geom, R, P_max), dev)
+        workspace = _workspace(vsd_verify_workspace_size(geom, R, P_max), dev, "verify")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.vsd_verify_attn_collect(ctypes.byref(geom), R, _ptr(q), _ptr(k_cache),
                                      _ptr(v_cache), _ptr(block_table), _ptr(prefix_len),
@@ -224,8 +225,16 @@ def vsd_select_topk(partial, prefix_len, *, k: int, n_sink: int, n_recent: int, 
     return idx, n_sel, scores_out
 
 
+def vsd_sparse_workspace_size(geom: Geom, k_max: int, max_tail: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().vsd_sparse_workspace_size(ctypes.byref(geom), int(k_max), int(max_tail),
+                                            ctypes.byref(out)), "vsd_sparse_workspace_size")
+    return int(out.value)
+
+
 def vsd_sparse_decode_attn(q, k_cache, v_cache, block_table, idx, n_sel, tail_start, seq_len,
-                           *, scale: float, max_tail: int, out=None, stream=None):
+                           *, scale: float, max_tail: int, out=None, workspace=None,
+                           stream=None):
     """Sparse draft-step attention.  q: bf16 [B, Hq, d]; idx: int32 [B, k_max] or None."""
     lib = load()
     B, Hq, d = q.shape
@@ -236,10 +245,14 @@ def vsd_sparse_decode_attn(q, k_cache, v_cache, block_table, idx, n_sel, tail_st
     k_max = 0 if idx is None else int(idx.shape[1])
     if out is None:
         out = torch.empty_like(q)
+    if workspace is None:
+        workspace = _workspace(vsd_sparse_workspace_size(geom, k_max, max_tail), q.device,
+                               "sparse")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.vsd_sparse_decode_attn(ctypes.byref(geom), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(block_table), _ptr(idx), _ptr(n_sel), k_max,
                                     _ptr(tail_start), _ptr(seq_len), int(max_tail), float(scale),
-                                    _ptr(out), None, 0, _stream(stream))
+                                    _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "vsd_sparse_decode_attn")
     return out
 

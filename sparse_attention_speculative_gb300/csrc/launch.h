@@ -49,7 +49,8 @@ struct SelectArgs {
   int n_rows, Hkv, P_max, k, n_sink, n_recent;
 };
 
-int select_cluster_size(int P_max);
+int select_cluster_size(int P_max, int n_rows);
+int select_chunk(int P_max, int cs);  // prefix positions per CTA, or -1 if unsupported
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- sparse decode
@@ -63,11 +64,19 @@ struct SparseArgs {
   const int32_t* tail_start;
   const int32_t* seq_len;
   void* out;
+  float* ws;  // per-split partial results (m, l, o); NULL when one split suffices
   unsigned* status;
   int B, Hq, Hkv, G, d, max_blocks, num_blocks, k_max, max_tail;
   float scale;
 };
 
+struct SparsePlan {
+  int split_len;   // attended positions per CTA
+  int max_splits;  // CTAs (and workspace slots) per (sequence, KV head) pair
+};
+
+SparsePlan plan_sparse(int k_max, int max_tail);
+size_t sparse_workspace_bytes(const SparsePlan& plan, int B, int Hkv, int G, int head_dim);
 cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream);
 
 }  // namespace vsd

@@ -220,7 +220,8 @@ vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
 vsd_status vsd_select_workspace_size(int n_rows, int Hkv, int P_max, int k, size_t* bytes) {
   if (bytes == nullptr || n_rows < 0 || Hkv < 1 || P_max < 0 || k < 1)
     return VSD_ERR_INVALID_ARG;
-  if (vsd::select_cluster_size(P_max) < 1) return VSD_ERR_UNSUPPORTED;
+  if (vsd::select_chunk(P_max, vsd::select_cluster_size(P_max, n_rows)) < 0)
+    return VSD_ERR_UNSUPPORTED;
   *bytes = 0;
   return VSD_OK;
 }
@@ -234,7 +235,8 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
   if (n_rows < 0 || Hkv < 1 || P_max < 0 || k < 1 || n_sink < 0 || n_recent < 0)
     return VSD_ERR_INVALID_ARG;
   if (static_cast<long long>(n_sink) + n_recent > k) return VSD_ERR_INVALID_ARG;
-  if (vsd::select_cluster_size(P_max) < 1) return VSD_ERR_UNSUPPORTED;
+  if (vsd::select_chunk(P_max, vsd::select_cluster_size(P_max, n_rows)) < 0)
+    return VSD_ERR_UNSUPPORTED;
   if (n_rows == 0) return VSD_OK;
   if (!partial_scores || !prefix_len || !idx || !n_sel) return VSD_ERR_INVALID_ARG;
   if (!aligned(partial_scores, 16) || !aligned(idx, 4) || !aligned(n_sel, 4) ||
@@ -267,7 +269,8 @@ vsd_status vsd_sparse_workspace_size(const vsd_geom* geom, int k_max, int max_ta
   vsd_status st = check_geom(geom);
   if (st != VSD_OK) return st;
   if (geom->Hq / geom->Hkv > 16) return VSD_ERR_UNSUPPORTED;
-  *bytes = 0;
+  *bytes = vsd::sparse_workspace_bytes(vsd::plan_sparse(k_max, max_tail), geom->B, geom->Hkv,
+                                       geom->Hq / geom->Hkv, geom->head_dim);
   return VSD_OK;
 }
 
@@ -277,13 +280,17 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
                                   const int32_t* tail_start, const int32_t* seq_len,
                                   int max_tail, float scale, void* out, void* workspace,
                                   size_t workspace_bytes, void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   vsd_status st = check_geom(geom);
   if (st != VSD_OK) return st;
   if (geom->Hq / geom->Hkv > 16) return VSD_ERR_UNSUPPORTED;
   if (k_max < 0 || max_tail < 0) return VSD_ERR_INVALID_ARG;
+  if (geom->B > 65535) return VSD_ERR_UNSUPPORTED;
   if (geom->B == 0) return VSD_OK;
+  const size_t need = vsd::sparse_workspace_bytes(vsd::plan_sparse(k_max, max_tail), geom->B,
+                                                  geom->Hkv, geom->Hq / geom->Hkv,
+                                                  geom->head_dim);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
+    return VSD_ERR_WORKSPACE;
   if (!q || !k_cache || !v_cache || !block_table || !tail_start || !seq_len || !out)
     return VSD_ERR_INVALID_ARG;
   if (k_max > 0 && (!idx || !n_sel)) return VSD_ERR_INVALID_ARG;
@@ -305,6 +312,7 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
   sa.tail_start = tail_start;
   sa.seq_len = seq_len;
   sa.out = out;
+  sa.ws = need > 0 ? static_cast<float*>(workspace) : nullptr;
   sa.status = status;
   sa.B = geom->B;
   sa.Hq = geom->Hq;
