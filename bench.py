@@ -203,25 +203,28 @@ def run_gpu(args, world, rank, local):
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 + gamma)]
 
-    def step():
+    def step(events=True):
         vsd.vsd_verify_attn_collect(batch.q, batch.k_cache, batch.v_cache, batch.block_table,
                                     batch.prefix_len, P_max=P_max, scale=w.scale, row0=0,
                                     row1=R - 1, logits=logits, partial=partial, out=out,
                                     workspace=workspace)
-        ev[1].record(stream)
+        if events:
+            ev[1].record(stream)
         vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
                             n_recent=w.n_recent, idx=idx, n_sel=n_sel)
-        ev[2].record(stream)
+        if events:
+            ev[2].record(stream)
         for i in range(gamma):
             vsd.vsd_sparse_decode_attn(batch.q_draft[i], batch.k_cache, batch.v_cache,
                                        batch.block_table, idx, n_sel, tail_start, seq_len[i],
                                        scale=w.scale, max_tail=max_tail, out=d_out[i])
-            ev[3 + i].record(stream)
+            if events:
+                ev[3 + i].record(stream)
 
-    # count this library's kernel launches per step from the device-side counters is not
-    # possible without a profiler; the count follows from the launch plan instead
-    launches_per_step = 1 + (1 if ws_bytes > 0 else 0) + 1 + gamma * getattr(
-        vsd, "SPARSE_LAUNCHES_PER_CALL", 1)
+    # this library's kernel launches per step, from the launch plan: verification (+ its
+    # split-K merge kernel), selection, and one kernel per draft step (the draft step
+    # merges its splits inside the kernel)
+    launches_per_step = 1 + (1 if ws_bytes > 0 else 0) + 1 + gamma
     enqueue_s = []
     sleep_cycles = 8_000_000  # ~4 ms: the whole step is enqueued before the GPU gets to it
 
@@ -242,7 +245,28 @@ def run_gpu(args, world, rank, local):
     if status:
         raise RuntimeError("device status 0x%x during warm-up" % status)
 
-    per = {"verify": [], "select": [], "sparse": [], "step": []}
+    # the whole iteration as one CUDA graph: the kernels are chained by programmatic
+    # dependent launch, so each one's launch overlaps the tail of its predecessor
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(events=False)
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def graph_step(sl):
+        seq_len.copy_(torch.from_numpy(sl))
+        flush_l2(flush_w, flush_r)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(sleep_cycles)
+        g0.record(stream)
+        graph.replay()
+        g1.record(stream)
+
+    for _ in range(args.warmup):
+        graph_step(draw_seq_len())
+    torch.cuda.synchronize()
+
+    per = {"verify": [], "select": [], "sparse": [], "step": [], "graph": []}
     tails_seen = []
     if world > 1:
         torch.distributed.barrier()
@@ -252,7 +276,12 @@ def run_gpu(args, world, rank, local):
             sl = draw_seq_len()
             tails_seen.append([[int(sl[i, b] - prefix[b]) for b in range(B)]
                                for i in range(gamma)])
-            timed_step(sl)
+            graph_step(sl)
+            torch.cuda.synchronize()
+            per["graph"].append(g0.elapsed_time(g1) * 1e-3)
+        # per-kernel breakdown: the same iteration launched eagerly, events between kernels
+        for _ in range(args.steps):
+            timed_step(draw_seq_len())
             torch.cuda.synchronize()
             per["verify"].append(ev[0].elapsed_time(ev[1]) * 1e-3)
             per["select"].append(ev[1].elapsed_time(ev[2]) * 1e-3)
@@ -271,7 +300,7 @@ def run_gpu(args, world, rank, local):
                   for i in range(gamma)]
     vb, sb, spb = iteration_bytes(w, prefix, n_sel_host, mean_tails)
     total_bytes = vb + sb + sum(spb)
-    t_step = sum(per["step"])
+    t_step = sum(per["graph"])
     t_tensor = torch.tensor([t_step], dtype=torch.float64, device=dev)
     if world > 1:
         torch.distributed.all_reduce(t_tensor, op=torch.distributed.ReduceOp.MAX)
@@ -312,6 +341,10 @@ def run_gpu(args, world, rank, local):
                    "l2": "flushed before every timed iteration (512 MB write, then 512 MB "
                          "read so no dirty lines remain)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "timing": "value: one CUDA-graph replay of the iteration per step (device events "
+                  "around the replay); kernels: the same iteration launched eagerly with "
+                  "events between kernels, so each figure includes its launch gap",
+        "us_per_iter_eager": statistics.mean(per["step"]) * 1e6,
         "kernels": kernels,
         "select_over_verify": t_select / t_verify,
         "roofline": {"bound": "hbm", "kernel": "vsd_verify_attn_collect",
@@ -319,6 +352,7 @@ def run_gpu(args, world, rank, local):
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": profile_traffic(w.name)},
         "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches_per_step": launches_per_step,
         "clocks": clk,
         # the device timestamps only measure kernels if the host finished enqueueing a
         # step while the GPU was still asleep

@@ -102,8 +102,8 @@ typedef struct vsd_geom {
  *   logits         fp32 [B][2][Hq][P_max] or NULL; only j < P_b are written
  *   partial_scores fp32 [B][Hkv][P_max] or NULL; only j < P_b are written
  *   out            bf16 [B][R][Hq][head_dim]
- *   workspace      >= vsd_verify_workspace_size(...) bytes; contents on entry
- *                  are ignored and on exit unspecified
+ *   workspace      >= vsd_verify_workspace_size(...) bytes (0 bytes: may be NULL);
+ *                  contents on entry are ignored and on exit unspecified
  * Supported: head_dim in {64, 128}, page_size 16, G <= 16, 1 <= R <= 16, R * G <= 64.
  * ------------------------------------------------------------------------------ */
 vsd_status vsd_verify_workspace_size(const vsd_geom* geom, int R, int P_max, size_t* bytes);
@@ -193,7 +193,13 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
  *   max_tail   host-side upper bound of seq_len[b] - tail_start[b]; it only
  *              sizes the split of the work, results do not depend on it
  *   out        bf16 [B][Hq][head_dim]
- *   workspace  >= vsd_sparse_workspace_size(...) bytes
+ *   workspace  >= vsd_sparse_workspace_size(...) bytes (0 bytes: may be NULL),
+ *              256-byte aligned.  It starts with per-(sequence, KV head) counters
+ *              that must be zero before the first use; every call returns them to
+ *              zero, so the buffer can be reused by later calls of this entry point
+ *              of any geometry.  Zero it again after a call that raised
+ *              VSD_DEV_TIMEOUT, and do not share it with other entry points or with
+ *              calls that may run concurrently.
  * Supported: head_dim in {64, 128}, page_size 16, G <= 16.
  * ------------------------------------------------------------------------------ */
 vsd_status vsd_sparse_workspace_size(const vsd_geom* geom, int k_max, int max_tail,

@@ -115,13 +115,14 @@ _ws_cache = {}
 
 
 def _workspace(nbytes: int, device, tag: str) -> Optional[torch.Tensor]:
-    """Cached device scratch, one buffer per (call kind, device, size)."""
+    """Cached device scratch, one buffer per (call kind, device, size), zero-filled
+    when allocated as the workspace contract asks (every call leaves it reusable)."""
     if nbytes == 0:
         return None
     key = (tag, str(device), nbytes)
     ws = _ws_cache.get(key)
     if ws is None:
-        ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        ws = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)
         _ws_cache[key] = ws
     off = (-ws.data_ptr()) % 256
     return ws[off:off + nbytes]

@@ -65,6 +65,7 @@ struct SparseArgs {
   const int32_t* seq_len;
   void* out;
   float* ws;  // per-split partial results (m, l, o); NULL when one split suffices
+  unsigned* counters;  // per (sequence, KV head): zero between calls (self-resetting)
   unsigned* status;
   int B, Hq, Hkv, G, d, max_blocks, num_blocks, k_max, max_tail;
   float scale;
@@ -76,6 +77,8 @@ struct SparsePlan {
 };
 
 SparsePlan plan_sparse(int k_max, int max_tail);
+// Workspace layout: per-pair counters (sparse_counter_bytes), then the partials.
+size_t sparse_counter_bytes(const SparsePlan& plan, int B, int Hkv);
 size_t sparse_workspace_bytes(const SparsePlan& plan, int B, int Hkv, int G, int head_dim);
 cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream);
 

@@ -8,22 +8,26 @@
 // How (GB300 design).  The step moves a few MB of randomly placed 256-byte rows, so it
 // is bound by the latency of its dependent loads (index -> block table -> K and V
 // rows), not by bandwidth.  The design therefore issues every load of a CTA at once
-// and spreads the list over as many SMs as there are batches of 64 positions:
+// and spreads the list over the SMs in splits of 128 positions:
 //   * The attended list of one (sequence, KV head) pair, idx[0 .. n_sel) followed by
-//     [tail_start, seq_len), is cut into splits of 64 positions (more per split only
-//     when the list is very long); one CTA of four warps takes one split, each warp
-//     16 positions.
-//   * Two lanes own one key: each gathers half of the key's K row with 16-byte
-//     loads (adjacent lanes read adjacent 16 bytes), and the warp also issues the V
-//     loads of its 16 rows (lane = 4 or 2 dims of every row, coalesced per row).
-//   * Logits of the G query heads of the group are fp32 dot products (q in shared
-//     memory), the pair of lanes combining its halves with one shuffle; the warp
-//     softmax over its 16 keys and the P.V product follow in registers.
-//   * The four warps merge in shared memory in a fixed order.  A pair with a single
+//     [tail_start, seq_len), is cut into splits of 128 positions (more per split
+//     only when the list is very long); one CTA of eight warps takes one split, each
+//     warp 16 positions.
+//   * A row of K or V is read by head_dim/8 adjacent lanes, 16 bytes each, so one
+//     warp instruction fetches whole rows of 2 (head_dim 128) or 4 (64) keys and the
+//     16 keys of a warp take 8 or 4 instructions for K and as many for V, all in
+//     flight together (the first index loads are issued speculatively, before the
+//     list lengths are known).
+//   * Each lane forms partial dot products of its 8 dims with the G queries of the
+//     group (fp32, q in shared memory); a shuffle tree over the row's lanes
+//     completes the logits.  The warp softmax over its 16 keys and the P.V product
+//     on the lane's 8 dims follow in registers.
+//   * The eight warps merge in shared memory in a fixed order.  A pair with a single
 //     split writes its output directly; otherwise each split writes (m, l, o) to the
-//     workspace and a merge kernel (one block per pair and head, launched as a
-//     programmatic dependent so it is resident before the splits finish) combines
-//     them in split order.  Results are bit-reproducible; no atomics.
+//     workspace and the split that finishes last (a per-pair counter in the
+//     workspace, reset to zero by that split) combines them with all its threads,
+//     every load of a round in flight at once, in split order.  Results are
+//     bit-reproducible; the only atomics are the counters.
 #include <cfloat>
 
 #include "common.cuh"
@@ -33,7 +37,7 @@
 namespace vsd {
 namespace {
 
-constexpr int kSWarps = 4;
+constexpr int kSWarps = 8;
 constexpr int kSThreads = kSWarps * 32;
 constexpr int kKeysPerWarp = 16;
 constexpr int kBatch = kSWarps * kKeysPerWarp;  // positions per CTA per batch
@@ -51,6 +55,7 @@ struct SParams {
   const int32_t* seq_len;
   uint16_t* out;
   float* ws;
+  unsigned* counters;  // per pair: splits that have written their partial
   unsigned* status;
   int Hq, Hkv, max_blocks, num_blocks, k_max;
   int split_len;   // positions per split (a multiple of kBatch)
@@ -58,38 +63,35 @@ struct SParams {
   float scale_log2;
 };
 
+// Thread layout of one warp's batch for head dimension D: a K / V row is read by
+// LPR = D / 8 lanes (8 dims = 16 bytes each), one instruction covers KPI = 32 / LPR
+// rows, and the warp's 16 keys take U = 16 / KPI instructions ("slots").
+template <int D>
+struct SLayout {
+  static constexpr int LPR = D / 8;
+  static constexpr int KPI = 32 / LPR;
+  static constexpr int U = kKeysPerWarp / KPI;
+};
+
 template <int D, int G>
 struct SSmem {
   float q[G][D];
-  float p[kSWarps][kKeysPerWarp][G];
   float wm[kSWarps][G];
   float wl[kSWarps][G];
-  float wo[kSWarps][G][D];
+  union {
+    float wo[kSWarps][G][D];
+    float merge_scratch[kSThreads * 6];  // m, l and a float4 o per thread
+  };
 };
 
-__device__ __forceinline__ float wmax_pairs(float x) {
-  // max over the 16 keys of a warp (lanes 2k and 2k+1 hold the same value)
-#pragma unroll
-  for (int o = 2; o < 32; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-
-__device__ __forceinline__ float wsum_pairs(float x) {
-#pragma unroll
-  for (int o = 2; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-
-// The attended list of sequence b and its validity (false: bad lengths, nothing read).
+// The attended list of sequence b (false lengths: an empty list, flagged).
 struct SList {
   int ns, t0, total;
 };
 
-__device__ __forceinline__ SList attended_list(const SParams& a, int b, bool flag) {
+__device__ __forceinline__ SList attended_list(int ns, int t0, int t1, const SParams& a,
+                                               bool flag) {
   SList L;
-  int ns = a.n_sel != nullptr ? __ldg(a.n_sel + b) : 0;
-  const int t0 = __ldg(a.tail_start + b);
-  const int t1 = __ldg(a.seq_len + b);
   const bool ok = ns >= 0 && ns <= a.k_max && t0 >= 0 && t0 <= t1 &&
                   static_cast<long long>(t1) <= static_cast<long long>(a.max_blocks) * kPageS;
   if (!ok && flag) flag_status(a.status, VSD_DEV_BAD_LENGTH);
@@ -99,169 +101,328 @@ __device__ __forceinline__ SList attended_list(const SParams& a, int b, bool fla
   return L;
 }
 
+// Combine the n partial (m, l, o) of one pair's splits and write its G output rows.
+// Thread = (float4 group of (head, dims), part); part p takes splits p, p + kParts,
+// ... with all loads of a round in flight; the parts then combine in shared memory.
 template <int D, int G>
-__global__ void __launch_bounds__(kSThreads) sparse_decode_kernel(const SParams a) {
-  constexpr int DPL = D / 32;       // dims per lane for V and the output
-  constexpr int KH = D / 2;         // K dims per lane (half a row)
-  constexpr int KV16 = KH / 8;      // 16-byte K loads per lane
-  __shared__ __align__(16) SSmem<D, G> sm;
+__device__ __forceinline__ void merge_splits(const SParams& a, SSmem<D, G>& sm, int pair, int b,
+                                             int g, int n) {
+  constexpr int kQ = D / 4;
+  constexpr int NG = G * kQ;                              // float4 groups of the output
+  constexpr int kGPT = NG > kSThreads ? NG / kSThreads : 1;  // groups per thread
+  constexpr int kParts = NG >= kSThreads ? 1 : kSThreads / NG;
+  constexpr int kU = 16 / kGPT > 1 ? 16 / kGPT : 1;       // splits per load round
+  static_assert(NG * kParts / kGPT == kSThreads || NG >= kSThreads, "merge layout");
+  const int t = threadIdx.x;
+  const int part = kParts > 1 ? t / NG : 0;
+  const size_t stride = static_cast<size_t>(G) * (D + 2);
+  const float* base = a.ws + static_cast<size_t>(pair) * a.max_splits * stride;
+  float M[kGPT], L[kGPT];
+  float4 O[kGPT];
+#pragma unroll
+  for (int i = 0; i < kGPT; ++i) {
+    M[i] = -INFINITY;
+    L[i] = 0.f;
+    O[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int k0 = part; k0 < n; k0 += kU * kParts) {
+    float mk[kGPT][kU], lk[kGPT][kU];
+    float4 ok[kGPT][kU];
+#pragma unroll
+    for (int i = 0; i < kGPT; ++i) {
+      const int gi = (kParts > 1 ? t % NG : t) + i * kSThreads;
+      const int hh = gi / kQ, q4 = gi % kQ;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int k = k0 + u * kParts;
+        if (k < n) {
+          const float* sl = base + k * stride;
+          mk[i][u] = __ldcg(sl + hh);
+          lk[i][u] = __ldcg(sl + G + hh);
+          ok[i][u] = __ldcg(reinterpret_cast<const float4*>(sl + 2 * G + hh * D) + q4);
+        } else {
+          mk[i][u] = -INFINITY;
+          lk[i][u] = 0.f;
+          ok[i][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kGPT; ++i) {
+      float mn = M[i];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) mn = fmaxf(mn, mk[i][u]);
+      const float sc = (M[i] == -INFINITY) ? 0.f : exp2f(M[i] - mn);
+      L[i] *= sc;
+      O[i].x *= sc;
+      O[i].y *= sc;
+      O[i].z *= sc;
+      O[i].w *= sc;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const float w = (mk[i][u] == -INFINITY) ? 0.f : exp2f(mk[i][u] - mn);
+        L[i] += w * lk[i][u];
+        O[i].x += w * ok[i][u].x;
+        O[i].y += w * ok[i][u].y;
+        O[i].z += w * ok[i][u].z;
+        O[i].w += w * ok[i][u].w;
+      }
+      M[i] = mn;
+    }
+  }
+  if constexpr (kParts > 1) {
+    // parts meet in shared memory: [part][group] of m, l and the float4 o
+    float* pm = sm.merge_scratch;
+    float* pl = pm + kParts * NG;
+    float4* po = reinterpret_cast<float4*>(pl + kParts * NG);
+    const int gi = t % NG;
+    pm[part * NG + gi] = M[0];
+    pl[part * NG + gi] = L[0];
+    po[part * NG + gi] = O[0];
+    __syncthreads();
+    if (part == 0) {
+      float mn = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kParts; ++r) mn = fmaxf(mn, pm[r * NG + gi]);
+      float Lt = 0.f;
+      float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < kParts; ++r) {
+        const float mr = pm[r * NG + gi];
+        const float w = (mr == -INFINITY) ? 0.f : exp2f(mr - mn);
+        const float4 o = po[r * NG + gi];
+        Lt += w * pl[r * NG + gi];
+        Ot.x += w * o.x;
+        Ot.y += w * o.y;
+        Ot.z += w * o.z;
+        Ot.w += w * o.w;
+      }
+      L[0] = Lt;
+      O[0] = Ot;
+    }
+    if (part != 0) return;
+  }
+#pragma unroll
+  for (int i = 0; i < kGPT; ++i) {
+    const int gi = (kParts > 1 ? t % NG : t) + i * kSThreads;
+    const int hh = gi / kQ, q4 = gi % kQ;
+    const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
+    uint2 pk;
+    pk.x = pack_bf16x2(O[i].x * inv, O[i].y * inv);
+    pk.y = pack_bf16x2(O[i].z * inv, O[i].w * inv);
+    *reinterpret_cast<uint2*>(a.out + (static_cast<size_t>(b) * a.Hq + g * G + hh) * D +
+                              q4 * 4) = pk;
+  }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kSThreads, 1) sparse_decode_kernel(const SParams a) {
+  using Lay = SLayout<D>;
+  constexpr int LPR = Lay::LPR, KPI = Lay::KPI, U = Lay::U;
+  extern __shared__ __align__(16) uint8_t sparse_smem[];
+  SSmem<D, G>& sm = *reinterpret_cast<SSmem<D, G>*>(sparse_smem);
   const int split = blockIdx.x;
   const int g = blockIdx.y;
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane & 1;
+  const int sub = lane / LPR;  // which row of an instruction
+  const int lr = lane % LPR;   // which 8 dims of the row
 
-  ptx::pdl_launch_dependents();  // the merge kernel may become resident now
+  ptx::pdl_launch_dependents();  // the next kernel on the stream may become resident
   ptx::pdl_wait_primary();       // idx / n_sel come from the preceding kernel
 
-  const int t1 = __ldg(a.seq_len + b);
-  const SList L = attended_list(a, b, split == 0 && g == 0 && threadIdx.x == 0);
+  // First round of loads, independent of one another: the list lengths, the first
+  // batch's indices (speculatively: used only for positions that turn out to be
+  // selected ones) and the queries.
   const int lo = split * a.split_len;
+  const int wbase0 = lo + warp * kKeysPerWarp;
+  int j_spec[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int pos = wbase0 + u * KPI + sub;
+    j_spec[u] = (a.idx != nullptr && pos < a.k_max)
+                    ? __ldg(a.idx + static_cast<size_t>(b) * a.k_max + pos)
+                    : 0;
+  }
+  constexpr int kQLoads = (G * D / 8 + kSThreads - 1) / kSThreads;
+  uint4 qraw[kQLoads];
+#pragma unroll
+  for (int u = 0; u < kQLoads; ++u) {
+    const int i = threadIdx.x + u * kSThreads;
+    if (i < G * D / 8) {
+      const int hh = i / (D / 8), c8 = i % (D / 8);
+      qraw[u] = *reinterpret_cast<const uint4*>(
+          a.q + (static_cast<size_t>(b) * a.Hq + g * G + hh) * D + c8 * 8);
+    }
+  }
+  const int ns_raw = a.n_sel != nullptr ? __ldg(a.n_sel + b) : 0;
+  const int t0_raw = __ldg(a.tail_start + b);
+  const int t1 = __ldg(a.seq_len + b);
+  const SList L = attended_list(ns_raw, t0_raw, t1, a, split == 0 && g == 0 && threadIdx.x == 0);
   if (lo >= L.total && !(split == 0 && L.total == 0)) return;  // no work in this split
   const int hi = min(lo + a.split_len, L.total);
   const int n_splits = (L.total + a.split_len - 1) / a.split_len;
 
-  for (int i = threadIdx.x; i < G * D / 8; i += kSThreads) {
-    const int hh = i / (D / 8), c8 = i % (D / 8);
-    const uint4 raw = *reinterpret_cast<const uint4*>(
-        a.q + (static_cast<size_t>(b) * a.Hq + g * G + hh) * D + c8 * 8);
-    float* dst = &sm.q[hh][c8 * 8];
-    dst[0] = bf16_lo(raw.x);
-    dst[1] = bf16_hi(raw.x);
-    dst[2] = bf16_lo(raw.y);
-    dst[3] = bf16_hi(raw.y);
-    dst[4] = bf16_lo(raw.z);
-    dst[5] = bf16_hi(raw.z);
-    dst[6] = bf16_lo(raw.w);
-    dst[7] = bf16_hi(raw.w);
+#pragma unroll
+  for (int u = 0; u < kQLoads; ++u) {
+    const int i = threadIdx.x + u * kSThreads;
+    if (i < G * D / 8) {
+      const int hh = i / (D / 8), c8 = i % (D / 8);
+      const uint4 raw = qraw[u];
+      float4 lo4, hi4;
+      lo4.x = bf16_lo(raw.x);
+      lo4.y = bf16_hi(raw.x);
+      lo4.z = bf16_lo(raw.y);
+      lo4.w = bf16_hi(raw.y);
+      hi4.x = bf16_lo(raw.z);
+      hi4.y = bf16_hi(raw.z);
+      hi4.z = bf16_lo(raw.w);
+      hi4.w = bf16_hi(raw.w);
+      *reinterpret_cast<float4*>(&sm.q[hh][c8 * 8]) = lo4;
+      *reinterpret_cast<float4*>(&sm.q[hh][c8 * 8 + 4]) = hi4;
+    }
   }
   __syncthreads();
 
-  float m[G], lsum[G], acc[G][DPL];
+  float m[G], lsum[G], acc[G][8];
 #pragma unroll
   for (int hh = 0; hh < G; ++hh) {
     m[hh] = -INFINITY;
     lsum[hh] = 0.f;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[hh][e] = 0.f;
+    for (int e = 0; e < 8; ++e) acc[hh][e] = 0.f;
   }
 
-  for (int base = lo + warp * kKeysPerWarp; base < hi; base += kBatch) {
-    // ---- this lane pair's key: list position -> token -> cache row
-    const int pos = base + (lane >> 1);
-    int row = -1;
-    if (pos < hi) {
-      const int j = pos < L.ns ? __ldg(a.idx + static_cast<size_t>(b) * a.k_max + pos)
-                               : L.t0 + (pos - L.ns);
-      if (j < 0 || j >= t1) {
-        if (half == 0) flag_status(a.status, VSD_DEV_BAD_INDEX);
-      } else {
-        const int blk = __ldg(a.block_table + static_cast<size_t>(b) * a.max_blocks + j / kPageS);
-        if (blk < 0 || blk >= a.num_blocks) {
-          if (half == 0) flag_status(a.status, VSD_DEV_BAD_BLOCK);
+  for (int wbase = wbase0; wbase < hi; wbase += kBatch) {
+    // ---- list position -> token -> cache row, for each slot of this lane's row group
+    int row[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int pos = wbase + u * KPI + sub;
+      row[u] = -1;
+      if (pos < hi) {
+        const int j = pos >= L.ns ? L.t0 + (pos - L.ns)
+                      : wbase == wbase0 ? j_spec[u]
+                                        : __ldg(a.idx + static_cast<size_t>(b) * a.k_max + pos);
+        if (j < 0 || j >= t1) {
+          if (lr == 0) flag_status(a.status, VSD_DEV_BAD_INDEX);
         } else {
-          row = (blk * a.Hkv + g) * kPageS + (j % kPageS);
+          const int blk =
+              __ldg(a.block_table + static_cast<size_t>(b) * a.max_blocks + j / kPageS);
+          if (blk < 0 || blk >= a.num_blocks) {
+            if (lr == 0) flag_status(a.status, VSD_DEV_BAD_BLOCK);
+          } else {
+            row[u] = (blk * a.Hkv + g) * kPageS + (j % kPageS);
+          }
         }
       }
     }
-    // ---- all loads of the batch in flight: half a K row per lane, V slices
-    uint4 kr[KV16];
-    if (row >= 0) {
-      const uint16_t* src = a.k_cache + static_cast<size_t>(row) * D + half * KH;
+    // ---- every K and V load of the batch in flight: 16 bytes of each row per lane
+    uint4 kr[U], vr[U];
 #pragma unroll
-      for (int i = 0; i < KV16; ++i) kr[i] = ldg_stream16(src + i * 8);
-    } else {
-#pragma unroll
-      for (int i = 0; i < KV16; ++i) kr[i] = make_uint4(0, 0, 0, 0);
-    }
-    uint32_t vr[kKeysPerWarp][DPL / 2];
-#pragma unroll
-    for (int kk = 0; kk < kKeysPerWarp; ++kk) {
-      const int r = __shfl_sync(0xffffffffu, row, 2 * kk);
-      if (r >= 0) {
-        const uint16_t* src = a.v_cache + static_cast<size_t>(r) * D + lane * DPL;
-        if constexpr (DPL == 4) {
-          const uint2 v2 = ldg_stream8(src);
-          vr[kk][0] = v2.x;
-          vr[kk][1] = v2.y;
-        } else {
-          vr[kk][0] = ldg_stream4(src);
-        }
+    for (int u = 0; u < U; ++u) {
+      if (row[u] >= 0) {
+        const size_t off = static_cast<size_t>(row[u]) * D + lr * 8;
+        kr[u] = ldg_stream16(a.k_cache + off);
+        vr[u] = ldg_stream16(a.v_cache + off);
       } else {
-#pragma unroll
-        for (int e = 0; e < DPL / 2; ++e) vr[kk][e] = 0u;
+        kr[u] = make_uint4(0, 0, 0, 0);
+        vr[u] = make_uint4(0, 0, 0, 0);
       }
     }
-    // ---- logits: half-row dot products, combined across the lane pair
-    float z[G];
+    // ---- logits: partial dot products of the lane's 8 dims, completed over the row
+    float z[U][G];
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) z[hh] = 0.f;
-#pragma unroll
-    for (int i = 0; i < KV16; ++i) {
+    for (int u = 0; u < U; ++u) {
       float kf[8];
-      kf[0] = bf16_lo(kr[i].x); kf[1] = bf16_hi(kr[i].x);
-      kf[2] = bf16_lo(kr[i].y); kf[3] = bf16_hi(kr[i].y);
-      kf[4] = bf16_lo(kr[i].z); kf[5] = bf16_hi(kr[i].z);
-      kf[6] = bf16_lo(kr[i].w); kf[7] = bf16_hi(kr[i].w);
+      kf[0] = bf16_lo(kr[u].x); kf[1] = bf16_hi(kr[u].x);
+      kf[2] = bf16_lo(kr[u].y); kf[3] = bf16_hi(kr[u].y);
+      kf[4] = bf16_lo(kr[u].z); kf[5] = bf16_hi(kr[u].z);
+      kf[6] = bf16_lo(kr[u].w); kf[7] = bf16_hi(kr[u].w);
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        const float4 qa = *reinterpret_cast<const float4*>(&sm.q[hh][half * KH + i * 8]);
-        const float4 qb = *reinterpret_cast<const float4*>(&sm.q[hh][half * KH + i * 8 + 4]);
-        float s = z[hh];
-        s = fmaf(qa.x, kf[0], s); s = fmaf(qa.y, kf[1], s);
-        s = fmaf(qa.z, kf[2], s); s = fmaf(qa.w, kf[3], s);
+        const float4 qa = *reinterpret_cast<const float4*>(&sm.q[hh][lr * 8]);
+        const float4 qb = *reinterpret_cast<const float4*>(&sm.q[hh][lr * 8 + 4]);
+        float s = qa.x * kf[0];
+        s = fmaf(qa.y, kf[1], s); s = fmaf(qa.z, kf[2], s); s = fmaf(qa.w, kf[3], s);
         s = fmaf(qb.x, kf[4], s); s = fmaf(qb.y, kf[5], s);
         s = fmaf(qb.z, kf[6], s); s = fmaf(qb.w, kf[7], s);
-        z[hh] = s;
+        z[u][hh] = s;
       }
     }
-    const bool valid = row >= 0;
+#pragma unroll
+    for (int o = 1; o < LPR; o <<= 1)
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) z[u][hh] += __shfl_xor_sync(0xffffffffu, z[u][hh], o);
+    // ---- online softmax over the warp's 16 keys (slots x row groups)
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
-      const float zz = z[hh] + __shfl_xor_sync(0xffffffffu, z[hh], 1);
-      const float y = valid ? zz * a.scale_log2 : -INFINITY;
-      const float mn = fmaxf(m[hh], wmax_pairs(y));
+      float bm = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        z[u][hh] = row[u] >= 0 ? z[u][hh] * a.scale_log2 : -INFINITY;
+        bm = fmaxf(bm, z[u][hh]);
+      }
+#pragma unroll
+      for (int o = LPR; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+      const float mn = fmaxf(m[hh], bm);
       const float alpha = (m[hh] == -INFINITY) ? 0.f : exp2f(m[hh] - mn);
-      const float p = valid ? exp2f(y - mn) : 0.f;
-      lsum[hh] = lsum[hh] * alpha + wsum_pairs(p);
+      float ps = 0.f;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) acc[hh][e] *= alpha;
+      for (int u = 0; u < U; ++u) {
+        const float p = (z[u][hh] == -INFINITY) ? 0.f : exp2f(z[u][hh] - mn);
+        z[u][hh] = p;
+        ps += p;
+      }
+      lsum[hh] = lsum[hh] * alpha + ps;  // this row group's keys; groups combine at the end
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[hh][e] *= alpha;
       m[hh] = mn;
-      if (half == 0) sm.p[warp][lane >> 1][hh] = p;
     }
-    __syncwarp();
-    // ---- P.V: lane owns DPL dims of every row
+    // ---- P.V on the lane's 8 dims
 #pragma unroll
-    for (int kk = 0; kk < kKeysPerWarp; ++kk) {
-      float vf[DPL];
+    for (int u = 0; u < U; ++u) {
+      float vf[8];
+      vf[0] = bf16_lo(vr[u].x); vf[1] = bf16_hi(vr[u].x);
+      vf[2] = bf16_lo(vr[u].y); vf[3] = bf16_hi(vr[u].y);
+      vf[4] = bf16_lo(vr[u].z); vf[5] = bf16_hi(vr[u].z);
+      vf[6] = bf16_lo(vr[u].w); vf[7] = bf16_hi(vr[u].w);
 #pragma unroll
-      for (int e = 0; e < DPL / 2; ++e) {
-        vf[2 * e] = bf16_lo(vr[kk][e]);
-        vf[2 * e + 1] = bf16_hi(vr[kk][e]);
-      }
+      for (int hh = 0; hh < G; ++hh)
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        const float p = sm.p[warp][kk][hh];
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[hh][e] = fmaf(p, vf[e], acc[hh][e]);
-      }
+        for (int e = 0; e < 8; ++e) acc[hh][e] = fmaf(z[u][hh], vf[e], acc[hh][e]);
     }
-    __syncwarp();
   }
+  // the row groups of the warp hold disjoint keys: add them up
+#pragma unroll
+  for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      lsum[hh] += __shfl_xor_sync(0xffffffffu, lsum[hh], o);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[hh][e] += __shfl_xor_sync(0xffffffffu, acc[hh][e], o);
+    }
 
-  // ---- merge the four warps in a fixed order
+  // ---- merge the eight warps in a fixed order
 #pragma unroll
   for (int hh = 0; hh < G; ++hh) {
     if (lane == 0) {
       sm.wm[warp][hh] = m[hh];
       sm.wl[warp][hh] = lsum[hh];
     }
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) sm.wo[warp][hh][lane * DPL + e] = acc[hh][e];
+    if (sub == 0) {
+      *reinterpret_cast<float4*>(&sm.wo[warp][hh][lr * 8]) =
+          make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+      *reinterpret_cast<float4*>(&sm.wo[warp][hh][lr * 8 + 4]) =
+          make_float4(acc[hh][4], acc[hh][5], acc[hh][6], acc[hh][7]);
+    }
   }
   __syncthreads();
   const bool direct = n_splits <= 1;
-  const size_t slot = (static_cast<size_t>(b) * a.Hkv + g) * a.max_splits + split;
+  const int pair = b * a.Hkv + g;
+  const size_t slot = static_cast<size_t>(pair) * a.max_splits + split;
   float* wsl = direct ? nullptr : a.ws + slot * G * (D + 2);
   for (int i = threadIdx.x; i < G * D; i += kSThreads) {
     const int hh = i / D, dim = i % D;
@@ -289,53 +450,23 @@ __global__ void __launch_bounds__(kSThreads) sparse_decode_kernel(const SParams 
       }
     }
   }
-}
-
-// Combine the splits of one (pair, head): block (pair, head), thread = dim.
-template <int D, int G>
-__global__ void __launch_bounds__(D) sparse_merge_kernel(const SParams a) {
-  __shared__ float wgt[kMaxSplits];
-  __shared__ float inv_l;
-  const int pair = blockIdx.x;
-  const int hh = blockIdx.y;
-  const int b = pair / a.Hkv, g = pair - (pair / a.Hkv) * a.Hkv;
-  ptx::pdl_wait_primary();  // every split has written its partial
-  const SList L = attended_list(a, b, false);
-  const int n_splits = (L.total + a.split_len - 1) / a.split_len;
-  if (n_splits <= 1) return;  // written directly by the split kernel
-  const size_t stride = static_cast<size_t>(G) * (D + 2);
-  const float* ws = a.ws + static_cast<size_t>(pair) * a.max_splits * stride;
-  if (threadIdx.x < 32) {
-    float M = -INFINITY;
-    for (int s = threadIdx.x; s < n_splits; s += 32) M = fmaxf(M, ws[s * stride + hh]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Ls = 0.f;
-    for (int s = threadIdx.x; s < n_splits; s += 32) {
-      const float ms = ws[s * stride + hh];
-      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      wgt[s] = w;
-      Ls += w * ws[s * stride + G + hh];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-    if (threadIdx.x == 0) inv_l = Ls > 0.f ? 1.f / Ls : 0.f;
+  if (direct) return;
+  // The last split of the pair to get here combines them all.  Every thread makes
+  // its partial stores visible GPU-wide before the CTA counts itself in; the
+  // counter goes back to zero for the next call.
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();  // also: every thread is done reading sm.wo
+  if (threadIdx.x == 0) {
+    const unsigned old = atomicAdd(a.counters + pair, 1u);
+    const int last = old == static_cast<unsigned>(n_splits - 1);
+    if (last) atomicExch(a.counters + pair, 0u);
+    s_last = last;
   }
   __syncthreads();
-  const int dim = threadIdx.x;
-  const float* po = ws + 2 * G + hh * D + dim;
-  float acc = 0.f;
-  for (int s0 = 0; s0 < n_splits; s0 += 8) {
-    float x[8];  // eight partials in flight, summed in split order
-#pragma unroll
-    for (int u = 0; u < 8; ++u) x[u] = s0 + u < n_splits ? po[(s0 + u) * stride] : 0.f;
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (s0 + u < n_splits) acc += wgt[s0 + u] * x[u];
-  }
-  const __nv_bfloat16 bv = __float2bfloat16_rn(acc * inv_l);
-  a.out[(static_cast<size_t>(b) * a.Hq + g * G + hh) * D + dim] =
-      *reinterpret_cast<const uint16_t*>(&bv);
+  if (!s_last) return;
+  __threadfence();
+  merge_splits<D, G>(a, sm, pair, b, g, n_splits);
 }
 
 template <int D, int G>
@@ -343,18 +474,20 @@ cudaError_t launch_dg(const SParams& p, int B, int Hkv, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  constexpr int smem = static_cast<int>(sizeof(SSmem<D, G>));
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.max_splits, Hkv, B);
   cfg.blockDim = dim3(kSThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_decode_kernel<D, G>, p);
-  if (e != cudaSuccess || p.max_splits <= 1) return e;
-  cfg.gridDim = dim3(B * Hkv, G, 1);
-  cfg.blockDim = dim3(D, 1, 1);
-  return cudaLaunchKernelEx(&cfg, sparse_merge_kernel<D, G>, p);
+  return cudaLaunchKernelEx(&cfg, sparse_decode_kernel<D, G>, p);
 }
 
 }  // namespace
@@ -370,9 +503,15 @@ SparsePlan plan_sparse(int k_max, int max_tail) {
   return plan;
 }
 
+size_t sparse_counter_bytes(const SparsePlan& plan, int B, int Hkv) {
+  if (plan.max_splits <= 1) return 0;
+  return (static_cast<size_t>(B) * Hkv * sizeof(unsigned) + 255) / 256 * 256;
+}
+
 size_t sparse_workspace_bytes(const SparsePlan& plan, int B, int Hkv, int G, int head_dim) {
   if (plan.max_splits <= 1) return 0;
-  return static_cast<size_t>(B) * Hkv * plan.max_splits * G * (head_dim + 2) * sizeof(float);
+  return sparse_counter_bytes(plan, B, Hkv) +
+         static_cast<size_t>(B) * Hkv * plan.max_splits * G * (head_dim + 2) * sizeof(float);
 }
 
 cudaError_t launch_sparse(const SparseArgs& sa, cudaStream_t stream) {
@@ -389,6 +528,7 @@ cudaError_t launch_sparse(const SparseArgs& sa, cudaStream_t stream) {
   p.seq_len = sa.seq_len;
   p.out = static_cast<uint16_t*>(sa.out);
   p.ws = sa.ws;
+  p.counters = sa.counters;
   p.status = sa.status;
   p.Hq = sa.Hq;
   p.Hkv = sa.Hkv;

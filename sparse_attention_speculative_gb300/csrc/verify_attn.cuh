@@ -13,7 +13,9 @@
 //     times 128-key tiles; CTA c streams the contiguous range [c W / C, (c+1) W / C)
 //     of that list, so every SM gets the same number of tiles (split-K over the
 //     context, balanced to the tile).  A pair cut by CTA boundaries leaves one
-//     partial (m, l, o) per CTA; a small merge kernel combines them.
+//     partial (m, l, o) per CTA; a merge kernel (one block per pair and verify row,
+//     a programmatic dependent, all partial loads of a block in one round)
+//     combines them.
 //   * Warps 0 and 10 stream K and V pages with 4-D TMA loads (128-byte swizzle) into
 //     two separate shared-memory rings (3 stages of 32 KB each for head_dim 128, 5
 //     of 16 KB for 64), so a K stage is refilled as soon as its QK MMA has read it.
@@ -218,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_launch_dependents();  // the merge kernel may become resident and wait
+  pdl_launch_dependents();  // the next kernel on the stream may become resident
+  pdl_wait_primary();       // inputs may come from the preceding kernel on the stream
   const uint32_t tmem_s0 = tmem;       // S^T buffer b: columns [64 b, 64 b + NQ)
   const uint32_t tmem_o = tmem + 128;  // O^T: columns [128, 128 + NQ)
 
@@ -659,13 +662,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Combine the partial (m, l, o) of the CTAs that shared a pair: block (pair, row).
+// Combine the partial (m, l, o) of the CTAs that shared a pair: block (pair, verify
+// row c), thread = dim.  With B = 1 a pair is spread over ~C / Hkv CTAs, so each block
+// issues the loads of up to 32 partials at once and combines them in chunk order.
 template <int D, int NQ, int G>
 __global__ void __launch_bounds__(D) verify_merge_kernel(const VParams a, int ctas) {
-  __shared__ float wgt[256];
-  __shared__ float inv_l;
+  constexpr int kU = 32;
   const int p = blockIdx.x;
   const int c = blockIdx.y;
+  const int dim = threadIdx.x;
+  pdl_launch_dependents();
   pdl_wait_primary();  // partials of the verification kernel are complete
   const long long W = static_cast<long long>(a.pairs) * a.t_max;
   const long long first_v = static_cast<long long>(p) * a.t_max;
@@ -673,38 +679,41 @@ __global__ void __launch_bounds__(D) verify_merge_kernel(const VParams a, int ct
   const int c_last = cta_of(first_v + a.t_max - 1, W, ctas);
   if (c_first == c_last) return;
   const int n = c_last - c_first + 1;
-  const size_t slot_stride = static_cast<size_t>(NQ) * (D + 2);
-  const float* ws = a.ws + static_cast<size_t>(p) * a.max_chunks * slot_stride;
-  if (threadIdx.x < 32) {
-    float M = -INFINITY;
-    for (int k = threadIdx.x; k < n; k += 32) M = fmaxf(M, ws[k * slot_stride + c]);
-    M = warp_max(M);
-    float L = 0.f;
-    for (int k = threadIdx.x; k < n; k += 32) {
-      const float mk = ws[k * slot_stride + c];
-      const float w = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
-      wgt[k] = w;
-      L += w * ws[k * slot_stride + NQ + c];
+  const size_t stride = static_cast<size_t>(NQ) * (D + 2);
+  const float* base = a.ws + static_cast<size_t>(p) * a.max_chunks * stride;
+  float M = -INFINITY, L = 0.f, O = 0.f;
+  for (int k0 = 0; k0 < n; k0 += kU) {
+    float mk[kU], lk[kU], ok[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (k0 + u < n) {
+        const float* sl = base + (k0 + u) * stride;
+        mk[u] = __ldcg(sl + c);
+        lk[u] = __ldcg(sl + NQ + c);
+        ok[u] = __ldcg(sl + 2 * NQ + static_cast<size_t>(c) * D + dim);
+      } else {
+        mk[u] = -INFINITY;
+        lk[u] = 0.f;
+        ok[u] = 0.f;
+      }
     }
-    L = warp_sum(L);
-    if (threadIdx.x == 0) inv_l = L > 0.f ? 1.f / L : 0.f;
-  }
-  __syncthreads();
-  const int dim = threadIdx.x;
-  float acc = 0.f;
-  for (int k0 = 0; k0 < n; k0 += 8) {
-    float x[8];  // eight partials in flight, summed in chunk order
+    float mn = M;
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      x[u] = k0 + u < n ? ws[(k0 + u) * slot_stride + 2 * NQ + static_cast<size_t>(c) * D + dim]
-                        : 0.f;
+    for (int u = 0; u < kU; ++u) mn = fmaxf(mn, mk[u]);
+    const float sc = (M == -INFINITY) ? 0.f : exp2f(M - mn);
+    L *= sc;
+    O *= sc;
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (k0 + u < n) acc += wgt[k0 + u] * x[u];
+    for (int u = 0; u < kU; ++u) {
+      const float w = (mk[u] == -INFINITY) ? 0.f : exp2f(mk[u] - mn);
+      L += w * lk[u];
+      O += w * ok[u];
+    }
+    M = mn;
   }
   const int b = p / a.Hkv, g = p - (p / a.Hkv) * a.Hkv;
   const int t = c / G, hl = c % G;
-  const __nv_bfloat16 bv = __float2bfloat16_rn(acc * inv_l);
+  const __nv_bfloat16 bv = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
   a.out[((static_cast<size_t>(b) * a.R + t) * a.Hq + g * G + hl) * D + dim] =
       *reinterpret_cast<const uint16_t*>(&bv);
 }
@@ -717,24 +726,25 @@ cudaError_t launch_dng(const VerifyArgs& va, const VerifyPlan& plan, const VPara
   // set on every call: the attribute is per device and the call costs no GPU work
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<plan.ctas, kThreads, smem, stream>>>(va.kmap, va.vmap, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (plan.max_chunks > 1) {
-    // programmatic dependent launch: resident while the verification kernel runs
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(plan.pairs, p.NV, 1);
-    cfg.blockDim = dim3(D, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G>, p, plan.ctas);
-  }
-  return e;
+  // Both kernels are programmatic dependents of their predecessor on the stream:
+  // their launch and prologue overlap it, and they wait for its results before
+  // reading any input.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.ctas, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, va.kmap, va.vmap, p);
+  if (e != cudaSuccess || plan.max_chunks <= 1) return e;
+  cfg.gridDim = dim3(plan.pairs, p.NV, 1);
+  cfg.blockDim = dim3(D, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G>, p, plan.ctas);
 }
 
 inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {

@@ -286,10 +286,10 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
   if (k_max < 0 || max_tail < 0) return VSD_ERR_INVALID_ARG;
   if (geom->B > 65535) return VSD_ERR_UNSUPPORTED;
   if (geom->B == 0) return VSD_OK;
-  const size_t need = vsd::sparse_workspace_bytes(vsd::plan_sparse(k_max, max_tail), geom->B,
-                                                  geom->Hkv, geom->Hq / geom->Hkv,
-                                                  geom->head_dim);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
+  const vsd::SparsePlan splan = vsd::plan_sparse(k_max, max_tail);
+  const size_t need = vsd::sparse_workspace_bytes(splan, geom->B, geom->Hkv,
+                                                  geom->Hq / geom->Hkv, geom->head_dim);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
     return VSD_ERR_WORKSPACE;
   if (!q || !k_cache || !v_cache || !block_table || !tail_start || !seq_len || !out)
     return VSD_ERR_INVALID_ARG;
@@ -312,7 +312,11 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
   sa.tail_start = tail_start;
   sa.seq_len = seq_len;
   sa.out = out;
-  sa.ws = need > 0 ? static_cast<float*>(workspace) : nullptr;
+  sa.counters = need > 0 ? static_cast<unsigned*>(workspace) : nullptr;
+  sa.ws = need > 0 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                               vsd::sparse_counter_bytes(splan, geom->B,
+                                                                         geom->Hkv))
+                   : nullptr;
   sa.status = status;
   sa.B = geom->B;
   sa.Hq = geom->Hq;

@@ -1,0 +1,35 @@
+"""bench.py contract checks that need no GPU: the reference arm's JSON line and the
+binding names the GPU arm calls."""
+import json
+import os
+import re
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_bench_calls_only_exported_names():
+    import sparse_attention_speculative_gb300 as vsd
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    names = set(re.findall(r"\bvsd\.(\w+)", src))
+    missing = sorted(n for n in names if not hasattr(vsd, n))
+    assert not missing, "bench.py uses names the package does not export: %s" % missing
+
+
+def test_reference_arm_prints_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_p512_d64", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1]
+    res = json.loads(line)
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in res, key
+    assert res["impl"] == "reference"
+    assert res["value"] > 0
+    assert res["cpu_baseline"]["kind"] == "oracle" and res["cpu_baseline"]["cores"] >= 1
+    assert res["e2e"]["h2d_bytes_per_step"] == 0 and res["e2e"]["value"] == res["value"]
+    assert res["config"]["workload"] == "tiny_p512_d64"

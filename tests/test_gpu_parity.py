@@ -283,3 +283,49 @@ def test_sparse_all_prefix_equals_verify_row():
     torch.cuda.synchronize()
     diff = (d_out.float() - out[:, t].float()).abs().max().item()
     assert diff <= 2e-2
+
+
+def test_workspaces_are_left_ready_for_the_next_call():
+    """The sparse step's split partials are combined by the last CTA of each
+    (sequence, KV head) pair, found through counters at the start of its workspace;
+    every call must leave them at zero so the next call starts clean.  Repeated
+    calls on one workspace give identical results (verification included)."""
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("ws", B=2, P=6000, Hq=16, Hkv=4, d=128, gamma=3, k=256, n_sink=4,
+                 n_recent=32, seed=21, prefix_lens=(6000, 2500))
+    batch = make_batch(w, "cuda")
+    geom = vsd.geom_for(w.B, w.Hq, batch.k_cache, batch.block_table)
+    nb = vsd.vsd_verify_workspace_size(geom, w.R, w.P_max)
+    assert nb > 0, "this geometry must split pairs across CTAs"
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    counter_bytes = ((w.B * w.Hkv * 4 + 255) // 256) * 256
+    for rep in range(3):
+        out, logits, partial = vsd.vsd_verify_attn_collect(
+            batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+            P_max=w.P_max, scale=w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert vsd.vsd_read_device_status() == 0
+        if rep == 0:
+            first = out.clone()
+        else:
+            assert torch.equal(out, first)
+    idx, n_sel, _ = vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                        n_recent=w.n_recent)
+    tail = batch.prefix_len.clone()
+    seq_len = batch.prefix_len + 3
+    sb = vsd.vsd_sparse_workspace_size(geom, w.k, 3)
+    assert sb > 0
+    sws = torch.zeros(sb, dtype=torch.uint8, device="cuda")
+    outs = []
+    for rep in range(3):
+        o = vsd.vsd_sparse_decode_attn(batch.q_draft[0], batch.k_cache, batch.v_cache,
+                                       batch.block_table, idx, n_sel, tail, seq_len,
+                                       scale=w.scale, max_tail=3, workspace=sws)
+        torch.cuda.synchronize()
+        assert vsd.vsd_read_device_status() == 0
+        assert int(sws[:counter_bytes].count_nonzero()) == 0, "sparse counters not reset"
+        outs.append(o.clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    check_sparse(batch, w, idx, n_sel, tail, seq_len, max_tail=3)
