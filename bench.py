@@ -33,6 +33,7 @@ import torch  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 512 << 20  # > 129 MB of L2
+B2B_CALLS = 20
 METRIC = ("KV-read GB/s of one Vegas iteration (verify+collect2, top-k select, "
           "gamma sparse draft steps)")
 
@@ -224,7 +225,8 @@ def run_gpu(args, world, rank, local):
     # this library's kernel launches per step, from the launch plan: verification (+ its
     # split-K merge kernel), selection, and one kernel per draft step (the draft step
     # merges its splits inside the kernel)
-    launches_per_step = 1 + (1 if ws_bytes > 0 else 0) + 1 + gamma
+    launches_per_verify = 1 + (1 if ws_bytes > 0 else 0)
+    launches_per_step = launches_per_verify + 1 + gamma
     enqueue_s = []
     sleep_cycles = 8_000_000  # ~4 ms: the whole step is enqueued before the GPU gets to it
 
@@ -252,6 +254,7 @@ def run_gpu(args, world, rank, local):
         step(events=False)
     torch.cuda.synchronize()
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def graph_step(sl):
         seq_len.copy_(torch.from_numpy(sl))
@@ -287,6 +290,21 @@ def run_gpu(args, world, rank, local):
             per["select"].append(ev[1].elapsed_time(ev[2]) * 1e-3)
             per["sparse"].append([ev[2 + i].elapsed_time(ev[3 + i]) * 1e-3 for i in range(gamma)])
             per["step"].append(ev[0].elapsed_time(ev[2 + gamma]) * 1e-3)
+        # the verification call alone, back to back: K and V (>= 134 MB at these sizes)
+        # exceed L2, so every call streams them from HBM; per-call time = span / calls
+        per["verify_b2b"] = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            torch.cuda._sleep(sleep_cycles)
+            v0.record(stream)
+            for _ in range(B2B_CALLS):
+                vsd.vsd_verify_attn_collect(batch.q, batch.k_cache, batch.v_cache,
+                                            batch.block_table, batch.prefix_len, P_max=P_max,
+                                            scale=w.scale, row0=0, row1=R - 1, logits=logits,
+                                            partial=partial, out=out, workspace=workspace)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            per["verify_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -319,7 +337,8 @@ def run_gpu(args, world, rank, local):
                               "frac_of_%s_hbm" % peak_kind:
                                   statistics.mean(spb) / t_sparse / 1e9 / peak},
     }
-    achieved = vb / t_verify / 1e9
+    t_verify_b2b = statistics.median(per["verify_b2b"])
+    achieved = vb / t_verify_b2b / 1e9
     clk = clocks.summary()
     result = {
         "metric": METRIC,
@@ -347,11 +366,17 @@ def run_gpu(args, world, rank, local):
         "us_per_iter_eager": statistics.mean(per["step"]) * 1e6,
         "kernels": kernels,
         "select_over_verify": t_select / t_verify,
+        "verify_back_to_back_us": t_verify_b2b * 1e6,
         "roofline": {"bound": "hbm", "kernel": "vsd_verify_attn_collect",
+                     "timing": "%d verification calls back to back between two events on "
+                               "the launching stream (K/V larger than L2), per-call mean; "
+                               "bytes = algorithmic bytes of one call" % B2B_CALLS,
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": profile_traffic(w.name)},
         "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches_all_timed_loops": (2 * launches_per_step * args.steps +
+                                         3 * B2B_CALLS * launches_per_verify),
         "gpu_launches_per_step": launches_per_step,
         "clocks": clk,
         # the device timestamps only measure kernels if the host finished enqueueing a

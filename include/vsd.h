@@ -163,7 +163,7 @@ vsd_status vsd_verify_attn_collect_noalloc(const vsd_geom* geom, int R, const vo
  *   scores_out     fp32 [n_rows][P_max] or NULL: the aggregated s (j < P written)
  *   workspace      >= vsd_select_workspace_size(...) bytes (may be 0)
  * Requires n_sink + n_recent <= k.  One launch covers all rows.
- * Supported: P_max <= 524288 for up to 7 rows, P_max <= 262144 for more rows
+ * Supported: P_max <= 262144 for up to 7 rows, P_max <= 131072 for more rows
  * (VSD_ERR_UNSUPPORTED otherwise).  The kernel is launched as a programmatic
  * dependent of the preceding kernel on the stream: it waits for that kernel's
  * results before reading anything.

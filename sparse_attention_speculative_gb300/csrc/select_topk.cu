@@ -7,28 +7,29 @@
 // the rest of the budget is filled by score).  Equal scores go to the lower position;
 // the output is in ascending position order.
 //
-// How (GB300 design).  One thread-block cluster per row (layer x sequence), each CTA
-// owning a contiguous slice of the prefix, each thread a contiguous run of KPT
-// positions.  Scores become order-preserving uint32 keys; the task is to find the
-// threshold key T and the tie cut c such that exactly r = k - |protected| candidates
-// satisfy  key > T  or  (key == T and position <= c).
+// How (GB300 design).  The step is short and latency-bound, so the design minimises
+// dependent rounds between the SMs: one thread-block cluster per row (layer x
+// sequence), each CTA owning a contiguous slice of the prefix, and three cluster
+// barriers in the common case.  Scores become order-preserving uint32 keys.
 //   A. Every CTA sums the per-KV-group partial scores of its slice (fp32, groups in
-//      order; the partials are L2-resident after verification), keeps the keys in
-//      shared memory and builds a 4096-bin histogram of their top 12 bits.
-//   B. Cluster barrier.  CTA i adds up bins [i n/CS, (i+1) n/CS) of all CTAs'
-//      histograms (distributed shared memory, all loads in flight at once).
-//   C. Cluster barrier.  Every CTA finds the slice, then the bin, holding the r-th
-//      largest key.  If that bin still holds more than the gather capacity, the
-//      next 10 bits are histogrammed the same way (rare; at most two more levels).
-//   D. Every CTA copies its keys of the boundary bin, in position order, to rank 0
-//      (offsets from the per-CTA bin counts) and reports its counts.
-//   E. Cluster barrier.  Rank 0 alone resolves the remaining bits and the tie cut on
-//      the gathered keys with block-local passes, then writes T, c and the output
-//      offset of every CTA into that CTA's shared memory.
-//   F. Cluster barrier.  Every CTA writes its selected positions in order.
-// Four cluster barriers in the common case, no global workspace, no atomics on
-// results, and deterministic output.  The kernel is launched as a programmatic
-// dependent: its launch overlaps the tail of the verification kernels.
+//      order), keeps the keys in shared memory and builds a 4096-bin histogram of
+//      the top 12 key bits of its candidates (positions outside the protected sink
+//      and recent windows).
+//   B. Every CTA adds its non-zero bins into rank 0's histogram (distributed shared
+//      memory atomics).  Cluster barrier.
+//   C. Rank 0 finds the boundary bin, the one that holds the r-th largest candidate
+//      key (r = k - |protected|), and writes it into every CTA.  Cluster barrier.  If
+//      that bin holds more keys than rank 0 can take, the next 10 bits are
+//      histogrammed the same way (rare; at most two more levels).
+//   D. Every CTA builds its words of the position bitmap (its candidates above the
+//      boundary bin) and stores them to rank 0, and appends its boundary-bin keys
+//      (with positions) to rank 0's buffer.  Cluster barrier; the other CTAs are done.
+//   E. Rank 0 alone resolves the remaining key bits and the tie cut (equal keys go to
+//      the lower position) on the gathered keys with block-local passes, marks the
+//      winners, and writes the row: sinks, the marked positions in order (a block
+//      scan over the bitmap), the recent window, -1 padding.
+// Results are deterministic; no global workspace.  The kernel is launched as a
+// programmatic dependent: its launch overlaps the tail of the verification kernels.
 #include <cooperative_groups.h>
 
 #include <climits>
@@ -46,7 +47,7 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kMaxSelCluster = 16;
 constexpr int kChunkQuantum = 4 * kSelThreads;  // keys per CTA come in multiples of this
-constexpr int kMaxChunk = 32768;
+constexpr int kMaxChunk = 16384;
 constexpr int kBins0 = 4096;                     // level 0: top 12 bits
 constexpr int kBinsL = 1024;                     // levels 1, 2: 10 bits each
 constexpr int kGatherCap = 8192;                 // boundary-bin keys rank 0 can hold
@@ -60,35 +61,52 @@ struct SelParams {
   int32_t* n_sel;
   float* scores_out;
   unsigned* status;
-  int Hkv, P_max, k, n_sink, n_recent, chunk;
+  int Hkv, P_max, k, n_sink, n_recent, chunk, bitmap_words;
 };
 
 struct SelShared {
   uint32_t scan[kSelWarps];
-  uint32_t slice_tot;
-  uint32_t tmp[kSelWarps];
-  // result of a bin search
-  int f_bin;
-  int f_rem;
-  int f_cnt;
-  // counts reported to rank 0 by every CTA
-  uint32_t above[kMaxSelCluster];
-  uint32_t inbin[kMaxSelCluster];
-  uint32_t sel_in[kMaxSelCluster];
-  uint32_t stot[kMaxSelCluster];
-  // decision broadcast by rank 0
-  uint32_t T;
-  int cut;
-  uint32_t out_off;
+  uint32_t tmp[kMaxSelCluster];
+  int f_bin, f_rem, f_cnt;  // result of a bin search
+  uint32_t gcount;          // rank 0: gathered boundary keys
 };
+
+// Dynamic shared memory of one CTA (the rank-0-only parts are laid out everywhere).
+struct SelLayout {
+  uint2* gbuf;       // [kGatherCap] rank 0: boundary-bin (key, position)
+  uint32_t* keys;    // [chunk]
+  uint32_t* hist;    // [kBins0] this CTA's histogram (rank 0's scratch in E)
+  uint32_t* loc;     // [kBins0] this CTA's words of the selection bitmap
+  uint32_t* ghist;   // [kBins0 + 2 * kBinsL] rank 0: cluster histograms of the levels
+  uint32_t* bitmap;  // [bitmap_words] rank 0: selected candidate positions
+};
+
+__device__ __forceinline__ SelLayout sel_layout(uint8_t* base, int chunk) {
+  SelLayout L;
+  L.gbuf = reinterpret_cast<uint2*>(base);
+  L.keys = reinterpret_cast<uint32_t*>(base + static_cast<size_t>(kGatherCap) * 8);
+  L.hist = L.keys + chunk;
+  L.loc = L.hist + kBins0;
+  L.ghist = L.loc + kBins0;
+  L.bitmap = L.ghist + kBins0 + 2 * kBinsL;
+  return L;
+}
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Exclusive prefix sum over the threads of the block in thread order; *total gets
-// the block sum.  Contains two __syncthreads and leaves `scratch` reusable.
+// the block sum.  Two __syncthreads; `scratch` is reusable afterwards.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch,
                                                     uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -112,8 +130,8 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratc
   return base + x - v;
 }
 
-// Among bins cnt[0..n) (ascending key order) find the bin b holding the r-th
-// largest element (1 <= r <= sum): S(b+1) < r <= S(b) with S(b) = sum of cnt[b..n).
+// Among bins cnt[0..n) (ascending key order) find the bin b holding the r-th largest
+// element (1 <= r <= sum): S(b+1) < r <= S(b) with S(b) = sum of cnt[b..n).
 // Result in sh.f_bin, sh.f_rem (= r - S(b+1)) and sh.f_cnt (= cnt[b]).
 __device__ void find_bin(const uint32_t* cnt, int n, int r, SelShared& sh) {
   const int E = (n + kSelThreads - 1) / kSelThreads;
@@ -141,23 +159,67 @@ __device__ void find_bin(const uint32_t* cnt, int n, int r, SelShared& sh) {
   __syncthreads();
 }
 
+// The same search from the low end: the bin holding the r-th smallest element.
+__device__ void find_bin_low(const uint32_t* cnt, int n, int r, SelShared& sh) {
+  const int E = (n + kSelThreads - 1) / kSelThreads;
+  const int lo = static_cast<int>(threadIdx.x) * E;
+  uint32_t s = 0;
+  for (int e = 0; e < E; ++e)
+    if (lo + e < n) s += cnt[lo + e];
+  uint32_t tot;
+  const uint32_t before = block_excl_scan(s, sh.scan, &tot);
+  const uint32_t ur = static_cast<uint32_t>(r);
+  if (before < ur && ur <= before + s) {
+    uint32_t acc = before;
+    for (int e = 0; e < E; ++e) {
+      const int b = lo + e;
+      const uint32_t c = cnt[b];
+      if (acc + c >= ur) {
+        sh.f_bin = b;
+        sh.f_rem = static_cast<int>(ur - acc);
+        sh.f_cnt = static_cast<int>(c);
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+}
+
+// Set this thread's selected positions (bit q of `sel` = position my0 + q) in the
+// bitmap `bm`, one atomic per word.
+__device__ __forceinline__ void mark_bits(uint32_t* bm, int my0, uint64_t sel) {
+  while (sel) {
+    const int q = __ffsll(static_cast<long long>(sel)) - 1;
+    const int pos = my0 + q;
+    const int span = 32 - (pos & 31);  // positions of this word from pos on
+    const uint64_t m = (span >= 64 - q) ? (~0ull << q) : (((1ull << span) - 1) << q);
+    const uint64_t part = sel & m;
+    atomicOr(bm + (pos >> 5), static_cast<uint32_t>((part >> q) << (pos & 31)));
+    sel &= ~m;
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelParams a) {
   extern __shared__ __align__(16) uint8_t sel_smem[];
   __shared__ SelShared sh;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
-  const int CS = static_cast<int>(cluster.num_blocks());
   const int row = blockIdx.y;
   const int t = threadIdx.x;
   const int chunk = a.chunk;
-  const int KPT = chunk / kSelThreads;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(sel_smem);           // [chunk]
-  uint32_t* hist = keys + chunk;                                      // [kBins0]
-  uint32_t* red = hist + kBins0;                                      // [kBins0 / CS]
-  uint32_t* loc = red + kBins0 / CS;                                  // [kBins0 / CS]
-  uint2* gather = reinterpret_cast<uint2*>(loc + kBins0 / CS);       // [kGatherCap]
+  const int KPT = chunk / kSelThreads;  // 4, 8, 16 or 32 positions per thread
+  const SelLayout L = sel_layout(sel_smem, chunk);
 
   ptx::pdl_launch_dependents();
+  // rank 0's cluster-wide arrays start at zero before anyone adds to them
+  if (rank == 0) {
+    for (int i = t; i < kBins0 + 2 * kBinsL; i += kSelThreads) L.ghist[i] = 0u;
+    if (t == 0) sh.gcount = 0u;
+  }
+  for (int i = t; i < kBins0; i += kSelThreads) L.hist[i] = 0u;
+  __syncthreads();
+  cluster_arrive();  // this CTA's shared memory is ready; waited on before remote use
   ptx::pdl_wait_primary();  // the partial scores come from the preceding kernels
 
   int P = __ldg(a.prefix_len + row);
@@ -171,25 +233,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   const int rb = rb0 > sink_end ? rb0 : sink_end;  // candidates: [sink_end, rb)
   const int n_cand = rb - sink_end;
   const int r_need = n - (P - n_cand);
-  const int lo = rank * chunk;
-  const int my0 = lo + t * KPT;  // this thread's positions [my0, my0 + KPT)
+  const int my0 = rank * chunk + t * KPT;  // this thread's positions [my0, my0 + KPT)
+  const bool take_all = r_need >= n_cand;
+  const bool ranking = r_need > 0 && !take_all;
 
-  // protected positions in [x0, x1)
-  auto prot_in = [&](int x0, int x1) {
-    const int a0 = max(x0, 0), a1 = min(x1, sink_end);
-    const int b0 = max(x0, rb), b1 = min(x1, P);
-    return max(a1 - a0, 0) + max(b1 - b0, 0);
-  };
-  auto cand_in = [&](int x0, int x1) {
-    return max(min(x1, rb) - max(x0, sink_end), 0);
-  };
-  const bool all_or_none = r_need <= 0 || r_need >= n_cand;
-
-  if (!all_or_none)
-    for (int i = t; i < kBins0; i += kSelThreads) hist[i] = 0u;
-  if (!all_or_none || a.scores_out != nullptr) {
-    if (!all_or_none) __syncthreads();
-    // ---- A. aggregated scores, keys and the level-0 histogram
+  // ---- A. aggregated scores, keys and the level-0 histogram of the candidates
+  if (ranking || a.scores_out != nullptr) {
     const float* base = a.partial + static_cast<size_t>(row) * a.Hkv * a.P_max;
     const bool vec = (a.P_max & 3) == 0;
     for (int q = 0; q < KPT; q += 4) {
@@ -211,7 +260,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
           }
         }
         for (; g < a.Hkv; ++g) {
-          const float4 x = __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g) * a.P_max + j));
+          const float4 x =
+              __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g) * a.P_max + j));
           s[0] += x.x;
           s[1] += x.y;
           s[2] += x.z;
@@ -227,89 +277,66 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
       for (int u = 0; u < 4; ++u) {
         const int jj = j + u;
         const uint32_t key = jj < P ? order_key(s[u]) : 0u;
-        keys[t * KPT + q + u] = key;
+        L.keys[t * KPT + q + u] = key;
         if (jj < P && a.scores_out != nullptr)
           a.scores_out[static_cast<size_t>(row) * a.P_max + jj] = s[u];
-        if (!all_or_none && jj >= sink_end && jj < rb) atomicAdd(&hist[key >> 20], 1u);
+        if (ranking && jj >= sink_end && jj < rb) atomicAdd(&L.hist[key >> 20], 1u);
       }
     }
   }
+  __syncthreads();
+  cluster_wait();  // every CTA's shared memory is ready
 
-  uint32_t T = 0u;
-  int cut = INT_MAX;
-  uint32_t out_off = 0;
-  if (all_or_none) {
-    // nothing to rank: every candidate or none of them is taken
-    T = r_need <= 0 ? 0xFFFFFFFFu : 0u;
-    cut = r_need <= 0 ? -1 : INT_MAX;
-    out_off = prot_in(0, lo) + (r_need <= 0 ? 0 : cand_in(0, lo));
-  } else {
-    // ---- B/C. cluster histogram levels until the boundary bin is small enough
-    uint32_t prefix = 0u, mask = 0u;
-    int r_rem = r_need;
-    int mode = kModeTie;
-    int level_bin = 0;  // bin of the final level (index into every CTA's hist)
+  uint32_t* bm0 = cluster.map_shared_rank(L.bitmap, 0);
+  uint32_t prefix = 0u, mask = 0u;
+  int r_rem = r_need;
+  int mode = kModeWhole;
+  int level_bin = 0;
+  if (ranking) {
+    // ---- B/C. cluster histograms, level by level, until the boundary bin is small
+    mode = kModeTie;
     for (int level = 0; level < 3; ++level) {
       const int nb = level == 0 ? kBins0 : kBinsL;
       const int shift = level == 0 ? 20 : (level == 1 ? 10 : 0);
       const uint32_t dmask = static_cast<uint32_t>(nb - 1);
+      uint32_t* gh_local = L.ghist + (level == 0 ? 0 : kBins0 + (level - 1) * kBinsL);
       if (level > 0) {
-        // every CTA has read the previous level's histograms (barrier below), so
-        // they can be rebuilt for this level's digit
-        for (int i = t; i < nb; i += kSelThreads) hist[i] = 0u;
+        for (int i = t; i < nb; i += kSelThreads) L.hist[i] = 0u;
         __syncthreads();
         for (int q = 0; q < KPT; ++q) {
           const int j = my0 + q;
-          const uint32_t key = keys[t * KPT + q];
+          const uint32_t key = L.keys[t * KPT + q];
           if (j >= sink_end && j < rb && (key & mask) == prefix)
-            atomicAdd(&hist[(key >> shift) & dmask], 1u);
+            atomicAdd(&L.hist[(key >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+      }
+      uint32_t* gh0 = cluster.map_shared_rank(gh_local, 0);
+      for (int b = t; b < nb; b += kSelThreads) {
+        const uint32_t c = L.hist[b];
+        if (c) atomicAdd(gh0 + b, c);
+      }
+      cluster_arrive();
+      cluster_wait();  // rank 0's histogram of this level is complete
+      if (rank == 0) {
+        // rank 0 searches its histogram and hands the result to every CTA
+        find_bin(gh_local, nb, r_rem, sh);
+        if (t < static_cast<int>(cluster.num_blocks())) {
+          SelShared* d = cluster.map_shared_rank(&sh, t);
+          d->f_bin = sh.f_bin;
+          d->f_rem = sh.f_rem;
+          d->f_cnt = sh.f_cnt;
         }
       }
-      cluster.sync();  // all histograms of this level complete
-      const int sl = nb / CS;
-      const int sbase = rank * sl;
-      uint32_t part = 0;
-      for (int b = t; b < sl; b += kSelThreads) {
-        uint32_t v[kMaxSelCluster];
-#pragma unroll
-        for (int r = 0; r < kMaxSelCluster; ++r)
-          v[r] = r < CS ? *cluster.map_shared_rank(hist + sbase + b, r) : 0u;
-        uint32_t s = 0;
-#pragma unroll
-        for (int r = 0; r < kMaxSelCluster; ++r) s += v[r];
-        red[b] = s;
-        part += s;
-      }
-      uint32_t tot;
-      (void)block_excl_scan(part, sh.scan, &tot);
-      if (t == 0) sh.slice_tot = tot;
-      cluster.sync();  // all slices reduced
-      // slice holding the r_rem-th largest: read every CTA's slice total
-      if (t < CS) sh.stot[t] = *cluster.map_shared_rank(&sh.slice_tot, t);
-      __syncthreads();
-      int s_star = 0;
-      uint32_t above = 0;
-      for (int r = CS - 1; r >= 0; --r) {
-        const uint32_t c = sh.stot[r];
-        if (above + c >= static_cast<uint32_t>(r_rem)) {
-          s_star = r;
-          break;
-        }
-        above += c;
-      }
-      // copy that slice locally, then search it
-      for (int b = t; b < sl; b += kSelThreads)
-        loc[b] = *cluster.map_shared_rank(red + b, s_star);
-      __syncthreads();
-      find_bin(loc, sl, r_rem - static_cast<int>(above), sh);
-      const int b_local = sh.f_bin;
-      const int bin = s_star * sl + b_local;
+      cluster_arrive();
+      cluster_wait();  // every CTA has the boundary bin of this level
+      const int bin = sh.f_bin;
       const int c_star = sh.f_cnt;
       r_rem = sh.f_rem;
       prefix |= static_cast<uint32_t>(bin) << shift;
       mask |= dmask << shift;
       level_bin = bin;
-      __syncthreads();  // sh.f_* and loc are written again by the next level
+      __syncthreads();  // sh.f_* is written again by the next level
       if (r_rem == c_star) {
         mode = kModeWhole;  // the whole boundary bin is taken
         break;
@@ -320,206 +347,175 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
       }
       // level 2 fixes all 32 bits: more than kGatherCap keys equal to one value
     }
+  }
 
-    // ---- D. counts (and the boundary-bin keys) to rank 0
-    uint32_t c_above = 0, c_in = 0;
+  // ---- D. mark the sure winners, hand the boundary bin to rank 0
+  {
+    uint64_t sure = 0, inbin = 0;
     for (int q = 0; q < KPT; ++q) {
       const int j = my0 + q;
       if (j >= sink_end && j < rb) {
-        const uint32_t km = keys[t * KPT + q] & mask;
-        c_above += km > prefix ? 1u : 0u;
-        c_in += km == prefix ? 1u : 0u;
+        if (take_all) {
+          sure |= 1ull << q;
+        } else if (ranking) {
+          const uint32_t km = L.keys[t * KPT + q] & mask;
+          if (km > prefix) sure |= 1ull << q;
+          else if (km == prefix) inbin |= 1ull << q;
+        }
       }
     }
-    uint32_t tot_above, tot_in;
-    const uint32_t packed = c_above | (c_in << 16);  // both below 2^16 per CTA
-    uint32_t tot_packed;
-    const uint32_t pre = block_excl_scan(packed, sh.scan, &tot_packed);
-    tot_above = tot_packed & 0xFFFFu;
-    tot_in = tot_packed >> 16;
+    if (mode == kModeWhole) {
+      sure |= inbin;
+      inbin = 0;
+    } else if (mode == kModeTie) {
+      // every boundary key equals the threshold: the first r_rem of them in position
+      // order are taken; this CTA's share follows from the lower ranks' counts
+      if (t < rank) sh.tmp[t] = *cluster.map_shared_rank(L.hist + level_bin, t);
+      __syncthreads();
+      long long before = 0;
+      for (int r = 0; r < rank; ++r) before += sh.tmp[r];
+      uint32_t tot_in;
+      const int cnt = __popcll(inbin);
+      const uint32_t pre = block_excl_scan(static_cast<uint32_t>(cnt), sh.scan, &tot_in);
+      const long long left = static_cast<long long>(r_rem) - before - pre;
+      uint64_t take = inbin;
+      if (left <= 0) {
+        take = 0;
+      } else if (left < cnt) {
+        for (int drop = cnt - static_cast<int>(left); drop > 0; --drop)
+          take &= ~(1ull << (63 - __clzll(static_cast<long long>(take))));  // the highest
+      }
+      sure |= take;
+      inbin = 0;
+    }
+    // this CTA's words of the bitmap are built here and stored to rank 0 whole
+    uint32_t* lbm = L.loc;
+    const int nw_cta = chunk / 32;
+    for (int i = t; i < nw_cta; i += kSelThreads) lbm[i] = 0u;
+    __syncthreads();
+    mark_bits(lbm, t * KPT, sure);
+    __syncthreads();
+    for (int i = t; i < nw_cta; i += kSelThreads) bm0[rank * nw_cta + i] = lbm[i];
     if (mode == kModeGather) {
-      // this CTA's first slot: boundary-bin keys of the lower ranks
-      if (t < rank) sh.tmp[t] = *cluster.map_shared_rank(hist + level_bin, t);
-      __syncthreads();
-      uint32_t base = 0;
-      for (int r = 0; r < rank; ++r) base += sh.tmp[r];
-      uint2* dst = cluster.map_shared_rank(gather, 0);
-      uint32_t o = base + (pre >> 16);
-      for (int q = 0; q < KPT; ++q) {
-        const int j = my0 + q;
-        const uint32_t key = keys[t * KPT + q];
-        if (j >= sink_end && j < rb && (key & mask) == prefix) {
-          dst[o] = make_uint2(key, static_cast<uint32_t>(j));
-          ++o;
-        }
+      // append (key, position) of the boundary bin to rank 0's buffer, one atomic per warp
+      const int lane = t & 31;
+      const uint32_t mine = static_cast<uint32_t>(__popcll(inbin));
+      uint32_t incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+      uint32_t wbase = 0;
+      if (lane == 31 && wtot) wbase = atomicAdd(cluster.map_shared_rank(&sh.gcount, 0), wtot);
+      wbase = __shfl_sync(0xffffffffu, wbase, 31);
+      uint2* gb0 = cluster.map_shared_rank(L.gbuf, 0);
+      uint32_t o = wbase + incl - mine;
+      while (inbin) {
+        const int q = __ffsll(static_cast<long long>(inbin)) - 1;
+        inbin &= inbin - 1;
+        gb0[o++] = make_uint2(L.keys[t * KPT + q], static_cast<uint32_t>(my0 + q));
       }
     }
-    if (t == 0) {
-      *cluster.map_shared_rank(&sh.above[rank], 0) = tot_above;
-      *cluster.map_shared_rank(&sh.inbin[rank], 0) = tot_in;
-    }
-    cluster.sync();  // gathered keys and counts are at rank 0
+  }
+  cluster_arrive();
+  cluster_wait();  // rank 0 holds every mark and every boundary key
+  if (rank != 0) return;
 
-    // ---- E. rank 0 resolves the threshold and the output offsets
-    if (rank == 0) {
-      uint32_t n_in = 0;
-      for (int r = 0; r < CS; ++r) n_in += sh.inbin[r];
-      if (t < kMaxSelCluster) sh.sel_in[t] = 0u;
-      if (t == 0) sh.cut = INT_MAX;
-      if (mode == kModeWhole) {
-        T = prefix;
-        cut = INT_MAX;
-        if (t < CS) sh.sel_in[t] = sh.inbin[t];
-      } else if (mode == kModeGather) {
-        // remaining digits of the gathered keys
-        int start_level = 1;
-        if ((mask & 0x000FFC00u) != 0) start_level = 2;
-        if (mask == 0xFFFFFFFFu) start_level = 3;
-        for (int level = start_level; level < 3; ++level) {
-          const int shift = level == 1 ? 10 : 0;
-          for (int i = t; i < kBinsL; i += kSelThreads) hist[i] = 0u;
-          __syncthreads();
-          for (uint32_t i = t; i < n_in; i += kSelThreads) {
-            const uint32_t key = gather[i].x;
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (kBinsL - 1)], 1u);
-          }
-          __syncthreads();
-          find_bin(hist, kBinsL, r_rem, sh);
-          prefix |= static_cast<uint32_t>(sh.f_bin) << shift;
-          mask |= static_cast<uint32_t>(kBinsL - 1) << shift;
-          const bool whole = sh.f_rem == sh.f_cnt;
-          r_rem = sh.f_rem;
-          __syncthreads();
-          if (whole) break;
-        }
-        // T = prefix.  If the mask is complete, r_rem keys equal to T are taken in
-        // position order; otherwise the whole bin below the mask is taken.
-        T = prefix;
-        const bool full = mask == 0xFFFFFFFFu;
-        const int E = (static_cast<int>(n_in) + kSelThreads - 1) / kSelThreads;
-        const int i0 = t * E;
-        const int i1 = min(i0 + E, static_cast<int>(n_in));
-        if (full) {
-          uint32_t ce = 0;
-          for (int i = i0; i < i1; ++i) ce += gather[i].x == T ? 1u : 0u;
-          uint32_t tot_eq;
-          const uint32_t before = block_excl_scan(ce, sh.scan, &tot_eq);
-          const uint32_t ur = static_cast<uint32_t>(r_rem);
-          if (before < ur && ur <= before + ce) {
-            uint32_t acc = before;
-            for (int i = i0; i < i1; ++i) {
-              if (gather[i].x == T && ++acc == ur) {
-                sh.cut = static_cast<int>(gather[i].y);
-                break;
-              }
-            }
-          }
-          __syncthreads();
-          cut = sh.cut;
-        } else {
-          T = prefix;  // smallest key with this prefix: every key of the bin is >= T
-          cut = INT_MAX;
-        }
-        for (int i = i0; i < i1; ++i) {
-          const uint32_t key = gather[i].x;
-          const int j = static_cast<int>(gather[i].y);
-          const bool sel = full ? (key > T || (key == T && j <= cut)) : ((key & mask) >= prefix);
-          if (sel) atomicAdd(&sh.sel_in[j / chunk], 1u);
-        }
-      } else {
-        // kModeTie: every boundary key equals T; take the first r_rem in position order
-        T = prefix;
-        int rc = 0;
-        uint32_t before_rc = 0;
-        for (int r = 0; r < CS; ++r) {
-          const uint32_t c = sh.inbin[r];
-          if (before_rc + c >= static_cast<uint32_t>(r_rem)) {
-            rc = r;
-            break;
-          }
-          before_rc += c;
-        }
-        const uint32_t e = static_cast<uint32_t>(r_rem) - before_rc;  // 1-based within rc
-        const uint32_t* rkeys = cluster.map_shared_rank(keys, rc);
-        const int base_j = rc * chunk + t * KPT;
-        uint32_t ce = 0;
-        for (int q = 0; q < KPT; ++q) {
-          const int j = base_j + q;
-          ce += (j >= sink_end && j < rb && rkeys[t * KPT + q] == T) ? 1u : 0u;
-        }
-        uint32_t tot_eq;
-        const uint32_t before = block_excl_scan(ce, sh.scan, &tot_eq);
-        if (before < e && e <= before + ce) {
-          uint32_t acc = before;
-          for (int q = 0; q < KPT; ++q) {
-            const int j = base_j + q;
-            if (j >= sink_end && j < rb && rkeys[t * KPT + q] == T && ++acc == e) {
-              sh.cut = j;
-              break;
-            }
-          }
-        }
-        __syncthreads();
-        cut = sh.cut;
-        if (t < CS) {
-          uint32_t bef = 0;
-          for (int r = 0; r < t; ++r) bef += sh.inbin[r];
-          const int left = r_rem - static_cast<int>(bef);
-          sh.sel_in[t] = static_cast<uint32_t>(min(max(left, 0), static_cast<int>(sh.inbin[t])));
-        }
+  // ---- E. rank 0: resolve the boundary bin, then write the row
+  if (mode == kModeGather) {
+    const int n_in = static_cast<int>(sh.gcount);
+    uint32_t* h = L.hist;  // scratch
+    const int start_level = (mask == 0xFFF00000u) ? 1 : ((mask == 0xFFFFFC00u) ? 2 : 3);
+    for (int level = start_level; level < 3; ++level) {
+      const int shift = level == 1 ? 10 : 0;
+      for (int i = t; i < kBinsL; i += kSelThreads) h[i] = 0u;
+      __syncthreads();
+      for (int i = t; i < n_in; i += kSelThreads) {
+        const uint32_t key = L.gbuf[i].x;
+        if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & (kBinsL - 1)], 1u);
       }
       __syncthreads();
-      if (t < CS) {
-        uint32_t off = 0;
-        for (int r = 0; r < t; ++r) off += prot_in(r * chunk, (r + 1) * chunk) + sh.above[r] + sh.sel_in[r];
-        SelShared* dst = cluster.map_shared_rank(&sh, t);
-        dst->T = T;
-        dst->cut = cut;
-        dst->out_off = off;
+      find_bin(h, kBinsL, r_rem, sh);
+      const bool whole = sh.f_rem == sh.f_cnt;
+      prefix |= static_cast<uint32_t>(sh.f_bin) << shift;
+      mask |= static_cast<uint32_t>(kBinsL - 1) << shift;
+      r_rem = sh.f_rem;
+      __syncthreads();
+      if (whole) break;
+    }
+    // winners among the gathered keys: above the prefix, or within it -- all of them,
+    // unless all 32 bits are fixed and only r_rem of the equal keys are taken: then
+    // the r_rem lowest positions (positions are below 2^20: two 10-bit passes)
+    int cut = INT_MAX;
+    if (mask == 0xFFFFFFFFu) {
+      uint32_t n_eq = 0;
+      for (int i = t; i < n_in; i += kSelThreads) n_eq += L.gbuf[i].x == prefix ? 1u : 0u;
+      uint32_t tot_eq;
+      (void)block_excl_scan(n_eq, sh.scan, &tot_eq);
+      if (tot_eq > static_cast<uint32_t>(r_rem)) {
+        uint32_t pos_prefix = 0, pos_mask = 0;
+        int rr = r_rem;
+        for (int pl = 0; pl < 2; ++pl) {
+          const int shift = pl == 0 ? 10 : 0;
+          for (int i = t; i < kBinsL; i += kSelThreads) h[i] = 0u;
+          __syncthreads();
+          for (int i = t; i < n_in; i += kSelThreads) {
+            const uint2 e = L.gbuf[i];
+            if (e.x == prefix && (e.y & pos_mask) == pos_prefix)
+              atomicAdd(&h[(e.y >> shift) & (kBinsL - 1)], 1u);
+          }
+          __syncthreads();
+          find_bin_low(h, kBinsL, rr, sh);
+          pos_prefix |= static_cast<uint32_t>(sh.f_bin) << shift;
+          pos_mask |= static_cast<uint32_t>(kBinsL - 1) << shift;
+          rr = sh.f_rem;
+          __syncthreads();
+        }
+        cut = static_cast<int>(pos_prefix);
       }
     }
-    cluster.sync();  // every CTA has its threshold and offset
-    T = sh.T;
-    cut = sh.cut;
-    out_off = sh.out_off;
+    for (int i = t; i < n_in; i += kSelThreads) {
+      const uint2 e = L.gbuf[i];
+      const uint32_t km = e.x & mask;
+      const bool sel = km > prefix || (km == prefix && static_cast<int>(e.y) <= cut);
+      if (sel) atomicOr(&L.bitmap[e.y >> 5], 1u << (e.y & 31));
+    }
+    __syncthreads();
   }
 
-  // ---- F. selected positions of this slice, in order
-  uint32_t cs = 0;
-  for (int q = 0; q < KPT; ++q) {
-    const int j = my0 + q;
-    if (j >= P) break;
-    bool sel;
-    if (j < sink_end || j >= rb) {
-      sel = true;
-    } else {
-      const uint32_t key = all_or_none ? 0u : keys[t * KPT + q];
-      sel = all_or_none ? (r_need > 0) : (key > T || (key == T && j <= cut));
-    }
-    cs += sel ? 1u : 0u;
-  }
-  uint32_t cs_total;
-  uint32_t o = out_off + block_excl_scan(cs, sh.scan, &cs_total);
+  // the row: sinks, marked candidates in position order, the recent window, padding
   int32_t* dst = a.idx + static_cast<size_t>(row) * a.k;
-  for (int q = 0; q < KPT; ++q) {
-    const int j = my0 + q;
-    if (j >= P) break;
-    bool sel;
-    if (j < sink_end || j >= rb) {
-      sel = true;
-    } else {
-      const uint32_t key = all_or_none ? 0u : keys[t * KPT + q];
-      sel = all_or_none ? (r_need > 0) : (key > T || (key == T && j <= cut));
-    }
-    if (sel) {
-      if (o < static_cast<uint32_t>(n)) dst[o] = j;
+  const int w_lo = sink_end >> 5;
+  const int w_hi = (rb + 31) >> 5;
+  const int WPT = (w_hi - w_lo + kSelThreads - 1) / kSelThreads;
+  uint32_t c = 0;
+  for (int e = 0; e < WPT; ++e) {
+    const int w = w_lo + t * WPT + e;
+    if (w < w_hi) c += __popc(L.bitmap[w]);
+  }
+  uint32_t c_tot;
+  uint32_t o = static_cast<uint32_t>(sink_end) + block_excl_scan(c, sh.scan, &c_tot);
+  for (int e = 0; e < WPT; ++e) {
+    const int w = w_lo + t * WPT + e;
+    if (w >= w_hi) break;
+    uint32_t bits = L.bitmap[w];
+    while (bits) {
+      const int bit = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (o < static_cast<uint32_t>(n)) dst[o] = w * 32 + bit;
       ++o;
     }
   }
-  // unused slots and the count
-  for (int m = n + rank * kSelThreads + t; m < a.k; m += CS * kSelThreads) dst[m] = -1;
-  if (rank == 0 && t == 0) a.n_sel[row] = n;
+  const int n_recent_kept = P - rb;
+  for (int i = t; i < sink_end; i += kSelThreads) dst[i] = i;
+  for (int i = t; i < n_recent_kept; i += kSelThreads) dst[n - n_recent_kept + i] = rb + i;
+  for (int m = n + t; m < a.k; m += kSelThreads) dst[m] = -1;
+  if (t == 0) a.n_sel[row] = n;
 }
+
+int bitmap_words_for(int chunk, int cs) { return (chunk * cs + 31) / 32; }
 
 }  // namespace
 
@@ -528,11 +524,9 @@ int select_cluster_size(int P_max, int n_rows) {
   if (cs < 1) cs = 1;
   const int cap = n_rows > 7 ? 8 : kMaxSelCluster;  // 16-CTA clusters: few fit at once
   if (cs > cap) cs = cap;
-  // power of two, so every slice of the histograms has the same size
   int p2 = 1;
   while (p2 < cs) p2 <<= 1;
-  cs = p2 > cap ? cap : p2;
-  return cs;
+  return p2 > cap ? cap : p2;
 }
 
 int select_chunk(int P_max, int cs) {
@@ -543,8 +537,9 @@ int select_chunk(int P_max, int cs) {
 }
 
 size_t select_smem_bytes(int chunk, int cs) {
-  return static_cast<size_t>(chunk) * 4 + kBins0 * 4 + static_cast<size_t>(kBins0 / cs) * 8 +
-         static_cast<size_t>(kGatherCap) * 8;
+  return static_cast<size_t>(kGatherCap) * 8 +
+         (static_cast<size_t>(chunk) + 2 * kBins0 + kBins0 + 2 * kBinsL +
+          bitmap_words_for(chunk, cs)) * 4;
 }
 
 cudaError_t launch_select(const SelectArgs& sa, cudaStream_t stream) {
@@ -565,6 +560,7 @@ cudaError_t launch_select(const SelectArgs& sa, cudaStream_t stream) {
   p.n_sink = sa.n_sink;
   p.n_recent = sa.n_recent;
   p.chunk = chunk;
+  p.bitmap_words = bitmap_words_for(chunk, CS);
   const size_t smem = select_smem_bytes(chunk, CS);
   cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,

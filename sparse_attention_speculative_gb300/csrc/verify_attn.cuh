@@ -250,31 +250,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) tma_prefetch_desc(map);
     uint32_t it = 0, issued = 0;
     for (long long v = v0; v < v1;) {
+      // Block-table entries come 4 tiles (32 pages, one per lane) per load round and
+      // two rounds ahead; the first two rounds are issued together with the prefix
+      // length load, so the first copies leave one memory latency after the start.
+      const int p0 = static_cast<int>(v / a.t_max);
+      const int b0 = p0 / a.Hkv;
+      const int tb0 = static_cast<int>(v - static_cast<long long>(p0) * a.t_max);
+      const int32_t* bt_row = a.block_table + static_cast<size_t>(b0) * a.max_blocks;
+      auto raw_entry = [&](int tile_base) {
+        const int lp = (tile_base + (lane >> 3)) * kPagesPerTile + (lane & 7);
+        return lp < a.max_blocks ? __ldg(bt_row + lp) : a.num_blocks;
+      };
+      int ent_cur = raw_entry(tb0);
+      int ent_nxt = raw_entry(tb0 + 4);
       const Seg s = segment_at(v, v1, a);
       v = s.next_v;
       if (is_k && s.bad_len && lane == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
-      // block id of page `lane` of a tile (lanes 0-7); out of range -> zero fill
-      auto fetch_blk = [&](int tile, bool& bad) {
-        int blk = a.num_blocks;
-        bad = false;
-        if (lane < kPagesPerTile && tile < s.t_end) {
-          const int lp = tile * kPagesPerTile + lane;
-          if (lp * kPage < s.L) {
-            const int e = __ldg(a.block_table + static_cast<size_t>(s.b) * a.max_blocks + lp);
-            if (e < 0 || e >= a.num_blocks) bad = true;
-            else blk = e;
-          }
-        }
-        return blk;
-      };
-      bool bad_next = false;
-      int blk_next = fetch_blk(s.t_begin, bad_next);
       for (int tile = s.t_begin; tile < s.t_end; ++tile, ++it) {
+        const int k4 = (tile - s.t_begin) & 3;
+        if (k4 == 0 && tile != s.t_begin) {
+          ent_cur = ent_nxt;
+          ent_nxt = raw_entry(tile + 4);  // in flight during the next 4 tiles
+        }
+        // block id of page `lane` (lanes 0-7) of this tile; outside the sequence or
+        // invalid -> an out-of-range block, which the copy fills with zeros
+        const int e = __shfl_sync(0xffffffffu, ent_cur, k4 * 8 + (lane & 7));
+        const int lp = tile * kPagesPerTile + (lane & 7);
+        const bool inside = lane < kPagesPerTile && lp * kPage < s.L;
+        const bool bad = inside && (e < 0 || e >= a.num_blocks);
+        const int blk = (inside && !bad) ? e : a.num_blocks;
         const int stage = it % S;
         const uint32_t use = it / S;
-        const int blk = blk_next;
-        const bool bad = bad_next;
-        blk_next = fetch_blk(tile + 1, bad_next);  // in flight while we wait below
         int ok = 1;
         if (lane == 0 && use > 0) ok = mbar_wait(&empty[stage], (use - 1) & 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -411,6 +417,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool collect = a.logits != nullptr || a.partial != nullptr;
     uint32_t it = 0;
     for (long long v = v0; v < v1;) {
+      // Loads that need no prefix length go out first: the segment's Q rows and this
+      // thread's first block-table entry, then the length itself.
+      const int p0 = static_cast<int>(v / a.t_max);
+      const int b0 = p0 / a.Hkv, g0 = p0 - (p0 / a.Hkv) * a.Hkv;
+      const int tb0 = static_cast<int>(v - static_cast<long long>(p0) * a.t_max);
+      constexpr int kQL = (NQ * (D / 8) + kSoftmaxThreads - 1) / kSoftmaxThreads;
+      uint4 qv[kQL];
+#pragma unroll
+      for (int u = 0; u < kQL; ++u) {
+        const int idx = ts + u * kSoftmaxThreads;
+        const int r = idx / (D / 8), ch = idx % (D / 8);
+        qv[u] = make_uint4(0, 0, 0, 0);
+        if (idx < NQ * (D / 8) && r < a.NV) {
+          const int t = r / G, hl = r % G;
+          qv[u] = *reinterpret_cast<const uint4*>(
+              a.q + ((static_cast<size_t>(b0) * a.R + t) * a.Hq + g0 * G + hl) * D + ch * 8);
+        }
+      }
+      const int lp0 = (tb0 * kTile + row) / kPage;
+      const int entry_first =
+          lp0 < a.max_blocks ? __ldg(a.block_table + static_cast<size_t>(b0) * a.max_blocks + lp0)
+                             : 0;
       const Seg s = segment_at(v, v1, a);
       v = s.next_v;
       const long long first_v = static_cast<long long>(s.p) * a.t_max;
@@ -430,17 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (has_tiles) {
         // Q rows of this (sequence, KV group): row r = t * G + hl -> q[b, t, g*G + hl, :]
-        for (int idx = ts; idx < NQ * (D / 8); idx += kSoftmaxThreads) {
-          const int r = idx / (D / 8), ch = idx % (D / 8);
-          uint4 val = make_uint4(0, 0, 0, 0);
-          if (r < a.NV) {
-            const int t = r / G, hl = r % G;
-            val = *reinterpret_cast<const uint4*>(
-                a.q + ((static_cast<size_t>(s.b) * a.R + t) * a.Hq + s.g * G + hl) * D + ch * 8);
+#pragma unroll
+        for (int u = 0; u < kQL; ++u) {
+          const int idx = ts + u * kSoftmaxThreads;
+          if (idx < NQ * (D / 8)) {
+            const int r = idx / (D / 8), ch = idx % (D / 8);
+            const int hh = ch >> 3, w = ch & 7;
+            *reinterpret_cast<uint4*>(q_smem + hh * NQ * 128 + r * 128 + ((w ^ (r & 7)) << 4)) =
+                qv[u];
           }
-          const int hh = ch >> 3, w = ch & 7;
-          *reinterpret_cast<uint4*>(q_smem + hh * NQ * 128 + r * 128 + ((w ^ (r & 7)) << 4)) =
-              val;
         }
         if (ts < 64) m2s[ts] = (ts < a.NV) ? -INFINITY : INFINITY;
         fence_proxy_async_smem();
@@ -455,7 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    ? __ldg(a.block_table + static_cast<size_t>(s.b) * a.max_blocks + jj / kPage)
                    : 0;
       };
-      int entry_next = page_entry(s.t_begin);
+      int entry_next =
+          (s.t_begin < s.t_end && s.t_begin * kTile + row < s.L) ? entry_first : 0;
       for (int tile = s.t_begin; tile < s.t_end; ++tile, ++it) {
         const int stage = it % S;
         const int buf = it & 1;

@@ -209,6 +209,27 @@ def test_select_ties_and_small_prefixes():
         check_select(pt, pl, w)
 
 
+def test_select_rare_paths():
+    """Boundary bins the first histogram level cannot split: every score equal (all
+    three levels, then the tie rule alone decides by position), and scores packed in a
+    narrow range (a second level, then the gathered keys resolve the rest)."""
+    rng = np.random.default_rng(7)
+    from sparse_attention_speculative_gb300.workloads import Workload
+    for n_rows in (1, 9):
+        P_max, Hkv = 32768, 2
+        prefix = np.full(n_rows, P_max, np.int32)
+        prefix[1:] = rng.integers(20000, P_max + 1, size=n_rows - 1)
+        equal = np.zeros((n_rows, Hkv, P_max), np.float32)
+        narrow = (50.0 + rng.uniform(0.0, 0.01, size=(n_rows, Hkv, P_max))).astype(np.float32)
+        mixed = np.where(rng.random((n_rows, 1, P_max)) < 0.5, 0.0,
+                         rng.normal(size=(n_rows, Hkv, P_max))).astype(np.float32)
+        for partial in (equal, narrow, mixed):
+            w = Workload("rare", B=n_rows, P=P_max, Hq=8, Hkv=Hkv, d=128, gamma=1, k=2048,
+                         n_sink=16, n_recent=256)
+            check_select(torch.tensor(partial, device="cuda"), torch.tensor(prefix, device="cuda"),
+                         w)
+
+
 def test_select_many_rows_one_launch():
     rng = np.random.default_rng(1)
     n_rows, Hkv, P_max = 40, 8, 65536
