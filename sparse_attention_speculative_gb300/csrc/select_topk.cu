@@ -222,6 +222,47 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   cluster_arrive();  // this CTA's shared memory is ready; waited on before remote use
   ptx::pdl_wait_primary();  // the partial scores come from the preceding kernels
 
+  // Sums of 4 consecutive positions over the KV groups (fp32, groups in order).  Every
+  // position below P_max is valid memory, so the first group of 4 is loaded before
+  // the prefix length is known; positions at or past P are masked afterwards.
+  const float* base = a.partial + static_cast<size_t>(row) * a.Hkv * a.P_max;
+  const bool vec = (a.P_max & 3) == 0;
+  auto sum4 = [&](int j, float (&s)[4]) {
+    s[0] = s[1] = s[2] = s[3] = 0.f;
+    if (vec && j + 3 < a.P_max) {
+      int g = 0;
+      for (; g + 8 <= a.Hkv; g += 8) {
+        float4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          x[u] = __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g + u) * a.P_max + j));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          s[0] += x[u].x;
+          s[1] += x[u].y;
+          s[2] += x[u].z;
+          s[3] += x[u].w;
+        }
+      }
+      for (; g < a.Hkv; ++g) {
+        const float4 x =
+            __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g) * a.P_max + j));
+        s[0] += x.x;
+        s[1] += x.y;
+        s[2] += x.z;
+        s[3] += x.w;
+      }
+    } else {
+      for (int g = 0; g < a.Hkv; ++g)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (j + u < a.P_max) s[u] += __ldg(base + static_cast<size_t>(g) * a.P_max + j + u);
+    }
+  };
+  const int my0 = rank * chunk + t * KPT;  // this thread's positions [my0, my0 + KPT)
+  float s_first[4];
+  sum4(my0, s_first);
+
   int P = __ldg(a.prefix_len + row);
   if (P < 0 || P > a.P_max) {
     if (t == 0 && rank == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
@@ -233,45 +274,19 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   const int rb = rb0 > sink_end ? rb0 : sink_end;  // candidates: [sink_end, rb)
   const int n_cand = rb - sink_end;
   const int r_need = n - (P - n_cand);
-  const int my0 = rank * chunk + t * KPT;  // this thread's positions [my0, my0 + KPT)
   const bool take_all = r_need >= n_cand;
   const bool ranking = r_need > 0 && !take_all;
 
-  // ---- A. aggregated scores, keys and the level-0 histogram of the candidates
+  // ---- A. keys and the level-0 histogram of the candidates
   if (ranking || a.scores_out != nullptr) {
-    const float* base = a.partial + static_cast<size_t>(row) * a.Hkv * a.P_max;
-    const bool vec = (a.P_max & 3) == 0;
     for (int q = 0; q < KPT; q += 4) {
       const int j = my0 + q;
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
-      if (vec && j + 3 < P) {
-        int g = 0;
-        for (; g + 8 <= a.Hkv; g += 8) {
-          float4 x[8];
+      float s[4];
+      if (q == 0) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            x[u] = __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g + u) * a.P_max + j));
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            s[0] += x[u].x;
-            s[1] += x[u].y;
-            s[2] += x[u].z;
-            s[3] += x[u].w;
-          }
-        }
-        for (; g < a.Hkv; ++g) {
-          const float4 x =
-              __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g) * a.P_max + j));
-          s[0] += x.x;
-          s[1] += x.y;
-          s[2] += x.z;
-          s[3] += x.w;
-        }
+        for (int u = 0; u < 4; ++u) s[u] = s_first[u];
       } else {
-        for (int g = 0; g < a.Hkv; ++g)
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (j + u < P) s[u] += __ldg(base + static_cast<size_t>(g) * a.P_max + j + u);
+        sum4(j, s);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {

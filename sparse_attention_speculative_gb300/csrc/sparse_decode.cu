@@ -451,21 +451,21 @@ __global__ void __launch_bounds__(kSThreads, 1) sparse_decode_kernel(const SPara
     }
   }
   if (direct) return;
-  // The last split of the pair to get here combines them all.  Every thread makes
-  // its partial stores visible GPU-wide before the CTA counts itself in; the
-  // counter goes back to zero for the next call.
+  // The last split of the pair to get here combines them all.  The CTA barrier orders
+  // every thread's partial stores before thread 0's acquire-release count, which
+  // publishes them GPU-wide; the last counter (acquire) sees every other split's, and
+  // the barrier after it extends that to the whole CTA.  The counter goes back to
+  // zero for the next call.
   __shared__ int s_last;
-  __threadfence();
   __syncthreads();  // also: every thread is done reading sm.wo
   if (threadIdx.x == 0) {
-    const unsigned old = atomicAdd(a.counters + pair, 1u);
+    const unsigned old = ptx::atom_add_acq_rel_gpu(a.counters + pair, 1u);
     const int last = old == static_cast<unsigned>(n_splits - 1);
-    if (last) atomicExch(a.counters + pair, 0u);
+    if (last) ptx::st_relaxed_gpu(a.counters + pair, 0u);
     s_last = last;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   merge_splits<D, G>(a, sm, pair, b, g, n_splits);
 }
 
