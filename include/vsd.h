@@ -190,8 +190,10 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
  *   idx        int32 [B][k_max] (may be NULL when k_max == 0)
  *   n_sel      int32 [B] (may be NULL when k_max == 0), 0 <= n_sel[b] <= k_max
  *   tail_start int32 [B]; seq_len int32 [B]; tail_start <= seq_len
- *   max_tail   host-side upper bound of seq_len[b] - tail_start[b]; it only
- *              sizes the split of the work, results do not depend on it
+ *   max_tail   host-side upper bound of seq_len[b] - tail_start[b]; it sizes
+ *              the split of the work (results do not depend on it); a sequence
+ *              whose list is longer than k_max + max_tail allows is flagged
+ *              VSD_DEV_BAD_LENGTH and gets a zero output
  *   out        bf16 [B][Hq][head_dim]
  *   workspace  >= vsd_sparse_workspace_size(...) bytes (0 bytes: may be NULL),
  *              256-byte aligned.  It starts with per-(sequence, KV head) counters

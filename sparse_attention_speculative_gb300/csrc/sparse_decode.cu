@@ -92,8 +92,12 @@ struct SList {
 __device__ __forceinline__ SList attended_list(int ns, int t0, int t1, const SParams& a,
                                                bool flag) {
   SList L;
+  // the list must fit the launch's splits: a tail longer than the declared max_tail
+  // is refused (flagged, nothing attended) rather than partly dropped
   const bool ok = ns >= 0 && ns <= a.k_max && t0 >= 0 && t0 <= t1 &&
-                  static_cast<long long>(t1) <= static_cast<long long>(a.max_blocks) * kPageS;
+                  static_cast<long long>(t1) <= static_cast<long long>(a.max_blocks) * kPageS &&
+                  static_cast<long long>(ns) + (t1 - t0) <=
+                      static_cast<long long>(a.split_len) * a.max_splits;
   if (!ok && flag) flag_status(a.status, VSD_DEV_BAD_LENGTH);
   L.ns = ok ? ns : 0;
   L.t0 = t0;

@@ -67,14 +67,16 @@ def _planted_positions(w: Workload, P_b: int, gen: torch.Generator, device) -> t
 
 
 def make_batch(w: Workload, device="cpu", layer: int = 0,
-               prefix_lens: Optional[List[int]] = None) -> Batch:
-    """Build one layer's seeded inputs for workload `w` on `device`."""
+               prefix_lens: Optional[List[int]] = None, extra_capacity: int = 0) -> Batch:
+    """Build one layer's seeded inputs for workload `w` on `device`.  Each sequence's
+    cache holds `extra_capacity` more tokens than one iteration needs (for loops that
+    append the accepted tokens of several iterations)."""
     device = torch.device(device)
     prefix = list(prefix_lens) if prefix_lens is not None else list(w.prefix())
     B, R, Hq, Hkv, d, page = w.B, w.R, w.Hq, w.Hkv, w.d, w.page
     assert len(prefix) == B and Hq % Hkv == 0
     G = Hq // Hkv
-    caps = [w.capacity(p) for p in prefix]
+    caps = [w.capacity(p) + extra_capacity for p in prefix]
     nblk = [math.ceil(c / page) for c in caps]
     max_blocks = max(nblk)
     NB = sum(nblk)
@@ -134,3 +136,21 @@ def host_arrays(batch: Batch) -> Dict[str, object]:
         block_table=batch.block_table.cpu().numpy(),
         prefix_len=batch.prefix_len.cpu().numpy(),
     )
+
+
+def seeded_bf16(shape, seed: int, device) -> torch.Tensor:
+    """N(0,1) values of `shape` from a generator seeded with `seed`, rounded to bf16."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return torch.randn(shape, generator=gen, device=device).to(torch.bfloat16)
+
+
+def write_tokens(batch: Batch, b: int, positions: torch.Tensor, k_rows: torch.Tensor,
+                 v_rows: torch.Tensor) -> None:
+    """Store K/V rows [n, Hkv, d] of sequence b at logical token positions (int64 [n])
+    through its block table (the cache append of a decode loop; plain indexing)."""
+    page = batch.k_cache.shape[2]
+    blocks = batch.block_table[b].to(torch.int64)[positions // page]
+    offs = positions % page
+    batch.k_cache[blocks, :, offs, :] = k_rows
+    batch.v_cache[blocks, :, offs, :] = v_rows

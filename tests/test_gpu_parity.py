@@ -285,6 +285,32 @@ def test_sparse_bad_index_is_flagged():
     assert vsd.vsd_read_device_status() & vsd.DEV_BAD_INDEX
 
 
+def test_sparse_tail_beyond_the_plan_is_refused():
+    """A tail longer than the launch was planned for (k_max + max_tail) must not be
+    partly attended: the sequence is flagged and gets a zero output."""
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("sptail", B=2, P=600, Hq=8, Hkv=2, d=128, gamma=1, k=8, n_sink=0, n_recent=0,
+                 seed=3)
+    batch = make_batch(w, "cuda")
+    tail_start = torch.tensor([0, 590], dtype=torch.int32, device="cuda")
+    seq_len = torch.tensor([300, 592], dtype=torch.int32, device="cuda")  # 300 > 1 split
+    out = vsd.vsd_sparse_decode_attn(batch.q_draft[0], batch.k_cache, batch.v_cache,
+                                     batch.block_table, None, None, tail_start, seq_len,
+                                     scale=w.scale, max_tail=2)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() & vsd.DEV_BAD_LENGTH
+    assert torch.count_nonzero(out[0]) == 0
+    # the other sequence is unaffected
+    from sparse_attention_speculative_gb300.synth import host_arrays, to_u16
+    h = host_arrays(batch)
+    ref = oracle.sparse_decode(to_u16(batch.q_draft[0]), h["k_cache"], h["v_cache"],
+                               h["block_table"], None, None, tail_start.cpu().numpy(),
+                               seq_len.cpu().numpy(), scale=w.scale)
+    assert_attn_close(out[1:].float().cpu().numpy(), ref[1:], "sparse output, valid sequence")
+
+
 def test_sparse_all_prefix_equals_verify_row():
     """k = P (all indices) sparse draft equals the full verify row it mirrors."""
     from sparse_attention_speculative_gb300.synth import make_batch
