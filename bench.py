@@ -390,61 +390,42 @@ def run_gpu(args, world, rank, local):
 
 
 def run_e2e(args, w, batch, vsd, dev, stream, workspace, prefix, total_bytes):
-    """Same iteration through the Python API with host (pinned) inputs and outputs:
-    H2D of the step's queries and lengths, the calls, D2H of every result."""
+    """The same iteration through the package's public iteration object: every step
+    copies the step's inputs from pinned host memory, runs verify -> select -> gamma
+    draft steps, and copies every result back to pinned host memory -- all recorded
+    once as a CUDA graph and replayed with one launch per step."""
     B, R, Hq, d, gamma = w.B, w.R, w.Hq, w.d, w.gamma
-    h_q = batch.q.cpu().pin_memory()
-    h_qd = batch.q_draft.cpu().pin_memory()
-    h_pl = batch.prefix_len.cpu().pin_memory()
+    it = vsd.IterationGraph(batch.k_cache, batch.v_cache, batch.block_table, B=B, R=R, Hq=Hq,
+                            gamma=gamma, P_max=w.P_max, k=w.k, n_sink=w.n_sink,
+                            n_recent=w.n_recent, max_tail=2 * gamma + 1, scale=w.scale)
+    it.h_q.copy_(batch.q.cpu())
+    it.h_q_draft.copy_(batch.q_draft.cpu())
+    it.h_prefix_len.copy_(batch.prefix_len.cpu())
+    it.h_tail_start.copy_(batch.prefix_len.cpu())
     rng = np.random.default_rng(w.seed + 91)
-    h_sl = torch.empty((gamma, B), dtype=torch.int32).pin_memory()
-    d_q = torch.empty_like(batch.q)
-    d_qd = torch.empty_like(batch.q_draft)
-    d_pl = torch.empty_like(batch.prefix_len)
-    d_sl = torch.empty((gamma, B), dtype=torch.int32, device=dev)
-    h_out = torch.empty((B, R, Hq, d), dtype=torch.bfloat16).pin_memory()
-    h_idx = torch.empty((B, w.k), dtype=torch.int32).pin_memory()
-    h_ns = torch.empty((B,), dtype=torch.int32).pin_memory()
-    h_dout = torch.empty((gamma, B, Hq, d), dtype=torch.bfloat16).pin_memory()
     flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_qd, h_pl, h_sl))
-    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_idx, h_ns, h_dout))
     times = []
-    for it in range(args.warmup + args.steps):
+    for step in range(args.warmup + args.steps):
         a = rng.integers(0, gamma + 1, size=B)
-        h_sl.copy_(torch.tensor([[prefix[b] + a[b] + 2 + i for b in range(B)]
-                                 for i in range(gamma)], dtype=torch.int32))
+        it.h_seq_len.copy_(torch.tensor([[prefix[b] + a[b] + 2 + i for b in range(B)]
+                                         for i in range(gamma)], dtype=torch.int32))
         flush_l2(flush_w, flush_r)
         torch.cuda.synchronize()
-        e0.record(stream)
-        d_q.copy_(h_q, non_blocking=True)
-        d_qd.copy_(h_qd, non_blocking=True)
-        d_pl.copy_(h_pl, non_blocking=True)
-        d_sl.copy_(h_sl, non_blocking=True)
-        out, _, partial = vsd.vsd_verify_attn_collect(
-            d_q, batch.k_cache, batch.v_cache, batch.block_table, d_pl, P_max=w.P_max,
-            scale=w.scale, workspace=workspace)
-        idx, n_sel, _ = vsd.vsd_select_topk(partial, d_pl, k=w.k, n_sink=w.n_sink,
-                                            n_recent=w.n_recent)
-        outs = [vsd.vsd_sparse_decode_attn(d_qd[i], batch.k_cache, batch.v_cache,
-                                           batch.block_table, idx, n_sel, d_pl, d_sl[i],
-                                           scale=w.scale, max_tail=2 * gamma + 1)
-                for i in range(gamma)]
-        h_out.copy_(out, non_blocking=True)
-        h_idx.copy_(idx, non_blocking=True)
-        h_ns.copy_(n_sel, non_blocking=True)
-        for i in range(gamma):
-            h_dout[i].copy_(outs[i], non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if it >= args.warmup:
+        with torch.cuda.stream(it.stream):
+            torch.cuda._sleep(2_000_000)  # the replay is queued before the GPU gets to it
+            e0.record(it.stream)
+            it.graph.replay()
+            e1.record(it.stream)
+        it.synchronize()
+        if step >= args.warmup:
             times.append(e0.elapsed_time(e1) * 1e-3)
     t = statistics.mean(times)
     return {"value": total_bytes / t / 1e9, "unit": "GB/s", "us_per_iter": t * 1e6,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "Python API, eager launches, pinned host buffers"}
+            "h2d_bytes_per_step": it.h2d_bytes, "d2h_bytes_per_step": it.d2h_bytes,
+            "path": "IterationGraph: pinned host inputs -> verify -> select -> %d draft steps "
+                    "-> pinned host results, one CUDA-graph replay per step" % gamma}
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm

@@ -4,10 +4,11 @@ The hot path is three C-ABI calls of ``libvsd.so`` (see ``include/vsd.h``):
 verification attention with Collect-2-Query, protected top-k selection over the
 aggregated logits, and the sparse draft-step attention.  This package holds the
 CUDA sources (``csrc/``), the in-tree build (``build.py``), the ctypes binding
-(``_lib.py``), the workload table (``workloads.py``) and the seeded input generators
-(``synth.py``).
+(``_lib.py``), one decode iteration as a CUDA graph (``iteration.py``), the workload
+table (``workloads.py``) and the seeded input generators (``synth.py``).
 """
 from ._lib import (DEV_BAD_BLOCK, DEV_BAD_INDEX, DEV_BAD_LENGTH, DEV_TIMEOUT, Geom,  # noqa: F401
                    VsdError, geom_for, load, vsd_read_device_status, vsd_select_topk,
                    vsd_sparse_decode_attn, vsd_sparse_workspace_size, vsd_verify_attn_collect,
                    vsd_verify_attn_collect_noalloc, vsd_verify_workspace_size)
+from .iteration import IterationGraph  # noqa: F401

@@ -376,3 +376,42 @@ def test_workspaces_are_left_ready_for_the_next_call():
         outs.append(o.clone())
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
     check_sparse(batch, w, idx, n_sel, tail, seq_len, max_tail=3)
+
+
+def test_iteration_graph_matches_eager_calls():
+    """The graph-recorded iteration (H2D copies, verify, select, draft steps, D2H copies)
+    gives bit-identical results to the same calls made one by one, twice in a row."""
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("graph", B=2, P=7000, Hq=32, Hkv=8, d=128, gamma=4, k=512, n_sink=16,
+                 n_recent=64, planted_frac=0.01, seed=31, prefix_lens=(7000, 4321))
+    batch = make_batch(w, "cuda")
+    it = vsd.IterationGraph(batch.k_cache, batch.v_cache, batch.block_table, B=w.B, R=w.R,
+                            Hq=w.Hq, gamma=w.gamma, P_max=w.P_max, k=w.k, n_sink=w.n_sink,
+                            n_recent=w.n_recent, max_tail=2 * w.gamma + 1, scale=w.scale)
+    it.h_q.copy_(batch.q.cpu())
+    it.h_q_draft.copy_(batch.q_draft.cpu())
+    it.h_prefix_len.copy_(batch.prefix_len.cpu())
+    it.h_tail_start.copy_(batch.prefix_len.cpu())
+    for rep, acc in enumerate(([1, 3], [4, 0])):
+        seq = torch.tensor([[P + a + 2 + i for P, a in zip(w.prefix(), acc)]
+                            for i in range(w.gamma)], dtype=torch.int32)
+        it.h_seq_len.copy_(seq)
+        it.run(sync=True)
+        assert vsd.vsd_read_device_status() == 0
+        out, _, partial = vsd.vsd_verify_attn_collect(
+            batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+            P_max=w.P_max, scale=w.scale)
+        idx, n_sel, _ = vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                            n_recent=w.n_recent)
+        seq_d = seq.cuda()
+        drafts = [vsd.vsd_sparse_decode_attn(batch.q_draft[i], batch.k_cache, batch.v_cache,
+                                             batch.block_table, idx, n_sel, batch.prefix_len,
+                                             seq_d[i], scale=w.scale, max_tail=2 * w.gamma + 1)
+                  for i in range(w.gamma)]
+        torch.cuda.synchronize()
+        assert torch.equal(it.h_out, out.cpu())
+        assert torch.equal(it.h_idx, idx.cpu()) and torch.equal(it.h_n_sel, n_sel.cpu())
+        for i in range(w.gamma):
+            assert torch.equal(it.h_draft_out[i], drafts[i].cpu()), "draft step %d" % i
