@@ -52,12 +52,14 @@ def _load():
             D = ctypes.c_double
             lib.oracle_verify.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, I, I, I, D,
                                           P, P, P]
+            lib.oracle_verify_all_rows.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, I,
+                                                   D, P, P, P]
             lib.oracle_score_from_logits.argtypes = [I, I, I, P, P, P]
             lib.oracle_score_from_partials.argtypes = [I, I, I, P, P, P]
             lib.oracle_select.argtypes = [I, I, P, P, I, I, I, P, P]
             lib.oracle_sparse_decode.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, I, P,
                                                  P, D, P]
-            for name in ("oracle_verify", "oracle_score_from_logits",
+            for name in ("oracle_verify", "oracle_verify_all_rows", "oracle_score_from_logits",
                          "oracle_score_from_partials", "oracle_select", "oracle_sparse_decode",
                          "oracle_num_threads"):
                 getattr(lib, name).restype = ctypes.c_int
@@ -125,6 +127,29 @@ def verify(q, k_cache, v_cache, block_table, prefix_len, *, scale, P_max,
                                _ptr(logits) if collect else None,
                                _ptr(partial) if collect else None, _ptr(out))
     _check(rc, "oracle_verify")
+    return out, logits, partial
+
+
+def verify_all_rows(q, k_cache, v_cache, block_table, prefix_len, *, scale, P_max):
+    """Full-attention verification collecting every verify row (the selection equation
+    as printed).  Returns (out [B,R,Hq,d], logits [B,R,Hq,P_max], partial [B,Hkv,P_max])
+    as float64; positions j >= P_b of logits/partial are 0."""
+    q = _u16(q)
+    k_cache = _u16(k_cache)
+    v_cache = _u16(v_cache)
+    bt = _i32(block_table)
+    pl = _i32(prefix_len)
+    B, R, Hq, d = q.shape
+    NB, Hkv, page, d2 = k_cache.shape
+    assert d2 == d and v_cache.shape == k_cache.shape and bt.shape[0] == B
+    out = np.zeros((B, R, Hq, d), dtype=np.float64)
+    logits = np.zeros((B, R, Hq, P_max), dtype=np.float64)
+    partial = np.zeros((B, Hkv, P_max), dtype=np.float64)
+    rc = _load().oracle_verify_all_rows(B, Hq, Hkv, d, page, bt.shape[1], NB, R, _ptr(q),
+                                        _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(pl),
+                                        int(P_max), float(scale), _ptr(logits), _ptr(partial),
+                                        _ptr(out))
+    _check(rc, "oracle_verify_all_rows")
     return out, logits, partial
 
 

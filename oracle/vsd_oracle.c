@@ -31,6 +31,7 @@
  *   block_table  [B][max_blocks]          logical page p of sequence b lives in
  *                                         physical block block_table[b][p]
  *   logits       [B][2][Hq][P_max]        pre-softmax (scaled) logits, j < P_b
+ *                [B][R][Hq][P_max]        (every verify row: oracle_verify_all_rows)
  *   partial      [B][Hkv][P_max]          sum over the two collected rows and the
  *                                         query heads of one KV group
  *   score        [n_rows][P_max]          sum over rows and all query heads
@@ -189,6 +190,78 @@ int oracle_verify(int B, int Hq, int Hkv, int d, int page, int max_blocks, int n
                 for (int which = 0; which < 2; ++which)
                     for (int h = g * G; h < (g + 1) * G; ++h)
                         s += logits[(((size_t)b * 2 + which) * Hq + h) * P_max + j];
+                prow[j] = s;
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Verification with every verify row collected (the selection equation as printed).
+ *   [Vegas] sec. 2.A: the objective sums the logits over the draft rows t = 1..gamma+1
+ *   of the verification block and over the query heads; sec. 2.B (Collect-2-Query)
+ *   keeps two of those rows, which is what oracle_verify collects.  This variant keeps
+ *   all R of them, the reference Collect-2-Query is measured against.
+ * Outputs: out[b][t][h][:] as oracle_verify; logits[b][t][h][j] for every row t and
+ * j < P_b; partial[b][g][j] = sum over t < R and h in group g of logits[b][t][h][j].
+ * logits / partial may be NULL (partial needs logits).
+ */
+int oracle_verify_all_rows(int B, int Hq, int Hkv, int d, int page, int max_blocks,
+                           int num_blocks, int R, const uint16_t *q, const uint16_t *k_cache,
+                           const uint16_t *v_cache, const int32_t *block_table,
+                           const int32_t *prefix_len, int P_max, double scale, double *logits,
+                           double *partial, double *out) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page <= 0 || R <= 0)
+        return ORACLE_BAD_ARG;
+    if (partial && !logits) return ORACLE_BAD_ARG;
+    const int G = Hq / Hkv;
+    int status = ORACLE_OK;
+    const int n_items = B * R * Hq;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int item = 0; item < n_items; ++item) {
+        int b = item / (R * Hq);
+        int t = (item / Hq) % R;
+        int h = item % Hq;
+        int g = h / G;
+        int P = prefix_len[b];
+        if (P < 0 || P > P_max) { status = ORACLE_BAD_ARG; continue; }
+        int n_keys = P + t + 1;
+        int *pos = (int *)malloc(sizeof(int) * (size_t)n_keys);
+        double *z = (double *)malloc(sizeof(double) * (size_t)n_keys);
+        double *qv = (double *)malloc(sizeof(double) * (size_t)d);
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!pos || !z || !qv || !o) {
+            status = ORACLE_NO_MEMORY;
+        } else {
+            for (int j = 0; j < n_keys; ++j) pos[j] = j;
+            const uint16_t *qr = q + (((size_t)b * R + t) * Hq + h) * d;
+            for (int c = 0; c < d; ++c) qv[c] = bf16_to_double(qr[c]);
+            int rc = attend(qv, d, pos, n_keys, k_cache, v_cache, block_table, b, max_blocks,
+                            num_blocks, Hkv, page, g, scale, o, z);
+            if (rc != ORACLE_OK) {
+                status = rc;
+            } else {
+                double *dst = out + (((size_t)b * R + t) * Hq + h) * d;
+                for (int c = 0; c < d; ++c) dst[c] = o[c];
+                if (logits) {
+                    double *lrow = logits + (((size_t)b * R + t) * Hq + h) * P_max;
+                    for (int j = 0; j < P; ++j) lrow[j] = z[j];
+                }
+            }
+        }
+        free(pos); free(z); free(qv); free(o);
+    }
+    if (status != ORACLE_OK || !partial) return status;
+    for (int b = 0; b < B; ++b) {
+        int P = prefix_len[b];
+        for (int g = 0; g < Hkv; ++g) {
+            double *prow = partial + ((size_t)b * Hkv + g) * P_max;
+            for (int j = 0; j < P; ++j) {
+                double s = 0.0;
+                for (int t = 0; t < R; ++t)
+                    for (int h = g * G; h < (g + 1) * G; ++h)
+                        s += logits[(((size_t)b * R + t) * Hq + h) * P_max + j];
                 prow[j] = s;
             }
         }

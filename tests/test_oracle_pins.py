@@ -175,6 +175,35 @@ def test_verify_logits_closed_form():
                                    want_s, rtol=0, atol=1e-9)
 
 
+def test_verify_all_rows_closed_form():
+    """Every verify row collected (the selection equation summed over all gamma+1 rows):
+    each row's logits and the per-group sum over all rows against the closed form."""
+    s = _structured_verify(R=4)
+    scale = 1.0 / math.sqrt(s["d"])
+    P_max = 64
+    out, logits, partial = oracle.verify_all_rows(s["q"], s["k"], s["v"], s["table"],
+                                                  s["prefix"], scale=scale, P_max=P_max)
+    R, Hq, G, Hkv = s["R"], s["Hq"], s["G"], s["Hkv"]
+    assert logits.shape == (2, R, Hq, P_max)
+    for b, P in enumerate(s["prefix"]):
+        j = np.arange(P)
+        for t in range(R):
+            for h in range(Hq):
+                want = scale * ((t + 1) * ((j % 7) - 3) + (h + 1) * (h // G + 1) + (b + 1))
+                np.testing.assert_allclose(logits[b, t, h, :P], want, rtol=0, atol=1e-12)
+        assert np.all(logits[b, :, :, P:] == 0)
+        for g in range(Hkv):
+            want = np.zeros(P)
+            for t in range(R):
+                for h in range(g * G, (g + 1) * G):
+                    want += scale * ((t + 1) * ((j % 7) - 3) + (h + 1) * (g + 1) + (b + 1))
+            np.testing.assert_allclose(partial[b, g, :P], want, rtol=0, atol=1e-10)
+    # the attention output does not depend on what is collected
+    out2, _, _ = oracle.verify(s["q"], s["k"], s["v"], s["table"], s["prefix"], scale=scale,
+                               P_max=P_max)
+    np.testing.assert_array_equal(out, out2)
+
+
 def test_verify_collects_requested_rows():
     s = _structured_verify(R=4)
     scale = 1.0 / math.sqrt(s["d"])
