@@ -305,6 +305,23 @@ def run_gpu(args, world, rank, local):
             v1.record(stream)
             torch.cuda.synchronize()
             per["verify_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
+        # the same, collecting every verify row (the selection equation as printed):
+        # what Collect-2-Query saves
+        per["verify_all_b2b"] = []
+        if R * (Hq // w.Hkv) <= 48:
+            logits_all = torch.empty((B, R, Hq, P_max), dtype=torch.float32, device=dev)
+            for _ in range(3):
+                torch.cuda.synchronize()
+                torch.cuda._sleep(sleep_cycles)
+                v0.record(stream)
+                for _ in range(B2B_CALLS):
+                    vsd.vsd_verify_attn_collect_all(batch.q, batch.k_cache, batch.v_cache,
+                                                    batch.block_table, batch.prefix_len,
+                                                    P_max=P_max, scale=w.scale, logits=logits_all,
+                                                    partial=partial, out=out, workspace=workspace)
+                v1.record(stream)
+                torch.cuda.synchronize()
+                per["verify_all_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -367,6 +384,13 @@ def run_gpu(args, world, rank, local):
         "kernels": kernels,
         "select_over_verify": t_select / t_verify,
         "verify_back_to_back_us": t_verify_b2b * 1e6,
+        "collect2_vs_all_rows": None if not per["verify_all_b2b"] else {
+            "collect2_us": t_verify_b2b * 1e6,
+            "all_rows_us": statistics.median(per["verify_all_b2b"]) * 1e6,
+            "logits_bytes_collect2": sum(2 * Hq * P * 4 for P in prefix),
+            "logits_bytes_all_rows": sum(R * Hq * P * 4 for P in prefix),
+            "note": "back-to-back calls; all rows = every verify row's logits written and "
+                    "summed (the selection equation as printed)"},
         "roofline": {"bound": "hbm", "kernel": "vsd_verify_attn_collect",
                      "timing": "%d verification calls back to back between two events on "
                                "the launching stream (K/V larger than L2), per-call mean; "
@@ -376,7 +400,8 @@ def run_gpu(args, world, rank, local):
                      "traffic": profile_traffic(w.name)},
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_all_timed_loops": (2 * launches_per_step * args.steps +
-                                         3 * B2B_CALLS * launches_per_verify),
+                                         (6 if per["verify_all_b2b"] else 3) * B2B_CALLS *
+                                         launches_per_verify),
         "gpu_launches_per_step": launches_per_step,
         "clocks": clk,
         # the device timestamps only measure kernels if the host finished enqueueing a

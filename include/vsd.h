@@ -116,6 +116,28 @@ vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------
+ * Verification attention collecting every verify row (Vegas summary sec. 2.A: the
+ * selection equation sums the logits over all gamma+1 rows of the verification
+ * block and over the query heads; Collect-2-Query, sec. 2.B, keeps two of them).
+ * This is the reference against which Collect-2-Query's savings are measured.
+ *
+ * Same attention, arguments and workspace as vsd_verify_attn_collect, except:
+ *   logits[b,t,h,j] = z[b,t,h,j]                          t in [0, R), j < P_b
+ *   partial_scores[b,g,j] = sum_{t < R} sum_{h in group g} logits[b,t,h,j]
+ *
+ *   logits         fp32 [B][R][Hq][P_max] or NULL; only j < P_b are written
+ *   partial_scores fp32 [B][Hkv][P_max] or NULL; only j < P_b are written
+ * Supported: as vsd_verify_attn_collect with R * G <= 48 (VSD_ERR_UNSUPPORTED
+ * otherwise).
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_verify_attn_collect_all(const vsd_geom* geom, int R, const void* q,
+                                       const void* k_cache, const void* v_cache,
+                                       const int32_t* block_table, const int32_t* prefix_len,
+                                       int P_max, float scale, float* logits,
+                                       float* partial_scores, void* out, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------
  * Verification attention without a caller-provided workspace.  The pages have no
  * counterpart: this is a convenience of this library.
  *

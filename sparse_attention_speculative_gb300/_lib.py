@@ -65,6 +65,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_verify_attn_collect.argtypes = [GP, I, P, P, P, P, P, I, I, I, F, P, P, P, P, SZ, P]
         lib.vsd_verify_attn_collect_noalloc.argtypes = [GP, I, P, P, P, P, P, I, I, I, F, P, P,
                                                         P, P]
+        lib.vsd_verify_attn_collect_all.argtypes = [GP, I, P, P, P, P, P, I, F, P, P, P, P, SZ,
+                                                    P]
         lib.vsd_select_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(SZ)]
         lib.vsd_select_topk.argtypes = [I, I, P, P, I, I, I, I, P, P, P, P, SZ, P]
         lib.vsd_sparse_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
@@ -74,6 +76,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_get_error_string.restype = ctypes.c_char_p
         lib.vsd_last_cuda_error.argtypes = []
         for name in ("vsd_verify_workspace_size", "vsd_verify_attn_collect",
+                     "vsd_verify_attn_collect_all",
                      "vsd_verify_attn_collect_noalloc",
                      "vsd_select_workspace_size", "vsd_select_topk", "vsd_sparse_workspace_size",
                      "vsd_sparse_decode_attn", "vsd_read_device_status", "vsd_last_cuda_error"):
@@ -167,6 +170,38 @@ def vsd_verify_attn_collect(q, k_cache, v_cache, block_table, prefix_len, *, P_m
                                      _ptr(logits), _ptr(partial), _ptr(out), _ptr(workspace),
                                      ws_bytes, _stream(stream))
     _check(rc, "vsd_verify_attn_collect")
+    return out, logits, partial
+
+
+def vsd_verify_attn_collect_all(q, k_cache, v_cache, block_table, prefix_len, *, P_max: int,
+                                scale: float, logits=None, partial=None, out=None,
+                                collect: bool = True, workspace=None, stream=None):
+    """Verification collecting every verify row (logits fp32 [B, R, Hq, P_max]; the
+    partial scores sum all R rows).  Returns (out, logits, partial)."""
+    lib = load()
+    B, R, Hq, d = q.shape
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(block_table, torch.int32, "block_table")
+    _need(prefix_len, torch.int32, "prefix_len")
+    geom = geom_for(B, Hq, k_cache, block_table)
+    dev = q.device
+    if out is None:
+        out = torch.empty_like(q)
+    if collect:
+        if logits is None:
+            logits = torch.empty((B, R, Hq, P_max), dtype=torch.float32, device=dev)
+        if partial is None:
+            partial = torch.empty((B, geom.Hkv, P_max), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = _workspace(vsd_verify_workspace_size(geom, R, P_max), dev, "verify")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.vsd_verify_attn_collect_all(ctypes.byref(geom), R, _ptr(q), _ptr(k_cache),
+                                         _ptr(v_cache), _ptr(block_table), _ptr(prefix_len),
+                                         int(P_max), float(scale), _ptr(logits), _ptr(partial),
+                                         _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc, "vsd_verify_attn_collect_all")
     return out, logits, partial
 
 

@@ -33,6 +33,7 @@ struct VerifyArgs {
   unsigned* status;
   int B, Hq, Hkv, G, R, d, max_blocks, num_blocks, P_max;
   int row0, row1;
+  int collect_all;  // 1: every verify row's logits, partial summed over all rows
   float scale;
 };
 

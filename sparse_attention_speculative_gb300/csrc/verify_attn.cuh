@@ -92,6 +92,7 @@ struct VParams {
   unsigned* status;
   int B, Hq, Hkv, R, NV, max_blocks, num_blocks, P_max;
   int row0, row1;
+  int collect_all;  // every verify row collected; partial sums over all rows
   int pairs, t_max, max_chunks;
   float scale;
 };
@@ -414,7 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float scale = a.scale;
     const float scale_log2 = a.scale * kLog2e;
-    const bool collect = a.logits != nullptr || a.partial != nullptr;
+    const bool collect_any = a.logits != nullptr || a.partial != nullptr;
+    constexpr bool kAllFits = NQ * D * 2 + 2 * kTile * 4 <= Cfg::kQBytesMax;
+    const bool collect_all = kAllFits && collect_any && a.collect_all != 0;
+    const bool collect = collect_any && !collect_all;  // the two chosen rows
+    // all rows: the upper column half's per-key sums reach the lower half through
+    // [2][kTile] floats after the Q rows (NQ <= 48 leaves that much of the area free)
+    float* xsum = reinterpret_cast<float*>(q_smem + NQ * D * 2);
     uint32_t it = 0;
     for (long long v = v0; v < v1;) {
       // Loads that need no prefix length go out first: the segment's Q rows and this
@@ -527,6 +534,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (a.partial) a.partial[(static_cast<size_t>(s.b) * a.Hkv + s.g) * a.P_max + j] = acc;
         }
+        // all rows: every column of this thread, then the two halves' sums
+        float call = 0.f;
+        if (collect_all && j < s.P) {
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            const int cc = col0 + c;
+            if (cc < a.NV) {
+              const float z = sv[c] * scale;
+              if (a.logits)
+                __stcs(a.logits + ((static_cast<size_t>(s.b) * a.R + cc / G) * a.Hq + s.g * G +
+                                   cc % G) * a.P_max + j, z);
+              call += z;
+            }
+          }
+          if (half == 1) xsum[(it & 1) * kTile + row] = call;
+        }
 
         // d = y - m2 in log2 units (y = scaled logit); masks only where a key can be hidden
         const bool bad = entry < 0 || entry >= a.num_blocks;
@@ -542,7 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float d = fmaf(sv[c], scale_log2, -m2[c]);
           if (!masked || col0 + c >= c_lo) dmax = fmaxf(dmax, d);
         }
-        if (softmax_vote(dmax > kTau)) {
+        const bool raise = softmax_vote(dmax > kTau);  // also orders the xsum stores
+        if (collect_all && half == 0 && j < s.P && a.partial)
+          a.partial[(static_cast<size_t>(s.b) * a.Hkv + s.g) * a.P_max + j] =
+              call + xsum[(it & 1) * kTile + row];
+        if (raise) {
           // rare: some visible logit is far above its column's running max
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
@@ -794,6 +821,7 @@ inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {
   p.P_max = va.P_max;
   p.row0 = va.row0;
   p.row1 = va.row1;
+  p.collect_all = va.collect_all;
   p.pairs = plan.pairs;
   p.t_max = plan.t_max;
   p.max_chunks = plan.max_chunks;

@@ -159,14 +159,19 @@ vsd_status vsd_verify_workspace_size(const vsd_geom* geom, int R, int P_max, siz
   return VSD_OK;
 }
 
-vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
-                                   const void* k_cache, const void* v_cache,
-                                   const int32_t* block_table, const int32_t* prefix_len,
-                                   int collect_row0, int collect_row1, int P_max, float scale,
-                                   float* logits, float* partial_scores, void* out,
-                                   void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+vsd_status verify_call(const vsd_geom* geom, int R, const void* q, const void* k_cache,
+                       const void* v_cache, const int32_t* block_table,
+                       const int32_t* prefix_len, bool collect_all, int collect_row0,
+                       int collect_row1, int P_max, float scale, float* logits,
+                       float* partial_scores, void* out, void* workspace,
+                       size_t workspace_bytes, void* stream) {
   vsd_status st = verify_checks(geom, R, P_max);
   if (st != VSD_OK) return st;
+  // all rows: the two halves of every key's columns meet in the part of the Q
+  // staging area that 64 query rows would need and 48 leave free
+  if (collect_all && R * (geom->Hq / geom->Hkv) > 48) return VSD_ERR_UNSUPPORTED;
   if (geom->B == 0) return VSD_OK;
   if (!q || !k_cache || !v_cache || !block_table || !prefix_len || !out)
     return VSD_ERR_INVALID_ARG;
@@ -174,7 +179,7 @@ vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
       !aligned(logits, 16) || !aligned(partial_scores, 16) || !aligned(block_table, 4) ||
       !aligned(prefix_len, 4))
     return VSD_ERR_INVALID_ARG;
-  if ((logits || partial_scores) &&
+  if (!collect_all && (logits || partial_scores) &&
       (collect_row0 < 0 || collect_row0 >= R || collect_row1 < 0 || collect_row1 >= R))
     return VSD_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return VSD_ERR_INVALID_ARG;
@@ -209,12 +214,36 @@ vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
   va.max_blocks = geom->max_blocks_per_seq;
   va.num_blocks = geom->num_blocks;
   va.P_max = P_max;
-  va.row0 = collect_row0;
-  va.row1 = collect_row1;
+  va.row0 = collect_all ? 0 : collect_row0;
+  va.row1 = collect_all ? 0 : collect_row1;
+  va.collect_all = collect_all ? 1 : 0;
   va.scale = scale;
   cudaError_t e = vsd::launch_verify(va, plan, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return VSD_OK;
+}
+
+}  // namespace
+
+vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
+                                   const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, const int32_t* prefix_len,
+                                   int collect_row0, int collect_row1, int P_max, float scale,
+                                   float* logits, float* partial_scores, void* out,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  return verify_call(geom, R, q, k_cache, v_cache, block_table, prefix_len, false,
+                     collect_row0, collect_row1, P_max, scale, logits, partial_scores, out,
+                     workspace, workspace_bytes, stream);
+}
+
+vsd_status vsd_verify_attn_collect_all(const vsd_geom* geom, int R, const void* q,
+                                       const void* k_cache, const void* v_cache,
+                                       const int32_t* block_table, const int32_t* prefix_len,
+                                       int P_max, float scale, float* logits,
+                                       float* partial_scores, void* out, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  return verify_call(geom, R, q, k_cache, v_cache, block_table, prefix_len, true, 0, 0, P_max,
+                     scale, logits, partial_scores, out, workspace, workspace_bytes, stream);
 }
 
 vsd_status vsd_select_workspace_size(int n_rows, int Hkv, int P_max, int k, size_t* bytes) {

@@ -89,3 +89,12 @@ def test_sparse_rejects_missing_index_arrays(lib):
     rc = lib.vsd_sparse_decode_attn(ctypes.byref(g), p, p, p, p, None, None, 16, p, p, 0,
                                     ctypes.c_float(0.088), p, None, 0, None)
     assert rc == -1
+
+
+def test_collect_all_rejects_wide_groups(lib):
+    # the all-rows variant supports R * G <= 48; G = 8 with R = 8 is 64
+    geom = _geom(Hq=64, Hkv=8)
+    rc = lib.vsd_verify_attn_collect_all(ctypes.byref(geom), 8, None, None, None, None, None,
+                                         1024, ctypes.c_float(0.1), None, None, None, None, 0,
+                                         None)
+    assert rc == -2

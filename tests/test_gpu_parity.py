@@ -415,3 +415,39 @@ def test_iteration_graph_matches_eager_calls():
         assert torch.equal(it.h_idx, idx.cpu()) and torch.equal(it.h_n_sel, n_sel.cpu())
         for i in range(w.gamma):
             assert torch.equal(it.h_draft_out[i], drafts[i].cpu()), "draft step %d" % i
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,gamma,prefix", [
+    (128, 32, 8, 4, (4000, 129, 0)),     # Qwen3-8B geometry: R*G = 20
+    (128, 16, 2, 5, (3001, 1000, 128)),  # R*G = 48, the largest supported
+    (64, 8, 8, 3, (127, 2049, 777)),     # G = 1
+])
+def test_verify_collect_all_rows(d, Hq, Hkv, gamma, prefix):
+    """Every verify row collected and the partial score summed over all rows (the
+    selection equation as printed), against the all-rows oracle; the attention output
+    is the same as with Collect-2-Query."""
+    from sparse_attention_speculative_gb300.synth import host_arrays, make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("all", B=len(prefix), P=max(prefix), Hq=Hq, Hkv=Hkv, d=d, gamma=gamma, k=64,
+                 n_sink=4, n_recent=16, seed=41, prefix_lens=prefix)
+    batch = make_batch(w, "cuda")
+    out, logits, partial = vsd.vsd_verify_attn_collect_all(
+        batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+        P_max=w.P_max, scale=w.scale)
+    out2, _, _ = vsd.vsd_verify_attn_collect(batch.q, batch.k_cache, batch.v_cache,
+                                             batch.block_table, batch.prefix_len, P_max=w.P_max,
+                                             scale=w.scale)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    assert torch.equal(out, out2)
+    h = host_arrays(batch)
+    o_ref, l_ref, p_ref = oracle.verify_all_rows(h["q"], h["k_cache"], h["v_cache"],
+                                                 h["block_table"], h["prefix_len"],
+                                                 scale=w.scale, P_max=w.P_max)
+    assert_attn_close(out.float().cpu().numpy(), o_ref, "all-rows verify output")
+    lg, pa = logits.cpu().numpy(), partial.cpu().numpy()
+    for b, P in enumerate(prefix):
+        assert_rel_close(lg[b, :, :, :P], l_ref[b, :, :, :P], "all-rows logits")
+        assert_rel_close(pa[b, :, :P], p_ref[b, :, :P], "all-rows partial scores")
+
