@@ -64,15 +64,21 @@ constexpr int kThreads = 96 + kSoftmaxThreads;
 constexpr int kVWarp = 10;
 constexpr int kSoftmaxBar = 1;  // named barrier of the softmax threads
 
-template <int D>
+// Shared-memory plan for head dimension D and NQ verify columns.  P^T is always
+// double-buffered: for NQ <= 32 the two buffers are the two halves of each 128-byte
+// row of one region; for wider NQ they are two regions, paid for with one V stage.
+template <int D, int NQ>
 struct VCfg {
-  static constexpr int kStages = (D == 128) ? 3 : 5;  // depth of each of the K and V rings
+  static constexpr int kStagesK = (D == 128) ? 3 : 5;  // depth of the K ring
+  static constexpr bool kSplitP = NQ <= 32;             // P buffers share 128-byte rows
+  static constexpr int kStagesV = kSplitP ? kStagesK : kStagesK - 1;  // depth of the V ring
   static constexpr int kKVBytes = kTile * D * 2;      // K (or V) of one tile
   static constexpr int kHalfBytes = kTile * 128;      // 64-column half of a tile
   static constexpr int kQBytesMax = 64 * D * 2;
-  static constexpr int kPBytes = kTile * 128;
-  static constexpr int kOffV = kStages * kKVBytes;
-  static constexpr int kOffQ = kOffV + kStages * kKVBytes;
+  static constexpr int kPRegion = kTile * 128;         // one 128 keys x 128 B region
+  static constexpr int kPBytes = kSplitP ? kPRegion : 2 * kPRegion;
+  static constexpr int kOffV = kStagesK * kKVBytes;
+  static constexpr int kOffQ = kOffV + kStagesV * kKVBytes;
   static constexpr int kOffP = kOffQ + kQBytesMax;
   static constexpr int kOffMisc = kOffP + kPBytes;
   static constexpr int kMiscBytes = 1920;
@@ -165,10 +171,11 @@ template <int D, int NQ, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_attn_collect_kernel(const __grid_constant__ CUtensorMap kmap,
                                const __grid_constant__ CUtensorMap vmap, const VParams a) {
-  using Cfg = VCfg<D>;
-  constexpr int S = Cfg::kStages;
-  constexpr int NC = NQ / 2;              // columns per softmax thread
-  constexpr int PB = (NQ <= 32) ? 2 : 1;  // P^T buffers: two halves of each 128-byte row
+  using Cfg = VCfg<D, NQ>;
+  constexpr int SK = Cfg::kStagesK;
+  constexpr int SV = Cfg::kStagesV;
+  constexpr int NC = NQ / 2;  // columns per softmax thread
+  constexpr int PB = 2;       // P^T buffers
   static_assert(NQ % 16 == 0 && NQ <= 64, "NQ");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -179,13 +186,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* p_smem = base + Cfg::kOffP;
   uint8_t* misc = base + Cfg::kOffMisc;
   uint64_t* k_full = reinterpret_cast<uint64_t*>(misc);
-  uint64_t* k_empty = k_full + S;
-  uint64_t* v_full = k_empty + S;
-  uint64_t* v_empty = v_full + S;
-  uint64_t* s_full = v_empty + S;     // [2]
+  uint64_t* k_empty = k_full + SK;
+  uint64_t* v_full = k_empty + SK;
+  uint64_t* v_empty = v_full + SV;
+  uint64_t* s_full = v_empty + SV;    // [2]
   uint64_t* s_empty = s_full + 2;     // [2]
-  uint64_t* p_full = s_empty + 2;     // [2] (PB used)
-  uint64_t* pv_done = p_full + 2;     // [2] (PB used)
+  uint64_t* p_full = s_empty + 2;     // [2]
+  uint64_t* pv_done = p_full + 2;     // [2]
   uint64_t* q_ready = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
@@ -197,9 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < SV; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
@@ -247,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = is_k ? k_ring : v_ring;
     uint64_t* full = is_k ? k_full : v_full;
     uint64_t* empty = is_k ? k_empty : v_empty;
+    const int S = is_k ? SK : SV;  // depth of this warp's ring
     const uint64_t pol = l2_policy_evict_first();
     if (lane == 0) tma_prefetch_desc(map);
     uint32_t it = 0, issued = 0;
@@ -335,12 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool progressed = false;
         // ---- PV of tile pi (accumulates unless first of its segment)
         if (pi < qi && mbar_test(&p_full[pi % PB], (pi / PB) & 1) &&
-            mbar_test(&v_full[pi % S], (pi / S) & 1)) {
+            mbar_test(&v_full[pi % SV], (pi / SV) & 1)) {
           tc_fence_after();
-          const int stage_i = static_cast<int>(pi % S);
+          const int stage_i = static_cast<int>(pi % SV);
           const bool first_i = (first_bits >> (pi & 31)) & 1u;
           const uint32_t v_addr = v_addr0 + stage_i * Cfg::kKVBytes;
-          const uint32_t pb_addr = p_addr + (pi % PB) * 64;
+          const uint32_t pb_addr =
+              p_addr + (pi % PB) * (Cfg::kSplitP ? 64u : static_cast<uint32_t>(Cfg::kPRegion));
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint64_t adesc = sdesc_sw128(v_addr + kk * 2048, Cfg::kHalfBytes, 1024);
@@ -360,10 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             q_tile = qs.t_begin;
           }
           const bool first = q_tile == qs.t_begin;
-          const int stage = static_cast<int>(qi % S);
+          const int stage = static_cast<int>(qi % SK);
           const int buf = qi & 1;
           const bool ready = (!first || mbar_test(q_ready, nseg & 1)) &&
-                             mbar_test(&k_full[stage], (qi / S) & 1) &&
+                             mbar_test(&k_full[stage], (qi / SK) & 1) &&
                              (qi < 2 || mbar_test(&s_empty[buf], ((qi >> 1) - 1) & 1));
           if (ready) {
             tc_fence_after();
@@ -422,6 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // all rows: the upper column half's per-key sums reach the lower half through
     // [2][kTile] floats after the Q rows (NQ <= 48 leaves that much of the area free)
     float* xsum = reinterpret_cast<float*>(q_smem + NQ * D * 2);
+    // two rows: where that area exists the lower half writes row0 and the upper half
+    // row1 (their sums meet there too), else the lower half writes both
+    const bool split_collect = kAllFits && collect;
     uint32_t it = 0;
     for (long long v = v0; v < v1;) {
       // Loads that need no prefix length go out first: the segment's Q rows and this
@@ -491,20 +505,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       int entry_next =
           (s.t_begin < s.t_end && s.t_begin * kTile + row < s.L) ? entry_first : 0;
       for (int tile = s.t_begin; tile < s.t_end; ++tile, ++it) {
-        const int stage = it % S;
+        const int stage = it % SV;  // V stage of this tile (masked rows are zeroed there)
         const int buf = it & 1;
         const int pb = it % PB;
         const int entry = entry_next;
         entry_next = page_entry(tile + 1);
         if (!mbar_wait(&s_full[buf], (it >> 1) & 1, abort_flag)) set_abort();
         const int j = tile * kTile + row;
-        const bool want_collect = collect && half == 0 && j < s.P;
+        const bool want_collect = collect && !split_collect && half == 0 && j < s.P;
         tc_fence_after();
         const uint32_t s_addr = tmem_s0 + buf * 64 + lane_addr;
         float sv[NC];
         uint32_t c0raw[G], c1raw[G];
         tmem_ld_cols<NC>(s_addr + col0, reinterpret_cast<uint32_t*>(sv));
-        if (collect && half == 0) {
+        if (split_collect) {
+          // warp-uniform: each half reads its collected row
+          tmem_ld<G>(s_addr + (half == 0 ? a.row0 : a.row1) * G, c0raw);
+        } else if (collect && half == 0) {
           // warp-uniform: the lower-half warps read the two collected rows
           tmem_ld<G>(s_addr + a.row0 * G, c0raw);
           tmem_ld<G>(s_addr + a.row1 * G, c1raw);
@@ -534,8 +551,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (a.partial) a.partial[(static_cast<size_t>(s.b) * a.Hkv + s.g) * a.P_max + j] = acc;
         }
-        // all rows: every column of this thread, then the two halves' sums
+        // all rows: every column of this thread, then the two halves' sums; two rows
+        // split between the halves: this half's row, then the two halves' sums
         float call = 0.f;
+        if (split_collect && j < s.P) {
+#pragma unroll
+          for (int hl = 0; hl < G; ++hl) {
+            const float z = __uint_as_float(c0raw[hl]) * scale;
+            if (a.logits)
+              __stcs(a.logits + ((static_cast<size_t>(s.b) * 2 + half) * a.Hq + s.g * G + hl) *
+                                    a.P_max + j, z);
+            call += z;
+          }
+          if (half == 1) xsum[(it & 1) * kTile + row] = call;
+        }
         if (collect_all && j < s.P) {
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
@@ -566,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!masked || col0 + c >= c_lo) dmax = fmaxf(dmax, d);
         }
         const bool raise = softmax_vote(dmax > kTau);  // also orders the xsum stores
-        if (collect_all && half == 0 && j < s.P && a.partial)
+        if ((collect_all || split_collect) && half == 0 && j < s.P && a.partial)
           a.partial[(static_cast<size_t>(s.b) * a.Hkv + s.g) * a.P_max + j] =
               call + xsum[(it & 1) * kTile + row];
         if (raise) {
@@ -622,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= s.L) {
           // rows past the sequence end hold whatever the cache holds: zero V there once
           // the tile has landed (each half of the pair zeroes one 64-column half)
-          if (!mbar_wait(&v_full[stage], (it / S) & 1, abort_flag)) set_abort();
+          if (!mbar_wait(&v_full[stage], (it / SV) & 1, abort_flag)) set_abort();
           if (half < D / 64) {
             uint8_t* vrow = v_ring + stage * Cfg::kKVBytes + half * Cfg::kHalfBytes + row * 128;
 #pragma unroll
@@ -630,10 +659,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(vrow + ch * 16) = make_uint4(0, 0, 0, 0);
           }
         }
-        uint8_t* prow = p_smem + row * 128;
+        uint8_t* prow = p_smem + (Cfg::kSplitP ? 0 : pb * Cfg::kPRegion) + row * 128;
 #pragma unroll
         for (int k = 0; k < NC / 8; ++k) {
-          const int ch = pb * 4 + col0 / 8 + k;  // buffer 1 starts 32 elements in
+          // split rows: buffer 1 starts 32 elements in; else each buffer has its region
+          const int ch = (Cfg::kSplitP ? pb * 4 : 0) + col0 / 8 + k;
           uint4 pk;
           pk.x = pack_bf16x2(sv[k * 8 + 0], sv[k * 8 + 1]);
           pk.y = pack_bf16x2(sv[k * 8 + 2], sv[k * 8 + 3]);
@@ -776,7 +806,7 @@ template <int D, int NQ, int G>
 cudaError_t launch_dng(const VerifyArgs& va, const VerifyPlan& plan, const VParams& p,
                        cudaStream_t stream) {
   auto kern = verify_attn_collect_kernel<D, NQ, G>;
-  constexpr int smem = VCfg<D>::kSmemBytes;
+  constexpr int smem = VCfg<D, NQ>::kSmemBytes;
   // set on every call: the attribute is per device and the call costs no GPU work
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
