@@ -54,6 +54,8 @@ def _load():
                                           P, P, P]
             lib.oracle_verify_all_rows.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, I,
                                                    D, P, P, P]
+            lib.oracle_sparse_verify.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P,
+                                                 I, D, P]
             lib.oracle_score_from_logits.argtypes = [I, I, I, P, P, P]
             lib.oracle_score_from_partials.argtypes = [I, I, I, P, P, P]
             lib.oracle_select.argtypes = [I, I, P, P, I, I, I, P, P]
@@ -61,6 +63,7 @@ def _load():
                                                  P, D, P]
             for name in ("oracle_verify", "oracle_verify_all_rows", "oracle_score_from_logits",
                          "oracle_score_from_partials", "oracle_select", "oracle_sparse_decode",
+                         "oracle_sparse_verify",
                          "oracle_num_threads"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -207,4 +210,25 @@ def sparse_decode(q, k_cache, v_cache, block_table, idx, n_sel, tail_start, seq_
                                         _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(idx),
                                         _ptr(ns), k_max, _ptr(ts), _ptr(sl), float(scale),
                                         _ptr(out)), "oracle_sparse_decode")
+    return out
+
+
+def sparse_verify(q, k_cache, v_cache, block_table, prefix_len, idx, n_sel, *, scale):
+    """Sparse verification: verify row t of sequence b attends idx[b, :n_sel[b]] and
+    the verify block positions P_b .. P_b + t.  q: uint16 [B, R, Hq, d]; idx [B, k_max].
+    Returns out [B, R, Hq, d] float64."""
+    q = _u16(q)
+    k_cache = _u16(k_cache)
+    v_cache = _u16(v_cache)
+    bt = _i32(block_table)
+    pl = _i32(prefix_len)
+    idx = _i32(idx)
+    ns = _i32(n_sel)
+    B, R, Hq, d = q.shape
+    NB, Hkv, page, _ = k_cache.shape
+    out = np.zeros((B, R, Hq, d), dtype=np.float64)
+    _check(_load().oracle_sparse_verify(B, Hq, Hkv, d, page, bt.shape[1], NB, R, _ptr(q),
+                                        _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(pl),
+                                        _ptr(idx), _ptr(ns), idx.shape[1], float(scale),
+                                        _ptr(out)), "oracle_sparse_verify")
     return out

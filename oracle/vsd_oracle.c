@@ -429,6 +429,61 @@ int oracle_sparse_decode(int B, int Hq, int Hkv, int d, int page, int max_blocks
     return status;
 }
 
+/*
+ * Sparse verification.
+ *   [Dustin] "Verification workflow", steps 3-4: a compressed target KV cache is
+ *   formed from the selected tokens only, and the target model verifies the draft
+ *   tokens against that sparse cache.  The draft tokens being verified are the
+ *   verify block itself (positions P_b .. P_b + R - 1), causal as in full
+ *   verification.
+ * For every b, verify row t and head h: attended positions = idx[b][0 .. n_sel[b])
+ * followed by P_b .. P_b + t; out[b][t][h][:] = softmax attention over them.
+ */
+int oracle_sparse_verify(int B, int Hq, int Hkv, int d, int page, int max_blocks,
+                         int num_blocks, int R, const uint16_t *q, const uint16_t *k_cache,
+                         const uint16_t *v_cache, const int32_t *block_table,
+                         const int32_t *prefix_len, const int32_t *idx, const int32_t *n_sel,
+                         int k_max, double scale, double *out) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page <= 0 || R <= 0 ||
+        k_max < 0)
+        return ORACLE_BAD_ARG;
+    const int G = Hq / Hkv;
+    int status = ORACLE_OK;
+    const int n_items = B * R * Hq;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int item = 0; item < n_items; ++item) {
+        int b = item / (R * Hq);
+        int t = (item / Hq) % R;
+        int h = item % Hq;
+        int g = h / G;
+        int ns = n_sel ? n_sel[b] : 0;
+        int P = prefix_len[b];
+        if (ns < 0 || ns > k_max || P < 0) { status = ORACLE_BAD_ARG; continue; }
+        int n_pos = ns + t + 1;
+        int *pos = (int *)malloc(sizeof(int) * (size_t)n_pos);
+        double *qv = (double *)malloc(sizeof(double) * (size_t)d);
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!pos || !qv || !o) {
+            status = ORACLE_NO_MEMORY;
+        } else {
+            for (int m = 0; m < ns; ++m) pos[m] = idx[(size_t)b * k_max + m];
+            for (int u = 0; u <= t; ++u) pos[ns + u] = P + u;
+            const uint16_t *qr = q + (((size_t)b * R + t) * Hq + h) * d;
+            for (int c = 0; c < d; ++c) qv[c] = bf16_to_double(qr[c]);
+            int rc = attend(qv, d, pos, n_pos, k_cache, v_cache, block_table, b, max_blocks,
+                            num_blocks, Hkv, page, g, scale, o, NULL);
+            if (rc != ORACLE_OK) {
+                status = rc;
+            } else {
+                double *dst = out + (((size_t)b * R + t) * Hq + h) * d;
+                for (int c = 0; c < d; ++c) dst[c] = o[c];
+            }
+        }
+        free(pos); free(qv); free(o);
+    }
+    return status;
+}
+
 /* Number of threads the parallel loops above use (1 without OpenMP). */
 #ifdef _OPENMP
 #include <omp.h>

@@ -375,6 +375,49 @@ def test_sparse_uniform_mean_of_attended_positions():
             assert out[b, h, 1] == pytest.approx(np.mean(np.array(pos) % 3), abs=1e-12)
 
 
+def test_sparse_verify_uniform_mean_over_selection_and_block():
+    """Equal keys: verify row t averages V over exactly idx[:n_sel] and the verify
+    block positions P .. P + t (Dustin's compressed cache, causal in the block)."""
+    B, Hq, Hkv, d, page, R = 2, 4, 2, 64, 16, 3
+    prefix = [50, 33]
+    lengths = [p + R for p in prefix]
+    table, NB = make_table(lengths, page, shuffle_seed=8)
+    Ks = [np.zeros((L, Hkv, d), np.float32) for L in lengths]
+    Vs = []
+    for L in lengths:
+        V = np.zeros((L, Hkv, d), np.float32)
+        V[:, :, 0] = np.arange(L)[:, None]
+        V[:, :, 1] = (np.arange(L) % 5)[:, None]
+        Vs.append(V)
+    idx = np.array([[0, 1, 7, 30, 49, -3], [4, 19, 32, -3, -3, -3]], np.int32)
+    n_sel = [5, 3]
+    rng = np.random.default_rng(1)
+    q = bf16_round_bits(rng.normal(size=(B, R, Hq, d)))
+    out = oracle.sparse_verify(q, paged_cache(Ks, table, NB, page), paged_cache(Vs, table, NB, page),
+                               table, prefix, idx, n_sel, scale=0.125)
+    for b in range(B):
+        for t in range(R):
+            pos = list(idx[b, :n_sel[b]]) + list(range(prefix[b], prefix[b] + t + 1))
+            for h in range(Hq):
+                assert out[b, t, h, 0] == pytest.approx(np.mean(pos), abs=1e-12)
+                assert out[b, t, h, 1] == pytest.approx(np.mean(np.array(pos) % 5), abs=1e-12)
+
+
+def test_sparse_verify_with_the_whole_prefix_is_full_verification():
+    """Selecting every prefix position turns sparse verification into the full one."""
+    s = _structured_verify(R=3)
+    scale = 1.0 / math.sqrt(s["d"])
+    out_full, _, _ = oracle.verify(s["q"], s["k"], s["v"], s["table"], s["prefix"], scale=scale,
+                                   P_max=64, collect=False)
+    k_max = int(max(s["prefix"]))
+    idx = np.full((len(s["prefix"]), k_max), -1, np.int32)
+    for b, P in enumerate(s["prefix"]):
+        idx[b, :P] = np.arange(P)
+    out = oracle.sparse_verify(s["q"], s["k"], s["v"], s["table"], s["prefix"], idx,
+                               s["prefix"], scale=scale)
+    np.testing.assert_allclose(out, out_full, rtol=0, atol=1e-12)
+
+
 def test_sparse_single_position_is_value_row():
     rng = np.random.default_rng(4)
     d, page = 128, 16
