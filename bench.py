@@ -305,6 +305,24 @@ def run_gpu(args, world, rank, local):
             v1.record(stream)
             torch.cuda.synchronize()
             per["verify_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
+        # sparse verification (Dustin) over this iteration's selection, back to back
+        per["sparse_verify_b2b"] = []
+        sv_out = torch.empty_like(batch.q)
+        sv_geom = vsd.geom_for(B, Hq, batch.k_cache, batch.block_table)
+        sv_ws = torch.zeros(vsd.vsd_sparse_verify_workspace_size(sv_geom, R, w.k) + 256,
+                            dtype=torch.uint8, device=dev)
+        sv_ws = sv_ws[(-sv_ws.data_ptr()) % 256:]
+        for _ in range(3):
+            torch.cuda.synchronize()
+            torch.cuda._sleep(sleep_cycles)
+            v0.record(stream)
+            for _ in range(B2B_CALLS):
+                vsd.vsd_sparse_verify_attn(batch.q, batch.k_cache, batch.v_cache,
+                                           batch.block_table, batch.prefix_len, idx, n_sel,
+                                           scale=w.scale, out=sv_out, workspace=sv_ws)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            per["sparse_verify_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
         # the same, collecting every verify row (the selection equation as printed):
         # what Collect-2-Query saves
         per["verify_all_b2b"] = []
@@ -384,6 +402,13 @@ def run_gpu(args, world, rank, local):
         "kernels": kernels,
         "select_over_verify": t_select / t_verify,
         "verify_back_to_back_us": t_verify_b2b * 1e6,
+        "sparse_verify": {
+            "us": statistics.median(per["sparse_verify_b2b"]) * 1e6,
+            "full_verify_us": t_verify_b2b * 1e6,
+            "attended_keys_per_head": [int(n) + R for n in n_sel_host],
+            "note": "verify rows attend the selection plus the verify block (a compressed "
+                    "cache gathered into the workspace, then the verification kernel); "
+                    "back-to-back calls"},
         "collect2_vs_all_rows": None if not per["verify_all_b2b"] else {
             "collect2_us": t_verify_b2b * 1e6,
             "all_rows_us": statistics.median(per["verify_all_b2b"]) * 1e6,
@@ -401,7 +426,7 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_all_timed_loops": (2 * launches_per_step * args.steps +
                                          (6 if per["verify_all_b2b"] else 3) * B2B_CALLS *
-                                         launches_per_verify),
+                                         launches_per_verify + 3 * B2B_CALLS * 3),
         "gpu_launches_per_step": launches_per_step,
         "clocks": clk,
         # the device timestamps only measure kernels if the host finished enqueueing a

@@ -237,6 +237,39 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
                                   size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------
+ * Sparse verification (Dustin summary, "Verification workflow", steps 3-4: a
+ * compressed target KV cache is formed from the selected tokens only and the draft
+ * block is verified against it).
+ *
+ * For sequence b with prefix length P_b, verify row t in [0, R) attends
+ *   J_bt = idx[b, 0 .. n_sel[b])  followed by  P_b .. P_b + t
+ *   out[b,t,h,:] = sum_{j in J_bt} softmax_j(scale * <q[b,t,h,:], K[b,j,h/G,:]>) V[b,j,h/G,:]
+ * The cache must hold the verify block (positions P_b .. P_b + R - 1).  The call
+ * writes the compressed cache into the workspace and runs the verification kernel on
+ * it; no logits are collected.
+ *
+ *   q          bf16 [B][R][Hq][head_dim]
+ *   prefix_len int32 [B]; P_b + R <= max_blocks_per_seq * page_size
+ *   idx        int32 [B][k_max] selected prefix positions (< P_b), n_sel int32 [B]
+ *              (0 <= n_sel[b] <= k_max); a position outside [0, P_b + R) is flagged
+ *              VSD_DEV_BAD_INDEX and that sequence's output is unspecified
+ *   out        bf16 [B][R][Hq][head_dim]
+ *   workspace  >= vsd_sparse_verify_workspace_size(...) bytes, 256-byte aligned
+ *              (holds the compressed cache: about 2 * B * Hkv * (k_max + R) *
+ *              head_dim * 2 bytes); contents on entry are ignored
+ * Supported: as vsd_verify_attn_collect with P_max = k_max.
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_sparse_verify_workspace_size(const vsd_geom* geom, int R, int k_max,
+                                            size_t* bytes);
+
+vsd_status vsd_sparse_verify_attn(const vsd_geom* geom, int R, const void* q,
+                                  const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, const int32_t* prefix_len,
+                                  const int32_t* idx, const int32_t* n_sel, int k_max,
+                                  float scale, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------
  * Device status word and errors.
  * vsd_read_device_status synchronizes `stream`, returns the accumulated
  * VSD_DEV_* bits of every kernel of this library on the current device since the

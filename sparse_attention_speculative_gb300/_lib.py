@@ -67,6 +67,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                         P, P]
         lib.vsd_verify_attn_collect_all.argtypes = [GP, I, P, P, P, P, P, I, F, P, P, P, P, SZ,
                                                     P]
+        lib.vsd_sparse_verify_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
+        lib.vsd_sparse_verify_attn.argtypes = [GP, I, P, P, P, P, P, P, P, I, F, P, P, SZ, P]
         lib.vsd_select_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(SZ)]
         lib.vsd_select_topk.argtypes = [I, I, P, P, I, I, I, I, P, P, P, P, SZ, P]
         lib.vsd_sparse_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
@@ -76,7 +78,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_get_error_string.restype = ctypes.c_char_p
         lib.vsd_last_cuda_error.argtypes = []
         for name in ("vsd_verify_workspace_size", "vsd_verify_attn_collect",
-                     "vsd_verify_attn_collect_all",
+                     "vsd_verify_attn_collect_all", "vsd_sparse_verify_workspace_size",
+                     "vsd_sparse_verify_attn",
                      "vsd_verify_attn_collect_noalloc",
                      "vsd_select_workspace_size", "vsd_select_topk", "vsd_sparse_workspace_size",
                      "vsd_sparse_decode_attn", "vsd_read_device_status", "vsd_last_cuda_error"):
@@ -298,3 +301,37 @@ def vsd_read_device_status(stream=None) -> int:
     _check(load().vsd_read_device_status(_stream(stream), ctypes.byref(flags)),
            "vsd_read_device_status")
     return int(flags.value)
+
+
+def vsd_sparse_verify_workspace_size(geom: Geom, R: int, k_max: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().vsd_sparse_verify_workspace_size(ctypes.byref(geom), int(R), int(k_max),
+                                                   ctypes.byref(out)),
+           "vsd_sparse_verify_workspace_size")
+    return int(out.value)
+
+
+def vsd_sparse_verify_attn(q, k_cache, v_cache, block_table, prefix_len, idx, n_sel, *,
+                           scale: float, out=None, workspace=None, stream=None):
+    """Sparse verification: verify row t attends idx[b, :n_sel[b]] and the verify block
+    positions P_b .. P_b + t.  q: bf16 [B, R, Hq, d]; idx: int32 [B, k_max].  Returns out."""
+    lib = load()
+    B, R, Hq, d = q.shape
+    _need(q, torch.bfloat16, "q")
+    _need(prefix_len, torch.int32, "prefix_len")
+    _need(idx, torch.int32, "idx")
+    _need(n_sel, torch.int32, "n_sel")
+    geom = geom_for(B, Hq, k_cache, block_table)
+    k_max = int(idx.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = _workspace(vsd_sparse_verify_workspace_size(geom, R, k_max), q.device,
+                               "sparse_verify")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.vsd_sparse_verify_attn(ctypes.byref(geom), R, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(block_table), _ptr(prefix_len), _ptr(idx), _ptr(n_sel),
+                                    k_max, float(scale), _ptr(out), _ptr(workspace), ws_bytes,
+                                    _stream(stream))
+    _check(rc, "vsd_sparse_verify_attn")
+    return out

@@ -83,4 +83,27 @@ size_t sparse_counter_bytes(const SparsePlan& plan, int B, int Hkv);
 size_t sparse_workspace_bytes(const SparsePlan& plan, int B, int Hkv, int G, int head_dim);
 cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- sparse verification
+// The compressed cache: sequence b's compact position p holds token idx[b][p]
+// (p < n_sel[b]) or P_b + p - n_sel[b] (the R verify rows), as a paged cache of
+// sparse_verify_pages(k_max, R) pages per sequence with its own block table and
+// prefix lengths (n_sel).
+struct SparseVerifyArgs {
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const int32_t* idx;
+  const int32_t* n_sel;
+  uint16_t* compact_k;        // [B * pages][Hkv][16][d]
+  uint16_t* compact_v;
+  int32_t* compact_table;     // [B][pages]
+  int32_t* compact_prefix;    // [B]
+  unsigned* status;
+  int B, Hkv, d, R, max_blocks, num_blocks, k_max;
+};
+
+int sparse_verify_pages(int k_max, int R);
+cudaError_t launch_sparse_verify_gather(const SparseVerifyArgs& a, cudaStream_t stream);
+
 }  // namespace vsd

@@ -246,6 +246,139 @@ vsd_status vsd_verify_attn_collect_all(const vsd_geom* geom, int R, const void* 
                      scale, logits, partial_scores, out, workspace, workspace_bytes, stream);
 }
 
+namespace {
+
+// Workspace of sparse verification: compact K, compact V, compact block table and
+// prefix lengths, then the verification kernel's own workspace (all 256-byte aligned).
+struct SparseVerifyLayout {
+  size_t off_k, off_v, off_table, off_prefix, off_verify, total;
+  int pages;
+  vsd::VerifyPlan plan;
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+vsd_status sparse_verify_layout(const vsd_geom* geom, int R, int k_max, int sms,
+                                SparseVerifyLayout* L) {
+  L->pages = vsd::sparse_verify_pages(k_max, R);
+  const size_t cache = static_cast<size_t>(geom->B) * L->pages * geom->Hkv * 16 *
+                       geom->head_dim * 2;
+  L->off_k = 0;
+  L->off_v = round256(cache);
+  L->off_table = L->off_v + round256(cache);
+  L->off_prefix = L->off_table + round256(static_cast<size_t>(geom->B) * L->pages * 4);
+  L->off_verify = L->off_prefix + round256(static_cast<size_t>(geom->B) * 4);
+  L->plan = vsd::plan_verify(geom->B, geom->Hkv, R, geom->Hq / geom->Hkv, k_max, sms);
+  L->total = L->off_verify + round256(vsd::verify_workspace_bytes(L->plan, geom->head_dim));
+  return VSD_OK;
+}
+
+vsd_status sparse_verify_checks(const vsd_geom* geom, int R, int k_max) {
+  vsd_status st = verify_checks(geom, R, k_max);
+  if (st != VSD_OK) return st;
+  if (k_max < 0) return VSD_ERR_INVALID_ARG;
+  if (static_cast<long long>(geom->B) * vsd::sparse_verify_pages(k_max, R) > (1ll << 30))
+    return VSD_ERR_UNSUPPORTED;
+  return VSD_OK;
+}
+
+}  // namespace
+
+vsd_status vsd_sparse_verify_workspace_size(const vsd_geom* geom, int R, int k_max,
+                                            size_t* bytes) {
+  if (bytes == nullptr) return VSD_ERR_INVALID_ARG;
+  vsd_status st = sparse_verify_checks(geom, R, k_max);
+  if (st != VSD_OK) return st;
+  int sms = 0;
+  st = device_info(nullptr, &sms);
+  if (st != VSD_OK) return st;
+  SparseVerifyLayout L;
+  sparse_verify_layout(geom, R, k_max, sms, &L);
+  *bytes = L.total;
+  return VSD_OK;
+}
+
+vsd_status vsd_sparse_verify_attn(const vsd_geom* geom, int R, const void* q,
+                                  const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, const int32_t* prefix_len,
+                                  const int32_t* idx, const int32_t* n_sel, int k_max,
+                                  float scale, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  vsd_status st = sparse_verify_checks(geom, R, k_max);
+  if (st != VSD_OK) return st;
+  if (geom->B == 0) return VSD_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !prefix_len || !out || !workspace)
+    return workspace ? VSD_ERR_INVALID_ARG : VSD_ERR_WORKSPACE;
+  if (k_max > 0 && (!idx || !n_sel)) return VSD_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(block_table, 4) || !aligned(prefix_len, 4) || !aligned(idx, 4) ||
+      !aligned(n_sel, 4))
+    return VSD_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return VSD_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  int sms = 0;
+  st = device_info(&status, &sms);
+  if (st != VSD_OK) return st;
+  SparseVerifyLayout L;
+  sparse_verify_layout(geom, R, k_max, sms, &L);
+  if (workspace_bytes < L.total || !aligned(workspace, 256)) return VSD_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  vsd::SparseVerifyArgs ga;
+  ga.k_cache = k_cache;
+  ga.v_cache = v_cache;
+  ga.block_table = block_table;
+  ga.prefix_len = prefix_len;
+  ga.idx = k_max > 0 ? idx : nullptr;
+  ga.n_sel = k_max > 0 ? n_sel : nullptr;
+  ga.compact_k = reinterpret_cast<uint16_t*>(ws + L.off_k);
+  ga.compact_v = reinterpret_cast<uint16_t*>(ws + L.off_v);
+  ga.compact_table = reinterpret_cast<int32_t*>(ws + L.off_table);
+  ga.compact_prefix = reinterpret_cast<int32_t*>(ws + L.off_prefix);
+  ga.status = status;
+  ga.B = geom->B;
+  ga.Hkv = geom->Hkv;
+  ga.d = geom->head_dim;
+  ga.R = R;
+  ga.max_blocks = geom->max_blocks_per_seq;
+  ga.num_blocks = geom->num_blocks;
+  ga.k_max = k_max;
+  // the compressed cache as a paged cache of its own
+  vsd_geom cg = *geom;
+  cg.max_blocks_per_seq = L.pages;
+  cg.num_blocks = geom->B * L.pages;
+  vsd::VerifyArgs va;
+  st = make_cache_map(&va.kmap, ga.compact_k, &cg);
+  if (st != VSD_OK) return st;
+  st = make_cache_map(&va.vmap, ga.compact_v, &cg);
+  if (st != VSD_OK) return st;
+  cudaError_t e = vsd::launch_sparse_verify_gather(ga, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  va.q = q;
+  va.block_table = ga.compact_table;
+  va.prefix_len = ga.compact_prefix;
+  va.logits = nullptr;
+  va.partial = nullptr;
+  va.out = out;
+  va.ws = reinterpret_cast<float*>(ws + L.off_verify);
+  va.status = status;
+  va.B = geom->B;
+  va.Hq = geom->Hq;
+  va.Hkv = geom->Hkv;
+  va.G = geom->Hq / geom->Hkv;
+  va.R = R;
+  va.d = geom->head_dim;
+  va.max_blocks = L.pages;
+  va.num_blocks = geom->B * L.pages;
+  va.P_max = k_max;
+  va.row0 = 0;
+  va.row1 = 0;
+  va.collect_all = 0;
+  va.scale = scale;
+  e = vsd::launch_verify(va, L.plan, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
 vsd_status vsd_select_workspace_size(int n_rows, int Hkv, int P_max, int k, size_t* bytes) {
   if (bytes == nullptr || n_rows < 0 || Hkv < 1 || P_max < 0 || k < 1)
     return VSD_ERR_INVALID_ARG;

@@ -451,3 +451,79 @@ def test_verify_collect_all_rows(d, Hq, Hkv, gamma, prefix):
         assert_rel_close(lg[b, :, :, :P], l_ref[b, :, :, :P], "all-rows logits")
         assert_rel_close(pa[b, :, :P], p_ref[b, :, :P], "all-rows partial scores")
 
+
+
+def test_results_do_not_depend_on_the_split():
+    """The split of the work is not part of the result: a sequence verified alone and
+    inside a batch (different CTA ranges and split-K merges) agree within the attention
+    tolerance with identical collected logits; a draft step planned for a longer tail
+    (more, emptier splits) gives the same output."""
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("split", B=3, P=9000, Hq=32, Hkv=8, d=128, gamma=4, k=512, n_sink=16,
+                 n_recent=64, seed=51, prefix_lens=(9000, 2500, 6000))
+    batch = make_batch(w, "cuda")
+    out, logits, partial = run_verify(batch, w)
+    for b in range(w.B):
+        one = type(batch)(w, batch.q[b:b + 1].contiguous(), batch.q_draft[:, b:b + 1].contiguous(),
+                          batch.k_cache, batch.v_cache, batch.block_table[b:b + 1].contiguous(),
+                          batch.prefix_len[b:b + 1].contiguous(), [batch.planted[b]])
+        o1, l1, p1 = run_verify(one, w)
+        assert vsd.vsd_read_device_status() == 0
+        diff = (o1[0].float() - out[b].float()).abs().max().item()
+        assert diff <= 2e-2, diff
+        P = int(batch.prefix_len[b])
+        assert torch.equal(l1[0, :, :, :P], logits[b, :, :, :P])
+        assert torch.equal(p1[0, :, :P], partial[b, :, :P])
+    idx, n_sel, _ = vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                        n_recent=w.n_recent)
+    tail = batch.prefix_len.clone()
+    seq_len = batch.prefix_len + 3
+    outs = [vsd.vsd_sparse_decode_attn(batch.q_draft[0], batch.k_cache, batch.v_cache,
+                                       batch.block_table, idx, n_sel, tail, seq_len,
+                                       scale=w.scale, max_tail=mt) for mt in (3, 200, 2000)]
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,gamma,prefix,k", [
+    (128, 32, 8, 4, (6000, 1500, 300), 512),   # Qwen3-8B geometry, ragged, n_sel < k_max
+    (128, 64, 8, 5, (4096, 2049), 256),        # Qwen2.5-72B geometry (NQ = 48)
+    (64, 8, 2, 3, (777, 31), 64),              # head_dim 64, a prefix shorter than k
+])
+def test_sparse_verify(d, Hq, Hkv, gamma, prefix, k):
+    """Dustin's sparse verification: each verify row attends the selected set plus the
+    verify block up to itself, against the oracle; selecting the whole prefix gives
+    full verification."""
+    from sparse_attention_speculative_gb300.synth import host_arrays, make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("spv", B=len(prefix), P=max(prefix), Hq=Hq, Hkv=Hkv, d=d, gamma=gamma, k=k,
+                 n_sink=4, n_recent=32, planted_frac=0.01, seed=61, prefix_lens=prefix)
+    batch = make_batch(w, "cuda")
+    _, _, partial = run_verify(batch, w)
+    idx, n_sel, _ = vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                        n_recent=w.n_recent)
+    out = vsd.vsd_sparse_verify_attn(batch.q, batch.k_cache, batch.v_cache, batch.block_table,
+                                     batch.prefix_len, idx, n_sel, scale=w.scale)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    h = host_arrays(batch)
+    ref = oracle.sparse_verify(h["q"], h["k_cache"], h["v_cache"], h["block_table"],
+                               h["prefix_len"], idx.cpu().numpy(), n_sel.cpu().numpy(),
+                               scale=w.scale)
+    assert_attn_close(out.float().cpu().numpy(), ref, "sparse verify output")
+    # every prefix position selected: the same as full verification
+    full = torch.full((w.B, w.P_max), -1, dtype=torch.int32, device="cuda")
+    for b, P in enumerate(prefix):
+        full[b, :P] = torch.arange(P, dtype=torch.int32, device="cuda")
+    out_all = vsd.vsd_sparse_verify_attn(batch.q, batch.k_cache, batch.v_cache,
+                                         batch.block_table, batch.prefix_len, full,
+                                         batch.prefix_len.clone(), scale=w.scale)
+    out_dense, _, _ = run_verify(batch, w)
+    assert vsd.vsd_read_device_status() == 0
+    diff = (out_all.float() - out_dense.float()).abs().max().item()
+    assert diff <= 2e-2, diff
