@@ -56,6 +56,8 @@ def _load():
                                                    D, P, P, P]
             lib.oracle_sparse_verify.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P,
                                                  I, D, P]
+            lib.oracle_select_hybrid.argtypes = [I, I, P, P, P, I, I, I, I, P, P]
+            lib.oracle_partial_masked.argtypes = [I, I, I, I, I, P, P, P, P]
             lib.oracle_score_from_logits.argtypes = [I, I, I, P, P, P]
             lib.oracle_score_from_partials.argtypes = [I, I, I, P, P, P]
             lib.oracle_select.argtypes = [I, I, P, P, I, I, I, P, P]
@@ -63,7 +65,7 @@ def _load():
                                                  P, D, P]
             for name in ("oracle_verify", "oracle_verify_all_rows", "oracle_score_from_logits",
                          "oracle_score_from_partials", "oracle_select", "oracle_sparse_decode",
-                         "oracle_sparse_verify",
+                         "oracle_sparse_verify", "oracle_select_hybrid", "oracle_partial_masked",
                          "oracle_num_threads"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -232,3 +234,32 @@ def sparse_verify(q, k_cache, v_cache, block_table, prefix_len, idx, n_sel, *, s
                                         _ptr(idx), _ptr(ns), idx.shape[1], float(scale),
                                         _ptr(out)), "oracle_sparse_verify")
     return out
+
+
+def select_hybrid(score_target, score_draft, prefix_len, *, k, m, n_sink, n_recent):
+    """Dustin's hybrid budget: protected sinks and recent window, then the top-m by the
+    draft signal, then the rest by the target signal.  Returns (idx [n_rows, k], n_sel)."""
+    st = _f64(score_target)
+    sd = _f64(score_draft)
+    pl = _i32(prefix_len)
+    n_rows, P_max = st.shape
+    assert sd.shape == st.shape
+    idx = np.full((n_rows, k), -1, dtype=np.int32)
+    n_sel = np.zeros((n_rows,), dtype=np.int32)
+    _check(_load().oracle_select_hybrid(n_rows, P_max, _ptr(st), _ptr(sd), _ptr(pl), int(k),
+                                        int(m), int(n_sink), int(n_recent), _ptr(idx),
+                                        _ptr(n_sel)), "oracle_select_hybrid")
+    return idx, n_sel
+
+
+def partial_masked(logits, prefix_len, head_mask, Hkv):
+    """Per-KV-group partial scores over the heads with head_mask[h] != 0.
+    logits: [B, C, Hq, P_max] (C collected rows).  Returns [B, Hkv, P_max]."""
+    lg = _f64(logits)
+    pl = _i32(prefix_len)
+    hm = np.ascontiguousarray(np.asarray(head_mask, dtype=np.uint8))
+    B, C, Hq, P_max = lg.shape
+    partial = np.zeros((B, Hkv, P_max), dtype=np.float64)
+    _check(_load().oracle_partial_masked(B, C, Hq, Hkv, P_max, _ptr(lg), _ptr(pl), _ptr(hm),
+                                         _ptr(partial)), "oracle_partial_masked")
+    return partial

@@ -376,6 +376,91 @@ int oracle_select(int n_rows, int P_max, const double *score, const int32_t *pre
 }
 
 /*
+ * Hybrid budget with two signals.
+ *   [Dustin] Methodology sec. 1 (hybrid attention aggregation): after the
+ *   attention-sink prefix and the local window of recent tokens are protected, the
+ *   rest of the budget is allocated hierarchically: first the top-m tokens by the
+ *   draft-lookahead signal, then the most relevant remaining tokens by the
+ *   target-historical signal.
+ * For each row r with prefix length P (n = min(k, P), S as in oracle_select):
+ *   D  = the min(m, n - |S|) positions outside S with the highest draft score
+ *        (ties: lower position first)
+ *   T' = the n - |S| - |D| positions outside S and D with the highest target score
+ *        (ties: lower position first)
+ *   idx[r][0 .. n) = S U D U T', ascending;  n_sel[r] = n.
+ * Requires n_sink + n_recent <= k and m >= 0.
+ */
+int oracle_select_hybrid(int n_rows, int P_max, const double *score_target,
+                         const double *score_draft, const int32_t *prefix_len, int k, int m,
+                         int n_sink, int n_recent, int32_t *idx, int32_t *n_sel) {
+    if (k < 0 || m < 0 || n_sink < 0 || n_recent < 0 || n_sink + n_recent > k)
+        return ORACLE_BAD_ARG;
+    for (int r = 0; r < n_rows; ++r) {
+        int P = prefix_len[r];
+        if (P < 0 || P > P_max) return ORACLE_BAD_ARG;
+        int n = k < P ? k : P;
+        int sink_end = n_sink < P ? n_sink : P;
+        int recent_begin = P - n_recent > 0 ? P - n_recent : 0;
+        int *chosen = (int *)malloc(sizeof(int) * (size_t)(n > 0 ? n : 1));
+        char *taken = (char *)calloc((size_t)(P > 0 ? P : 1), 1);
+        scored_pos *rest = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)(P > 0 ? P : 1));
+        if (!chosen || !taken || !rest) {
+            free(chosen); free(taken); free(rest);
+            return ORACLE_NO_MEMORY;
+        }
+        int n_chosen = 0;
+        for (int j = 0; j < P; ++j)
+            if (j < sink_end || j >= recent_begin) { chosen[n_chosen++] = j; taken[j] = 1; }
+        if (n_chosen > n) { free(chosen); free(taken); free(rest); return ORACLE_BAD_ARG; }
+        /* draft signal first, at most m of them */
+        int n_rest = 0;
+        for (int j = 0; j < P; ++j)
+            if (!taken[j]) { rest[n_rest].s = score_draft[(size_t)r * P_max + j]; rest[n_rest].j = j; ++n_rest; }
+        qsort(rest, (size_t)n_rest, sizeof(scored_pos), by_score_then_position);
+        int n_draft = n - n_chosen < m ? n - n_chosen : m;
+        for (int q = 0; q < n_draft; ++q) { chosen[n_chosen++] = rest[q].j; taken[rest[q].j] = 1; }
+        /* then the target signal over what is left */
+        n_rest = 0;
+        for (int j = 0; j < P; ++j)
+            if (!taken[j]) { rest[n_rest].s = score_target[(size_t)r * P_max + j]; rest[n_rest].j = j; ++n_rest; }
+        qsort(rest, (size_t)n_rest, sizeof(scored_pos), by_score_then_position);
+        for (int q = 0; n_chosen < n; ++q) chosen[n_chosen++] = rest[q].j;
+        qsort(chosen, (size_t)n_chosen, sizeof(int), by_int);
+        for (int q = 0; q < n_chosen; ++q) idx[(size_t)r * k + q] = chosen[q];
+        n_sel[r] = n_chosen;
+        free(chosen); free(taken); free(rest);
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Per-KV-group partial scores restricted to a subset of query heads.
+ *   [Dustin] Methodology sec. 2 (semantic retrieval heads): online, the importance
+ *   computation is restricted to the few heads identified offline.
+ * partial[b][g][j] = sum over the collected rows c and the heads h of group g with
+ * head_mask[h] != 0 of logits[b][c][h][j], j < P_b (logits [B][C][Hq][P_max]).
+ */
+int oracle_partial_masked(int B, int C, int Hq, int Hkv, int P_max, const double *logits,
+                          const int32_t *prefix_len, const uint8_t *head_mask,
+                          double *partial) {
+    if (B < 0 || C <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ORACLE_BAD_ARG;
+    const int G = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        int P = prefix_len[b];
+        if (P < 0 || P > P_max) return ORACLE_BAD_ARG;
+        for (int g = 0; g < Hkv; ++g)
+            for (int j = 0; j < P; ++j) {
+                double s = 0.0;
+                for (int c = 0; c < C; ++c)
+                    for (int h = g * G; h < (g + 1) * G; ++h)
+                        if (head_mask[h]) s += logits[(((size_t)b * C + c) * Hq + h) * P_max + j];
+                partial[((size_t)b * Hkv + g) * P_max + j] = s;
+            }
+    }
+    return ORACLE_OK;
+}
+
+/*
  * Sparse draft-step attention.
  *   [Vegas] sec. 2, drafting phase: the draft step uses attention restricted to the
  *   selected KV entries.  sec. 3: this is paged attention with page size 1 whose

@@ -454,3 +454,76 @@ def test_tiny_workload_selects_planted_keys():
     assert planted <= set(idx[0].tolist())
     np.testing.assert_allclose(oracle.score_from_partials(partial, h["prefix_len"]), score,
                                atol=1e-9)
+
+
+
+# --------------------------------------------------------------------------------------
+# Dustin hybrid budget (Methodology sec. 1) and semantic-retrieval-head mask (sec. 2)
+# --------------------------------------------------------------------------------------
+
+def test_select_hybrid_golden():
+    with open(os.path.join(GOLDEN, "select_hybrid.json")) as f:
+        g = json.load(f)
+    st = np.array([g["score_target"]], np.float64)
+    sd = np.array([g["score_draft"]], np.float64)
+    idx, n_sel = oracle.select_hybrid(st, sd, [g["P"]], k=g["k"], m=g["m"], n_sink=g["n_sink"],
+                                      n_recent=g["n_recent"])
+    assert n_sel[0] == len(g["expected_idx"])
+    assert idx[0, :n_sel[0]].tolist() == g["expected_idx"]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_select_hybrid_limits_and_invariants(seed):
+    rng = np.random.default_rng(seed)
+    rows, P_max = 4, 300
+    prefix = rng.integers(0, P_max + 1, size=rows).astype(np.int32)
+    st = rng.integers(-5, 6, size=(rows, P_max)).astype(np.float64)  # ties on purpose
+    sd = rng.normal(size=(rows, P_max))
+    k, ns, nr = 60, 4, 16
+    # m = 0: the target signal alone
+    a, an = oracle.select_hybrid(st, sd, prefix, k=k, m=0, n_sink=ns, n_recent=nr)
+    b, bn = oracle.select(st, prefix, k=k, n_sink=ns, n_recent=nr)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(an, bn)
+    # m covering the whole remaining budget: the draft signal alone
+    a, an = oracle.select_hybrid(st, sd, prefix, k=k, m=k, n_sink=ns, n_recent=nr)
+    b, bn = oracle.select(sd, prefix, k=k, n_sink=ns, n_recent=nr)
+    np.testing.assert_array_equal(a, b)
+    # in between: protected kept, the best m by draft kept, the rest the best by target
+    m = 7
+    a, an = oracle.select_hybrid(st, sd, prefix, k=k, m=m, n_sink=ns, n_recent=nr)
+    for r, P in enumerate(prefix.tolist()):
+        n = min(k, P)
+        got = a[r, :an[r]].tolist()
+        assert an[r] == n and got == sorted(set(got))
+        prot = set(range(min(ns, P))) | set(range(max(0, P - nr), P))
+        assert prot <= set(got)
+        cand = [j for j in range(P) if j not in prot]
+        nd = min(m, n - len(prot))
+        draft_best = sorted(cand, key=lambda j: (-sd[r, j], j))[:nd]
+        assert set(draft_best) <= set(got)
+        rest = [j for j in cand if j not in draft_best]
+        want_t = sorted(rest, key=lambda j: (-st[r, j], j))[:n - len(prot) - nd]
+        assert set(got) == prot | set(draft_best) | set(want_t)
+
+
+def test_partial_masked_closed_form():
+    s = _structured_verify(R=3)
+    scale = 1.0 / math.sqrt(s["d"])
+    _, logits, partial = oracle.verify(s["q"], s["k"], s["v"], s["table"], s["prefix"],
+                                       scale=scale, P_max=64)
+    Hq, G, Hkv, R = s["Hq"], s["G"], s["Hkv"], s["R"]
+    np.testing.assert_array_equal(
+        oracle.partial_masked(logits, s["prefix"], np.ones(Hq, np.uint8), Hkv), partial)
+    assert np.all(oracle.partial_masked(logits, s["prefix"], np.zeros(Hq, np.uint8), Hkv) == 0)
+    mask = np.array([1 if h % 3 == 0 else 0 for h in range(Hq)], np.uint8)
+    got = oracle.partial_masked(logits, s["prefix"], mask, Hkv)
+    for b, P in enumerate(s["prefix"]):
+        j = np.arange(P)
+        for g in range(Hkv):
+            want = np.zeros(P)
+            for t in (0, R - 1):
+                for h in range(g * G, (g + 1) * G):
+                    if mask[h]:
+                        want += scale * ((t + 1) * ((j % 7) - 3) + (h + 1) * (g + 1) + (b + 1))
+            np.testing.assert_allclose(got[b, g, :P], want, rtol=0, atol=1e-10)
