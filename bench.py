@@ -323,6 +323,47 @@ def run_gpu(args, world, rank, local):
             v1.record(stream)
             torch.cuda.synchronize()
             per["sparse_verify_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
+        # Dustin's hybrid budget (a synthetic draft-lookahead signal, m = k / 4) and the
+        # collect restricted to a quarter of the query heads (semantic retrieval heads)
+        per["hybrid_b2b"], per["srh_b2b"], per["select_b2b"] = [], [], []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            torch.cuda._sleep(sleep_cycles)
+            v0.record(stream)
+            for _ in range(B2B_CALLS):
+                vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                    n_recent=w.n_recent, idx=idx, n_sel=n_sel)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            per["select_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
+        g_d = torch.Generator(device=dev)
+        g_d.manual_seed(w.seed + 5)
+        partial_draft = torch.randn((B, 2, P_max), generator=g_d, device=dev)
+        idx_h = torch.empty_like(idx)
+        nsel_h = torch.empty_like(n_sel)
+        head_mask = torch.tensor([1 if h % 4 == 0 else 0 for h in range(Hq)], dtype=torch.uint8,
+                                 device=dev)
+        for _ in range(3):
+            torch.cuda.synchronize()
+            torch.cuda._sleep(sleep_cycles)
+            v0.record(stream)
+            for _ in range(B2B_CALLS):
+                vsd.vsd_select_topk_hybrid(partial, partial_draft, batch.prefix_len, k=w.k,
+                                           m=w.k // 4, n_sink=w.n_sink, n_recent=w.n_recent,
+                                           idx=idx_h, n_sel=nsel_h)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            per["hybrid_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
+            torch.cuda._sleep(sleep_cycles)
+            v0.record(stream)
+            for _ in range(B2B_CALLS):
+                vsd.vsd_verify_attn_collect_srh(batch.q, batch.k_cache, batch.v_cache,
+                                                batch.block_table, batch.prefix_len, head_mask,
+                                                P_max=P_max, scale=w.scale, logits=logits,
+                                                partial=partial, out=out, workspace=workspace)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            per["srh_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
         # the same, collecting every verify row (the selection equation as printed):
         # what Collect-2-Query saves
         per["verify_all_b2b"] = []
@@ -409,6 +450,9 @@ def run_gpu(args, world, rank, local):
             "note": "verify rows attend the selection plus the verify block (a compressed "
                     "cache gathered into the workspace, then the verification kernel); "
                     "back-to-back calls"},
+        "hybrid_select_us": statistics.median(per["hybrid_b2b"]) * 1e6,
+        "select_back_to_back_us": statistics.median(per["select_b2b"]) * 1e6,
+        "srh_verify_us": statistics.median(per["srh_b2b"]) * 1e6,
         "collect2_vs_all_rows": None if not per["verify_all_b2b"] else {
             "collect2_us": t_verify_b2b * 1e6,
             "all_rows_us": statistics.median(per["verify_all_b2b"]) * 1e6,
@@ -426,7 +470,8 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_all_timed_loops": (2 * launches_per_step * args.steps +
                                          (6 if per["verify_all_b2b"] else 3) * B2B_CALLS *
-                                         launches_per_verify + 3 * B2B_CALLS * 3),
+                                         launches_per_verify + 3 * B2B_CALLS * 3 +
+                                         3 * B2B_CALLS * (3 + launches_per_verify)),
         "gpu_launches_per_step": launches_per_step,
         "clocks": clk,
         # the device timestamps only measure kernels if the host finished enqueueing a

@@ -116,6 +116,25 @@ vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------
+ * Verification with the collected importance restricted to a set of query heads
+ * (Dustin summary, Methodology sec. 2: online, the importance computation is limited
+ * to the semantic retrieval heads identified offline).
+ *
+ * Same as vsd_verify_attn_collect, except that only heads h with head_mask[h] != 0
+ * are collected:
+ *   partial_scores[b,g,j] = sum_{c in {0,1}} sum_{h in group g, head_mask[h]} logits[b,c,h,j]
+ * and the logits of the other heads are not written.
+ *   head_mask  uint8 [Hq], device memory (not NULL)
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_verify_attn_collect_srh(const vsd_geom* geom, int R, const void* q,
+                                       const void* k_cache, const void* v_cache,
+                                       const int32_t* block_table, const int32_t* prefix_len,
+                                       int collect_row0, int collect_row1,
+                                       const uint8_t* head_mask, int P_max, float scale,
+                                       float* logits, float* partial_scores, void* out,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------
  * Verification attention collecting every verify row (Vegas summary sec. 2.A: the
  * selection equation sums the logits over all gamma+1 rows of the verification
  * block and over the query heads; Collect-2-Query, sec. 2.B, keeps two of them).
@@ -196,6 +215,32 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
                            const int32_t* prefix_len, int P_max, int k, int n_sink,
                            int n_recent, int32_t* idx, int32_t* n_sel, float* scores_out,
                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * Hybrid budget with two signals (Dustin summary, Methodology sec. 1: after the
+ * protected sinks and recent window, the top-m tokens by the draft-lookahead signal,
+ * then the most relevant remaining tokens by the target-historical signal).
+ *
+ * For row r with prefix length P (n = min(k, P), S as in vsd_select_topk):
+ *   s_t[j] = sum_g partial_target[r,g,j],  s_d[j] = sum_g partial_draft[r,g,j]
+ *   D  = the min(m, n - |S|) positions outside S with the highest s_d
+ *   T' = the n - |S| - |D| positions outside S and D with the highest s_t
+ *   (equal scores: the lower position first)
+ *   idx[r, 0..n) = S U D U T', ascending; idx[r, n..k) = -1; n_sel[r] = n
+ *
+ *   partial_target fp32 [n_rows][Hkv_target][P_max]; partial_draft fp32
+ *   [n_rows][Hkv_draft][P_max] (any per-group decomposition of the draft score)
+ *   workspace      >= vsd_select_hybrid_workspace_size(...) bytes, 256-byte aligned;
+ *                  contents on entry are ignored
+ * Two launches of the selection kernel; supported sizes as vsd_select_topk.
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_select_hybrid_workspace_size(int n_rows, int P_max, size_t* bytes);
+
+vsd_status vsd_select_topk_hybrid(int n_rows, int Hkv_target, const float* partial_target,
+                                  int Hkv_draft, const float* partial_draft,
+                                  const int32_t* prefix_len, int P_max, int k, int m,
+                                  int n_sink, int n_recent, int32_t* idx, int32_t* n_sel,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------
  * Sparse draft-step attention (Vegas summary sec. 2 drafting phase; sec. 3 sparse

@@ -10,7 +10,8 @@ table (``workloads.py``) and the seeded input generators (``synth.py``).
 from ._lib import (DEV_BAD_BLOCK, DEV_BAD_INDEX, DEV_BAD_LENGTH, DEV_TIMEOUT, Geom,  # noqa: F401
                    VsdError, geom_for, load, vsd_read_device_status, vsd_select_topk,
                    vsd_sparse_decode_attn, vsd_sparse_workspace_size, vsd_verify_attn_collect,
-                   vsd_sparse_verify_attn, vsd_sparse_verify_workspace_size,
+                   vsd_select_topk_hybrid, vsd_sparse_verify_attn,
+                   vsd_sparse_verify_workspace_size, vsd_verify_attn_collect_srh,
                    vsd_verify_attn_collect_all,
                    vsd_verify_attn_collect_noalloc, vsd_verify_workspace_size)
 from .iteration import IterationGraph  # noqa: F401

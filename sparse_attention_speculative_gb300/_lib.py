@@ -69,6 +69,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                     P]
         lib.vsd_sparse_verify_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
         lib.vsd_sparse_verify_attn.argtypes = [GP, I, P, P, P, P, P, P, P, I, F, P, P, SZ, P]
+        lib.vsd_verify_attn_collect_srh.argtypes = [GP, I, P, P, P, P, P, I, I, P, I, F, P, P, P,
+                                                    P, SZ, P]
+        lib.vsd_select_hybrid_workspace_size.argtypes = [I, I, ctypes.POINTER(SZ)]
+        lib.vsd_select_topk_hybrid.argtypes = [I, I, P, I, P, P, I, I, I, I, I, P, P, P, SZ, P]
         lib.vsd_select_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(SZ)]
         lib.vsd_select_topk.argtypes = [I, I, P, P, I, I, I, I, P, P, P, P, SZ, P]
         lib.vsd_sparse_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
@@ -79,6 +83,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_last_cuda_error.argtypes = []
         for name in ("vsd_verify_workspace_size", "vsd_verify_attn_collect",
                      "vsd_verify_attn_collect_all", "vsd_sparse_verify_workspace_size",
+                     "vsd_verify_attn_collect_srh", "vsd_select_hybrid_workspace_size",
+                     "vsd_select_topk_hybrid",
                      "vsd_sparse_verify_attn",
                      "vsd_verify_attn_collect_noalloc",
                      "vsd_select_workspace_size", "vsd_select_topk", "vsd_sparse_workspace_size",
@@ -335,3 +341,67 @@ def vsd_sparse_verify_attn(q, k_cache, v_cache, block_table, prefix_len, idx, n_
                                     _stream(stream))
     _check(rc, "vsd_sparse_verify_attn")
     return out
+
+
+def vsd_verify_attn_collect_srh(q, k_cache, v_cache, block_table, prefix_len, head_mask, *,
+                                P_max: int, scale: float, row0: int = 0,
+                                row1: Optional[int] = None, logits=None, partial=None,
+                                out=None, workspace=None, stream=None):
+    """Verification with the collected logits and partial scores restricted to the query
+    heads with head_mask[h] != 0 (uint8 [Hq] on the device).  Returns (out, logits,
+    partial); the logits of the other heads are left untouched."""
+    lib = load()
+    B, R, Hq, d = q.shape
+    _need(q, torch.bfloat16, "q")
+    _need(head_mask, torch.uint8, "head_mask")
+    geom = geom_for(B, Hq, k_cache, block_table)
+    if row1 is None:
+        row1 = R - 1
+    dev = q.device
+    if out is None:
+        out = torch.empty_like(q)
+    if logits is None:
+        logits = torch.zeros((B, 2, Hq, P_max), dtype=torch.float32, device=dev)
+    if partial is None:
+        partial = torch.empty((B, geom.Hkv, P_max), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = _workspace(vsd_verify_workspace_size(geom, R, P_max), dev, "verify")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.vsd_verify_attn_collect_srh(ctypes.byref(geom), R, _ptr(q), _ptr(k_cache),
+                                         _ptr(v_cache), _ptr(block_table), _ptr(prefix_len),
+                                         int(row0), int(row1), _ptr(head_mask), int(P_max),
+                                         float(scale), _ptr(logits), _ptr(partial), _ptr(out),
+                                         _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc, "vsd_verify_attn_collect_srh")
+    return out, logits, partial
+
+
+def vsd_select_topk_hybrid(partial_target, partial_draft, prefix_len, *, k: int, m: int,
+                           n_sink: int, n_recent: int, idx=None, n_sel=None, workspace=None,
+                           stream=None):
+    """Dustin's hybrid budget: protected sinks and recent window, then the top-m by the
+    draft score, then the rest by the target score.  partial_*: fp32 [n_rows, Hkv*, P_max]."""
+    lib = load()
+    _need(partial_target, torch.float32, "partial_target")
+    _need(partial_draft, torch.float32, "partial_draft")
+    _need(prefix_len, torch.int32, "prefix_len")
+    n_rows, Hkv_t, P_max = partial_target.shape
+    Hkv_d = int(partial_draft.shape[1])
+    assert partial_draft.shape[0] == n_rows and partial_draft.shape[2] == P_max
+    dev = partial_target.device
+    if idx is None:
+        idx = torch.empty((n_rows, k), dtype=torch.int32, device=dev)
+    if n_sel is None:
+        n_sel = torch.empty((n_rows,), dtype=torch.int32, device=dev)
+    if workspace is None:
+        nb = ctypes.c_size_t(0)
+        _check(lib.vsd_select_hybrid_workspace_size(n_rows, P_max, ctypes.byref(nb)),
+               "vsd_select_hybrid_workspace_size")
+        workspace = _workspace(int(nb.value), dev, "select_hybrid")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.vsd_select_topk_hybrid(n_rows, Hkv_t, _ptr(partial_target), Hkv_d,
+                                    _ptr(partial_draft), _ptr(prefix_len), P_max, int(k), int(m),
+                                    int(n_sink), int(n_recent), _ptr(idx), _ptr(n_sel),
+                                    _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc, "vsd_select_topk_hybrid")
+    return idx, n_sel

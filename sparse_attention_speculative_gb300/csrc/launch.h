@@ -34,6 +34,7 @@ struct VerifyArgs {
   int B, Hq, Hkv, G, R, d, max_blocks, num_blocks, P_max;
   int row0, row1;
   int collect_all;  // 1: every verify row's logits, partial summed over all rows
+  const uint8_t* head_mask = nullptr;  // [Hq] or NULL: collected heads
   float scale;
 };
 
@@ -48,6 +49,12 @@ struct SelectArgs {
   float* scores_out;
   unsigned* status;
   int n_rows, Hkv, P_max, k, n_sink, n_recent;
+  // hybrid budget passes (all optional; see select_topk.cu)
+  int m_limit = -1;
+  const uint32_t* pre_bitmap = nullptr;
+  const int32_t* pre_count = nullptr;
+  uint32_t* out_bitmap = nullptr;
+  int32_t* out_count = nullptr;
 };
 
 int select_cluster_size(int P_max, int n_rows);

@@ -62,6 +62,13 @@ struct SelParams {
   float* scores_out;
   unsigned* status;
   int Hkv, P_max, k, n_sink, n_recent, chunk, bitmap_words;
+  // hybrid budget (Dustin Methodology sec. 1), both passes optional:
+  int m_limit;                  // >= 0: take at most this many candidates by score
+  const uint32_t* pre_bitmap;   // [n_rows][bm_words]: candidates chosen beforehand
+  const int32_t* pre_count;     // [n_rows]: how many
+  uint32_t* out_bitmap;         // [n_rows][bm_words]: this pass's chosen candidates
+  int32_t* out_count;           // [n_rows]
+  int bm_words;                 // words per row of those bitmaps: ceil(P_max / 32)
 };
 
 struct SelShared {
@@ -272,31 +279,48 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   const int sink_end = a.n_sink < P ? a.n_sink : P;
   const int rb0 = P - a.n_recent > 0 ? P - a.n_recent : 0;
   const int rb = rb0 > sink_end ? rb0 : sink_end;  // candidates: [sink_end, rb)
-  const int n_cand = rb - sink_end;
-  const int r_need = n - (P - n_cand);
+  // candidates chosen beforehand (first pass of the hybrid budget) are always taken
+  // and not ranked; this thread's KPT positions sit in one word of that bitmap
+  uint32_t pre_bits = 0u;
+  int n_pre = 0;
+  if (a.pre_bitmap != nullptr) {
+    const int wi = my0 >> 5;
+    if (wi < a.bm_words) {
+      const uint32_t wv = __ldg(a.pre_bitmap + static_cast<size_t>(row) * a.bm_words + wi);
+      pre_bits = (wv >> (my0 & 31)) & (KPT >= 32 ? 0xFFFFFFFFu : ((1u << KPT) - 1u));
+    }
+    n_pre = __ldg(a.pre_count + row);
+  }
+  const int n_cand = rb - sink_end - n_pre;  // rankable candidates
+  int r_need = n - (P - (rb - sink_end)) - n_pre;
+  if (a.m_limit >= 0 && r_need > a.m_limit) r_need = a.m_limit;
   const bool take_all = r_need >= n_cand;
   const bool ranking = r_need > 0 && !take_all;
+  auto rankable = [&](int jj, int q) {
+    return jj >= sink_end && jj < rb && !((pre_bits >> q) & 1u);
+  };
 
   // ---- A. keys and the level-0 histogram of the candidates
   if (ranking || a.scores_out != nullptr) {
-    for (int q = 0; q < KPT; q += 4) {
-      const int j = my0 + q;
-      float s[4];
-      if (q == 0) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) s[u] = s_first[u];
-      } else {
-        sum4(j, s);
-      }
+    auto finish4 = [&](int q, const float (&s)[4]) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int jj = j + u;
+        const int jj = my0 + q + u;
         const uint32_t key = jj < P ? order_key(s[u]) : 0u;
         L.keys[t * KPT + q + u] = key;
         if (jj < P && a.scores_out != nullptr)
           a.scores_out[static_cast<size_t>(row) * a.P_max + jj] = s[u];
-        if (ranking && jj >= sink_end && jj < rb) atomicAdd(&L.hist[key >> 20], 1u);
+        if (ranking && rankable(jj, q + u)) atomicAdd(&L.hist[key >> 20], 1u);
       }
+    };
+    finish4(0, s_first);
+    // the rest two groups of 4 per round, both groups' loads in flight together
+    for (int q = 4; q < KPT; q += 8) {
+      float s0[4], s1[4];
+      sum4(my0 + q, s0);
+      if (q + 4 < KPT) sum4(my0 + q + 4, s1);
+      finish4(q, s0);
+      if (q + 4 < KPT) finish4(q + 4, s1);
     }
   }
   __syncthreads();
@@ -321,7 +345,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
         for (int q = 0; q < KPT; ++q) {
           const int j = my0 + q;
           const uint32_t key = L.keys[t * KPT + q];
-          if (j >= sink_end && j < rb && (key & mask) == prefix)
+          if (rankable(j, q) && (key & mask) == prefix)
             atomicAdd(&L.hist[(key >> shift) & dmask], 1u);
         }
         __syncthreads();
@@ -366,10 +390,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
 
   // ---- D. mark the sure winners, hand the boundary bin to rank 0
   {
-    uint64_t sure = 0, inbin = 0;
+    uint64_t sure = static_cast<uint64_t>(pre_bits), inbin = 0;
     for (int q = 0; q < KPT; ++q) {
       const int j = my0 + q;
-      if (j >= sink_end && j < rb) {
+      if (rankable(j, q)) {
         if (take_all) {
           sure |= 1ull << q;
         } else if (ranking) {
@@ -500,28 +524,32 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
     __syncthreads();
   }
 
-  // the row: sinks, marked candidates in position order, the recent window, padding
+  // the row: sinks, marked candidates in position order, the recent window, padding.
+  // Bitmap words go out in rounds of one word per thread (consecutive threads,
+  // consecutive words), each round a block scan of the words' counts.
   int32_t* dst = a.idx + static_cast<size_t>(row) * a.k;
   const int w_lo = sink_end >> 5;
   const int w_hi = (rb + 31) >> 5;
-  const int WPT = (w_hi - w_lo + kSelThreads - 1) / kSelThreads;
-  uint32_t c = 0;
-  for (int e = 0; e < WPT; ++e) {
-    const int w = w_lo + t * WPT + e;
-    if (w < w_hi) c += __popc(L.bitmap[w]);
-  }
-  uint32_t c_tot;
-  uint32_t o = static_cast<uint32_t>(sink_end) + block_excl_scan(c, sh.scan, &c_tot);
-  for (int e = 0; e < WPT; ++e) {
-    const int w = w_lo + t * WPT + e;
-    if (w >= w_hi) break;
-    uint32_t bits = L.bitmap[w];
+  uint32_t o_base = static_cast<uint32_t>(sink_end);
+  for (int w0 = w_lo; w0 < w_hi; w0 += kSelThreads) {
+    const int w = w0 + t;
+    uint32_t bits = w < w_hi ? L.bitmap[w] : 0u;
+    uint32_t r_tot;
+    uint32_t o = o_base + block_excl_scan(static_cast<uint32_t>(__popc(bits)), sh.scan, &r_tot);
     while (bits) {
       const int bit = __ffs(bits) - 1;
       bits &= bits - 1;
       if (o < static_cast<uint32_t>(n)) dst[o] = w * 32 + bit;
       ++o;
     }
+    o_base += r_tot;
+  }
+  if (a.out_bitmap != nullptr) {
+    // this pass's chosen candidates (the whole bitmap: every word was stored in D),
+    // for the next pass of the hybrid budget, and their number
+    for (int i = t; i < a.bm_words; i += kSelThreads)
+      a.out_bitmap[static_cast<size_t>(row) * a.bm_words + i] = L.bitmap[i];
+    if (t == 0) a.out_count[row] = static_cast<int>(o_base) - sink_end;
   }
   const int n_recent_kept = P - rb;
   for (int i = t; i < sink_end; i += kSelThreads) dst[i] = i;
@@ -576,6 +604,12 @@ cudaError_t launch_select(const SelectArgs& sa, cudaStream_t stream) {
   p.n_recent = sa.n_recent;
   p.chunk = chunk;
   p.bitmap_words = bitmap_words_for(chunk, CS);
+  p.m_limit = sa.m_limit;
+  p.pre_bitmap = sa.pre_bitmap;
+  p.pre_count = sa.pre_count;
+  p.out_bitmap = sa.out_bitmap;
+  p.out_count = sa.out_count;
+  p.bm_words = (sa.P_max + 31) / 32;
   const size_t smem = select_smem_bytes(chunk, CS);
   cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,

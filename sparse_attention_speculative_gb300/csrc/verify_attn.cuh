@@ -99,6 +99,7 @@ struct VParams {
   int B, Hq, Hkv, R, NV, max_blocks, num_blocks, P_max;
   int row0, row1;
   int collect_all;  // every verify row collected; partial sums over all rows
+  const uint8_t* head_mask;  // [Hq] or NULL: only heads with a non-zero byte are collected
   int pairs, t_max, max_chunks;
   float scale;
 };
@@ -462,6 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                              : 0;
       const Seg s = segment_at(v, v1, a);
       v = s.next_v;
+      // heads of this group whose logits are collected (all unless a mask is given)
+      uint32_t gmask = (G >= 32) ? 0xFFFFFFFFu : ((1u << G) - 1u);
+      if (a.head_mask != nullptr) {
+        gmask = 0u;
+#pragma unroll
+        for (int hl = 0; hl < G; ++hl)
+          gmask |= (__ldg(a.head_mask + s.g * G + hl) != 0 ? 1u : 0u) << hl;
+      }
       const long long first_v = static_cast<long long>(s.p) * a.t_max;
       const int c_first = cta_of(first_v, W, C);
       const int c_last = cta_of(first_v + a.t_max - 1, W, C);
@@ -535,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float acc = 0.f;
 #pragma unroll
           for (int hl = 0; hl < G; ++hl) {
+            if (!((gmask >> hl) & 1u)) continue;
             const float z0 = __uint_as_float(c0raw[hl]) * scale;
             if (a.logits)
               __stcs(a.logits + ((static_cast<size_t>(s.b) * 2 + 0) * a.Hq + s.g * G + hl) *
@@ -543,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int hl = 0; hl < G; ++hl) {
+            if (!((gmask >> hl) & 1u)) continue;
             const float z1 = __uint_as_float(c1raw[hl]) * scale;
             if (a.logits)
               __stcs(a.logits + ((static_cast<size_t>(s.b) * 2 + 1) * a.Hq + s.g * G + hl) *
@@ -557,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (split_collect && j < s.P) {
 #pragma unroll
           for (int hl = 0; hl < G; ++hl) {
+            if (!((gmask >> hl) & 1u)) continue;
             const float z = __uint_as_float(c0raw[hl]) * scale;
             if (a.logits)
               __stcs(a.logits + ((static_cast<size_t>(s.b) * 2 + half) * a.Hq + s.g * G + hl) *
@@ -569,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
             const int cc = col0 + c;
-            if (cc < a.NV) {
+            if (cc < a.NV && ((gmask >> (cc % G)) & 1u)) {
               const float z = sv[c] * scale;
               if (a.logits)
                 __stcs(a.logits + ((static_cast<size_t>(s.b) * a.R + cc / G) * a.Hq + s.g * G +
@@ -852,6 +864,7 @@ inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {
   p.row0 = va.row0;
   p.row1 = va.row1;
   p.collect_all = va.collect_all;
+  p.head_mask = va.head_mask;
   p.pairs = plan.pairs;
   p.t_max = plan.t_max;
   p.max_chunks = plan.max_chunks;

@@ -164,8 +164,8 @@ namespace {
 vsd_status verify_call(const vsd_geom* geom, int R, const void* q, const void* k_cache,
                        const void* v_cache, const int32_t* block_table,
                        const int32_t* prefix_len, bool collect_all, int collect_row0,
-                       int collect_row1, int P_max, float scale, float* logits,
-                       float* partial_scores, void* out, void* workspace,
+                       int collect_row1, const uint8_t* head_mask, int P_max, float scale,
+                       float* logits, float* partial_scores, void* out, void* workspace,
                        size_t workspace_bytes, void* stream) {
   vsd_status st = verify_checks(geom, R, P_max);
   if (st != VSD_OK) return st;
@@ -217,6 +217,7 @@ vsd_status verify_call(const vsd_geom* geom, int R, const void* q, const void* k
   va.row0 = collect_all ? 0 : collect_row0;
   va.row1 = collect_all ? 0 : collect_row1;
   va.collect_all = collect_all ? 1 : 0;
+  va.head_mask = head_mask;
   va.scale = scale;
   cudaError_t e = vsd::launch_verify(va, plan, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -232,8 +233,21 @@ vsd_status vsd_verify_attn_collect(const vsd_geom* geom, int R, const void* q,
                                    float* logits, float* partial_scores, void* out,
                                    void* workspace, size_t workspace_bytes, void* stream) {
   return verify_call(geom, R, q, k_cache, v_cache, block_table, prefix_len, false,
-                     collect_row0, collect_row1, P_max, scale, logits, partial_scores, out,
-                     workspace, workspace_bytes, stream);
+                     collect_row0, collect_row1, nullptr, P_max, scale, logits,
+                     partial_scores, out, workspace, workspace_bytes, stream);
+}
+
+vsd_status vsd_verify_attn_collect_srh(const vsd_geom* geom, int R, const void* q,
+                                       const void* k_cache, const void* v_cache,
+                                       const int32_t* block_table, const int32_t* prefix_len,
+                                       int collect_row0, int collect_row1,
+                                       const uint8_t* head_mask, int P_max, float scale,
+                                       float* logits, float* partial_scores, void* out,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (head_mask == nullptr) return VSD_ERR_INVALID_ARG;
+  return verify_call(geom, R, q, k_cache, v_cache, block_table, prefix_len, false,
+                     collect_row0, collect_row1, head_mask, P_max, scale, logits,
+                     partial_scores, out, workspace, workspace_bytes, stream);
 }
 
 vsd_status vsd_verify_attn_collect_all(const vsd_geom* geom, int R, const void* q,
@@ -242,8 +256,9 @@ vsd_status vsd_verify_attn_collect_all(const vsd_geom* geom, int R, const void* 
                                        int P_max, float scale, float* logits,
                                        float* partial_scores, void* out, void* workspace,
                                        size_t workspace_bytes, void* stream) {
-  return verify_call(geom, R, q, k_cache, v_cache, block_table, prefix_len, true, 0, 0, P_max,
-                     scale, logits, partial_scores, out, workspace, workspace_bytes, stream);
+  return verify_call(geom, R, q, k_cache, v_cache, block_table, prefix_len, true, 0, 0,
+                     nullptr, P_max, scale, logits, partial_scores, out, workspace,
+                     workspace_bytes, stream);
 }
 
 namespace {
@@ -421,6 +436,80 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
   sa.n_sink = n_sink;
   sa.n_recent = n_recent;
   cudaError_t e = vsd::launch_select(sa, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
+namespace {
+size_t hybrid_bitmap_bytes(int n_rows, int P_max) {
+  return (static_cast<size_t>(n_rows) * ((P_max + 31) / 32) * 4 + 255) / 256 * 256;
+}
+}  // namespace
+
+vsd_status vsd_select_hybrid_workspace_size(int n_rows, int P_max, size_t* bytes) {
+  if (bytes == nullptr || n_rows < 0 || P_max < 0) return VSD_ERR_INVALID_ARG;
+  if (vsd::select_chunk(P_max, vsd::select_cluster_size(P_max, n_rows)) < 0)
+    return VSD_ERR_UNSUPPORTED;
+  *bytes = hybrid_bitmap_bytes(n_rows, P_max) + (static_cast<size_t>(n_rows) * 4 + 255) / 256 * 256;
+  return VSD_OK;
+}
+
+vsd_status vsd_select_topk_hybrid(int n_rows, int Hkv_target, const float* partial_target,
+                                  int Hkv_draft, const float* partial_draft,
+                                  const int32_t* prefix_len, int P_max, int k, int m,
+                                  int n_sink, int n_recent, int32_t* idx, int32_t* n_sel,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_rows < 0 || Hkv_target < 1 || Hkv_draft < 1 || P_max < 0 || k < 1 || m < 0 ||
+      n_sink < 0 || n_recent < 0)
+    return VSD_ERR_INVALID_ARG;
+  if (static_cast<long long>(n_sink) + n_recent > k) return VSD_ERR_INVALID_ARG;
+  if (vsd::select_chunk(P_max, vsd::select_cluster_size(P_max, n_rows)) < 0)
+    return VSD_ERR_UNSUPPORTED;
+  if (n_rows == 0) return VSD_OK;
+  if (!partial_target || !partial_draft || !prefix_len || !idx || !n_sel)
+    return VSD_ERR_INVALID_ARG;
+  if (!aligned(partial_target, 16) || !aligned(partial_draft, 16) || !aligned(idx, 4) ||
+      !aligned(n_sel, 4) || !aligned(prefix_len, 4))
+    return VSD_ERR_INVALID_ARG;
+  size_t need = 0;
+  vsd_status st = vsd_select_hybrid_workspace_size(n_rows, P_max, &need);
+  if (st != VSD_OK) return st;
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return VSD_ERR_WORKSPACE;
+  unsigned* status = nullptr;
+  st = device_info(&status, nullptr);
+  if (st != VSD_OK) return st;
+  uint32_t* bitmap = static_cast<uint32_t*>(workspace);
+  int32_t* counts = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
+                                               hybrid_bitmap_bytes(n_rows, P_max));
+  // pass 1: the draft signal, at most m candidates; their bitmap and count
+  vsd::SelectArgs sa;
+  sa.partial = partial_draft;
+  sa.prefix_len = prefix_len;
+  sa.idx = idx;
+  sa.n_sel = n_sel;
+  sa.scores_out = nullptr;
+  sa.status = status;
+  sa.n_rows = n_rows;
+  sa.Hkv = Hkv_draft;
+  sa.P_max = P_max;
+  sa.k = k;
+  sa.n_sink = n_sink;
+  sa.n_recent = n_recent;
+  sa.m_limit = m;
+  sa.out_bitmap = bitmap;
+  sa.out_count = counts;
+  cudaError_t e = vsd::launch_select(sa, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  // pass 2: the target signal over the rest of the budget
+  sa.partial = partial_target;
+  sa.Hkv = Hkv_target;
+  sa.m_limit = -1;
+  sa.out_bitmap = nullptr;
+  sa.out_count = nullptr;
+  sa.pre_bitmap = bitmap;
+  sa.pre_count = counts;
+  e = vsd::launch_select(sa, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return VSD_OK;
 }

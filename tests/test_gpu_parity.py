@@ -527,3 +527,59 @@ def test_sparse_verify(d, Hq, Hkv, gamma, prefix, k):
     assert vsd.vsd_read_device_status() == 0
     diff = (out_all.float() - out_dense.float()).abs().max().item()
     assert diff <= 2e-2, diff
+
+
+@pytest.mark.parametrize("n_rows,P_max", [(3, 20000), (9, 9000)])
+def test_select_hybrid(n_rows, P_max):
+    """Dustin's hybrid budget: the draft signal picks up to m, the target signal fills
+    the rest; exact against the oracle fed the same fp32 sums the kernel decides on."""
+    vsd = _vsd()
+    rng = np.random.default_rng(n_rows)
+    prefix = rng.integers(0, P_max + 1, size=n_rows).astype(np.int32)
+    prefix[0] = P_max
+    pt = rng.integers(-4, 5, size=(n_rows, 4, P_max)).astype(np.float32)  # ties
+    pd = rng.normal(size=(n_rows, 2, P_max)).astype(np.float32)
+    tpt, tpd = torch.tensor(pt, device="cuda"), torch.tensor(pd, device="cuda")
+    tpl = torch.tensor(prefix, device="cuda")
+    st, sd = fp32_row_sum(pt), fp32_row_sum(pd)
+    for k, m, ns, nr in [(512, 0, 4, 64), (512, 100, 4, 64), (300, 1000, 16, 32), (64, 5, 0, 0)]:
+        idx, n_sel = vsd.vsd_select_topk_hybrid(tpt, tpd, tpl, k=k, m=m, n_sink=ns, n_recent=nr)
+        torch.cuda.synchronize()
+        assert vsd.vsd_read_device_status() == 0
+        ri, rn = oracle.select_hybrid(st, sd, prefix, k=k, m=m, n_sink=ns, n_recent=nr)
+        gi, gn = idx.cpu().numpy(), n_sel.cpu().numpy()
+        for r in range(n_rows):
+            assert gn[r] == rn[r], (k, m, r)
+            np.testing.assert_array_equal(gi[r, :gn[r]], ri[r, :rn[r]])
+            assert np.all(gi[r, gn[r]:] == -1)
+
+
+def test_verify_collect_srh_head_mask():
+    """Collected importance restricted to a set of query heads (semantic retrieval
+    heads): masked-in logits and the masked partial sums against the oracle; the
+    masked-out heads' logits are not written."""
+    from sparse_attention_speculative_gb300.synth import host_arrays, make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    for Hq, Hkv, gamma in ((32, 8, 4), (64, 8, 5)):
+        w = Workload("srh", B=2, P=5000, Hq=Hq, Hkv=Hkv, d=128, gamma=gamma, k=256, n_sink=4,
+                     n_recent=32, seed=71, prefix_lens=(5000, 1234))
+        batch = make_batch(w, "cuda")
+        mask = np.array([1 if (h * 7) % 5 < 2 else 0 for h in range(Hq)], np.uint8)
+        out, logits, partial = vsd.vsd_verify_attn_collect_srh(
+            batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+            torch.tensor(mask, device="cuda"), P_max=w.P_max, scale=w.scale)
+        torch.cuda.synchronize()
+        assert vsd.vsd_read_device_status() == 0
+        h = host_arrays(batch)
+        o_ref, l_ref, _ = oracle.verify(h["q"], h["k_cache"], h["v_cache"], h["block_table"],
+                                        h["prefix_len"], scale=w.scale, P_max=w.P_max)
+        p_ref = oracle.partial_masked(l_ref, h["prefix_len"], mask, Hkv)
+        assert_attn_close(out.float().cpu().numpy(), o_ref, "srh verify output")
+        lg, pa = logits.cpu().numpy(), partial.cpu().numpy()
+        for b, P in enumerate(w.prefix()):
+            assert_rel_close(pa[b, :, :P], p_ref[b, :, :P], "srh partial scores")
+            on = np.nonzero(mask)[0]
+            off = np.nonzero(mask == 0)[0]
+            assert_rel_close(lg[b][:, on, :P], l_ref[b][:, on, :P], "srh logits")
+            assert np.all(lg[b][:, off, :] == 0)
