@@ -63,10 +63,12 @@ def _load():
             lib.oracle_select.argtypes = [I, I, P, P, I, I, I, P, P]
             lib.oracle_sparse_decode.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, I, P,
                                                  P, D, P]
+            lib.oracle_block_topk.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, I, D, P, I,
+                                              P]
             for name in ("oracle_verify", "oracle_verify_all_rows", "oracle_score_from_logits",
                          "oracle_score_from_partials", "oracle_select", "oracle_sparse_decode",
                          "oracle_sparse_verify", "oracle_select_hybrid", "oracle_partial_masked",
-                         "oracle_num_threads"):
+                         "oracle_block_topk", "oracle_num_threads"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -263,3 +265,25 @@ def partial_masked(logits, prefix_len, head_mask, Hkv):
     _check(_load().oracle_partial_masked(B, C, Hq, Hkv, P_max, _ptr(lg), _ptr(pl), _ptr(hm),
                                          _ptr(partial)), "oracle_partial_masked")
     return partial
+
+
+def block_topk(q, k_cache, block_table, prefix_len, *, kb, scale, page_blocks_max=None):
+    """Per-query block top-k: block scores r [B, R, Hq, page_blocks_max] (the scaled dot
+    product of each query with each prefix page's mean key; 0 past the prefix) and the
+    kb best pages of every (b, t, h), ascending, padded with -1: blocks [B, R, Hq, kb]."""
+    q = _u16(q)
+    k_cache = _u16(k_cache)
+    bt = _i32(block_table)
+    pl = _i32(prefix_len)
+    B, R, Hq, d = q.shape
+    NB, Hkv, page, d2 = k_cache.shape
+    assert d2 == d and bt.shape[0] == B
+    if page_blocks_max is None:
+        page_blocks_max = max([(int(p) + page - 1) // page for p in pl] + [1])
+    scores = np.zeros((B, R, Hq, page_blocks_max), dtype=np.float64)
+    blocks = np.full((B, R, Hq, kb), -1, dtype=np.int32)
+    _check(_load().oracle_block_topk(B, Hq, Hkv, d, page, bt.shape[1], NB, R, _ptr(q),
+                                     _ptr(k_cache), _ptr(bt), _ptr(pl), int(kb), float(scale),
+                                     _ptr(scores), int(page_blocks_max), _ptr(blocks)),
+           "oracle_block_topk")
+    return scores, blocks

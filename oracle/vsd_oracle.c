@@ -461,6 +461,74 @@ int oracle_partial_masked(int B, int C, int Hq, int Hkv, int P_max, const double
 }
 
 /*
+ * Per-query block top-k (the sparse-verification summary, "Sparse Verification
+ * Engine", attention sparsity: each query keeps only its top-k keys/values in
+ * structured blocks, chosen by a cheap relevance score).  Reading taken here: the
+ * blocks are the 16-token pages of the prefix, the cheap score of block beta for a
+ * query is the scaled dot product with the block's mean key
+ *   kbar[b][beta][g][:] = mean over j in block beta, j < P_b, of K[b][j][g][:]
+ *   r[b][t][h][beta]    = scale * <q[b][t][h][:], kbar[b][beta][h/G][:]>
+ * and each (b, t, h) keeps the kb blocks with the highest r (ties: lower block
+ * first), listed in ascending block order: blocks[b][t][h][0 .. min(kb, nblk_b)),
+ * nblk_b = ceil(P_b / page); unused entries -1.
+ */
+int oracle_block_topk(int B, int Hq, int Hkv, int d, int page, int max_blocks, int num_blocks,
+                      int R, const uint16_t *q, const uint16_t *k_cache,
+                      const int32_t *block_table, const int32_t *prefix_len, int kb,
+                      double scale, double *scores_out, int P_blk_max, int32_t *blocks) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page <= 0 || R <= 0 ||
+        kb <= 0)
+        return ORACLE_BAD_ARG;
+    const int G = Hq / Hkv;
+    int status = ORACLE_OK;
+    const int n_items = B * R * Hq;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int item = 0; item < n_items; ++item) {
+        int b = item / (R * Hq);
+        int t = (item / Hq) % R;
+        int h = item % Hq;
+        int g = h / G;
+        int P = prefix_len[b];
+        int nblk = (P + page - 1) / page;
+        if (P < 0 || nblk > P_blk_max) { status = ORACLE_BAD_ARG; continue; }
+        scored_pos *sc = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)(nblk > 0 ? nblk : 1));
+        double *kbar = (double *)malloc(sizeof(double) * (size_t)d);
+        int *chosen = (int *)malloc(sizeof(int) * (size_t)kb);
+        if (!sc || !kbar || !chosen) {
+            status = ORACLE_NO_MEMORY;
+        } else {
+            const uint16_t *qr = q + (((size_t)b * R + t) * Hq + h) * d;
+            for (int beta = 0; beta < nblk; ++beta) {
+                int j0 = beta * page, j1 = j0 + page < P ? j0 + page : P;
+                for (int c = 0; c < d; ++c) kbar[c] = 0.0;
+                int bad = 0;
+                for (int j = j0; j < j1; ++j) {
+                    const uint16_t *kr = kv_row(k_cache, block_table, b, max_blocks, num_blocks,
+                                                Hkv, page, d, j, g);
+                    if (!kr) { bad = 1; break; }
+                    for (int c = 0; c < d; ++c) kbar[c] += bf16_to_double(kr[c]);
+                }
+                if (bad) { status = ORACLE_BAD_INDEX; nblk = 0; break; }
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c) dot += bf16_to_double(qr[c]) * (kbar[c] / (j1 - j0));
+                sc[beta].s = scale * dot;
+                sc[beta].j = beta;
+                if (scores_out)
+                    scores_out[(((size_t)b * R + t) * Hq + h) * P_blk_max + beta] = sc[beta].s;
+            }
+            qsort(sc, (size_t)nblk, sizeof(scored_pos), by_score_then_position);
+            int n = kb < nblk ? kb : nblk;
+            for (int m = 0; m < n; ++m) chosen[m] = sc[m].j;
+            qsort(chosen, (size_t)n, sizeof(int), by_int);
+            int32_t *dst = blocks + (((size_t)b * R + t) * Hq + h) * kb;
+            for (int m = 0; m < kb; ++m) dst[m] = m < n ? chosen[m] : -1;
+        }
+        free(sc); free(kbar); free(chosen);
+    }
+    return status;
+}
+
+/*
  * Sparse draft-step attention.
  *   [Vegas] sec. 2, drafting phase: the draft step uses attention restricted to the
  *   selected KV entries.  sec. 3: this is paged attention with page size 1 whose

@@ -527,3 +527,124 @@ def test_partial_masked_closed_form():
                     if mask[h]:
                         want += scale * ((t + 1) * ((j % 7) - 3) + (h + 1) * (g + 1) + (b + 1))
             np.testing.assert_allclose(got[b, g, :P], want, rtol=0, atol=1e-10)
+
+
+# --------------------------------------------------------------------------------------
+# per-query block top-k (the sparse-verification summary, "Sparse Verification Engine":
+# each query keeps its top-k key/value blocks by a cheap relevance score; the score read
+# here is the query's scaled dot product with the page's mean key)
+# --------------------------------------------------------------------------------------
+
+def test_block_topk_scores_closed_form():
+    """On the structured input the logit of key j is known in closed form, so the page
+    score is that closed form averaged over the page's prefix rows (rows at or past the
+    prefix length, which hold the verify block's keys, are excluded)."""
+    s = _structured_verify(prefix=(37, 50), R=3)
+    scale = 1.0 / math.sqrt(s["d"])
+    R, Hq, G = s["R"], s["Hq"], s["G"]
+    scores, blocks = oracle.block_topk(s["q"], s["k"], s["table"], s["prefix"], kb=2,
+                                       scale=scale, page_blocks_max=5)
+    for b, P in enumerate(s["prefix"]):
+        nblk = (P + 15) // 16
+        for t in range(R):
+            for h in range(Hq):
+                for beta in range(nblk):
+                    j = np.arange(16 * beta, min(16 * beta + 16, P))
+                    want = scale * np.mean((t + 1) * ((j % 7) - 3) + (h + 1) * (h // G + 1)
+                                           + (b + 1))
+                    assert abs(scores[b, t, h, beta] - want) <= 1e-12
+                assert np.all(scores[b, t, h, nblk:] == 0)
+
+
+def _small_random_blocks(seed, prefix, Hq=4, Hkv=2, d=64, R=2, page=16):
+    rng = np.random.default_rng(seed)
+    lengths = [p + R for p in prefix]
+    table, NB, Ks, _ = _random_paged(rng, lengths, Hkv, d, page, seed)
+    q = bf16_round_bits(rng.normal(size=(len(prefix), R, Hq, d)))
+    return q, paged_cache(Ks, table, NB, page), table, np.array(prefix, np.int32)
+
+
+@pytest.mark.parametrize("kb", [1, 3, 5])
+def test_block_topk_matches_bruteforce(kb):
+    """For up to 9 pages, enumerate every kb-subset of pages; the chosen set maximises
+    the summed page score (ties to the lexicographically smallest set)."""
+    q, kc, table, prefix = _small_random_blocks(31 + kb, [130, 75, 16])
+    scores, blocks = oracle.block_topk(q, kc, table, prefix, kb=kb, scale=0.125)
+    B, R, Hq, _ = q.shape
+    for b, P in enumerate(prefix):
+        nblk = (P + 15) // 16
+        for t in range(R):
+            for h in range(Hq):
+                sc = scores[b, t, h, :nblk]
+                best, best_set = None, None
+                for T in itertools.combinations(range(nblk), min(kb, nblk)):
+                    total = sum(sc[i] for i in T)
+                    if best is None or total > best + 1e-12:
+                        best, best_set = total, T
+                got = blocks[b, t, h]
+                assert list(got[:len(best_set)]) == list(best_set)
+                assert np.all(got[len(best_set):] == -1)
+
+
+def test_block_topk_each_head_finds_its_planted_page():
+    """Heads of one KV group share keys but not queries: with orthogonal queries and one
+    page planted along each head's query, every head's top page is its own."""
+    B, R, Hq, Hkv, d, page = 1, 2, 8, 2, 64, 16
+    G = Hq // Hkv
+    P = 16 * 12
+    rng = np.random.default_rng(5)
+    q = np.zeros((B, R, Hq, d), np.float32)
+    for t in range(R):
+        for h in range(Hq):
+            q[0, t, h, h] = 1.0 + t
+    K = bits_to_float(bf16_round_bits(0.05 * rng.normal(size=(P + R, Hkv, d)))).astype(np.float32)
+    planted = {}
+    for h in range(Hq):
+        g = h // G
+        beta = 1 + (5 * h + 3) % 11
+        while beta in planted.values():
+            beta = 1 + beta % 11
+        planted[h] = beta
+        K[16 * beta:16 * beta + 16, g, h] += 4.0
+    K = bits_to_float(bf16_round_bits(K)).astype(np.float32)
+    table, NB = make_table([P + R], page, shuffle_seed=3)
+    kc = paged_cache([K], table, NB, page)
+    _, blocks = oracle.block_topk(bf16_bits(q), kc, table, np.array([P], np.int32), kb=1,
+                                  scale=0.125)
+    for t in range(R):
+        for h in range(Hq):
+            assert blocks[0, t, h, 0] == planted[h], (t, h)
+
+
+def test_block_topk_budget_limits_and_ties():
+    q, kc, table, prefix = _small_random_blocks(9, [0, 40, 64])
+    _, blocks = oracle.block_topk(q, kc, table, prefix, kb=6, scale=0.125)
+    assert np.all(blocks[0] == -1)                                  # empty prefix
+    assert np.all(blocks[1, :, :, :3] == np.arange(3))              # 3 pages, all kept
+    assert np.all(blocks[1, :, :, 3:] == -1)
+    assert np.all(blocks[2, :, :, :4] == np.arange(4))
+    # identical keys everywhere: every page scores the same, the lowest pages win
+    kc_same = np.broadcast_to(kc[:1, :, :1, :], kc.shape).copy()
+    scores, blocks = oracle.block_topk(q, kc_same, table, prefix, kb=2, scale=0.125)
+    assert np.all(blocks[1:, :, :, :] == np.array([0, 1]))
+    for b in (1, 2):
+        nblk = (prefix[b] + 15) // 16
+        assert np.all(scores[b, :, :, :nblk] == scores[b, :, :, :1])
+
+
+def test_block_topk_block_table_permutation_invariance():
+    rng = np.random.default_rng(12)
+    d, page, R, Hq, Hkv = 64, 16, 3, 8, 2
+    prefix = [200, 77]
+    lengths = [p + R for p in prefix]
+    Ks = [bits_to_float(bf16_round_bits(rng.normal(size=(L, Hkv, d)))).astype(np.float32)
+          for L in lengths]
+    q = bf16_round_bits(rng.normal(size=(2, R, Hq, d)))
+    results = []
+    for seed in (None, 4, 9):
+        table, NB = make_table(lengths, page, shuffle_seed=seed, extra_blocks=3)
+        results.append(oracle.block_topk(q, paged_cache(Ks, table, NB, page, fill=9.0), table,
+                                         prefix, kb=4, scale=0.125))
+    for other in results[1:]:
+        for a, b in zip(results[0], other):
+            np.testing.assert_array_equal(a, b)
