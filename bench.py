@@ -364,6 +364,32 @@ def run_gpu(args, world, rank, local):
             v1.record(stream)
             torch.cuda.synchronize()
             per["srh_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
+        # the contrasting per-query block top-k (page mean keys, then per-(t, h) page
+        # scores and top kb = k / 16 pages: the same token budget per query)
+        per["page_means_b2b"], per["block_topk_b2b"] = [], []
+        nblk_max = vsd.page_blocks(P_max)
+        kb = max(1, w.k // 16)
+        means = torch.zeros((B, w.Hkv, nblk_max, d), dtype=torch.float32, device=dev)
+        bscores = torch.zeros((B, R, Hq, nblk_max), dtype=torch.float32, device=dev)
+        bblocks = torch.empty((B, R, Hq, kb), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            torch.cuda.synchronize()
+            torch.cuda._sleep(sleep_cycles)
+            v0.record(stream)
+            for _ in range(B2B_CALLS):
+                vsd.vsd_page_key_means(batch.k_cache, batch.block_table, batch.prefix_len, B=B,
+                                       page_blocks_max=nblk_max, page_means=means)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            per["page_means_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
+            torch.cuda._sleep(sleep_cycles)
+            v0.record(stream)
+            for _ in range(B2B_CALLS):
+                vsd.vsd_block_topk(batch.q, means, batch.prefix_len, kb=kb, scale=w.scale,
+                                   scores=bscores, blocks=bblocks)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            per["block_topk_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
         # the same, collecting every verify row (the selection equation as printed):
         # what Collect-2-Query saves
         per["verify_all_b2b"] = []
@@ -453,6 +479,17 @@ def run_gpu(args, world, rank, local):
         "hybrid_select_us": statistics.median(per["hybrid_b2b"]) * 1e6,
         "select_back_to_back_us": statistics.median(per["select_b2b"]) * 1e6,
         "srh_verify_us": statistics.median(per["srh_b2b"]) * 1e6,
+        "block_topk": {
+            "kb_pages": kb,
+            "page_means_us": statistics.median(per["page_means_b2b"]) * 1e6,
+            "page_means_gbs": sum(P * w.Hkv * d * 2 + ((P + 15) // 16) * w.Hkv * d * 4
+                                  for P in prefix) / statistics.median(per["page_means_b2b"])
+                              * 1e-9,
+            "scores_and_topk_us": statistics.median(per["block_topk_b2b"]) * 1e6,
+            "note": "per-query block-sparse top-k: mean key of every 16-token page (a full "
+                    "recompute; a decode loop refreshes only the last page), then every "
+                    "(verify row, head) scores the pages and keeps its kb best; back-to-back "
+                    "calls"},
         "collect2_vs_all_rows": None if not per["verify_all_b2b"] else {
             "collect2_us": t_verify_b2b * 1e6,
             "all_rows_us": statistics.median(per["verify_all_b2b"]) * 1e6,

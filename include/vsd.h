@@ -315,6 +315,51 @@ vsd_status vsd_sparse_verify_attn(const vsd_geom* geom, int R, const void* q,
                                   size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------
+ * Per-query block top-k (the sparse-verification summary, "Sparse Verification
+ * Engine", attention sparsity: each query keeps only its top-k key/value blocks in
+ * structured block sparsity, chosen by a cheap relevance score).  A contrasting
+ * selector to the aggregated one above: the kept set differs per head and verify row.
+ * Blocks are the 16-token pages of the prefix; the cheap score of a page is the
+ * query's scaled dot product with the page's mean key.
+ *
+ * vsd_page_key_means: for every sequence b and page beta in
+ * [page_begin[b], ceil(P_b / 16)),
+ *   page_means[b][g][beta][:] = mean of K[b, j, g, :] over j in [16 beta, 16 beta + 16),
+ *                               j < P_b          (fp32)
+ *   page_means  fp32 [B][Hkv][page_blocks_max][head_dim], caller-owned; pages outside
+ *               the range are not written (a decode loop passes page_begin to refresh
+ *               only the pages that changed)
+ *   page_begin  int32 [B] or NULL (all pages); a negative entry is flagged
+ *               VSD_DEV_BAD_LENGTH
+ *   prefix_len  int32 [B]; P_b <= max_blocks_per_seq * 16 and
+ *               ceil(P_b / 16) <= page_blocks_max, else VSD_DEV_BAD_LENGTH and the
+ *               sequence is skipped
+ * A block-table entry outside [0, num_blocks) is flagged VSD_DEV_BAD_BLOCK and that
+ * page's mean is written as zeros.
+ *
+ * vsd_block_topk: for every b, verify row t < R and query head h,
+ *   scores[b][t][h][beta] = scale * <q[b,t,h,:], page_means[b][h/G][beta][:]>
+ *                           for beta < ceil(P_b / 16) (fp32; later entries not written)
+ *   blocks[b][t][h][0 .. min(kb, nblk_b)) = the kb pages with the highest score,
+ *                           ties to the lower page, ascending; the rest -1
+ *   q           bf16 [B][R][Hq][head_dim]
+ *   scores      fp32 [B][R][Hq][page_blocks_max], caller-owned (also the selection's
+ *               input, read back on the same stream)
+ *   blocks      int32 [B][R][Hq][kb], caller-owned
+ * Supported: head_dim 64 or 128, G a power of two, R * G <= 64, page_size 16,
+ * 0 <= page_blocks_max <= 16384 (prefixes up to 262144 tokens), kb >= 1,
+ * B * R * Hq <= 2^31 - 1.  Pointers 16-byte aligned (int32 arrays 4-byte).
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_page_key_means(const vsd_geom* geom, const void* k_cache,
+                              const int32_t* block_table, const int32_t* prefix_len,
+                              const int32_t* page_begin, int page_blocks_max,
+                              float* page_means, void* stream);
+
+vsd_status vsd_block_topk(const vsd_geom* geom, int R, const void* q, const float* page_means,
+                          const int32_t* prefix_len, int page_blocks_max, int kb, float scale,
+                          float* scores, int32_t* blocks, void* stream);
+
+/* ------------------------------------------------------------------------------
  * Device status word and errors.
  * vsd_read_device_status synchronizes `stream`, returns the accumulated
  * VSD_DEV_* bits of every kernel of this library on the current device since the

@@ -77,6 +77,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_select_topk.argtypes = [I, I, P, P, I, I, I, I, P, P, P, P, SZ, P]
         lib.vsd_sparse_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
         lib.vsd_sparse_decode_attn.argtypes = [GP, P, P, P, P, P, P, I, P, P, I, F, P, P, SZ, P]
+        lib.vsd_page_key_means.argtypes = [GP, P, P, P, P, I, P, P]
+        lib.vsd_block_topk.argtypes = [GP, I, P, P, P, I, I, F, P, P, P]
         lib.vsd_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
         lib.vsd_get_error_string.argtypes = [I]
         lib.vsd_get_error_string.restype = ctypes.c_char_p
@@ -88,7 +90,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                      "vsd_sparse_verify_attn",
                      "vsd_verify_attn_collect_noalloc",
                      "vsd_select_workspace_size", "vsd_select_topk", "vsd_sparse_workspace_size",
-                     "vsd_sparse_decode_attn", "vsd_read_device_status", "vsd_last_cuda_error"):
+                     "vsd_sparse_decode_attn", "vsd_page_key_means", "vsd_block_topk",
+                     "vsd_read_device_status", "vsd_last_cuda_error"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -405,3 +408,54 @@ def vsd_select_topk_hybrid(partial_target, partial_draft, prefix_len, *, k: int,
                                     _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "vsd_select_topk_hybrid")
     return idx, n_sel
+
+
+def page_blocks(P_max: int) -> int:
+    """Pages of 16 tokens covering a prefix of P_max tokens."""
+    return (int(P_max) + 15) // 16
+
+
+def vsd_page_key_means(k_cache, block_table, prefix_len, *, B: int, page_blocks_max: int,
+                       page_begin=None, page_means=None, stream=None):
+    """Mean key of every prefix page: fp32 [B, Hkv, page_blocks_max, d] (pages from
+    page_begin[b], default 0, to ceil(P_b / 16) are written).  Returns page_means."""
+    lib = load()
+    _need(prefix_len, torch.int32, "prefix_len")
+    if page_begin is not None:
+        _need(page_begin, torch.int32, "page_begin")
+    Hkv, d = int(k_cache.shape[1]), int(k_cache.shape[3])
+    geom = geom_for(B, Hkv, k_cache, block_table)
+    if page_means is None:
+        page_means = torch.zeros((B, Hkv, page_blocks_max, d), dtype=torch.float32,
+                                 device=k_cache.device)
+    rc = lib.vsd_page_key_means(ctypes.byref(geom), _ptr(k_cache), _ptr(block_table),
+                                _ptr(prefix_len), _ptr(page_begin), int(page_blocks_max),
+                                _ptr(page_means), _stream(stream))
+    _check(rc, "vsd_page_key_means")
+    return page_means
+
+
+def vsd_block_topk(q, page_means, prefix_len, *, kb: int, scale: float, k_cache=None,
+                   block_table=None, scores=None, blocks=None, stream=None):
+    """Per-query page scores fp32 [B, R, Hq, page_blocks_max] and the kb best pages of
+    every (b, t, h), ascending and padded with -1: int32 [B, R, Hq, kb].  q: bf16
+    [B, R, Hq, d]; page_means from vsd_page_key_means.  Returns (scores, blocks)."""
+    lib = load()
+    B, R, Hq, d = q.shape
+    _need(q, torch.bfloat16, "q")
+    _need(page_means, torch.float32, "page_means")
+    _need(prefix_len, torch.int32, "prefix_len")
+    Hkv, nblk = int(page_means.shape[1]), int(page_means.shape[2])
+    geom = Geom(B, Hq, Hkv, d, 16, 1, 1)
+    if k_cache is not None:
+        geom = geom_for(B, Hq, k_cache, block_table)
+    dev = q.device
+    if scores is None:
+        scores = torch.zeros((B, R, Hq, nblk), dtype=torch.float32, device=dev)
+    if blocks is None:
+        blocks = torch.empty((B, R, Hq, kb), dtype=torch.int32, device=dev)
+    rc = lib.vsd_block_topk(ctypes.byref(geom), R, _ptr(q), _ptr(page_means), _ptr(prefix_len),
+                            nblk, int(kb), float(scale), _ptr(scores), _ptr(blocks),
+                            _stream(stream))
+    _check(rc, "vsd_block_topk")
+    return scores, blocks

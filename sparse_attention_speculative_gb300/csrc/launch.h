@@ -113,4 +113,26 @@ struct SparseVerifyArgs {
 int sparse_verify_pages(int k_max, int R);
 cudaError_t launch_sparse_verify_gather(const SparseVerifyArgs& a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- per-query block top-k
+// Page mean keys kbar [B][Hkv][nblk_max][d] fp32, page scores [B][R][Hq][nblk_max] fp32,
+// kept pages [B][R][Hq][kb] int32 (ascending, padded with -1).
+struct BlockTopkArgs {
+  const void* k_cache;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const int32_t* page_begin;  // [B] first page to (re)compute, or null for 0
+  const void* q;              // bf16 [B][R][Hq][d]
+  float* kbar;
+  float* scores;
+  int32_t* blocks;
+  unsigned* status;
+  int B, R, Hq, Hkv, G, d, max_blocks, num_blocks, nblk_max, kb;
+  float scale;
+};
+
+// Threads' item count of the selection kernel for nblk_max pages, -1 above 16384.
+int block_select_items(int nblk_max);
+cudaError_t launch_page_means(const BlockTopkArgs& a, cudaStream_t stream);
+cudaError_t launch_block_topk(const BlockTopkArgs& a, cudaStream_t stream);
+
 }  // namespace vsd

@@ -584,4 +584,85 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
   return VSD_OK;
 }
 
+vsd_status vsd_page_key_means(const vsd_geom* geom, const void* k_cache,
+                              const int32_t* block_table, const int32_t* prefix_len,
+                              const int32_t* page_begin, int page_blocks_max,
+                              float* page_means, void* stream) {
+  vsd_status st = check_geom(geom);
+  if (st != VSD_OK) return st;
+  if (page_blocks_max < 0) return VSD_ERR_INVALID_ARG;
+  if (vsd::block_select_items(page_blocks_max) < 0 || geom->B > 65535 || geom->Hkv > 65535)
+    return VSD_ERR_UNSUPPORTED;
+  if (geom->B == 0 || page_blocks_max == 0) return VSD_OK;
+  if (!k_cache || !block_table || !prefix_len || !page_means) return VSD_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(page_means, 16) || !aligned(block_table, 4) ||
+      !aligned(prefix_len, 4) || !aligned(page_begin, 4))
+    return VSD_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  st = device_info(&status, nullptr);
+  if (st != VSD_OK) return st;
+  vsd::BlockTopkArgs a = {};
+  a.k_cache = k_cache;
+  a.block_table = block_table;
+  a.prefix_len = prefix_len;
+  a.page_begin = page_begin;
+  a.kbar = page_means;
+  a.status = status;
+  a.B = geom->B;
+  a.Hq = geom->Hq;
+  a.Hkv = geom->Hkv;
+  a.G = geom->Hq / geom->Hkv;
+  a.d = geom->head_dim;
+  a.max_blocks = geom->max_blocks_per_seq;
+  a.num_blocks = geom->num_blocks;
+  a.nblk_max = page_blocks_max;
+  cudaError_t e = vsd::launch_page_means(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
+vsd_status vsd_block_topk(const vsd_geom* geom, int R, const void* q, const float* page_means,
+                          const int32_t* prefix_len, int page_blocks_max, int kb, float scale,
+                          float* scores, int32_t* blocks, void* stream) {
+  vsd_status st = check_geom(geom);
+  if (st != VSD_OK) return st;
+  if (R < 1 || kb < 1 || page_blocks_max < 0) return VSD_ERR_INVALID_ARG;
+  const int G = geom->Hq / geom->Hkv;
+  if (R * G > 64 || vsd::block_select_items(page_blocks_max) < 0 || geom->B > 65535 ||
+      geom->Hkv > 65535)
+    return VSD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(geom->B) * R * geom->Hq > 0x7FFFFFFFll) return VSD_ERR_UNSUPPORTED;
+  if (geom->B == 0) return VSD_OK;
+  if (!q || !prefix_len || !blocks || (page_blocks_max > 0 && (!page_means || !scores)))
+    return VSD_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(page_means, 16) || !aligned(scores, 16) ||
+      !aligned(prefix_len, 4) || !aligned(blocks, 4))
+    return VSD_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return VSD_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  st = device_info(&status, nullptr);
+  if (st != VSD_OK) return st;
+  vsd::BlockTopkArgs a = {};
+  a.prefix_len = prefix_len;
+  a.q = q;
+  a.kbar = const_cast<float*>(page_means);
+  a.scores = scores;
+  a.blocks = blocks;
+  a.status = status;
+  a.B = geom->B;
+  a.R = R;
+  a.Hq = geom->Hq;
+  a.Hkv = geom->Hkv;
+  a.G = G;
+  a.d = geom->head_dim;
+  a.max_blocks = geom->max_blocks_per_seq;
+  a.num_blocks = geom->num_blocks;
+  a.nblk_max = page_blocks_max;
+  a.kb = kb;
+  a.scale = scale;
+  cudaError_t e = vsd::launch_block_topk(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
 }  // extern "C"
