@@ -11,18 +11,20 @@
 // and spreads the list over the SMs in splits of 128 positions:
 //   * The attended list of one (sequence, KV head) pair, idx[0 .. n_sel) followed by
 //     [tail_start, seq_len), is cut into splits of 128 positions (more per split
-//     only when the list is very long); one CTA of eight warps takes one split, each
-//     warp 16 positions.
+//     only when the list is very long); one CTA takes one split: sixteen warps of 8
+//     positions for up to 4 query heads per KV head, eight warps of 16 beyond.  The work of a warp is a short dependent chain (loads, dot
+//     products, shuffles, softmax, P.V), so the split is spread over many warps: the
+//     SM hides one warp's latencies behind the others'.
 //   * A row of K or V is read by head_dim/8 adjacent lanes, 16 bytes each, so one
 //     warp instruction fetches whole rows of 2 (head_dim 128) or 4 (64) keys and the
-//     16 keys of a warp take 8 or 4 instructions for K and as many for V, all in
+//     8 (16) keys of a warp take 4 or 2 (8 or 4) instructions for K and as many for V, all in
 //     flight together (the first index loads are issued speculatively, before the
 //     list lengths are known).
 //   * Each lane forms partial dot products of its 8 dims with the G queries of the
 //     group (fp32, q in shared memory); a shuffle tree over the row's lanes
-//     completes the logits.  The warp softmax over its 16 keys and the P.V product
+//     completes the logits.  The warp softmax over its keys and the P.V product
 //     on the lane's 8 dims follow in registers.
-//   * The eight warps merge in shared memory in a fixed order.  A pair with a single
+//   * The warps merge in shared memory in a fixed order.  A pair with a single
 //     split writes its output directly; otherwise each split writes (m, l, o) to the
 //     workspace and the split that finishes last (a per-pair counter in the
 //     workspace, reset to zero by that split) combines them with all its threads,
@@ -37,10 +39,17 @@
 namespace vsd {
 namespace {
 
-constexpr int kSWarps = 8;
-constexpr int kSThreads = kSWarps * 32;
-constexpr int kKeysPerWarp = 16;
-constexpr int kBatch = kSWarps * kKeysPerWarp;  // positions per CTA per batch
+constexpr int kBatch = 128;  // positions per CTA per batch
+
+// Warps per CTA and keys per warp for G query heads per KV head: sixteen warps of 8
+// keys while a warp's G * 8 accumulators leave room (512 threads get 128 registers
+// each), eight warps of 16 keys beyond.
+template <int G>
+struct SCfg {
+  static constexpr int kWarps = G <= 4 ? 16 : 8;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kKeysPerWarp = kBatch / kWarps;
+};
 constexpr int kPageS = 16;
 constexpr int kMaxSplits = 1024;
 
@@ -65,22 +74,22 @@ struct SParams {
 
 // Thread layout of one warp's batch for head dimension D: a K / V row is read by
 // LPR = D / 8 lanes (8 dims = 16 bytes each), one instruction covers KPI = 32 / LPR
-// rows, and the warp's 16 keys take U = 16 / KPI instructions ("slots").
-template <int D>
+// rows, and the warp's keys take U = keys / KPI instructions ("slots").
+template <int D, int G>
 struct SLayout {
   static constexpr int LPR = D / 8;
   static constexpr int KPI = 32 / LPR;
-  static constexpr int U = kKeysPerWarp / KPI;
+  static constexpr int U = SCfg<G>::kKeysPerWarp / KPI;
 };
 
 template <int D, int G>
 struct SSmem {
   float q[G][D];
-  float wm[kSWarps][G];
-  float wl[kSWarps][G];
+  float wm[SCfg<G>::kWarps][G];
+  float wl[SCfg<G>::kWarps][G];
   union {
-    float wo[kSWarps][G][D];
-    float merge_scratch[kSThreads * 6];  // m, l and a float4 o per thread
+    float wo[SCfg<G>::kWarps][G][D];
+    float merge_scratch[SCfg<G>::kThreads * 6];  // m, l and a float4 o per thread
   };
 };
 
@@ -108,8 +117,8 @@ __device__ __forceinline__ SList attended_list(int ns, int t0, int t1, const SPa
 // Combine the n partial (m, l, o) of one pair's splits and write its G output rows.
 // Thread = (float4 group of (head, dims), part); part p takes splits p, p + kParts,
 // ... with all loads of a round in flight; the parts then combine in shared memory.
-template <int D, int G>
-__device__ __forceinline__ void merge_splits(const SParams& a, SSmem<D, G>& sm, int pair, int b,
+template <int D, int G, int kSThreads>
+__device__ __forceinline__ void merge_splits(const SParams& a, float* scratch, int pair, int b,
                                              int g, int n) {
   constexpr int kQ = D / 4;
   constexpr int NG = G * kQ;                              // float4 groups of the output
@@ -176,7 +185,7 @@ __device__ __forceinline__ void merge_splits(const SParams& a, SSmem<D, G>& sm, 
   }
   if constexpr (kParts > 1) {
     // parts meet in shared memory: [part][group] of m, l and the float4 o
-    float* pm = sm.merge_scratch;
+    float* pm = scratch;  // kSThreads * 6 floats
     float* pl = pm + kParts * NG;
     float4* po = reinterpret_cast<float4*>(pl + kParts * NG);
     const int gi = t % NG;
@@ -220,8 +229,10 @@ __device__ __forceinline__ void merge_splits(const SParams& a, SSmem<D, G>& sm, 
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kSThreads, 1) sparse_decode_kernel(const SParams a) {
-  using Lay = SLayout<D>;
+__global__ void __launch_bounds__(SCfg<G>::kThreads, 1) sparse_decode_kernel(const SParams a) {
+  constexpr int kSWarps = SCfg<G>::kWarps, kSThreads = SCfg<G>::kThreads;
+  constexpr int kKeysPerWarp = SCfg<G>::kKeysPerWarp;
+  using Lay = SLayout<D, G>;
   constexpr int LPR = Lay::LPR, KPI = Lay::KPI, U = Lay::U;
   extern __shared__ __align__(16) uint8_t sparse_smem[];
   SSmem<D, G>& sm = *reinterpret_cast<SSmem<D, G>*>(sparse_smem);
@@ -360,7 +371,7 @@ __global__ void __launch_bounds__(kSThreads, 1) sparse_decode_kernel(const SPara
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) z[u][hh] += __shfl_xor_sync(0xffffffffu, z[u][hh], o);
-    // ---- online softmax over the warp's 16 keys (slots x row groups)
+    // ---- online softmax over the warp's keys (slots x row groups)
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
       float bm = -INFINITY;
@@ -409,7 +420,7 @@ __global__ void __launch_bounds__(kSThreads, 1) sparse_decode_kernel(const SPara
       for (int e = 0; e < 8; ++e) acc[hh][e] += __shfl_xor_sync(0xffffffffu, acc[hh][e], o);
     }
 
-  // ---- merge the eight warps in a fixed order
+  // ---- merge the warps in a fixed order
 #pragma unroll
   for (int hh = 0; hh < G; ++hh) {
     if (lane == 0) {
@@ -470,7 +481,282 @@ __global__ void __launch_bounds__(kSThreads, 1) sparse_decode_kernel(const SPara
   }
   __syncthreads();
   if (!s_last) return;
-  merge_splits<D, G>(a, sm, pair, b, g, n_splits);
+  merge_splits<D, G, kSThreads>(a, sm.merge_scratch, pair, b, g, n_splits);
+}
+
+// ---------------------------------------------------------------- tensor-core step
+// One split of up to 128 attended positions of one (sequence, KV head) pair per CTA of
+// four warps, on the 5th-generation tensor cores:
+//   * every thread resolves one position (index or tail -> block table -> cache row);
+//     the CTA then gathers the 128 K and V rows with 16-byte asynchronous copies, one
+//     instruction covering whole rows, straight into the 128-byte-swizzled K-major
+//     layout the MMA reads (absent rows are zero-filled), and stages the G query rows
+//     (padded to 16) the same way;
+//   * one thread issues S^T = K Q^T (M = 128 keys, N = 16, K = head_dim) into TMEM;
+//   * thread t owns key t (TMEM lane t): it reads its 16 logits, the CTA forms the
+//     per-head max and sum in shared memory, and the thread writes its probabilities
+//     as row t of P^T (bf16, swizzled);
+//   * one thread issues O^T = V^T P^T (M = 128 >= head_dim, N = 16, K = 128 keys) into TMEM;
+//     thread d < head_dim reads dimension d of the G heads and writes the output, or the
+//     split's (m, l, o) for the last-split merge shared with the CUDA-core kernel.
+constexpr int kTcThreads = 128;
+constexpr int kTcNQ = 16;  // MMA N: query heads of the group, padded
+
+template <int D>
+struct TcSmem {
+  static constexpr int kHalf = kBatch * 128;       // one 64-column half of a K/V tile
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kBatch * D * 2;
+  static constexpr int kOffQ = kOffV + kBatch * D * 2;
+  static constexpr int kOffP = kOffQ + kTcNQ * D * 2 < kOffQ + 2048 ? kOffQ + 2048
+                                                                     : kOffQ + kTcNQ * D * 2;
+  static constexpr int kOffRed = kOffP + kBatch * 128;   // [2][4][16] floats
+  static constexpr int kOffScratch = kOffRed + 2 * 4 * kTcNQ * 4;  // merge: 128 * 6 floats
+  static constexpr int kOffBar = kOffScratch + kTcThreads * 6 * 4;
+  static constexpr int kBytes = kOffBar + 64 + 1024;  // + alignment slack
+  static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1 KB alignment");
+  static_assert(kOffV + 2 * kHalf <= kOffBar, "the PV MMA reads 128 rows of V^T in bounds");
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) {
+  using Sm = TcSmem<D>;
+  constexpr int LPR = D / 8;        // 16-byte chunks per row
+  constexpr int RPI = 32 / LPR;     // rows per warp instruction
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* k_s = base + Sm::kOffK;
+  uint8_t* v_s = base + Sm::kOffV;
+  uint8_t* q_s = base + Sm::kOffQ;
+  uint8_t* p_s = base + Sm::kOffP;
+  float* red = reinterpret_cast<float*>(base + Sm::kOffRed);
+  float* scratch = reinterpret_cast<float*>(base + Sm::kOffScratch);
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(base + Sm::kOffBar);
+  uint64_t* bar_o = bar_s + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 2);
+  __shared__ int s_last;
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  if (t == 0) {
+    ptx::mbar_init(bar_s, 1);
+    ptx::mbar_init(bar_o, 1);
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(tmem_slot, 32);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S^T: columns [0, 16); O^T: columns [16, 32)
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait_primary();  // idx / n_sel come from the preceding kernel
+
+  const int ns_raw = a.n_sel != nullptr ? __ldg(a.n_sel + b) : 0;
+  const int t0_raw = __ldg(a.tail_start + b);
+  const int t1 = __ldg(a.seq_len + b);
+  const SList L = attended_list(ns_raw, t0_raw, t1, a, split == 0 && g == 0 && t == 0);
+  const int lo = split * a.split_len;
+  const bool work = lo < L.total || (split == 0 && L.total == 0);
+  const int n_splits = (L.total + a.split_len - 1) / a.split_len;
+  const bool direct = n_splits <= 1;
+  const int pair = b * a.Hkv + g;
+  bool timed_out = false;
+
+  if (work) {
+    // ---- this thread's position -> cache row (-1: absent, zero-filled)
+    const int pos = lo + t;
+    int crow = -1;
+    if (pos < L.total && pos < lo + kBatch) {
+      const int j = pos >= L.ns ? L.t0 + (pos - L.ns)
+                                : __ldg(a.idx + static_cast<size_t>(b) * a.k_max + pos);
+      if (j < 0 || j >= t1) {
+        flag_status(a.status, VSD_DEV_BAD_INDEX);
+      } else {
+        const int blk = __ldg(a.block_table + static_cast<size_t>(b) * a.max_blocks + j / kPageS);
+        if (blk < 0 || blk >= a.num_blocks)
+          flag_status(a.status, VSD_DEV_BAD_BLOCK);
+        else
+          crow = (blk * a.Hkv + g) * kPageS + (j % kPageS);
+      }
+    }
+    // ---- gather: warp w copies rows 32 w .. 32 w + 31, RPI whole rows per instruction
+    const int ch = lane % LPR;
+#pragma unroll
+    for (int u = 0; u < 32 / RPI; ++u) {
+      const int rl = u * RPI + lane / LPR;  // row within the warp
+      const int r = warp * 32 + rl;
+      const int cr = __shfl_sync(0xffffffffu, crow, rl);
+      const size_t src = cr >= 0 ? static_cast<size_t>(cr) * D + ch * 8 : 0;
+      const int off = (ch >> 3) * Sm::kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+      ptx::cp_async16(k_s + off, a.k_cache + src, cr >= 0 ? 16u : 0u);
+      ptx::cp_async16(v_s + off, a.v_cache + src, cr >= 0 ? 16u : 0u);
+    }
+    ptx::cp_async_commit();
+    // ---- the group's query rows, padded with zeros to 16
+    for (int i = t; i < kTcNQ * LPR; i += kTcThreads) {
+      const int r = i / LPR, c = i % LPR;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < G) v = *reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + g * G + r) * D + c * 8);
+      *reinterpret_cast<uint4*>(q_s + (c >> 3) * (kTcNQ * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+    }
+    ptx::cp_async_wait_all();
+    ptx::fence_proxy_async_smem();  // make the copies and stores visible to the tensor cores
+    __syncthreads();
+
+    // ---- S^T = K Q^T
+    if (t == 0) {
+      ptx::tc_fence_after();
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTcNQ, 0, 0);
+      const uint32_t ka = ptx::smem_u32(k_s), qa = ptx::smem_u32(q_s);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int hh = kk >> 2, w = kk & 3;
+        const uint64_t ad = ptx::sdesc_sw128(ka + hh * Sm::kHalf + w * 32, 16, 1024);
+        const uint64_t bd = ptx::sdesc_sw128(qa + hh * kTcNQ * 128 + w * 32, 16, 1024);
+        ptx::umma_bf16(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      ptx::umma_commit(bar_s);
+    }
+    if (!ptx::mbar_wait(bar_s, 0)) timed_out = true;
+    ptx::tc_fence_after();
+    float sv[kTcNQ];
+    ptx::tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16), reinterpret_cast<uint32_t(&)[16]>(sv));
+    ptx::tmem_wait_ld();
+    // ---- softmax over the CTA's keys, per head (log2 units)
+    const bool valid = crow >= 0;
+    float z[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      z[h] = valid ? sv[h] * a.scale_log2 : -INFINITY;
+      float mx = z[h];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) red[warp * kTcNQ + h] = mx;
+    }
+    __syncthreads();
+    float m[G], psum[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = fmaxf(fmaxf(red[h], red[kTcNQ + h]), fmaxf(red[2 * kTcNQ + h], red[3 * kTcNQ + h]));
+      const float p = (z[h] == -INFINITY) ? 0.f : exp2f(z[h] - m[h]);
+      z[h] = p;
+      float sp = p;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(0xffffffffu, sp, o);
+      if (lane == 0) red[4 * kTcNQ + warp * kTcNQ + h] = sp;
+    }
+    // row t of P^T: 16 bf16 (heads >= G are zero) in two swizzled 16-byte chunks
+    float pr[kTcNQ];
+#pragma unroll
+    for (int c = 0; c < kTcNQ; ++c) pr[c] = c < G ? z[c < G ? c : 0] : 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      uint4 pk;
+      pk.x = pack_bf16x2(pr[k * 8 + 0], pr[k * 8 + 1]);
+      pk.y = pack_bf16x2(pr[k * 8 + 2], pr[k * 8 + 3]);
+      pk.z = pack_bf16x2(pr[k * 8 + 4], pr[k * 8 + 5]);
+      pk.w = pack_bf16x2(pr[k * 8 + 6], pr[k * 8 + 7]);
+      *reinterpret_cast<uint4*>(p_s + t * 128 + ((k ^ (t & 7)) << 4)) = pk;
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      psum[h] = red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
+
+    // ---- O^T = V^T P^T
+    if (t == 0) {
+      ptx::tc_fence_after();
+      // M = 128 for either head dimension: with D = 64 the upper 64 rows of A are the
+      // next 16 KB of this CTA's shared memory and land in TMEM lanes 64-127, never read
+      // (the M = 64 shape keeps its rows in a different TMEM lane layout)
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTcNQ, 1, 1);
+      const uint32_t va = ptx::smem_u32(v_s), pa = ptx::smem_u32(p_s);
+#pragma unroll
+      for (int kk = 0; kk < kBatch / 16; ++kk) {
+        const uint64_t ad = ptx::sdesc_sw128(va + kk * 2048, Sm::kHalf, 1024);
+        const uint64_t bd = ptx::sdesc_sw128(pa + kk * 2048, Sm::kHalf, 1024);
+        ptx::umma_bf16(tmem + 16, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      ptx::umma_commit(bar_o);
+    }
+    if (!ptx::mbar_wait(bar_o, 0)) timed_out = true;
+    ptx::tc_fence_after();
+    if (warp < D / 32) {  // TMEM lanes 0 .. D-1 hold the output dimensions
+      float o[kTcNQ];
+      ptx::tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 16,
+                     reinterpret_cast<uint32_t(&)[16]>(o));
+      ptx::tmem_wait_ld();
+      const int dim = t;
+      if (direct) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float val = psum[h] > 0.f ? o[h] / psum[h] : 0.f;
+          const __nv_bfloat16 bv = __float2bfloat16_rn(val);
+          a.out[(static_cast<size_t>(b) * a.Hq + g * G + h) * D + dim] =
+              *reinterpret_cast<const uint16_t*>(&bv);
+        }
+      } else {
+        float* wsl = a.ws + (static_cast<size_t>(pair) * a.max_splits + split) * G * (D + 2);
+#pragma unroll
+        for (int h = 0; h < G; ++h) wsl[2 * G + h * D + dim] = o[h];
+        if (dim < G) {
+          // m and l of head `dim` (every thread holds all heads' values)
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            if (h == dim) {
+              wsl[h] = m[h];
+              wsl[G + h] = psum[h];
+            }
+          }
+        }
+      }
+    }
+    if (timed_out) flag_status(a.status, VSD_DEV_TIMEOUT);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 32);
+  }
+  if (!work || direct) return;
+  // The last split of the pair to get here combines them all (as in the CUDA-core
+  // kernel: the barrier above orders every thread's partial stores before thread 0's
+  // acquire-release count).
+  if (t == 0) {
+    const unsigned old = ptx::atom_add_acq_rel_gpu(a.counters + pair, 1u);
+    const int last = old == static_cast<unsigned>(n_splits - 1);
+    if (last) ptx::st_relaxed_gpu(a.counters + pair, 0u);
+    s_last = last;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  merge_splits<D, G, kTcThreads>(a, scratch, pair, b, g, n_splits);
+}
+
+template <int D, int G>
+cudaError_t launch_tc(const SParams& p, int B, int Hkv, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  constexpr int smem = TcSmem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(sparse_tc_kernel<D, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.max_splits, Hkv, B);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sparse_tc_kernel<D, G>, p);
 }
 
 template <int D, int G>
@@ -486,7 +772,7 @@ cudaError_t launch_dg(const SParams& p, int B, int Hkv, cudaStream_t stream) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.max_splits, Hkv, B);
-  cfg.blockDim = dim3(kSThreads, 1, 1);
+  cfg.blockDim = dim3(SCfg<G>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -542,8 +828,13 @@ cudaError_t launch_sparse(const SparseArgs& sa, cudaStream_t stream) {
   p.split_len = plan.split_len;
   p.max_splits = plan.max_splits;
   p.scale_log2 = sa.scale * kLog2e;
-#define VSD_SPARSE_CASE(DD, GG) \
-  if (sa.d == DD && sa.G == GG) return launch_dg<DD, GG>(p, sa.B, sa.Hkv, stream);
+  // splits of one 128-position batch run on the tensor cores; longer splits (lists
+  // beyond 1024 batches) on the CUDA-core kernel, which loops over batches
+  const bool tc = plan.split_len == kBatch;
+#define VSD_SPARSE_CASE(DD, GG)                                                   \
+  if (sa.d == DD && sa.G == GG)                                                   \
+    return tc ? launch_tc<DD, GG>(p, sa.B, sa.Hkv, stream)                        \
+              : launch_dg<DD, GG>(p, sa.B, sa.Hkv, stream);
   VSD_SPARSE_CASE(128, 1)
   VSD_SPARSE_CASE(128, 2)
   VSD_SPARSE_CASE(128, 4)
