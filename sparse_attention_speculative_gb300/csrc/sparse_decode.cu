@@ -508,14 +508,18 @@ struct TcSmem {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kBatch * D * 2;
   static constexpr int kOffQ = kOffV + kBatch * D * 2;
-  static constexpr int kOffP = kOffQ + kTcNQ * D * 2 < kOffQ + 2048 ? kOffQ + 2048
-                                                                     : kOffQ + kTcNQ * D * 2;
-  static constexpr int kOffRed = kOffP + kBatch * 128;   // [2][4][16] floats
-  static constexpr int kOffScratch = kOffRed + 2 * 4 * kTcNQ * 4;  // merge: 128 * 6 floats
-  static constexpr int kOffBar = kOffScratch + kTcThreads * 6 * 4;
-  static constexpr int kBytes = kOffBar + 64 + 1024;  // + alignment slack
+  static constexpr int kOffRed = kOffQ + (kTcNQ * D * 2 < 2048 ? 2048 : kTcNQ * D * 2);
+  static constexpr int kOffBar = kOffRed + 2 * 4 * kTcNQ * 4;  // after [2][4][16] floats
+  // P^T reuses the K tile (its QK MMA has completed before P^T is written) and the
+  // merge scratch the V tile (after the PV MMA); the PV MMA reads 128 rows of V^T,
+  // which for D = 64 run 16 KB past the V tile, still inside this allocation
+  static constexpr int kOffP = kOffK;
+  static constexpr int kOffScratch = kOffV;
+  static constexpr int kUsed = kOffBar + 64 > kOffV + 2 * kHalf ? kOffBar + 64 : kOffV + 2 * kHalf;
+  static constexpr int kBytes = kUsed + 1024;  // + alignment slack
   static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1 KB alignment");
-  static_assert(kOffV + 2 * kHalf <= kOffBar, "the PV MMA reads 128 rows of V^T in bounds");
+  static_assert(kBatch * 128 <= kOffV - kOffK, "P^T fits in the K tile");
+  static_assert(kTcThreads * 6 * 4 <= kBatch * D * 2, "merge scratch fits in the V tile");
 };
 
 template <int D, int G>
