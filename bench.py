@@ -187,6 +187,8 @@ def run_gpu(args, world, rank, local):
     out = torch.empty_like(batch.q)
     logits = torch.empty((B, 2, Hq, P_max), dtype=torch.float32, device=dev)
     partial = torch.empty((B, w.Hkv, P_max), dtype=torch.float32, device=dev)
+    score = torch.empty((B, P_max), dtype=torch.float32, device=dev)
+    score_hist = torch.empty((B, vsd.HIST_BINS), dtype=torch.int32, device=dev)
     idx = torch.empty((B, w.k), dtype=torch.int32, device=dev)
     n_sel = torch.empty((B,), dtype=torch.int32, device=dev)
     d_out = torch.empty((gamma, B, Hq, d), dtype=torch.bfloat16, device=dev)
@@ -205,14 +207,17 @@ def run_gpu(args, world, rank, local):
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 + gamma)]
 
     def step(events=True):
-        vsd.vsd_verify_attn_collect(batch.q, batch.k_cache, batch.v_cache, batch.block_table,
-                                    batch.prefix_len, P_max=P_max, scale=w.scale, row0=0,
-                                    row1=R - 1, logits=logits, partial=partial, out=out,
-                                    workspace=workspace)
+        # verification with Collect-2-Query and the fused aggregation (the score summed
+        # over the KV groups and its first histogram level), then the selection from them
+        vsd.vsd_verify_attn_collect_scored(batch.q, batch.k_cache, batch.v_cache,
+                                           batch.block_table, batch.prefix_len, P_max=P_max,
+                                           scale=w.scale, row0=0, row1=R - 1, logits=logits,
+                                           partial=partial, score=score, score_hist=score_hist,
+                                           out=out, workspace=workspace)
         if events:
             ev[1].record(stream)
-        vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
-                            n_recent=w.n_recent, idx=idx, n_sel=n_sel)
+        vsd.vsd_select_topk_scored(score, score_hist, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                   n_recent=w.n_recent, idx=idx, n_sel=n_sel)
         if events:
             ev[2].record(stream)
         for i in range(gamma):
@@ -222,10 +227,10 @@ def run_gpu(args, world, rank, local):
             if events:
                 ev[3 + i].record(stream)
 
-    # this library's kernel launches per step, from the launch plan: verification (+ its
-    # split-K merge kernel), selection, and one kernel per draft step (the draft step
-    # merges its splits inside the kernel)
-    launches_per_verify = 1 + (1 if ws_bytes > 0 else 0)
+    # this library's kernel launches per step: verification and its merge + aggregation
+    # kernel, selection, and one kernel per draft step (the draft step merges its splits
+    # inside the kernel)
+    launches_per_verify = 2
     launches_per_step = launches_per_verify + 1 + gamma
     enqueue_s = []
     sleep_cycles = 8_000_000  # ~4 ms: the whole step is enqueued before the GPU gets to it
@@ -305,6 +310,21 @@ def run_gpu(args, world, rank, local):
             v1.record(stream)
             torch.cuda.synchronize()
             per["verify_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
+        # the same with the fused aggregation (what the iteration runs)
+        per["verify_scored_b2b"] = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            torch.cuda._sleep(sleep_cycles)
+            v0.record(stream)
+            for _ in range(B2B_CALLS):
+                vsd.vsd_verify_attn_collect_scored(
+                    batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+                    P_max=P_max, scale=w.scale, row0=0, row1=R - 1, logits=logits,
+                    partial=partial, score=score, score_hist=score_hist, out=out,
+                    workspace=workspace)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            per["verify_scored_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
         # sparse verification (Dustin) over this iteration's selection, back to back
         per["sparse_verify_b2b"] = []
         sv_out = torch.empty_like(batch.q)
@@ -336,6 +356,18 @@ def run_gpu(args, world, rank, local):
             v1.record(stream)
             torch.cuda.synchronize()
             per["select_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
+        per["select_scored_b2b"] = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            torch.cuda._sleep(sleep_cycles)
+            v0.record(stream)
+            for _ in range(B2B_CALLS):
+                vsd.vsd_select_topk_scored(score, score_hist, batch.prefix_len, k=w.k,
+                                           n_sink=w.n_sink, n_recent=w.n_recent, idx=idx,
+                                           n_sel=n_sel)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            per["select_scored_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
         g_d = torch.Generator(device=dev)
         g_d.manual_seed(w.seed + 5)
         partial_draft = torch.randn((B, 2, P_max), generator=g_d, device=dev)
@@ -468,6 +500,16 @@ def run_gpu(args, world, rank, local):
         "us_per_iter_eager": statistics.mean(per["step"]) * 1e6,
         "kernels": kernels,
         "select_over_verify": t_select / t_verify,
+        "fused_aggregation": {
+            "verify_scored_us": statistics.median(per["verify_scored_b2b"]) * 1e6,
+            "select_scored_us": statistics.median(per["select_scored_b2b"]) * 1e6,
+            "verify_plain_us": t_verify_b2b * 1e6,
+            "select_plain_us": statistics.median(per["select_b2b"]) * 1e6,
+            "select_over_verify": statistics.median(per["select_scored_b2b"]) /
+                                  statistics.median(per["verify_scored_b2b"]),
+            "note": "back-to-back calls; scored = the verification call also sums the "
+                    "per-group partials into the score and counts its first histogram "
+                    "level, and the selection starts from them (what the iteration runs)"},
         "verify_back_to_back_us": t_verify_b2b * 1e6,
         "sparse_verify": {
             "us": statistics.median(per["sparse_verify_b2b"]) * 1e6,

@@ -217,6 +217,41 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------
+ * Fused aggregation (Vegas summary sec. 2.A: the selection objective sums the
+ * collected logits over every query head; here the verification call finishes that
+ * sum and the first histogram level of the selection, so the selection starts from
+ * one score per position).
+ *
+ * vsd_verify_attn_collect_scored: vsd_verify_attn_collect (same arguments; logits may
+ * be NULL, partial_scores may not) that also writes, for every sequence b,
+ *   score[b][j] = sum_g partial_scores[b][g][j]   (fp32, groups in order from zero;
+ *                                                  j < P_b; later entries not written)
+ *   score_hist[b][i] = #{ j < P_b : key(score[b][j]) >> 20 == i },  i < 4096
+ * where key(x) maps the fp32 bits order-preservingly to uint32 (sign bit set for
+ * x >= +0: bits | 0x80000000; else ~bits).  score fp32 [B][P_max] and score_hist
+ * uint32 [B][4096] are caller-owned; score_hist is overwritten (no zeroing needed).
+ *
+ * vsd_select_topk_scored: vsd_select_topk on n_rows = B rows of such a score
+ * (Hkv = 1) and its histogram -- the same index sets, bit for bit, as
+ * vsd_select_topk on the partial scores; the kernel skips the aggregation and its
+ * first two cluster rounds.  A histogram that does not match the scores (fewer
+ * candidates than the budget needs) raises VSD_DEV_BAD_LENGTH and the row's selection
+ * is unspecified.  Supported sizes as vsd_select_topk.
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const void* q,
+                                          const void* k_cache, const void* v_cache,
+                                          const int32_t* block_table, const int32_t* prefix_len,
+                                          int collect_row0, int collect_row1, int P_max,
+                                          float scale, float* logits, float* partial_scores,
+                                          float* score, uint32_t* score_hist, void* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* stream);
+
+vsd_status vsd_select_topk_scored(int n_rows, const float* score, const uint32_t* score_hist,
+                                  const int32_t* prefix_len, int P_max, int k, int n_sink,
+                                  int n_recent, int32_t* idx, int32_t* n_sel, void* stream);
+
+/* ------------------------------------------------------------------------------
  * Hybrid budget with two signals (Dustin summary, Methodology sec. 1: after the
  * protected sinks and recent window, the top-m tokens by the draft-lookahead signal,
  * then the most relevant remaining tokens by the target-historical signal).

@@ -14,5 +14,6 @@ from ._lib import (DEV_BAD_BLOCK, DEV_BAD_INDEX, DEV_BAD_LENGTH, DEV_TIMEOUT, Ge
                    vsd_sparse_verify_workspace_size, vsd_verify_attn_collect_srh,
                    vsd_verify_attn_collect_all,
                    vsd_verify_attn_collect_noalloc, vsd_verify_workspace_size,
-                   page_blocks, vsd_page_key_means, vsd_block_topk)
+                   page_blocks, vsd_page_key_means, vsd_block_topk,
+                   vsd_verify_attn_collect_scored, vsd_select_topk_scored, HIST_BINS)
 from .iteration import IterationGraph  # noqa: F401

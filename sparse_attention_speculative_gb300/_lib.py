@@ -77,6 +77,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_select_topk.argtypes = [I, I, P, P, I, I, I, I, P, P, P, P, SZ, P]
         lib.vsd_sparse_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
         lib.vsd_sparse_decode_attn.argtypes = [GP, P, P, P, P, P, P, I, P, P, I, F, P, P, SZ, P]
+        lib.vsd_verify_attn_collect_scored.argtypes = [GP, I, P, P, P, P, P, I, I, I, F, P, P,
+                                                       P, P, P, P, SZ, P]
+        lib.vsd_select_topk_scored.argtypes = [I, P, P, P, I, I, I, I, P, P, P]
         lib.vsd_page_key_means.argtypes = [GP, P, P, P, P, I, P, P]
         lib.vsd_block_topk.argtypes = [GP, I, P, P, P, I, I, F, P, P, P]
         lib.vsd_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
@@ -91,6 +94,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                      "vsd_verify_attn_collect_noalloc",
                      "vsd_select_workspace_size", "vsd_select_topk", "vsd_sparse_workspace_size",
                      "vsd_sparse_decode_attn", "vsd_page_key_means", "vsd_block_topk",
+                     "vsd_verify_attn_collect_scored", "vsd_select_topk_scored",
                      "vsd_read_device_status", "vsd_last_cuda_error"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -459,3 +463,60 @@ def vsd_block_topk(q, page_means, prefix_len, *, kb: int, scale: float, k_cache=
                             _stream(stream))
     _check(rc, "vsd_block_topk")
     return scores, blocks
+
+
+HIST_BINS = 4096
+
+
+def vsd_verify_attn_collect_scored(q, k_cache, v_cache, block_table, prefix_len, *, P_max: int,
+                                   scale: float, row0: int = 0, row1: Optional[int] = None,
+                                   logits=None, partial=None, score=None, score_hist=None,
+                                   out=None, workspace=None, stream=None):
+    """Verification with Collect-2-Query that also sums the partial scores over the KV
+    groups (score fp32 [B, P_max]) and counts their level-0 histogram (uint32-valued
+    int32 [B, 4096]).  Returns (out, logits, partial, score, score_hist)."""
+    lib = load()
+    B, R, Hq, d = q.shape
+    _need(q, torch.bfloat16, "q")
+    geom = geom_for(B, Hq, k_cache, block_table)
+    if row1 is None:
+        row1 = R - 1
+    dev = q.device
+    if out is None:
+        out = torch.empty_like(q)
+    if partial is None:
+        partial = torch.empty((B, geom.Hkv, P_max), dtype=torch.float32, device=dev)
+    if score is None:
+        score = torch.empty((B, P_max), dtype=torch.float32, device=dev)
+    if score_hist is None:
+        score_hist = torch.empty((B, HIST_BINS), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _workspace(vsd_verify_workspace_size(geom, R, P_max), dev, "verify")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.vsd_verify_attn_collect_scored(ctypes.byref(geom), R, _ptr(q), _ptr(k_cache),
+                                            _ptr(v_cache), _ptr(block_table), _ptr(prefix_len),
+                                            int(row0), int(row1), int(P_max), float(scale),
+                                            _ptr(logits), _ptr(partial), _ptr(score),
+                                            _ptr(score_hist), _ptr(out), _ptr(workspace),
+                                            ws_bytes, _stream(stream))
+    _check(rc, "vsd_verify_attn_collect_scored")
+    return out, logits, partial, score, score_hist
+
+
+def vsd_select_topk_scored(score, score_hist, prefix_len, *, k: int, n_sink: int, n_recent: int,
+                           idx=None, n_sel=None, stream=None):
+    """The protected top-k from an aggregated score [n_rows, P_max] and its histogram
+    (from vsd_verify_attn_collect_scored).  Returns (idx [n_rows, k], n_sel)."""
+    lib = load()
+    _need(score, torch.float32, "score")
+    n_rows, P_max = score.shape
+    dev = score.device
+    if idx is None:
+        idx = torch.empty((n_rows, k), dtype=torch.int32, device=dev)
+    if n_sel is None:
+        n_sel = torch.empty((n_rows,), dtype=torch.int32, device=dev)
+    rc = lib.vsd_select_topk_scored(int(n_rows), _ptr(score), _ptr(score_hist), _ptr(prefix_len),
+                                    int(P_max), int(k), int(n_sink), int(n_recent), _ptr(idx),
+                                    _ptr(n_sel), _stream(stream))
+    _check(rc, "vsd_select_topk_scored")
+    return idx, n_sel

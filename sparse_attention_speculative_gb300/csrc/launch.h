@@ -35,6 +35,11 @@ struct VerifyArgs {
   int row0, row1;
   int collect_all;  // 1: every verify row's logits, partial summed over all rows
   const uint8_t* head_mask = nullptr;  // [Hq] or NULL: collected heads
+  // fused aggregation (both or neither): score[b][j] = sum over groups of partial[b][g][j]
+  // in group order, j < P_b; hist[b][bin] counts the top 12 bits of the order-preserving
+  // keys of those scores (zeroed by the call)
+  float* score = nullptr;
+  uint32_t* hist = nullptr;
   float scale;
 };
 
@@ -55,6 +60,9 @@ struct SelectArgs {
   const int32_t* pre_count = nullptr;
   uint32_t* out_bitmap = nullptr;
   int32_t* out_count = nullptr;
+  // scored input (Hkv = 1, partial = the aggregated score): [n_rows][4096] counts of
+  // the top 12 key bits over every prefix position, as the fused verification writes
+  const uint32_t* hist = nullptr;
 };
 
 int select_cluster_size(int P_max, int n_rows);

@@ -28,6 +28,10 @@
 //      the lower position) on the gathered keys with block-local passes, marks the
 //      winners, and writes the row: sinks, the marked positions in order (a block
 //      scan over the bitmap), the recent window, -1 padding.
+// Scored input (the fused verification has already summed the groups and counted the
+// level-0 histogram of every prefix position): A reads one score per position, and
+// every CTA copies the row's histogram, takes the sinks and the recent window out of
+// it and finds the boundary bin itself, so B and C (two cluster barriers) are skipped.
 // Results are deterministic; no global workspace.  The kernel is launched as a
 // programmatic dependent: its launch overlaps the tail of the verification kernels.
 #include <cooperative_groups.h>
@@ -69,6 +73,7 @@ struct SelParams {
   uint32_t* out_bitmap;         // [n_rows][bm_words]: this pass's chosen candidates
   int32_t* out_count;           // [n_rows]
   int bm_words;                 // words per row of those bitmaps: ceil(P_max / 32)
+  const uint32_t* hist;         // scored input: level-0 histogram of all prefix positions
 };
 
 struct SelShared {
@@ -310,7 +315,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
         L.keys[t * KPT + q + u] = key;
         if (jj < P && a.scores_out != nullptr)
           a.scores_out[static_cast<size_t>(row) * a.P_max + jj] = s[u];
-        if (ranking && rankable(jj, q + u)) atomicAdd(&L.hist[key >> 20], 1u);
+        if (ranking && a.hist == nullptr && rankable(jj, q + u))
+          atomicAdd(&L.hist[key >> 20], 1u);
       }
     };
     finish4(0, s_first);
@@ -350,25 +356,57 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
         }
         __syncthreads();
       }
-      uint32_t* gh0 = cluster.map_shared_rank(gh_local, 0);
-      for (int b = t; b < nb; b += kSelThreads) {
-        const uint32_t c = L.hist[b];
-        if (c) atomicAdd(gh0 + b, c);
-      }
-      cluster_arrive();
-      cluster_wait();  // rank 0's histogram of this level is complete
-      if (rank == 0) {
-        // rank 0 searches its histogram and hands the result to every CTA
-        find_bin(gh_local, nb, r_rem, sh);
-        if (t < static_cast<int>(cluster.num_blocks())) {
-          SelShared* d = cluster.map_shared_rank(&sh, t);
-          d->f_bin = sh.f_bin;
-          d->f_rem = sh.f_rem;
-          d->f_cnt = sh.f_cnt;
+      if (level == 0 && a.hist != nullptr) {
+        // scored input: the histogram of every prefix position came with the scores;
+        // each CTA takes the positions that are not ranked (sinks, recent window) out
+        // of its own copy and searches it -- no cluster round
+        const uint32_t* src = a.hist + static_cast<size_t>(row) * kBins0;
+        for (int i = t; i < kBins0; i += kSelThreads) gh_local[i] = __ldg(src + i);
+        if (t == 0) {
+          // a histogram that does not hold r_rem candidates (not the one written with
+          // these scores) finds no bin: take bin 0 whole, and flag it
+          sh.f_bin = 0;
+          sh.f_rem = 0;
+          sh.f_cnt = -1;
         }
+        __syncthreads();
+        const int n_prot = sink_end + (P - rb);
+        for (int i = t; i < n_prot; i += kSelThreads) {
+          const int j = i < sink_end ? i : rb + (i - sink_end);
+          atomicSub(&gh_local[order_key(__ldg(base + j)) >> 20], 1u);
+        }
+        __syncthreads();
+        find_bin(gh_local, nb, r_rem, sh);
+        if (sh.f_cnt < 0) {
+          if (t == 0 && rank == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
+          __syncthreads();
+          if (t == 0) {
+            sh.f_rem = 1;
+            sh.f_cnt = 1;
+          }
+          __syncthreads();
+        }
+      } else {
+        uint32_t* gh0 = cluster.map_shared_rank(gh_local, 0);
+        for (int b = t; b < nb; b += kSelThreads) {
+          const uint32_t c = L.hist[b];
+          if (c) atomicAdd(gh0 + b, c);
+        }
+        cluster_arrive();
+        cluster_wait();  // rank 0's histogram of this level is complete
+        if (rank == 0) {
+          // rank 0 searches its histogram and hands the result to every CTA
+          find_bin(gh_local, nb, r_rem, sh);
+          if (t < static_cast<int>(cluster.num_blocks())) {
+            SelShared* d = cluster.map_shared_rank(&sh, t);
+            d->f_bin = sh.f_bin;
+            d->f_rem = sh.f_rem;
+            d->f_cnt = sh.f_cnt;
+          }
+        }
+        cluster_arrive();
+        cluster_wait();  // every CTA has the boundary bin of this level
       }
-      cluster_arrive();
-      cluster_wait();  // every CTA has the boundary bin of this level
       const int bin = sh.f_bin;
       const int c_star = sh.f_cnt;
       r_rem = sh.f_rem;
@@ -610,6 +648,7 @@ cudaError_t launch_select(const SelectArgs& sa, cudaStream_t stream) {
   p.out_bitmap = sa.out_bitmap;
   p.out_count = sa.out_count;
   p.bm_words = (sa.P_max + 31) / 32;
+  p.hist = sa.hist;
   const size_t smem = select_smem_bytes(chunk, CS);
   cudaError_t e = cudaFuncSetAttribute(select_topk_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,

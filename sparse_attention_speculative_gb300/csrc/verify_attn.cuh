@@ -100,9 +100,13 @@ struct VParams {
   int row0, row1;
   int collect_all;  // every verify row collected; partial sums over all rows
   const uint8_t* head_mask;  // [Hq] or NULL: only heads with a non-zero byte are collected
+  float* score;              // fused aggregation outputs, or NULL (see VerifyArgs)
+  uint32_t* hist;
   int pairs, t_max, max_chunks;
   float scale;
 };
+
+constexpr int kHistBins = 4096;  // top 12 bits of the score keys
 
 // CTA whose range holds virtual tile v (ranges are [c W / C, (c+1) W / C)).
 __device__ __forceinline__ int cta_of(long long v, long long W, int C) {
@@ -233,6 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();  // the next kernel on the stream may become resident
   pdl_wait_primary();       // inputs may come from the preceding kernel on the stream
+  if (a.hist != nullptr) {
+    // the aggregation in the merge kernel adds into a zeroed histogram
+    for (int i = blockIdx.x * kThreads + threadIdx.x; i < a.B * kHistBins; i += gridDim.x * kThreads)
+      a.hist[i] = 0u;
+  }
   const uint32_t tmem_s0 = tmem;       // S^T buffer b: columns [64 b, 64 b + NQ)
   const uint32_t tmem_o = tmem + 128;  // O^T: columns [128, 128 + NQ)
 
@@ -761,14 +770,71 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Combine the partial (m, l, o) of the CTAs that shared a pair: block (pair, verify
 // row c), thread = dim.  With B = 1 a pair is spread over ~C / Hkv CTAs, so each block
 // issues the loads of up to 32 partials at once and combines them in chunk order.
+// Fused aggregation (blocks past the merge blocks): 4 * D consecutive positions of one
+// sequence per block, 4 per thread.  The score of position j is the sum of its
+// per-group partials in group order (fp32, starting from zero: the same sum, in the
+// same order, as the selection kernel forms); the block counts the top 12 bits of the
+// scores' order-preserving keys in shared memory and adds its non-zero bins to the
+// sequence's histogram.
+template <int D>
+__device__ __forceinline__ void aggregate_scores(const VParams& a, int blk) {
+  constexpr int kPos = 4 * D;
+  __shared__ uint32_t h[kHistBins];
+  const int per_seq = (a.P_max + kPos - 1) / kPos;
+  const int b = blk / per_seq;
+  const int j0 = (blk - b * per_seq) * kPos + static_cast<int>(threadIdx.x) * 4;
+  for (int i = threadIdx.x; i < kHistBins; i += D) h[i] = 0u;
+  const int P = __ldg(a.prefix_len + b);
+  const bool ok = P >= 0 && P <= a.P_max;  // else flagged by the verification kernel
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  if (ok && j0 < P) {
+    const float* base = a.partial + static_cast<size_t>(b) * a.Hkv * a.P_max + j0;
+    if ((a.P_max & 3) == 0) {
+      for (int g = 0; g < a.Hkv; ++g) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g) * a.P_max));
+        s[0] += x.x;
+        s[1] += x.y;
+        s[2] += x.z;
+        s[3] += x.w;
+      }
+    } else {
+      for (int g = 0; g < a.Hkv; ++g)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (j0 + u < a.P_max) s[u] += __ldcg(base + static_cast<size_t>(g) * a.P_max + u);
+    }
+  }
+  __syncthreads();
+  if (ok) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      if (j < P) {
+        a.score[static_cast<size_t>(b) * a.P_max + j] = s[u];
+        const uint32_t bits = __float_as_uint(s[u]);
+        const uint32_t key = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+        atomicAdd(&h[key >> 20], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kHistBins; i += D)
+    if (h[i] != 0u) atomicAdd(a.hist + static_cast<size_t>(b) * kHistBins + i, h[i]);
+}
+
 template <int D, int NQ, int G>
-__global__ void __launch_bounds__(D) verify_merge_kernel(const VParams a, int ctas) {
+__global__ void __launch_bounds__(D) verify_merge_kernel(const VParams a, int ctas,
+                                                         int merge_pairs) {
   constexpr int kU = 32;
   const int p = blockIdx.x;
   const int c = blockIdx.y;
   const int dim = threadIdx.x;
   pdl_launch_dependents();
   pdl_wait_primary();  // partials of the verification kernel are complete
+  if (p >= merge_pairs) {
+    if (c == 0) aggregate_scores<D>(a, p - merge_pairs);
+    return;
+  }
   const long long W = static_cast<long long>(a.pairs) * a.t_max;
   const long long first_v = static_cast<long long>(p) * a.t_max;
   const int c_first = cta_of(first_v, W, ctas);
@@ -836,11 +902,14 @@ cudaError_t launch_dng(const VerifyArgs& va, const VerifyPlan& plan, const VPara
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, va.kmap, va.vmap, p);
-  if (e != cudaSuccess || plan.max_chunks <= 1) return e;
-  cfg.gridDim = dim3(plan.pairs, p.NV, 1);
+  // merge blocks for pairs cut by CTA boundaries, then the fused-aggregation blocks
+  const int merge_pairs = plan.max_chunks > 1 ? plan.pairs : 0;
+  const int agg = p.score != nullptr ? p.B * ((p.P_max + 4 * D - 1) / (4 * D)) : 0;
+  if (e != cudaSuccess || merge_pairs + agg == 0) return e;
+  cfg.gridDim = dim3(merge_pairs + agg, merge_pairs > 0 ? p.NV : 1, 1);
   cfg.blockDim = dim3(D, 1, 1);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G>, p, plan.ctas);
+  return cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G>, p, plan.ctas, merge_pairs);
 }
 
 inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {
@@ -865,6 +934,8 @@ inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {
   p.row1 = va.row1;
   p.collect_all = va.collect_all;
   p.head_mask = va.head_mask;
+  p.score = va.score;
+  p.hist = va.hist;
   p.pairs = plan.pairs;
   p.t_max = plan.t_max;
   p.max_chunks = plan.max_chunks;

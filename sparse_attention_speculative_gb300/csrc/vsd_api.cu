@@ -166,7 +166,8 @@ vsd_status verify_call(const vsd_geom* geom, int R, const void* q, const void* k
                        const int32_t* prefix_len, bool collect_all, int collect_row0,
                        int collect_row1, const uint8_t* head_mask, int P_max, float scale,
                        float* logits, float* partial_scores, void* out, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+                       size_t workspace_bytes, void* stream, float* score = nullptr,
+                       uint32_t* hist = nullptr) {
   vsd_status st = verify_checks(geom, R, P_max);
   if (st != VSD_OK) return st;
   // all rows: the two halves of every key's columns meet in the part of the Q
@@ -218,6 +219,8 @@ vsd_status verify_call(const vsd_geom* geom, int R, const void* q, const void* k
   va.row1 = collect_all ? 0 : collect_row1;
   va.collect_all = collect_all ? 1 : 0;
   va.head_mask = head_mask;
+  va.score = score;
+  va.hist = hist;
   va.scale = scale;
   cudaError_t e = vsd::launch_verify(va, plan, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -248,6 +251,23 @@ vsd_status vsd_verify_attn_collect_srh(const vsd_geom* geom, int R, const void* 
   return verify_call(geom, R, q, k_cache, v_cache, block_table, prefix_len, false,
                      collect_row0, collect_row1, head_mask, P_max, scale, logits,
                      partial_scores, out, workspace, workspace_bytes, stream);
+}
+
+vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const void* q,
+                                          const void* k_cache, const void* v_cache,
+                                          const int32_t* block_table, const int32_t* prefix_len,
+                                          int collect_row0, int collect_row1, int P_max,
+                                          float scale, float* logits, float* partial_scores,
+                                          float* score, uint32_t* score_hist, void* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* stream) {
+  if (partial_scores == nullptr || score == nullptr || score_hist == nullptr)
+    return geom != nullptr && geom->B == 0 ? VSD_OK : VSD_ERR_INVALID_ARG;
+  if (!aligned(score, 16) || !aligned(score_hist, 4)) return VSD_ERR_INVALID_ARG;
+  return verify_call(geom, R, q, k_cache, v_cache, block_table, prefix_len, false,
+                     collect_row0, collect_row1, nullptr, P_max, scale, logits,
+                     partial_scores, out, workspace, workspace_bytes, stream, score,
+                     score_hist);
 }
 
 vsd_status vsd_verify_attn_collect_all(const vsd_geom* geom, int R, const void* q,
@@ -435,6 +455,41 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
   sa.k = k;
   sa.n_sink = n_sink;
   sa.n_recent = n_recent;
+  cudaError_t e = vsd::launch_select(sa, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
+vsd_status vsd_select_topk_scored(int n_rows, const float* score, const uint32_t* score_hist,
+                                  const int32_t* prefix_len, int P_max, int k, int n_sink,
+                                  int n_recent, int32_t* idx, int32_t* n_sel, void* stream) {
+  if (n_rows < 0 || P_max < 0 || k < 1 || n_sink < 0 || n_recent < 0)
+    return VSD_ERR_INVALID_ARG;
+  if (static_cast<long long>(n_sink) + n_recent > k) return VSD_ERR_INVALID_ARG;
+  if (vsd::select_chunk(P_max, vsd::select_cluster_size(P_max, n_rows)) < 0)
+    return VSD_ERR_UNSUPPORTED;
+  if (n_rows == 0) return VSD_OK;
+  if (!score || !score_hist || !prefix_len || !idx || !n_sel) return VSD_ERR_INVALID_ARG;
+  if (!aligned(score, 16) || !aligned(score_hist, 4) || !aligned(idx, 4) ||
+      !aligned(n_sel, 4) || !aligned(prefix_len, 4))
+    return VSD_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  vsd_status st = device_info(&status, nullptr);
+  if (st != VSD_OK) return st;
+  vsd::SelectArgs sa;
+  sa.partial = score;
+  sa.prefix_len = prefix_len;
+  sa.idx = idx;
+  sa.n_sel = n_sel;
+  sa.scores_out = nullptr;
+  sa.status = status;
+  sa.n_rows = n_rows;
+  sa.Hkv = 1;
+  sa.P_max = P_max;
+  sa.k = k;
+  sa.n_sink = n_sink;
+  sa.n_recent = n_recent;
+  sa.hist = score_hist;
   cudaError_t e = vsd::launch_select(sa, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return VSD_OK;

@@ -1,8 +1,9 @@
 """One speculative-decoding iteration as a single CUDA graph.
 
 A decode loop calls the same sequence of kernels every iteration: verification with
-Collect-2-Query, the protected top-k selection, and gamma draft steps over the
-selection plus the dense tail.  `IterationGraph` records that sequence once -- with
+Collect-2-Query (which also sums the collected logits over the KV groups and counts
+the first histogram level of that score), the protected top-k selection starting from
+them, and gamma draft steps over the selection plus the dense tail.  `IterationGraph` records that sequence once -- with
 the host-to-device copies of the iteration's inputs and the device-to-host copies of
 its results -- and replays it with one launch per iteration.  The kernels inside are
 chained by programmatic dependent launch, so each one's launch overlaps the tail of
@@ -67,6 +68,8 @@ class IterationGraph:
         # device-only intermediates
         self.logits = dbuf((B, 2, Hq, P_max), torch.float32)
         self.partial = dbuf((B, Hkv, P_max), torch.float32)
+        self.score = dbuf((B, P_max), torch.float32)
+        self.score_hist = dbuf((B, _lib.HIST_BINS), torch.int32)
         geom = _lib.geom_for(B, Hq, k_cache, block_table)
         nb = _lib.vsd_verify_workspace_size(geom, R, P_max)
         self.verify_ws = dbuf((max(nb, 1),), torch.uint8)[:nb] if nb else None
@@ -102,13 +105,15 @@ class IterationGraph:
     def _record(self):
         s = self.stream
         self._d_in.copy_(self._h_in, non_blocking=True)
-        _lib.vsd_verify_attn_collect(self.q, self.k_cache, self.v_cache, self.block_table,
-                                     self.prefix_len, P_max=self.P_max, scale=self.scale,
-                                     row0=self.row0, row1=self.row1, logits=self.logits,
-                                     partial=self.partial, out=self.out,
-                                     workspace=self.verify_ws, stream=s)
-        _lib.vsd_select_topk(self.partial, self.prefix_len, k=self.k, n_sink=self.n_sink,
-                             n_recent=self.n_recent, idx=self.idx, n_sel=self.n_sel, stream=s)
+        _lib.vsd_verify_attn_collect_scored(self.q, self.k_cache, self.v_cache, self.block_table,
+                                            self.prefix_len, P_max=self.P_max, scale=self.scale,
+                                            row0=self.row0, row1=self.row1, logits=self.logits,
+                                            partial=self.partial, score=self.score,
+                                            score_hist=self.score_hist, out=self.out,
+                                            workspace=self.verify_ws, stream=s)
+        _lib.vsd_select_topk_scored(self.score, self.score_hist, self.prefix_len, k=self.k,
+                                    n_sink=self.n_sink, n_recent=self.n_recent, idx=self.idx,
+                                    n_sel=self.n_sel, stream=s)
         for i in range(self.gamma):
             _lib.vsd_sparse_decode_attn(self.q_draft[i], self.k_cache, self.v_cache,
                                         self.block_table, self.idx, self.n_sel, self.tail_start,

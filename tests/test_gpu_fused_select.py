@@ -1,0 +1,126 @@
+"""GPU checks of the fused aggregation: the verification call that also writes the
+aggregated score and its level-0 histogram, and the selection that starts from them
+(Vegas summary sec. 2.A: the objective sums the collected logits over every head)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity_utils import assert_rel_close, fp32_row_sum
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_attention_speculative_gb300 import build
+    build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+    yield
+
+
+def _vsd():
+    import sparse_attention_speculative_gb300 as vsd
+    return vsd
+
+
+def _keys(x):
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return np.where(u & 0x80000000, ~u, u | 0x80000000).astype(np.uint32)
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,gamma,prefix", [
+    (128, 32, 8, 4, (32768,)),                  # Qwen3-8B 32K layer
+    (128, 32, 8, 4, (6001, 0, 1, 511, 4096)),   # ragged, an empty prefix, P_max % 4 != 0
+    (128, 64, 8, 5, (3000, 2049)),              # Qwen2.5-72B geometry
+    (64, 8, 2, 3, (777, 31)),                   # head_dim 64
+])
+def test_fused_score_and_histogram(d, Hq, Hkv, gamma, prefix):
+    from sparse_attention_speculative_gb300.synth import host_arrays, make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("fused", B=len(prefix), P=max(prefix), Hq=Hq, Hkv=Hkv, d=d, gamma=gamma, k=256,
+                 n_sink=4, n_recent=32, planted_frac=0.01, seed=81, prefix_lens=prefix)
+    batch = make_batch(w, "cuda")
+    hist0 = torch.full((w.B, vsd.HIST_BINS), 12345, dtype=torch.int32, device="cuda")  # stale
+    out_f, lg_f, pa_f, score, hist = vsd.vsd_verify_attn_collect_scored(
+        batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+        P_max=w.P_max, scale=w.scale,
+        logits=torch.zeros((w.B, 2, Hq, w.P_max), dtype=torch.float32, device="cuda"),
+        score_hist=hist0)
+    out, lg, pa = vsd.vsd_verify_attn_collect(batch.q, batch.k_cache, batch.v_cache,
+                                              batch.block_table, batch.prefix_len, P_max=w.P_max,
+                                              scale=w.scale)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    assert torch.equal(out_f, out)
+    for b, P in enumerate(prefix):  # entries at or past P_b are not written
+        assert torch.equal(pa_f[b, :, :P], pa[b, :, :P])
+    pa_h = pa.cpu().numpy()
+    sc = score.cpu().numpy()
+    hs = hist.cpu().numpy().view(np.uint32)
+    want = fp32_row_sum(pa_h)
+    h = host_arrays(batch)
+    _, l_ref, _ = oracle.verify(h["q"], h["k_cache"], h["v_cache"], h["block_table"],
+                                h["prefix_len"], scale=w.scale, P_max=w.P_max)
+    s_ref = oracle.score_from_logits(l_ref, h["prefix_len"])
+    for b, P in enumerate(prefix):
+        np.testing.assert_array_equal(sc[b, :P], want[b, :P].astype(np.float32))
+        assert_rel_close(sc[b, :P], s_ref[b, :P], "aggregated score")
+        np.testing.assert_array_equal(hs[b], np.bincount(_keys(sc[b, :P]) >> 20,
+                                                         minlength=vsd.HIST_BINS))
+
+
+def test_scored_select_matches_plain_select():
+    """Same index sets, bit for bit, as the selection that aggregates itself: ties,
+    prefixes shorter than the budget, an empty prefix, every budget mix."""
+    vsd = _vsd()
+    rng = np.random.default_rng(5)
+    B, Hkv, P_max = 6, 4, 20000
+    prefix = np.array([20000, 3, 0, 1500, 19999, 8192], np.int32)
+    part = rng.integers(-3, 4, size=(B, Hkv, P_max)).astype(np.float32)   # many ties
+    part[3:] = rng.normal(size=(3, Hkv, P_max)).astype(np.float32)
+    tp = torch.tensor(part, device="cuda")
+    tl = torch.tensor(prefix, device="cuda")
+    s = fp32_row_sum(part).astype(np.float32)
+    score = torch.tensor(s, device="cuda")
+    hist = np.zeros((B, vsd.HIST_BINS), np.uint32)
+    for b in range(B):
+        hist[b] = np.bincount(_keys(s[b, :prefix[b]]) >> 20, minlength=vsd.HIST_BINS)
+    th = torch.tensor(hist.view(np.int32), device="cuda")
+    for k, ns, nr in [(2048, 16, 256), (512, 0, 0), (64, 4, 60), (1, 0, 0), (9000, 100, 900)]:
+        i1, n1 = vsd.vsd_select_topk(tp, tl, k=k, n_sink=ns, n_recent=nr)[:2]
+        i2, n2 = vsd.vsd_select_topk_scored(score, th, tl, k=k, n_sink=ns, n_recent=nr)
+        torch.cuda.synchronize()
+        assert vsd.vsd_read_device_status() == 0
+        assert torch.equal(i1, i2) and torch.equal(n1, n2), (k, ns, nr)
+
+
+def test_fused_path_end_to_end():
+    """verify (scored) -> select (scored) selects what verify -> select selects."""
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import QWEN3_8B_32K as w
+    vsd = _vsd()
+    batch = make_batch(w, "cuda")
+    _, _, partial, score, hist = vsd.vsd_verify_attn_collect_scored(
+        batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+        P_max=w.P_max, scale=w.scale)
+    i1, n1 = vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                 n_recent=w.n_recent)[:2]
+    i2, n2 = vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                        n_recent=w.n_recent)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    assert torch.equal(i1, i2) and torch.equal(n1, n2)
+
+
+def test_scored_select_flags_a_foreign_histogram():
+    vsd = _vsd()
+    score = torch.randn((1, 5000), device="cuda")
+    tl = torch.tensor([5000], dtype=torch.int32, device="cuda")
+    zero = torch.zeros((1, vsd.HIST_BINS), dtype=torch.int32, device="cuda")
+    idx, n_sel = vsd.vsd_select_topk_scored(score, zero, tl, k=100, n_sink=4, n_recent=8)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == vsd.DEV_BAD_LENGTH
+    assert int(n_sel[0]) == 100  # the selection itself is unspecified
