@@ -9,8 +9,10 @@
 //
 // How (GB300 design).  The step is short and latency-bound, so the design minimises
 // dependent rounds between the SMs: one thread-block cluster per row (layer x
-// sequence), each CTA owning a contiguous slice of the prefix, and three cluster
-// barriers in the common case.  Scores become order-preserving uint32 keys.
+// sequence), each CTA owning a contiguous slice of the prefix, and four cluster
+// barriers in the common case (two from a scored input; one more on rows longer than
+// 32768 positions).  Scores become
+// order-preserving uint32 keys.
 //   A. Every CTA sums the per-KV-group partial scores of its slice (fp32, groups in
 //      order), keeps the keys in shared memory and builds a 4096-bin histogram of
 //      the top 12 key bits of its candidates (positions outside the protected sink
@@ -21,13 +23,19 @@
 //      key (r = k - |protected|), and writes it into every CTA.  Cluster barrier.  If
 //      that bin holds more keys than rank 0 can take, the next 10 bits are
 //      histogrammed the same way (rare; at most two more levels).
-//   D. Every CTA builds its words of the position bitmap (its candidates above the
-//      boundary bin) and stores them to rank 0, and appends its boundary-bin keys
-//      (with positions) to rank 0's buffer.  Cluster barrier; the other CTAs are done.
-//   E. Rank 0 alone resolves the remaining key bits and the tie cut (equal keys go to
-//      the lower position) on the gathered keys with block-local passes, marks the
-//      winners, and writes the row: sinks, the marked positions in order (a block
-//      scan over the bitmap), the recent window, -1 padding.
+//   D. Every CTA builds its words of a position bitmap (its candidates above the
+//      boundary bin), sends its count of them to every CTA (rows of up to 32768
+//      positions: also the words themselves to rank 0), and appends its boundary-bin
+//      keys (with positions) to rank 0's buffer.  Cluster barrier.
+//   E. Rank 0 resolves the remaining key bits and the tie cut (equal keys go to the
+//      lower position) on the gathered keys with block-local passes.  Short rows: it
+//      marks the winners and writes the whole row (sinks, candidates in order by a
+//      block scan over the bitmap, recent window, -1 padding).  Longer rows: it counts
+//      the winners per owning CTA and hands every CTA the cut and where its candidates
+//      start (cluster barrier), and
+//   F. every CTA marks its boundary keys that made the cut and writes its candidates
+//      in position order from its own bitmap words; rank 0 adds the sinks, the recent
+//      window and the padding.
 // Scored input (the fused verification has already summed the groups and counted the
 // level-0 histogram of every prefix position): A reads one score per position, and
 // every CTA copies the row's histogram, takes the sinks and the recent window out of
@@ -55,6 +63,10 @@ constexpr int kMaxChunk = 16384;
 constexpr int kBins0 = 4096;                     // level 0: top 12 bits
 constexpr int kBinsL = 1024;                     // levels 1, 2: 10 bits each
 constexpr int kGatherCap = 8192;                 // boundary-bin keys rank 0 can hold
+// Rows of up to this many bitmap words (32768 positions) are written by rank 0 alone,
+// two rounds of its threads; longer rows by every CTA in parallel, which costs one more
+// cluster barrier.
+constexpr int kShortRowWords = 2 * kSelThreads;
 
 enum Mode : int { kModeWhole = 0, kModeGather = 1, kModeTie = 2 };
 
@@ -65,7 +77,7 @@ struct SelParams {
   int32_t* n_sel;
   float* scores_out;
   unsigned* status;
-  int Hkv, P_max, k, n_sink, n_recent, chunk, bitmap_words;
+  int Hkv, P_max, k, n_sink, n_recent, chunk;
   // hybrid budget (Dustin Methodology sec. 1), both passes optional:
   int m_limit;                  // >= 0: take at most this many candidates by score
   const uint32_t* pre_bitmap;   // [n_rows][bm_words]: candidates chosen beforehand
@@ -81,6 +93,11 @@ struct SelShared {
   uint32_t tmp[kMaxSelCluster];
   int f_bin, f_rem, f_cnt;  // result of a bin search
   uint32_t gcount;          // rank 0: gathered boundary keys
+  uint32_t cnt[kMaxSelCluster];    // candidates each CTA chose before the boundary cut
+  uint32_t taken[kMaxSelCluster];  // rank 0: boundary keys taken, per owning CTA
+  int out_base;                    // long rows: where this CTA's candidates start
+  uint32_t thr_prefix, thr_mask;   // long rows: the boundary cut (from rank 0)
+  int thr_cut;
 };
 
 // Dynamic shared memory of one CTA (the rank-0-only parts are laid out everywhere).
@@ -90,7 +107,7 @@ struct SelLayout {
   uint32_t* hist;    // [kBins0] this CTA's histogram (rank 0's scratch in E)
   uint32_t* loc;     // [kBins0] this CTA's words of the selection bitmap
   uint32_t* ghist;   // [kBins0 + 2 * kBinsL] rank 0: cluster histograms of the levels
-  uint32_t* bitmap;  // [bitmap_words] rank 0: selected candidate positions
+  uint32_t* bitmap;  // [kShortRowWords] rank 0, short rows: the row's candidate bitmap
 };
 
 __device__ __forceinline__ SelLayout sel_layout(uint8_t* base, int chunk) {
@@ -212,6 +229,62 @@ __device__ __forceinline__ void mark_bits(uint32_t* bm, int my0, uint64_t sel) {
   }
 }
 
+// Resolve the boundary bin on the n_in gathered (key, position) pairs: the remaining
+// key bits level by level, then -- when every bit is fixed and fewer equal keys are
+// taken than there are -- the position cut (equal keys go to the lower position;
+// positions are below 2^20: two 10-bit passes).  Winners: (key & mask) > prefix, or
+// == prefix at a position <= cut.  `h` is 1024 words of scratch.
+__device__ void resolve_boundary(const uint2* gbuf, int n_in, uint32_t* h, SelShared& sh,
+                                 uint32_t& prefix, uint32_t& mask, int r_rem, int& cut) {
+  const int t = threadIdx.x;
+  const int start_level = (mask == 0xFFF00000u) ? 1 : ((mask == 0xFFFFFC00u) ? 2 : 3);
+  for (int level = start_level; level < 3; ++level) {
+    const int shift = level == 1 ? 10 : 0;
+    for (int i = t; i < kBinsL; i += kSelThreads) h[i] = 0u;
+    __syncthreads();
+    for (int i = t; i < n_in; i += kSelThreads) {
+      const uint32_t key = gbuf[i].x;
+      if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & (kBinsL - 1)], 1u);
+    }
+    __syncthreads();
+    find_bin(h, kBinsL, r_rem, sh);
+    const bool whole = sh.f_rem == sh.f_cnt;
+    prefix |= static_cast<uint32_t>(sh.f_bin) << shift;
+    mask |= static_cast<uint32_t>(kBinsL - 1) << shift;
+    r_rem = sh.f_rem;
+    __syncthreads();
+    if (whole) break;
+  }
+  cut = INT_MAX;
+  if (mask == 0xFFFFFFFFu) {
+    uint32_t n_eq = 0;
+    for (int i = t; i < n_in; i += kSelThreads) n_eq += gbuf[i].x == prefix ? 1u : 0u;
+    uint32_t tot_eq;
+    (void)block_excl_scan(n_eq, sh.scan, &tot_eq);
+    if (tot_eq > static_cast<uint32_t>(r_rem)) {
+      uint32_t pos_prefix = 0, pos_mask = 0;
+      int rr = r_rem;
+      for (int pl = 0; pl < 2; ++pl) {
+        const int shift = pl == 0 ? 10 : 0;
+        for (int i = t; i < kBinsL; i += kSelThreads) h[i] = 0u;
+        __syncthreads();
+        for (int i = t; i < n_in; i += kSelThreads) {
+          const uint2 e = gbuf[i];
+          if (e.x == prefix && (e.y & pos_mask) == pos_prefix)
+            atomicAdd(&h[(e.y >> shift) & (kBinsL - 1)], 1u);
+        }
+        __syncthreads();
+        find_bin_low(h, kBinsL, rr, sh);
+        pos_prefix |= static_cast<uint32_t>(sh.f_bin) << shift;
+        pos_mask |= static_cast<uint32_t>(kBinsL - 1) << shift;
+        rr = sh.f_rem;
+        __syncthreads();
+      }
+      cut = static_cast<int>(pos_prefix);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelParams a) {
   extern __shared__ __align__(16) uint8_t sel_smem[];
   __shared__ SelShared sh;
@@ -225,10 +298,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
 
   ptx::pdl_launch_dependents();
   // rank 0's cluster-wide arrays start at zero before anyone adds to them
-  if (rank == 0) {
+  if (rank == 0)
     for (int i = t; i < kBins0 + 2 * kBinsL; i += kSelThreads) L.ghist[i] = 0u;
-    if (t == 0) sh.gcount = 0u;
-  }
+  if (t == 0) sh.gcount = 0u;
   for (int i = t; i < kBins0; i += kSelThreads) L.hist[i] = 0u;
   __syncthreads();
   cluster_arrive();  // this CTA's shared memory is ready; waited on before remote use
@@ -332,7 +404,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   __syncthreads();
   cluster_wait();  // every CTA's shared memory is ready
 
-  uint32_t* bm0 = cluster.map_shared_rank(L.bitmap, 0);
   uint32_t prefix = 0u, mask = 0u;
   int r_rem = r_need;
   int mode = kModeWhole;
@@ -427,6 +498,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   }
 
   // ---- D. mark the sure winners, hand the boundary bin to rank 0
+  uint32_t* lbm = L.loc;
+  const int nw_cta = chunk / 32;
+  const bool short_row = static_cast<int>(cluster.num_blocks()) * nw_cta <= kShortRowWords;
+  uint64_t inbin_kept = 0;  // gather mode: this thread's boundary-bin positions
   {
     uint64_t sure = static_cast<uint64_t>(pre_bits), inbin = 0;
     for (int q = 0; q < KPT; ++q) {
@@ -465,14 +540,19 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
       sure |= take;
       inbin = 0;
     }
-    // this CTA's words of the bitmap are built here and stored to rank 0 whole
-    uint32_t* lbm = L.loc;
-    const int nw_cta = chunk / 32;
+    // this CTA's words of the position bitmap (short rows: also stored to rank 0); its
+    // count goes to every CTA
     for (int i = t; i < nw_cta; i += kSelThreads) lbm[i] = 0u;
     __syncthreads();
     mark_bits(lbm, t * KPT, sure);
-    __syncthreads();
-    for (int i = t; i < nw_cta; i += kSelThreads) bm0[rank * nw_cta + i] = lbm[i];
+    uint32_t n_sure;
+    (void)block_excl_scan(static_cast<uint32_t>(__popcll(sure)), sh.scan, &n_sure);
+    if (t < static_cast<int>(cluster.num_blocks()))
+      cluster.map_shared_rank(&sh, t)->cnt[rank] = n_sure;
+    if (short_row) {
+      uint32_t* bm0 = cluster.map_shared_rank(L.bitmap, 0);
+      for (int i = t; i < nw_cta; i += kSelThreads) bm0[rank * nw_cta + i] = lbm[i];
+    }
     if (mode == kModeGather) {
       // append (key, position) of the boundary bin to rank 0's buffer, one atomic per warp
       const int lane = t & 31;
@@ -489,6 +569,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
       wbase = __shfl_sync(0xffffffffu, wbase, 31);
       uint2* gb0 = cluster.map_shared_rank(L.gbuf, 0);
       uint32_t o = wbase + incl - mine;
+      inbin_kept = inbin;
       while (inbin) {
         const int q = __ffsll(static_cast<long long>(inbin)) - 1;
         inbin &= inbin - 1;
@@ -497,106 +578,133 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
     }
   }
   cluster_arrive();
-  cluster_wait();  // rank 0 holds every mark and every boundary key
-  if (rank != 0) return;
+  cluster_wait();  // every CTA has every count; rank 0 holds every boundary key
+  const int CS = static_cast<int>(cluster.num_blocks());
+  int32_t* dst = a.idx + static_cast<size_t>(row) * a.k;
+  const int n_recent_kept = P - rb;
 
-  // ---- E. rank 0: resolve the boundary bin, then write the row
-  if (mode == kModeGather) {
-    const int n_in = static_cast<int>(sh.gcount);
-    uint32_t* h = L.hist;  // scratch
-    const int start_level = (mask == 0xFFF00000u) ? 1 : ((mask == 0xFFFFFC00u) ? 2 : 3);
-    for (int level = start_level; level < 3; ++level) {
-      const int shift = level == 1 ? 10 : 0;
-      for (int i = t; i < kBinsL; i += kSelThreads) h[i] = 0u;
-      __syncthreads();
+  if (short_row) {
+    // ---- E/F (short rows). Rank 0 alone: resolve the boundary bin, mark the winners
+    //      in its row bitmap, write the row from the bitmap
+    if (rank != 0) return;
+    if (mode == kModeGather) {
+      const int n_in = static_cast<int>(sh.gcount);
+      int cut;
+      resolve_boundary(L.gbuf, n_in, L.hist, sh, prefix, mask, r_rem, cut);
       for (int i = t; i < n_in; i += kSelThreads) {
-        const uint32_t key = L.gbuf[i].x;
-        if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & (kBinsL - 1)], 1u);
+        const uint2 e = L.gbuf[i];
+        const uint32_t km = e.x & mask;
+        if (km > prefix || (km == prefix && static_cast<int>(e.y) <= cut))
+          atomicOr(&L.bitmap[e.y >> 5], 1u << (e.y & 31));
       }
       __syncthreads();
-      find_bin(h, kBinsL, r_rem, sh);
-      const bool whole = sh.f_rem == sh.f_cnt;
-      prefix |= static_cast<uint32_t>(sh.f_bin) << shift;
-      mask |= static_cast<uint32_t>(kBinsL - 1) << shift;
-      r_rem = sh.f_rem;
-      __syncthreads();
-      if (whole) break;
     }
-    // winners among the gathered keys: above the prefix, or within it -- all of them,
-    // unless all 32 bits are fixed and only r_rem of the equal keys are taken: then
-    // the r_rem lowest positions (positions are below 2^20: two 10-bit passes)
-    int cut = INT_MAX;
-    if (mask == 0xFFFFFFFFu) {
-      uint32_t n_eq = 0;
-      for (int i = t; i < n_in; i += kSelThreads) n_eq += L.gbuf[i].x == prefix ? 1u : 0u;
-      uint32_t tot_eq;
-      (void)block_excl_scan(n_eq, sh.scan, &tot_eq);
-      if (tot_eq > static_cast<uint32_t>(r_rem)) {
-        uint32_t pos_prefix = 0, pos_mask = 0;
-        int rr = r_rem;
-        for (int pl = 0; pl < 2; ++pl) {
-          const int shift = pl == 0 ? 10 : 0;
-          for (int i = t; i < kBinsL; i += kSelThreads) h[i] = 0u;
-          __syncthreads();
-          for (int i = t; i < n_in; i += kSelThreads) {
-            const uint2 e = L.gbuf[i];
-            if (e.x == prefix && (e.y & pos_mask) == pos_prefix)
-              atomicAdd(&h[(e.y >> shift) & (kBinsL - 1)], 1u);
-          }
-          __syncthreads();
-          find_bin_low(h, kBinsL, rr, sh);
-          pos_prefix |= static_cast<uint32_t>(sh.f_bin) << shift;
-          pos_mask |= static_cast<uint32_t>(kBinsL - 1) << shift;
-          rr = sh.f_rem;
-          __syncthreads();
-        }
-        cut = static_cast<int>(pos_prefix);
+    const int nw_row = CS * nw_cta;
+    uint32_t o_base = static_cast<uint32_t>(sink_end);
+    for (int w0 = 0; w0 < nw_row; w0 += kSelThreads) {
+      const int w = w0 + t;
+      uint32_t bits = w < nw_row ? L.bitmap[w] : 0u;
+      if (a.out_bitmap != nullptr && w < a.bm_words)
+        a.out_bitmap[static_cast<size_t>(row) * a.bm_words + w] = bits;
+      uint32_t r_tot;
+      uint32_t o = o_base + block_excl_scan(static_cast<uint32_t>(__popc(bits)), sh.scan, &r_tot);
+      while (bits) {
+        const int bit = __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (o < static_cast<uint32_t>(n)) dst[o] = w * 32 + bit;
+        ++o;
       }
+      o_base += r_tot;
     }
-    for (int i = t; i < n_in; i += kSelThreads) {
-      const uint2 e = L.gbuf[i];
-      const uint32_t km = e.x & mask;
-      const bool sel = km > prefix || (km == prefix && static_cast<int>(e.y) <= cut);
-      if (sel) atomicOr(&L.bitmap[e.y >> 5], 1u << (e.y & 31));
-    }
-    __syncthreads();
+    if (a.out_count != nullptr && t == 0) a.out_count[row] = static_cast<int>(o_base) - sink_end;
+    for (int i = t; i < sink_end; i += kSelThreads) dst[i] = i;
+    for (int i = t; i < n_recent_kept; i += kSelThreads) dst[n - n_recent_kept + i] = rb + i;
+    for (int m = n + t; m < a.k; m += kSelThreads) dst[m] = -1;
+    if (t == 0) a.n_sel[row] = n;
+    return;
   }
 
-  // the row: sinks, marked candidates in position order, the recent window, padding.
-  // Bitmap words go out in rounds of one word per thread (consecutive threads,
-  // consecutive words), each round a block scan of the words' counts.
-  int32_t* dst = a.idx + static_cast<size_t>(row) * a.k;
-  const int w_lo = sink_end >> 5;
-  const int w_hi = (rb + 31) >> 5;
-  uint32_t o_base = static_cast<uint32_t>(sink_end);
-  for (int w0 = w_lo; w0 < w_hi; w0 += kSelThreads) {
+  // ---- E (long rows, gather mode): rank 0 resolves the boundary bin, counts the
+  //      winners per owning CTA and hands every CTA the cut and where its candidates
+  //      start in the row
+  int out_base = sink_end;
+  uint32_t total = 0;  // candidates chosen in the row (rank 0)
+  if (mode == kModeGather) {
+    if (rank == 0) {
+      const int n_in = static_cast<int>(sh.gcount);
+      int cut;
+      resolve_boundary(L.gbuf, n_in, L.hist, sh, prefix, mask, r_rem, cut);
+      if (t < CS) sh.taken[t] = 0u;
+      __syncthreads();
+      for (int i = t; i < n_in; i += kSelThreads) {
+        const uint2 e = L.gbuf[i];
+        const uint32_t km = e.x & mask;
+        if (km > prefix || (km == prefix && static_cast<int>(e.y) <= cut))
+          atomicAdd(&sh.taken[static_cast<int>(e.y) / chunk], 1u);
+      }
+      __syncthreads();
+      if (t < CS) {
+        uint32_t before = 0;
+        for (int r = 0; r < t; ++r) before += sh.cnt[r] + sh.taken[r];
+        SelShared* d = cluster.map_shared_rank(&sh, t);
+        d->out_base = sink_end + static_cast<int>(before);
+        d->thr_prefix = prefix;
+        d->thr_mask = mask;
+        d->thr_cut = cut;
+      }
+      for (int r = 0; r < CS; ++r) total += sh.cnt[r] + sh.taken[r];
+    }
+    cluster_arrive();
+    cluster_wait();  // every CTA has the cut and its start
+    // this CTA's boundary-bin positions that made the cut
+    const uint32_t tp = sh.thr_prefix, tm = sh.thr_mask;
+    const int tc = sh.thr_cut;
+    uint64_t take = 0;
+    for (uint64_t m = inbin_kept; m; m &= m - 1) {
+      const int q = __ffsll(static_cast<long long>(m)) - 1;
+      const uint32_t km = L.keys[t * KPT + q] & tm;
+      if (km > tp || (km == tp && my0 + q <= tc)) take |= 1ull << q;
+    }
+    mark_bits(lbm, t * KPT, take);
+    out_base = sh.out_base;
+    __syncthreads();
+  } else {
+    for (int r = 0; r < CS; ++r) {
+      if (r < rank) out_base += static_cast<int>(sh.cnt[r]);
+      total += sh.cnt[r];
+    }
+  }
+
+  // ---- F. every CTA writes its candidates in position order from its bitmap words
+  //      (one word per thread per round, a block scan of the words' counts); rank 0
+  //      writes the sinks, the recent window and the padding
+  uint32_t o_base = static_cast<uint32_t>(out_base);
+  for (int w0 = 0; w0 < nw_cta; w0 += kSelThreads) {
     const int w = w0 + t;
-    uint32_t bits = w < w_hi ? L.bitmap[w] : 0u;
+    uint32_t bits = w < nw_cta ? lbm[w] : 0u;
+    if (a.out_bitmap != nullptr && w < nw_cta) {
+      // this pass's chosen candidates, for the next pass of the hybrid budget
+      const int gw = rank * nw_cta + w;
+      if (gw < a.bm_words) a.out_bitmap[static_cast<size_t>(row) * a.bm_words + gw] = bits;
+    }
     uint32_t r_tot;
     uint32_t o = o_base + block_excl_scan(static_cast<uint32_t>(__popc(bits)), sh.scan, &r_tot);
     while (bits) {
       const int bit = __ffs(bits) - 1;
       bits &= bits - 1;
-      if (o < static_cast<uint32_t>(n)) dst[o] = w * 32 + bit;
+      if (o < static_cast<uint32_t>(n)) dst[o] = rank * chunk + w * 32 + bit;
       ++o;
     }
     o_base += r_tot;
   }
-  if (a.out_bitmap != nullptr) {
-    // this pass's chosen candidates (the whole bitmap: every word was stored in D),
-    // for the next pass of the hybrid budget, and their number
-    for (int i = t; i < a.bm_words; i += kSelThreads)
-      a.out_bitmap[static_cast<size_t>(row) * a.bm_words + i] = L.bitmap[i];
-    if (t == 0) a.out_count[row] = static_cast<int>(o_base) - sink_end;
-  }
-  const int n_recent_kept = P - rb;
+  if (rank != 0) return;
+  if (a.out_count != nullptr && t == 0) a.out_count[row] = static_cast<int>(total);
   for (int i = t; i < sink_end; i += kSelThreads) dst[i] = i;
   for (int i = t; i < n_recent_kept; i += kSelThreads) dst[n - n_recent_kept + i] = rb + i;
   for (int m = n + t; m < a.k; m += kSelThreads) dst[m] = -1;
   if (t == 0) a.n_sel[row] = n;
 }
 
-int bitmap_words_for(int chunk, int cs) { return (chunk * cs + 31) / 32; }
 
 }  // namespace
 
@@ -618,9 +726,9 @@ int select_chunk(int P_max, int cs) {
 }
 
 size_t select_smem_bytes(int chunk, int cs) {
+  (void)cs;
   return static_cast<size_t>(kGatherCap) * 8 +
-         (static_cast<size_t>(chunk) + 2 * kBins0 + kBins0 + 2 * kBinsL +
-          bitmap_words_for(chunk, cs)) * 4;
+         (static_cast<size_t>(chunk) + 2 * kBins0 + kBins0 + 2 * kBinsL + kShortRowWords) * 4;
 }
 
 cudaError_t launch_select(const SelectArgs& sa, cudaStream_t stream) {
@@ -641,7 +749,6 @@ cudaError_t launch_select(const SelectArgs& sa, cudaStream_t stream) {
   p.n_sink = sa.n_sink;
   p.n_recent = sa.n_recent;
   p.chunk = chunk;
-  p.bitmap_words = bitmap_words_for(chunk, CS);
   p.m_limit = sa.m_limit;
   p.pre_bitmap = sa.pre_bitmap;
   p.pre_count = sa.pre_count;

@@ -767,9 +767,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Combine the partial (m, l, o) of the CTAs that shared a pair: block (pair, verify
-// row c), thread = dim.  With B = 1 a pair is spread over ~C / Hkv CTAs, so each block
-// issues the loads of up to 32 partials at once and combines them in chunk order.
 // Fused aggregation (blocks past the merge blocks): 4 * D consecutive positions of one
 // sequence per block, 4 per thread.  The score of position j is the sum of its
 // per-group partials in group order (fp32, starting from zero: the same sum, in the
@@ -822,19 +819,25 @@ __device__ __forceinline__ void aggregate_scores(const VParams& a, int blk) {
     if (h[i] != 0u) atomicAdd(a.hist + static_cast<size_t>(b) * kHistBins + i, h[i]);
 }
 
+// Combine the partial (m, l, o) of the CTAs that shared a pair: block (pair, verify
+// row c), thread = dim.  With B = 1 a pair is spread over ~C / Hkv CTAs, so each block
+// issues the loads of up to 32 partials at once and combines them in chunk order.
+// One flat grid: blocks [0, merge_pairs * NV) merge (pair, verify row); the rest are
+// the fused-aggregation blocks.
 template <int D, int NQ, int G>
 __global__ void __launch_bounds__(D) verify_merge_kernel(const VParams a, int ctas,
                                                          int merge_pairs) {
   constexpr int kU = 32;
-  const int p = blockIdx.x;
-  const int c = blockIdx.y;
+  const int x = blockIdx.x;
   const int dim = threadIdx.x;
   pdl_launch_dependents();
   pdl_wait_primary();  // partials of the verification kernel are complete
-  if (p >= merge_pairs) {
-    if (c == 0) aggregate_scores<D>(a, p - merge_pairs);
+  if (x >= merge_pairs * a.NV) {
+    aggregate_scores<D>(a, x - merge_pairs * a.NV);
     return;
   }
+  const int p = x / a.NV;
+  const int c = x - p * a.NV;
   const long long W = static_cast<long long>(a.pairs) * a.t_max;
   const long long first_v = static_cast<long long>(p) * a.t_max;
   const int c_first = cta_of(first_v, W, ctas);
@@ -906,7 +909,7 @@ cudaError_t launch_dng(const VerifyArgs& va, const VerifyPlan& plan, const VPara
   const int merge_pairs = plan.max_chunks > 1 ? plan.pairs : 0;
   const int agg = p.score != nullptr ? p.B * ((p.P_max + 4 * D - 1) / (4 * D)) : 0;
   if (e != cudaSuccess || merge_pairs + agg == 0) return e;
-  cfg.gridDim = dim3(merge_pairs + agg, merge_pairs > 0 ? p.NV : 1, 1);
+  cfg.gridDim = dim3(merge_pairs * p.NV + agg, 1, 1);
   cfg.blockDim = dim3(D, 1, 1);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G>, p, plan.ctas, merge_pairs);
