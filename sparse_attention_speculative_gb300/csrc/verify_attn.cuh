@@ -43,6 +43,7 @@
 #pragma once
 
 #include <cfloat>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -473,13 +474,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Seg s = segment_at(v, v1, a);
       v = s.next_v;
       // heads of this group whose logits are collected (all unless a mask is given)
-      uint32_t gmask = (G >= 32) ? 0xFFFFFFFFu : ((1u << G) - 1u);
+      constexpr uint32_t kAllHeads = (G >= 32) ? 0xFFFFFFFFu : ((1u << G) - 1u);
+      uint32_t gmask = kAllHeads;
       if (a.head_mask != nullptr) {
         gmask = 0u;
 #pragma unroll
         for (int hl = 0; hl < G; ++hl)
           gmask |= (__ldg(a.head_mask + s.g * G + hl) != 0 ? 1u : 0u) << hl;
       }
+      const bool all_heads = gmask == kAllHeads;
       const long long first_v = static_cast<long long>(s.p) * a.t_max;
       const int c_first = cta_of(first_v, W, C);
       const int c_last = cta_of(first_v + a.t_max - 1, W, C);
@@ -548,26 +551,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&s_empty[buf]);
 
-        // Collect-2-Query: logits of rows row0 / row1 and their group sum, j < P_b
+        // Collect-2-Query: logits of rows row0 / row1 and their group sum, j < P_b.
+        // The per-head mask test is compiled in only for segments that have a mask (a
+        // uniform branch): unmasked calls keep the loop of the plain collect.
+        auto collect_row = [&](auto masked, const uint32_t* raw, int c, float& acc) {
+#pragma unroll
+          for (int hl = 0; hl < G; ++hl) {
+            if constexpr (decltype(masked)::value) {
+              if (!((gmask >> hl) & 1u)) continue;
+            }
+            const float z = __uint_as_float(raw[hl]) * scale;
+            if (a.logits)
+              __stcs(a.logits + ((static_cast<size_t>(s.b) * 2 + c) * a.Hq + s.g * G + hl) *
+                                    a.P_max + j, z);
+            acc += z;
+          }
+        };
         if (want_collect) {
           float acc = 0.f;
-#pragma unroll
-          for (int hl = 0; hl < G; ++hl) {
-            if (!((gmask >> hl) & 1u)) continue;
-            const float z0 = __uint_as_float(c0raw[hl]) * scale;
-            if (a.logits)
-              __stcs(a.logits + ((static_cast<size_t>(s.b) * 2 + 0) * a.Hq + s.g * G + hl) *
-                                    a.P_max + j, z0);
-            acc += z0;
-          }
-#pragma unroll
-          for (int hl = 0; hl < G; ++hl) {
-            if (!((gmask >> hl) & 1u)) continue;
-            const float z1 = __uint_as_float(c1raw[hl]) * scale;
-            if (a.logits)
-              __stcs(a.logits + ((static_cast<size_t>(s.b) * 2 + 1) * a.Hq + s.g * G + hl) *
-                                    a.P_max + j, z1);
-            acc += z1;
+          if (all_heads) {
+            collect_row(std::false_type{}, c0raw, 0, acc);
+            collect_row(std::false_type{}, c1raw, 1, acc);
+          } else {
+            collect_row(std::true_type{}, c0raw, 0, acc);
+            collect_row(std::true_type{}, c1raw, 1, acc);
           }
           if (a.partial) a.partial[(static_cast<size_t>(s.b) * a.Hkv + s.g) * a.P_max + j] = acc;
         }
@@ -575,22 +582,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // split between the halves: this half's row, then the two halves' sums
         float call = 0.f;
         if (split_collect && j < s.P) {
-#pragma unroll
-          for (int hl = 0; hl < G; ++hl) {
-            if (!((gmask >> hl) & 1u)) continue;
-            const float z = __uint_as_float(c0raw[hl]) * scale;
-            if (a.logits)
-              __stcs(a.logits + ((static_cast<size_t>(s.b) * 2 + half) * a.Hq + s.g * G + hl) *
-                                    a.P_max + j, z);
-            call += z;
-          }
+          if (all_heads)
+            collect_row(std::false_type{}, c0raw, half, call);
+          else
+            collect_row(std::true_type{}, c0raw, half, call);
           if (half == 1) xsum[(it & 1) * kTile + row] = call;
         }
         if (collect_all && j < s.P) {
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
             const int cc = col0 + c;
-            if (cc < a.NV && ((gmask >> (cc % G)) & 1u)) {
+            if (cc < a.NV && (all_heads || ((gmask >> (cc % G)) & 1u))) {
               const float z = sv[c] * scale;
               if (a.logits)
                 __stcs(a.logits + ((static_cast<size_t>(s.b) * a.R + cc / G) * a.Hq + s.g * G +
@@ -822,9 +824,10 @@ __device__ __forceinline__ void aggregate_scores(const VParams& a, int blk) {
 // Combine the partial (m, l, o) of the CTAs that shared a pair: block (pair, verify
 // row c), thread = dim.  With B = 1 a pair is spread over ~C / Hkv CTAs, so each block
 // issues the loads of up to 32 partials at once and combines them in chunk order.
-// One flat grid: blocks [0, merge_pairs * NV) merge (pair, verify row); the rest are
-// the fused-aggregation blocks.
-template <int D, int NQ, int G>
+// One flat grid: blocks [0, merge_pairs * NV) merge (pair, verify row); with kAgg the
+// rest are the fused-aggregation blocks (only that variant carries their 16 KB of
+// shared memory).
+template <int D, int NQ, int G, bool kAgg>
 __global__ void __launch_bounds__(D) verify_merge_kernel(const VParams a, int ctas,
                                                          int merge_pairs) {
   constexpr int kU = 32;
@@ -833,7 +836,7 @@ __global__ void __launch_bounds__(D) verify_merge_kernel(const VParams a, int ct
   pdl_launch_dependents();
   pdl_wait_primary();  // partials of the verification kernel are complete
   if (x >= merge_pairs * a.NV) {
-    aggregate_scores<D>(a, x - merge_pairs * a.NV);
+    if constexpr (kAgg) aggregate_scores<D>(a, x - merge_pairs * a.NV);
     return;
   }
   const int p = x / a.NV;
@@ -912,7 +915,9 @@ cudaError_t launch_dng(const VerifyArgs& va, const VerifyPlan& plan, const VPara
   cfg.gridDim = dim3(merge_pairs * p.NV + agg, 1, 1);
   cfg.blockDim = dim3(D, 1, 1);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G>, p, plan.ctas, merge_pairs);
+  if (agg > 0)
+    return cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G, true>, p, plan.ctas, merge_pairs);
+  return cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G, false>, p, plan.ctas, merge_pairs);
 }
 
 inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {
