@@ -10,18 +10,15 @@
 // in ascending page order.  Unlike the aggregated selection of the verification pass,
 // the set differs between heads and verify rows.
 //
-// How (GB300 design), three kernels, each an HBM or latency problem, none a tensor-core
-// contraction worth the name (R*G <= 64 query rows per KV group):
+// How (GB300 design), three kernels:
 //  * page_mean_kernel: one warp per (sequence, KV group, page).  The page's 16 rows are
 //    16 * d * 2 contiguous bytes; every lane issues all of its 16-byte loads before it
 //    adds, then lanes holding the same columns combine with shuffles.  An optional
 //    per-sequence first page lets a decode loop refresh only the pages that changed:
 //    the means are a resident summary of the cache, like the cache itself.
-//  * block_score_kernel: one CTA per (64 pages, KV group, sequence).  The 64 x d tile
-//    of means and the group's R*G query rows sit in shared memory (the means with a
-//    row stride of d + 4 floats, so the float4 reads of 8 consecutive pages hit
-//    distinct banks; the query reads are warp-wide broadcasts); a thread owns one page
-//    and every fourth query row.
+//  * block_score_tc_kernel: one CTA per (128 pages, KV group, sequence) on the tensor
+//    cores: TMA loads the fp32 means into swizzled tiles, tcgen05.mma kind::tf32 forms
+//    S^T = kbar Q^T in TMEM, and each thread writes one page's scores.
 //  * block_select_kernel: one CTA per query row.  The row's scores become
 //    order-preserving 32-bit keys held in registers (each thread a contiguous run of
 //    pages).  A first histogram buckets the values linearly between the row's minimum
@@ -42,8 +39,6 @@ namespace {
 
 constexpr int kPageB = 16;
 constexpr int kMeanWarps = 8;         // pages per page-mean CTA
-constexpr int kScorePages = 64;       // pages per score CTA
-constexpr int kScoreThreads = 256;
 constexpr int kSelThreads = 512;
 
 // ---------------------------------------------------------------- page means
@@ -112,99 +107,144 @@ __global__ void __launch_bounds__(kMeanWarps * 32) page_mean_kernel(const BlockT
 }
 
 // ---------------------------------------------------------------- page scores
-template <int D>
-struct ScoreSmem {
-  float kbar[kScorePages][D + 4];
-  float q[64][D];
+// One CTA of four warps per (128 pages, KV group, sequence), on the tensor cores:
+// S^T[128 pages x NQ] = kbar[128 x d] . Q^T[d x NQ] (NQ = R * G rounded up to 16).
+// TMA brings the fp32 page means straight into 128-byte-swizzled K-major tiles (32 fp32
+// per row, d / 32 boxes); the group's bf16 query rows are staged as fp32 in the same
+// layout; tcgen05.mma kind::tf32 accumulates in TMEM (bf16 queries are exact in tf32,
+// the means lose their low 13 mantissa bits: ~1e-4 on a score); thread t reads page t's
+// NQ scores and writes them, each column a coalesced run of pages.
+constexpr int kTcPages = 128;
+constexpr int kTcScoreThreads = 128;
+
+template <int D, int NQ>
+struct TcScoreSmem {
+  static constexpr int kBox = kTcPages * 128;           // one 32-column box of the means
+  static constexpr int kOffA = 0;
+  static constexpr int kOffQ = kOffA + (D / 32) * kBox;
+  static constexpr int kOffBar = kOffQ + (D / 32) * NQ * 128;
+  static constexpr int kBytes = kOffBar + 64 + 1024;    // + alignment slack
+  static_assert(kOffQ % 1024 == 0 && kOffBar % 8 == 0, "layout");
 };
 
-// NR: query rows per thread (every fourth row from the thread's start), at least
-// ceil(R * G / 4); slots past R * G are predicated off.
-template <int D, int NR>
-__global__ void __launch_bounds__(kScoreThreads, 2) block_score_kernel(const BlockTopkArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  ScoreSmem<D>& sm = *reinterpret_cast<ScoreSmem<D>*>(smem_raw);
+template <int D, int NQ>
+__global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
+    const __grid_constant__ CUtensorMap kbar_map, const BlockTopkArgs a) {
+  using Sm = TcScoreSmem<D, NQ>;
+  extern __shared__ uint8_t sc_smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(sc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* a_s = base + Sm::kOffA;
+  uint8_t* q_s = base + Sm::kOffQ;
+  uint64_t* bar_a = reinterpret_cast<uint64_t*>(base + Sm::kOffBar);
+  uint64_t* bar_s = bar_a + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_a + 2);
   const int b = blockIdx.z, g = blockIdx.y;
-  const int beta0 = blockIdx.x * kScorePages;
-  const int t = threadIdx.x;
+  const int beta0 = blockIdx.x * kTcPages;
+  const int t = threadIdx.x, warp = t >> 5;
   const int G = a.G, RG = a.R * a.G;
+  if (t == 0) {
+    ptx::mbar_init(bar_a, 1);
+    ptx::mbar_init(bar_s, 1);
+    ptx::fence_mbarrier_init();
+    ptx::tma_prefetch_desc(&kbar_map);
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(tmem_slot, NQ <= 32 ? 32 : 64);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   ptx::pdl_launch_dependents();
   ptx::pdl_wait_primary();  // the page means come from the preceding kernel
+  // the tile's means are fetched before the prefix length is known (rows past the
+  // buffer read as zeros; a tile past the sequence is never used); every CTA waits for
+  // its copy before it leaves
+  if (t == 0) {
+    ptx::mbar_arrive_expect_tx(bar_a, (D / 32) * Sm::kBox);
+    const int row0 = (b * a.Hkv + g) * a.nblk_max + beta0;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c)
+      ptx::tma_load_2d(a_s + c * Sm::kBox, &kbar_map, bar_a, c * 32, row0);
+  }
+  // the group's query rows r = t * G + hl as fp32, zero past R * G: every load in
+  // flight before the first store
+  constexpr int QL = NQ * (D / 8) / kTcScoreThreads;
+  static_assert(NQ * (D / 8) % kTcScoreThreads == 0, "query staging");
+  const uint16_t* qb = static_cast<const uint16_t*>(a.q);
+  uint4 qv[QL];
+#pragma unroll
+  for (int u = 0; u < QL; ++u) {
+    const int i = t + u * kTcScoreThreads, r = i / (D / 8), c8 = i % (D / 8);
+    qv[u] = make_uint4(0, 0, 0, 0);
+    if (r < RG)
+      qv[u] = __ldg(reinterpret_cast<const uint4*>(
+          qb + ((static_cast<size_t>(b) * a.R + r / G) * a.Hq + g * G + r % G) * D + c8 * 8));
+  }
   const int P = __ldg(a.prefix_len + b);
   const int nblk = (P + kPageB - 1) / kPageB;
-  if (P < 0 || nblk > a.nblk_max) {
-    if (t == 0 && g == 0 && blockIdx.x == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
-    return;
-  }
-  if (beta0 >= nblk) return;
-  const int n_pages = min(kScorePages, nblk - beta0);
-  // stage the means and the query rows (bf16 -> fp32): every load of a thread is
-  // issued before the first shared-memory store
-  constexpr int C4 = D / 4, C8 = D / 8;
-  constexpr int KL = kScorePages * C4 / kScoreThreads;  // float4 of means per thread
-  constexpr int QL = 64 * C8 / kScoreThreads;           // 16-byte query chunks per thread
-  const float* src = a.kbar + ((static_cast<size_t>(b) * a.Hkv + g) * a.nblk_max + beta0) * D;
-  const uint16_t* qb = static_cast<const uint16_t*>(a.q);
-  float4 kv_r[KL];
-  uint4 q_r[QL];
+  const bool ok = P >= 0 && nblk <= a.nblk_max;
+  if (!ok && t == 0 && g == 0 && blockIdx.x == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
+  const bool work = ok && beta0 < nblk;  // CTA-uniform
+  bool timed_out = false;
+  if (work) {
 #pragma unroll
-  for (int u = 0; u < KL; ++u) {
-    const int i = t + u * kScoreThreads, p = i / C4, c = (i % C4) * 4;
-    kv_r[u] = p < n_pages ? __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(p) * D + c))
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-#pragma unroll
-  for (int u = 0; u < QL; ++u) {
-    const int i = t + u * kScoreThreads, r = i / C8, c = (i % C8) * 8;
-    q_r[u] = make_uint4(0, 0, 0, 0);
-    if (r < RG)
-      q_r[u] = __ldg(reinterpret_cast<const uint4*>(
-          qb + ((static_cast<size_t>(b) * a.R + r / G) * a.Hq + g * G + r % G) * D + c));
-  }
-#pragma unroll
-  for (int u = 0; u < KL; ++u) {
-    const int i = t + u * kScoreThreads, p = i / C4, c = (i % C4) * 4;
-    *reinterpret_cast<float4*>(&sm.kbar[p][c]) = kv_r[u];
-  }
-#pragma unroll
-  for (int u = 0; u < QL; ++u) {
-    const int i = t + u * kScoreThreads, r = i / C8, c = (i % C8) * 8;
-    if (r < RG) {
-      float4* o = reinterpret_cast<float4*>(&sm.q[r][c]);
-      o[0] = make_float4(bf16_lo(q_r[u].x), bf16_hi(q_r[u].x), bf16_lo(q_r[u].y), bf16_hi(q_r[u].y));
-      o[1] = make_float4(bf16_lo(q_r[u].z), bf16_hi(q_r[u].z), bf16_lo(q_r[u].w), bf16_hi(q_r[u].w));
+    for (int u = 0; u < QL; ++u) {
+      const int i = t + u * kTcScoreThreads, r = i / (D / 8), c8 = i % (D / 8);
+      const int c = c8 >> 2;            // 32-dim box
+      const int u0 = (c8 & 3) * 2;      // first 16-byte unit of the 128-byte row
+      uint8_t* row = q_s + c * NQ * 128 + r * 128;
+      const uint4 v = qv[u];
+      *reinterpret_cast<float4*>(row + ((u0 ^ (r & 7)) << 4)) =
+          make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+      *reinterpret_cast<float4*>(row + (((u0 + 1) ^ (r & 7)) << 4)) =
+          make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
     }
-  }
-  __syncthreads();
-  const int p = t & (kScorePages - 1);
-  const int rs = t / kScorePages;  // 0..3, uniform within a warp
-  if (p >= n_pages) return;
-  float acc[NR];
+    ptx::fence_proxy_async_smem();
+    __syncthreads();
+    if (t == 0) {
+      if (!ptx::mbar_wait(bar_a, 0)) timed_out = true;
+      ptx::tc_fence_after();
+      constexpr uint32_t idesc = ptx::idesc_tf32_f32(128, NQ, 0, 0);
+      const uint32_t aa = ptx::smem_u32(a_s), qa = ptx::smem_u32(q_s);
 #pragma unroll
-  for (int i = 0; i < NR; ++i) acc[i] = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < D; c += 4) {
-    const float4 kv = *reinterpret_cast<const float4*>(&sm.kbar[p][c]);
+      for (int kk = 0; kk < D / 8; ++kk) {
+        const int c = kk >> 2, w = kk & 3;
+        const uint64_t ad = ptx::sdesc_sw128(aa + c * Sm::kBox + w * 32, 16, 1024);
+        const uint64_t bd = ptx::sdesc_sw128(qa + c * NQ * 128 + w * 32, 16, 1024);
+        ptx::umma_tf32(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      ptx::umma_commit(bar_s);
+    }
+    if (!ptx::mbar_wait(bar_s, 0)) timed_out = true;
+    ptx::tc_fence_after();
+    float sv[NQ];
+    ptx::tmem_ld_cols<NQ>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
+                          reinterpret_cast<uint32_t*>(sv));
+    ptx::tmem_wait_ld();
+    const int beta = beta0 + t;  // TMEM lane t = page beta0 + t
+    if (beta < nblk) {
 #pragma unroll
-    for (int i = 0; i < NR; ++i) {
-      const int r = rs + 4 * i;
-      if (i < NR - 1 || r < RG) {
-        const float4 qv = *reinterpret_cast<const float4*>(&sm.q[r][c]);
-        acc[i] = fmaf(qv.x, kv.x, acc[i]);
-        acc[i] = fmaf(qv.y, kv.y, acc[i]);
-        acc[i] = fmaf(qv.z, kv.z, acc[i]);
-        acc[i] = fmaf(qv.w, kv.w, acc[i]);
+      for (int c = 0; c < NQ; ++c) {
+        if (c < RG) {
+          const int tr = c / G, h = g * G + c % G;
+          a.scores[((static_cast<size_t>(b) * a.R + tr) * a.Hq + h) * a.nblk_max + beta] =
+              sv[c] * a.scale + 0.f;  // + 0 turns -0 into +0: equal scores compare equal as keys
+        }
       }
     }
+  } else if (t == 0) {
+    // no MMA reads this tile, but its copy must land before the CTA leaves
+    if (!ptx::mbar_wait(bar_a, 0)) timed_out = true;
   }
-#pragma unroll
-  for (int i = 0; i < NR; ++i) {
-    const int r = rs + 4 * i;
-    if (r < RG) {
-      const int tr = r / G, h = g * G + r % G;
-      a.scores[((static_cast<size_t>(b) * a.R + tr) * a.Hq + h) * a.nblk_max + beta0 + p] =
-          acc[i] * a.scale + 0.f;  // + 0 turns -0 into +0: equal scores compare equal as keys
-    }
+  if (timed_out) flag_status(a.status, VSD_DEV_TIMEOUT);
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, NQ <= 32 ? 32 : 64);
   }
 }
 
@@ -486,23 +526,32 @@ cudaError_t launch_pdl(K kernel, dim3 grid, int threads, int smem, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-template <int D, int NR>
-cudaError_t launch_scores_dn(const BlockTopkArgs& a, cudaStream_t stream) {
-  dim3 grid((a.nblk_max + kScorePages - 1) / kScorePages, a.Hkv, a.B);
-  return launch_pdl(block_score_kernel<D, NR>, grid, kScoreThreads,
-                    static_cast<int>(sizeof(ScoreSmem<D>)), stream, a);
+template <int D, int NQ>
+cudaError_t launch_scores_dn(const CUtensorMap& map, const BlockTopkArgs& a, cudaStream_t stream) {
+  auto kern = block_score_tc_kernel<D, NQ>;
+  constexpr int smem = TcScoreSmem<D, NQ>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.nblk_max + kTcPages - 1) / kTcPages, a.Hkv, a.B);
+  cfg.blockDim = dim3(kTcScoreThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, map, a);
 }
 
-// rows per thread rounded up to one of a few instantiations
 template <int D>
-cudaError_t launch_scores_d(const BlockTopkArgs& a, cudaStream_t stream) {
-  const int nr = (a.R * a.G + 3) / 4;
-  if (nr <= 2) return launch_scores_dn<D, 2>(a, stream);
-  if (nr <= 4) return launch_scores_dn<D, 4>(a, stream);
-  if (nr <= 6) return launch_scores_dn<D, 6>(a, stream);
-  if (nr <= 8) return launch_scores_dn<D, 8>(a, stream);
-  if (nr <= 12) return launch_scores_dn<D, 12>(a, stream);
-  return launch_scores_dn<D, 16>(a, stream);
+cudaError_t launch_scores_d(const CUtensorMap& map, const BlockTopkArgs& a, cudaStream_t stream) {
+  const int nq = (a.R * a.G + 15) / 16 * 16;
+  if (nq <= 16) return launch_scores_dn<D, 16>(map, a, stream);
+  if (nq <= 32) return launch_scores_dn<D, 32>(map, a, stream);
+  if (nq <= 48) return launch_scores_dn<D, 48>(map, a, stream);
+  return launch_scores_dn<D, 64>(map, a, stream);
 }
 
 }  // namespace
@@ -521,11 +570,12 @@ cudaError_t launch_page_means(const BlockTopkArgs& a, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_block_topk(const BlockTopkArgs& a, cudaStream_t stream) {
+cudaError_t launch_block_topk(const CUtensorMap& kbar_map, const BlockTopkArgs& a,
+                              cudaStream_t stream) {
   if (a.B == 0) return cudaSuccess;
   if (a.nblk_max > 0) {
-    cudaError_t e = a.d == 128   ? launch_scores_d<128>(a, stream)
-                    : a.d == 64 ? launch_scores_d<64>(a, stream)
+    cudaError_t e = a.d == 128   ? launch_scores_d<128>(kbar_map, a, stream)
+                    : a.d == 64 ? launch_scores_d<64>(kbar_map, a, stream)
                                 : cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
   }

@@ -141,6 +141,9 @@ struct BlockTopkArgs {
 // Threads' item count of the selection kernel for nblk_max pages, -1 above 16384.
 int block_select_items(int nblk_max);
 cudaError_t launch_page_means(const BlockTopkArgs& a, cudaStream_t stream);
-cudaError_t launch_block_topk(const BlockTopkArgs& a, cudaStream_t stream);
+// kbar_map: 2-D fp32 tensor map over the page means {d, B * Hkv * nblk_max}, box
+// {32, 128}, 128-byte swizzle.
+cudaError_t launch_block_topk(const CUtensorMap& kbar_map, const BlockTopkArgs& a,
+                              cudaStream_t stream);
 
 }  // namespace vsd

@@ -103,6 +103,25 @@ vsd_status make_cache_map(CUtensorMap* map, const void* cache, const vsd_geom* g
   return VSD_OK;
 }
 
+// 2-D fp32 map over page means [rows][d]: box = 32 columns (128 bytes) x 128 rows.
+vsd_status make_means_map(CUtensorMap* map, const float* means, int d, long long rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  vsd_status st = encoder(&enc);
+  if (st != VSD_OK) return st;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(means), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = static_cast<int>(r);
+    return VSD_ERR_CUDA;
+  }
+  return VSD_OK;
+}
+
 vsd_status verify_checks(const vsd_geom* geom, int R, int P_max) {
   vsd_status st = check_geom(geom);
   if (st != VSD_OK) return st;
@@ -686,7 +705,9 @@ vsd_status vsd_block_topk(const vsd_geom* geom, int R, const void* q, const floa
   if (R * G > 64 || vsd::block_select_items(page_blocks_max) < 0 || geom->B > 65535 ||
       geom->Hkv > 65535)
     return VSD_ERR_UNSUPPORTED;
-  if (static_cast<long long>(geom->B) * R * geom->Hq > 0x7FFFFFFFll) return VSD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(geom->B) * R * geom->Hq > 0x7FFFFFFFll ||
+      static_cast<long long>(geom->B) * geom->Hkv * page_blocks_max > 0x7FFFFFFFll)
+    return VSD_ERR_UNSUPPORTED;
   if (geom->B == 0) return VSD_OK;
   if (!q || !prefix_len || !blocks || (page_blocks_max > 0 && (!page_means || !scores)))
     return VSD_ERR_INVALID_ARG;
@@ -715,7 +736,13 @@ vsd_status vsd_block_topk(const vsd_geom* geom, int R, const void* q, const floa
   a.nblk_max = page_blocks_max;
   a.kb = kb;
   a.scale = scale;
-  cudaError_t e = vsd::launch_block_topk(a, static_cast<cudaStream_t>(stream));
+  CUtensorMap map;
+  if (page_blocks_max > 0) {
+    st = make_means_map(&map, page_means, geom->head_dim,
+                        static_cast<long long>(geom->B) * geom->Hkv * page_blocks_max);
+    if (st != VSD_OK) return st;
+  }
+  cudaError_t e = vsd::launch_block_topk(map, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return VSD_OK;
 }
