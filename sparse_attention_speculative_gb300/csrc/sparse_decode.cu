@@ -117,14 +117,15 @@ __device__ __forceinline__ SList attended_list(int ns, int t0, int t1, const SPa
 // Combine the n partial (m, l, o) of one pair's splits and write its G output rows.
 // Thread = (float4 group of (head, dims), part); part p takes splits p, p + kParts,
 // ... with all loads of a round in flight; the parts then combine in shared memory.
-template <int D, int G, int kSThreads>
+// kRound: splits per load round when a thread holds one output group.
+template <int D, int G, int kSThreads, int kRound = 16>
 __device__ __forceinline__ void merge_splits(const SParams& a, float* scratch, int pair, int b,
                                              int g, int n) {
   constexpr int kQ = D / 4;
   constexpr int NG = G * kQ;                              // float4 groups of the output
   constexpr int kGPT = NG > kSThreads ? NG / kSThreads : 1;  // groups per thread
   constexpr int kParts = NG >= kSThreads ? 1 : kSThreads / NG;
-  constexpr int kU = 16 / kGPT > 1 ? 16 / kGPT : 1;       // splits per load round
+  constexpr int kU = kGPT == 1 ? kRound : (16 / kGPT > 1 ? 16 / kGPT : 1);  // per load round
   static_assert(NG * kParts / kGPT == kSThreads || NG >= kSThreads, "merge layout");
   const int t = threadIdx.x;
   const int part = kParts > 1 ? t / NG : 0;
@@ -741,7 +742,9 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
   }
   __syncthreads();
   if (!s_last) return;
-  merge_splits<D, G, kTcThreads>(a, scratch, pair, b, g, n_splits);
+  // 24 splits per round: a head's 2048 selected positions plus its tail (17 splits)
+  // merge in one round of loads
+  merge_splits<D, G, kTcThreads, 24>(a, scratch, pair, b, g, n_splits);
 }
 
 template <int D, int G>
