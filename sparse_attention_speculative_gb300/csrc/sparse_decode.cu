@@ -560,11 +560,16 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
   ptx::pdl_launch_dependents();
   ptx::pdl_wait_primary();  // idx / n_sel come from the preceding kernel
 
+  // this thread's index is loaded together with the list lengths (every position
+  // below k_max is valid memory; it is used only if the position is a selected one)
+  const int lo = split * a.split_len;
+  const int j_spec = (a.idx != nullptr && lo + t < a.k_max)
+                         ? __ldg(a.idx + static_cast<size_t>(b) * a.k_max + lo + t)
+                         : 0;
   const int ns_raw = a.n_sel != nullptr ? __ldg(a.n_sel + b) : 0;
   const int t0_raw = __ldg(a.tail_start + b);
   const int t1 = __ldg(a.seq_len + b);
   const SList L = attended_list(ns_raw, t0_raw, t1, a, split == 0 && g == 0 && t == 0);
-  const int lo = split * a.split_len;
   const bool work = lo < L.total || (split == 0 && L.total == 0);
   const int n_splits = (L.total + a.split_len - 1) / a.split_len;
   const bool direct = n_splits <= 1;
@@ -576,8 +581,7 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
     const int pos = lo + t;
     int crow = -1;
     if (pos < L.total && pos < lo + kBatch) {
-      const int j = pos >= L.ns ? L.t0 + (pos - L.ns)
-                                : __ldg(a.idx + static_cast<size_t>(b) * a.k_max + pos);
+      const int j = pos >= L.ns ? L.t0 + (pos - L.ns) : j_spec;
       if (j < 0 || j >= t1) {
         flag_status(a.status, VSD_DEV_BAD_INDEX);
       } else {
