@@ -783,13 +783,27 @@ __device__ __forceinline__ void aggregate_scores(const VParams& a, int blk) {
   const int b = blk / per_seq;
   const int j0 = (blk - b * per_seq) * kPos + static_cast<int>(threadIdx.x) * 4;
   for (int i = threadIdx.x; i < kHistBins; i += D) h[i] = 0u;
-  const int P = __ldg(a.prefix_len + b);
-  const bool ok = P >= 0 && P <= a.P_max;  // else flagged by the verification kernel
+  // the partials are loaded before the prefix length arrives (every position below
+  // P_max is valid memory); positions at or past P_b are masked afterwards
   float s[4] = {0.f, 0.f, 0.f, 0.f};
-  if (ok && j0 < P) {
+  if (j0 < a.P_max) {
     const float* base = a.partial + static_cast<size_t>(b) * a.Hkv * a.P_max + j0;
     if ((a.P_max & 3) == 0) {
-      for (int g = 0; g < a.Hkv; ++g) {
+      int g = 0;
+      for (; g + 8 <= a.Hkv; g += 8) {
+        float4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          x[u] = __ldcg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g + u) * a.P_max));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          s[0] += x[u].x;
+          s[1] += x[u].y;
+          s[2] += x[u].z;
+          s[3] += x[u].w;
+        }
+      }
+      for (; g < a.Hkv; ++g) {
         const float4 x = __ldcg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g) * a.P_max));
         s[0] += x.x;
         s[1] += x.y;
@@ -803,6 +817,8 @@ __device__ __forceinline__ void aggregate_scores(const VParams& a, int blk) {
           if (j0 + u < a.P_max) s[u] += __ldcg(base + static_cast<size_t>(g) * a.P_max + u);
     }
   }
+  const int P = __ldg(a.prefix_len + b);
+  const bool ok = P >= 0 && P <= a.P_max;  // else flagged by the verification kernel
   __syncthreads();
   if (ok) {
 #pragma unroll
