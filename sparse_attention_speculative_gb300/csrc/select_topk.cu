@@ -346,6 +346,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   const int my0 = rank * chunk + t * KPT;  // this thread's positions [my0, my0 + KPT)
   float s_first[4];
   sum4(my0, s_first);
+  // scored input: the row's level-0 histogram is an input too -- its loads go out now
+  constexpr int kHistPerThread = kBins0 / kSelThreads;
+  uint32_t h_pre[kHistPerThread];
+  if (a.hist != nullptr) {
+#pragma unroll
+    for (int i = 0; i < kHistPerThread; ++i)
+      h_pre[i] = __ldg(a.hist + static_cast<size_t>(row) * kBins0 + t + i * kSelThreads);
+  }
 
   int P = __ldg(a.prefix_len + row);
   if (P < 0 || P > a.P_max) {
@@ -356,6 +364,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   const int sink_end = a.n_sink < P ? a.n_sink : P;
   const int rb0 = P - a.n_recent > 0 ? P - a.n_recent : 0;
   const int rb = rb0 > sink_end ? rb0 : sink_end;  // candidates: [sink_end, rb)
+  // scored input: the scores of the positions that are not ranked (sinks, recent
+  // window) are taken out of the histogram below; the first 512 of them load now
+  const int n_prot = sink_end + (P - rb);
+  uint32_t prot_key = 0u;
+  if (a.hist != nullptr && t < n_prot) {
+    const int j = t < sink_end ? t : rb + (t - sink_end);
+    prot_key = order_key(__ldg(base + j));
+  }
   // candidates chosen beforehand (first pass of the hybrid budget) are always taken
   // and not ranked; this thread's KPT positions sit in one word of that bitmap
   uint32_t pre_bits = 0u;
@@ -431,8 +447,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
         // scored input: the histogram of every prefix position came with the scores;
         // each CTA takes the positions that are not ranked (sinks, recent window) out
         // of its own copy and searches it -- no cluster round
-        const uint32_t* src = a.hist + static_cast<size_t>(row) * kBins0;
-        for (int i = t; i < kBins0; i += kSelThreads) gh_local[i] = __ldg(src + i);
+#pragma unroll
+        for (int i = 0; i < kHistPerThread; ++i) gh_local[t + i * kSelThreads] = h_pre[i];
         if (t == 0) {
           // a histogram that does not hold r_rem candidates (not the one written with
           // these scores) finds no bin: take bin 0 whole, and flag it
@@ -441,8 +457,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
           sh.f_cnt = -1;
         }
         __syncthreads();
-        const int n_prot = sink_end + (P - rb);
-        for (int i = t; i < n_prot; i += kSelThreads) {
+        if (t < n_prot) atomicSub(&gh_local[prot_key >> 20], 1u);
+        for (int i = t + kSelThreads; i < n_prot; i += kSelThreads) {
           const int j = i < sink_end ? i : rb + (i - sink_end);
           atomicSub(&gh_local[order_key(__ldg(base + j)) >> 20], 1u);
         }
