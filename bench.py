@@ -505,8 +505,9 @@ def run_gpu(args, world, rank, local):
                          "read so no dirty lines remain)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "timing": "value: one CUDA-graph replay of the iteration per step (device events "
-                  "around the replay); kernels: the same iteration launched eagerly with "
-                  "events between kernels, so each figure includes its launch gap",
+                  "around the replay); kernels: medians over the timed iterations of the "
+                  "same iteration launched eagerly with events between kernels, so each "
+                  "figure includes its launch gap",
         "us_per_iter_eager": statistics.mean(per["step"]) * 1e6,
         "kernels": kernels,
         "select_over_verify": t_select / t_verify,
