@@ -229,7 +229,9 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
  *   score_hist[b][i] = #{ j < P_b : key(score[b][j]) >> 20 == i },  i < 4096
  * where key(x) maps the fp32 bits order-preservingly to uint32 (sign bit set for
  * x >= +0: bits | 0x80000000; else ~bits).  score fp32 [B][P_max] and score_hist
- * uint32 [B][4096] are caller-owned; score_hist is overwritten (no zeroing needed).
+ * uint32 [B][4096] are caller-owned (4-byte aligned; the rows of several calls may
+ * share one buffer); score_hist is overwritten (no zeroing needed).  The selection
+ * reads a score buffer with 16-byte loads: its base must be 16-byte aligned.
  *
  * vsd_select_topk_scored: vsd_select_topk on n_rows = B rows of such a score
  * (Hkv = 1) and its histogram -- the same index sets, bit for bit, as

@@ -282,7 +282,8 @@ vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const voi
                                           void* stream) {
   if (partial_scores == nullptr || score == nullptr || score_hist == nullptr)
     return geom != nullptr && geom->B == 0 ? VSD_OK : VSD_ERR_INVALID_ARG;
-  if (!aligned(score, 16) || !aligned(score_hist, 4)) return VSD_ERR_INVALID_ARG;
+  // the aggregation writes the score one float at a time: 4-byte alignment suffices
+  if (!aligned(score, 4) || !aligned(score_hist, 4)) return VSD_ERR_INVALID_ARG;
   return verify_call(geom, R, q, k_cache, v_cache, block_table, prefix_len, false,
                      collect_row0, collect_row1, nullptr, P_max, scale, logits,
                      partial_scores, out, workspace, workspace_bytes, stream, score,

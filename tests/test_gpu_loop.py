@@ -32,6 +32,10 @@ def _loop(w, layers, iterations, seed):
     for it in range(iterations):
         pl = torch.tensor(prefix, dtype=torch.int32, device=dev)
         partial = torch.empty((layers * B, Hkv, P_max), dtype=torch.float32, device=dev)
+        # the fused path: each layer's scored verification fills its rows of one score
+        # buffer and one histogram buffer
+        score = torch.empty((layers * B, P_max), dtype=torch.float32, device=dev)
+        hist = torch.empty((layers * B, vsd.HIST_BINS), dtype=torch.int32, device=dev)
         s_ref_rows = []
         for l, batch in enumerate(batches):
             tag = (seed * 1000 + it) * 100 + l
@@ -45,8 +49,13 @@ def _loop(w, layers, iterations, seed):
             out, logits, _ = vsd.vsd_verify_attn_collect(
                 batch.q, batch.k_cache, batch.v_cache, batch.block_table, pl, P_max=P_max,
                 scale=w.scale, partial=partial[l * B:(l + 1) * B])
+            out_f = vsd.vsd_verify_attn_collect_scored(
+                batch.q, batch.k_cache, batch.v_cache, batch.block_table, pl, P_max=P_max,
+                scale=w.scale, score=score[l * B:(l + 1) * B],
+                score_hist=hist[l * B:(l + 1) * B])[0]
             torch.cuda.synchronize()
             assert vsd.vsd_read_device_status() == 0
+            assert torch.equal(out_f, out)
             h = host_arrays(batch)
             o_ref, l_ref, p_ref = oracle.verify(h["q"], h["k_cache"], h["v_cache"],
                                                 h["block_table"], h["prefix_len"],
@@ -60,8 +69,11 @@ def _loop(w, layers, iterations, seed):
         rows_pl = pl.repeat(layers)
         idx, n_sel, _ = vsd.vsd_select_topk(partial, rows_pl, k=w.k, n_sink=w.n_sink,
                                             n_recent=w.n_recent)
+        idx_f, n_sel_f = vsd.vsd_select_topk_scored(score, hist, rows_pl, k=w.k,
+                                                    n_sink=w.n_sink, n_recent=w.n_recent)
         torch.cuda.synchronize()
         assert vsd.vsd_read_device_status() == 0
+        assert torch.equal(idx_f, idx) and torch.equal(n_sel_f, n_sel)
         s_ref = np.concatenate(s_ref_rows, axis=0)
         rp = rows_pl.cpu().numpy()
         i64, n64 = oracle.select(s_ref, rp, k=w.k, n_sink=w.n_sink, n_recent=w.n_recent)
