@@ -583,3 +583,22 @@ def test_verify_collect_srh_head_mask():
             off = np.nonzero(mask == 0)[0]
             assert_rel_close(lg[b][:, on, :P], l_ref[b][:, on, :P], "srh logits")
             assert np.all(lg[b][:, off, :] == 0)
+
+
+def test_sparse_long_list_cuda_core_step():
+    """A selection longer than 1024 batches of 128 positions runs on the CUDA-core draft
+    kernel (splits of several batches); against the oracle."""
+    from sparse_attention_speculative_gb300.synth import host_arrays, make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    P, k = 200000, 140000
+    w = Workload("sparse_long", B=1, P=P, Hq=2, Hkv=1, d=64, gamma=2, k=k, n_sink=4,
+                 n_recent=64, seed=91, prefix_lens=(P,))
+    batch = make_batch(w, "cuda")
+    rng = np.random.default_rng(91)
+    sel = np.sort(rng.choice(P, size=k, replace=False)).astype(np.int32)
+    idx = torch.tensor(sel[None, :], device="cuda")
+    n_sel = torch.tensor([k], dtype=torch.int32, device="cuda")
+    tail_start = batch.prefix_len.clone()
+    seq_len = batch.prefix_len + w.R
+    check_sparse(batch, w, idx, n_sel, tail_start, seq_len, max_tail=w.R)
