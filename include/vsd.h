@@ -397,6 +397,15 @@ vsd_status vsd_block_topk(const vsd_geom* geom, int R, const void* q, const floa
                           float* scores, int32_t* blocks, void* stream);
 
 /* ------------------------------------------------------------------------------
+ * vsd_copy: dst <- src as a kernel on `stream` (a programmatic dependent of the
+ * preceding kernel).  Either pointer may be pinned host memory, which the device
+ * addresses directly; a decode loop moves its inputs in and its results out this way.
+ * bytes a multiple of 16, both pointers 16-byte aligned (VSD_ERR_INVALID_ARG
+ * otherwise); the ranges must not overlap.
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_copy(void* dst, const void* src, size_t bytes, void* stream);
+
+/* ------------------------------------------------------------------------------
  * Device status word and errors.
  * vsd_read_device_status synchronizes `stream`, returns the accumulated
  * VSD_DEV_* bits of every kernel of this library on the current device since the

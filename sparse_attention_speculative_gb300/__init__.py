@@ -15,5 +15,6 @@ from ._lib import (DEV_BAD_BLOCK, DEV_BAD_INDEX, DEV_BAD_LENGTH, DEV_TIMEOUT, Ge
                    vsd_verify_attn_collect_all,
                    vsd_verify_attn_collect_noalloc, vsd_verify_workspace_size,
                    page_blocks, vsd_page_key_means, vsd_block_topk,
-                   vsd_verify_attn_collect_scored, vsd_select_topk_scored, HIST_BINS)
+                   vsd_verify_attn_collect_scored, vsd_select_topk_scored, HIST_BINS,
+                   vsd_copy)
 from .iteration import IterationGraph  # noqa: F401

@@ -81,6 +81,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                        P, P, P, P, SZ, P]
         lib.vsd_select_topk_scored.argtypes = [I, P, P, P, I, I, I, I, P, P, P]
         lib.vsd_page_key_means.argtypes = [GP, P, P, P, P, I, P, P]
+        lib.vsd_copy.argtypes = [P, P, SZ, P]
         lib.vsd_block_topk.argtypes = [GP, I, P, P, P, I, I, F, P, P, P]
         lib.vsd_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
         lib.vsd_get_error_string.argtypes = [I]
@@ -94,7 +95,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                      "vsd_verify_attn_collect_noalloc",
                      "vsd_select_workspace_size", "vsd_select_topk", "vsd_sparse_workspace_size",
                      "vsd_sparse_decode_attn", "vsd_page_key_means", "vsd_block_topk",
-                     "vsd_verify_attn_collect_scored", "vsd_select_topk_scored",
+                     "vsd_verify_attn_collect_scored", "vsd_select_topk_scored", "vsd_copy",
                      "vsd_read_device_status", "vsd_last_cuda_error"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -520,3 +521,14 @@ def vsd_select_topk_scored(score, score_hist, prefix_len, *, k: int, n_sink: int
                                     _ptr(n_sel), _stream(stream))
     _check(rc, "vsd_select_topk_scored")
     return idx, n_sel
+
+
+def vsd_copy(dst, src, stream=None):
+    """dst <- src (same byte size, a multiple of 16) by a kernel; either tensor may be in
+    pinned host memory."""
+    lib = load()
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("vsd_copy: size mismatch")
+    _check(lib.vsd_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "vsd_copy")
+    return dst

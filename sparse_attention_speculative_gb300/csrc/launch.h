@@ -121,6 +121,11 @@ struct SparseVerifyArgs {
 int sparse_verify_pages(int k_max, int R);
 cudaError_t launch_sparse_verify_gather(const SparseVerifyArgs& a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- copies
+// dst <- src, `bytes` a multiple of 16, both 16-byte aligned; either may be pinned host
+// memory (addressable from the device).
+cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+
 // ---------------------------------------------------------------- per-query block top-k
 // Page mean keys kbar [B][Hkv][nblk_max][d] fp32, page scores [B][R][Hq][nblk_max] fp32,
 // kept pages [B][R][Hq][kb] int32 (ascending, padded with -1).

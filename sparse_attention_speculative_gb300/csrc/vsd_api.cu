@@ -659,6 +659,15 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
   return VSD_OK;
 }
 
+vsd_status vsd_copy(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return VSD_OK;
+  if (!dst || !src || bytes % 16 != 0 || !aligned(dst, 16) || !aligned(src, 16))
+    return VSD_ERR_INVALID_ARG;
+  cudaError_t e = vsd::launch_copy16(dst, src, bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
 vsd_status vsd_page_key_means(const vsd_geom* geom, const void* k_cache,
                               const int32_t* block_table, const int32_t* prefix_len,
                               const int32_t* page_begin, int page_blocks_max,

@@ -602,3 +602,19 @@ def test_sparse_long_list_cuda_core_step():
     tail_start = batch.prefix_len.clone()
     seq_len = batch.prefix_len + w.R
     check_sparse(batch, w, idx, n_sel, tail_start, seq_len, max_tail=w.R)
+
+
+def test_vsd_copy_host_device():
+    """The kernel copy between pinned host memory and the device, both directions,
+    bit for bit; sizes that are not a multiple of 16 bytes are refused."""
+    vsd = _vsd()
+    rng = np.random.default_rng(3)
+    src = torch.tensor(rng.integers(0, 256, size=4096 * 3 + 48, dtype=np.uint8)).pin_memory()
+    dev = torch.empty(src.numel(), dtype=torch.uint8, device="cuda")
+    back = torch.zeros(src.numel(), dtype=torch.uint8).pin_memory()
+    vsd.vsd_copy(dev, src)
+    vsd.vsd_copy(back, dev)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src) and torch.equal(dev.cpu(), src)
+    with pytest.raises(vsd.VsdError):
+        vsd.vsd_copy(dev[:20], src[:20])
