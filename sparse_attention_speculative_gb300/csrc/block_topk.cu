@@ -254,7 +254,8 @@ __device__ __forceinline__ uint32_t order_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Inclusive prefix sum over the CTA (kSelThreads threads); `wsum` holds the warp totals.
+// Inclusive prefix sum over the CTA (NT threads); `wsum` holds the warp totals.
+template <int NT>
 __device__ __forceinline__ int cta_inclusive_scan(int x, int* wsum) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
@@ -266,7 +267,7 @@ __device__ __forceinline__ int cta_inclusive_scan(int x, int* wsum) {
   __syncthreads();
   int add = 0;
 #pragma unroll
-  for (int i = 0; i < kSelThreads / 32; ++i)
+  for (int i = 0; i < NT / 32; ++i)
     if (i < w) add += wsum[i];
   return x + add;
 }
@@ -295,11 +296,12 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-constexpr int kMaxCand = kSelThreads;  // boundary-bucket candidates ranked directly
+// NT threads per row; the boundary bucket's candidates are ranked directly up to NT
 constexpr int kBins = 256;
 
-template <int ITEMS>
-__global__ void __launch_bounds__(kSelThreads) block_select_kernel(const BlockTopkArgs a) {
+template <int ITEMS, int NT>
+__global__ void __launch_bounds__(NT) block_select_kernel(const BlockTopkArgs a) {
+  constexpr int kSelThreads = NT, kMaxCand = NT;
   static_assert(kSelThreads >= kBins && ITEMS <= 32, "one bin per thread; keep mask in 32 bits");
   __shared__ int hist[2][kBins];
   __shared__ int wsum[kSelThreads / 32];
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const BlockTo
     __syncthreads();
     // counts from the highest bucket down: thread tid < 256 owns bucket 255 - tid
     const int c = tid < kBins ? hist[0][kBins - 1 - tid] : 0;
-    const int incl = cta_inclusive_scan(c, wsum);
+    const int incl = cta_inclusive_scan<NT>(c, wsum);
     const int excl = incl - c;
     if (c > 0 && excl < need && need <= incl) {
       s_digit = kBins - 1 - tid;
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const BlockTo
         if (tid < kBins) hist[(pass + 1) & 1][tid] = 0;  // its readers finished last pass
         __syncthreads();
         const int cd = tid < kBins ? Hp[kBins - 1 - tid] : 0;
-        const int incd = cta_inclusive_scan(cd, wsum);
+        const int incd = cta_inclusive_scan<NT>(cd, wsum);
         const int exd = incd - cd;
         if (cd > 0 && exd < need && need <= incd) {
           s_digit = kBins - 1 - tid;
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(kSelThreads) block_select_kernel(const BlockTo
     }
   }
   const int packed = __popc(keep) | (__popc(in_class) << 16);  // both < 2^16
-  const int excl = cta_inclusive_scan(packed, wsum) - packed;
+  const int excl = cta_inclusive_scan<NT>(packed, wsum) - packed;
   int eq_before = excl >> 16;
   const int eq_take = whole ? (1 << 30) : need;
   int pos = (excl & 0xFFFF) + min(eq_before, eq_take);
@@ -579,14 +581,36 @@ cudaError_t launch_block_topk(const CUtensorMap& kbar_map, const BlockTopkArgs& 
                                 : cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
   }
-  const dim3 grid(a.B * a.R * a.Hq);
+  const int rows = a.B * a.R * a.Hq;
+  const dim3 grid(rows);
+  // many rows: 256-thread CTAs (twice as many resident per SM); few rows: 512 threads,
+  // half the work per thread on each row's dependent chain
+  int sm_count = 152;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+  }
+  if (rows > 2 * sm_count && a.nblk_max <= 256 * 32) {
+    int items = 1;
+    while (items * 256 < a.nblk_max) items <<= 1;
+    switch (items) {
+      case 1: return launch_pdl(block_select_kernel<1, 256>, grid, 256, 0, stream, a);
+      case 2: return launch_pdl(block_select_kernel<2, 256>, grid, 256, 0, stream, a);
+      case 4: return launch_pdl(block_select_kernel<4, 256>, grid, 256, 0, stream, a);
+      case 8: return launch_pdl(block_select_kernel<8, 256>, grid, 256, 0, stream, a);
+      case 16: return launch_pdl(block_select_kernel<16, 256>, grid, 256, 0, stream, a);
+      case 32: return launch_pdl(block_select_kernel<32, 256>, grid, 256, 0, stream, a);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (block_select_items(a.nblk_max)) {
-    case 1: return launch_pdl(block_select_kernel<1>, grid, kSelThreads, 0, stream, a);
-    case 2: return launch_pdl(block_select_kernel<2>, grid, kSelThreads, 0, stream, a);
-    case 4: return launch_pdl(block_select_kernel<4>, grid, kSelThreads, 0, stream, a);
-    case 8: return launch_pdl(block_select_kernel<8>, grid, kSelThreads, 0, stream, a);
-    case 16: return launch_pdl(block_select_kernel<16>, grid, kSelThreads, 0, stream, a);
-    case 32: return launch_pdl(block_select_kernel<32>, grid, kSelThreads, 0, stream, a);
+    case 1: return launch_pdl(block_select_kernel<1, kSelThreads>, grid, kSelThreads, 0, stream, a);
+    case 2: return launch_pdl(block_select_kernel<2, kSelThreads>, grid, kSelThreads, 0, stream, a);
+    case 4: return launch_pdl(block_select_kernel<4, kSelThreads>, grid, kSelThreads, 0, stream, a);
+    case 8: return launch_pdl(block_select_kernel<8, kSelThreads>, grid, kSelThreads, 0, stream, a);
+    case 16: return launch_pdl(block_select_kernel<16, kSelThreads>, grid, kSelThreads, 0, stream, a);
+    case 32: return launch_pdl(block_select_kernel<32, kSelThreads>, grid, kSelThreads, 0, stream, a);
   }
   return cudaErrorInvalidValue;
 }

@@ -149,9 +149,10 @@ def test_page_means_incremental_and_bad_block():
     assert torch.equal(bad[0], full[0]) and torch.equal(bad[1, :, 4:], full[1, :, 4:])
 
 
-@pytest.mark.parametrize("nblk_max", [4096, 2048])   # a CTA per row / a warp per row
+@pytest.mark.parametrize("B,Hq,Hkv", [(2, 4, 2), (3, 64, 2)])  # 16 rows / 384 rows
+@pytest.mark.parametrize("nblk_max", [4096, 2048])
 @pytest.mark.parametrize("kind", ["outlier", "duplicates", "spread", "two_values"])
-def test_block_topk_selection_paths(kind, nblk_max):
+def test_block_topk_selection_paths(kind, nblk_max, B, Hq, Hkv):
     """Page means written directly, to drive each path of the selection: an outlier page
     (every other page in one value bucket: the exact-key radix), integer duplicates
     (buckets of equal keys: ties to the lower page), a smooth spread (few candidates
@@ -159,8 +160,8 @@ def test_block_topk_selection_paths(kind, nblk_max):
     kernel's fp32 scores."""
     vsd = _vsd()
     rng = np.random.default_rng(["outlier", "duplicates", "spread", "two_values"].index(kind))
-    B, R, Hq, Hkv, d, kb = 2, 2, 4, 2, 64, 300
-    prefix = np.array([nblk_max * 16, (nblk_max * 3 // 4) * 16 - 5], np.int32)
+    R, d, kb = 2, 64, 300
+    prefix = np.array([nblk_max * 16, (nblk_max * 3 // 4) * 16 - 5, nblk_max * 8][:B], np.int32)
     means = np.zeros((B, Hkv, nblk_max, d), np.float32)
     if kind == "outlier":
         means[..., 0] = rng.normal(size=(B, Hkv, nblk_max)) * 1e-3
