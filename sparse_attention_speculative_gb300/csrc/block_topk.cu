@@ -16,9 +16,11 @@
 //    adds, then lanes holding the same columns combine with shuffles.  An optional
 //    per-sequence first page lets a decode loop refresh only the pages that changed:
 //    the means are a resident summary of the cache, like the cache itself.
-//  * block_score_tc_kernel: one CTA per (128 pages, KV group, sequence) on the tensor
-//    cores: TMA loads the fp32 means into swizzled tiles, tcgen05.mma kind::tf32 forms
-//    S^T = kbar Q^T in TMEM, and each thread writes one page's scores.
+//  * block_score_tc_kernel: persistent CTAs, each over a contiguous run of (sequence,
+//    KV group, 128 pages) tiles on the tensor cores: TMA loads the fp32 means into
+//    swizzled tiles (the next tile's copy under the current tile's epilogue),
+//    tcgen05.mma kind::tf32 forms S^T = kbar Q^T in TMEM, and each thread writes one
+//    page's scores.
 //  * block_select_kernel: one CTA per query row.  The row's scores become
 //    order-preserving 32-bit keys held in registers (each thread a contiguous run of
 //    pages).  A first histogram buckets the values linearly between the row's minimum
@@ -107,13 +109,17 @@ __global__ void __launch_bounds__(kMeanWarps * 32) page_mean_kernel(const BlockT
 }
 
 // ---------------------------------------------------------------- page scores
-// One CTA of four warps per (128 pages, KV group, sequence), on the tensor cores:
+// Persistent CTAs of four warps on the tensor cores.  The (sequence, KV group,
+// 128-page tile) triples are numbered in that order and each CTA takes a contiguous run
+// of them, so a group's query block is staged once per run rather than once per tile:
 // S^T[128 pages x NQ] = kbar[128 x d] . Q^T[d x NQ] (NQ = R * G rounded up to 16).
 // TMA brings the fp32 page means straight into 128-byte-swizzled K-major tiles (32 fp32
 // per row, d / 32 boxes); the group's bf16 query rows are staged as fp32 in the same
 // layout; tcgen05.mma kind::tf32 accumulates in TMEM (bf16 queries are exact in tf32,
-// the means lose their low 13 mantissa bits: ~1e-4 on a score); thread t reads page t's
-// NQ scores and writes them, each column a coalesced run of pages.
+// the means lose their low 13 mantissa bits: ~1e-4 on a score).  Once a tile's product
+// is complete its buffer takes the next tile's copy, which then runs under this tile's
+// epilogue: thread t reads page t's NQ scores and writes them, each column a coalesced
+// run of pages.
 constexpr int kTcPages = 128;
 constexpr int kTcScoreThreads = 128;
 
@@ -129,7 +135,7 @@ struct TcScoreSmem {
 
 template <int D, int NQ>
 __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
-    const __grid_constant__ CUtensorMap kbar_map, const BlockTopkArgs a) {
+    const __grid_constant__ CUtensorMap kbar_map, const BlockTopkArgs a, const int tiles_per_cta) {
   using Sm = TcScoreSmem<D, NQ>;
   extern __shared__ uint8_t sc_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -139,10 +145,11 @@ __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
   uint64_t* bar_a = reinterpret_cast<uint64_t*>(base + Sm::kOffBar);
   uint64_t* bar_s = bar_a + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_a + 2);
-  const int b = blockIdx.z, g = blockIdx.y;
-  const int beta0 = blockIdx.x * kTcPages;
   const int t = threadIdx.x, warp = t >> 5;
   const int G = a.G, RG = a.R * a.G;
+  const int ntile = (a.nblk_max + kTcPages - 1) / kTcPages;
+  const int first = blockIdx.x * tiles_per_cta;
+  const int last = min(a.B * a.Hkv * ntile, first + tiles_per_cta);
   if (t == 0) {
     ptx::mbar_init(bar_a, 1);
     ptx::mbar_init(bar_s, 1);
@@ -159,53 +166,77 @@ __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
   const uint32_t tmem = *tmem_slot;
   ptx::pdl_launch_dependents();
   ptx::pdl_wait_primary();  // the page means come from the preceding kernel
-  // the tile's means are fetched before the prefix length is known (rows past the
-  // buffer read as zeros; a tile past the sequence is never used); every CTA waits for
-  // its copy before it leaves
-  if (t == 0) {
+
+  // tile id -> its (sequence, KV group) pair bg = b * Hkv + g and first page; a tile has
+  // work when its sequence's length is valid and reaches the tile
+  const auto pages_of = [&](int P) { return (P + kPageB - 1) / kPageB; };
+  const auto has_work = [&](int id, int P) {
+    return P >= 0 && pages_of(P) <= a.nblk_max && (id % ntile) * kTcPages < pages_of(P);
+  };
+  const auto fetch = [&](int id) {  // thread 0: the tile's means into the buffer
     ptx::mbar_arrive_expect_tx(bar_a, (D / 32) * Sm::kBox);
-    const int row0 = (b * a.Hkv + g) * a.nblk_max + beta0;
+    const int row0 = (id / ntile) * a.nblk_max + (id % ntile) * kTcPages;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c)
       ptx::tma_load_2d(a_s + c * Sm::kBox, &kbar_map, bar_a, c * 32, row0);
-  }
-  // the group's query rows r = t * G + hl as fp32, zero past R * G: every load in
-  // flight before the first store
+  };
+
   constexpr int QL = NQ * (D / 8) / kTcScoreThreads;
   static_assert(NQ * (D / 8) % kTcScoreThreads == 0, "query staging");
   const uint16_t* qb = static_cast<const uint16_t*>(a.q);
-  uint4 qv[QL];
-#pragma unroll
-  for (int u = 0; u < QL; ++u) {
-    const int i = t + u * kTcScoreThreads, r = i / (D / 8), c8 = i % (D / 8);
-    qv[u] = make_uint4(0, 0, 0, 0);
-    if (r < RG)
-      qv[u] = __ldg(reinterpret_cast<const uint4*>(
-          qb + ((static_cast<size_t>(b) * a.R + r / G) * a.Hq + g * G + r % G) * D + c8 * 8));
-  }
-  const int P = __ldg(a.prefix_len + b);
-  const int nblk = (P + kPageB - 1) / kPageB;
-  const bool ok = P >= 0 && nblk <= a.nblk_max;
-  if (!ok && t == 0 && g == 0 && blockIdx.x == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
-  const bool work = ok && beta0 < nblk;  // CTA-uniform
+  uint32_t a_phase = 0, s_phase = 0;
+  bool in_flight = false;  // thread 0: a copy into the buffer has not been waited for
   bool timed_out = false;
-  if (work) {
-#pragma unroll
-    for (int u = 0; u < QL; ++u) {
-      const int i = t + u * kTcScoreThreads, r = i / (D / 8), c8 = i % (D / 8);
-      const int c = c8 >> 2;            // 32-dim box
-      const int u0 = (c8 & 3) * 2;      // first 16-byte unit of the 128-byte row
-      uint8_t* row = q_s + c * NQ * 128 + r * 128;
-      const uint4 v = qv[u];
-      *reinterpret_cast<float4*>(row + ((u0 ^ (r & 7)) << 4)) =
-          make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
-      *reinterpret_cast<float4*>(row + (((u0 + 1) ^ (r & 7)) << 4)) =
-          make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+  int staged_bg = -1;
+  int P_next = first < last ? __ldg(a.prefix_len + first / ntile / a.Hkv) : 0;
+  for (int id = first; id < last; ++id) {
+    const int x = id % ntile, bg = id / ntile, g = bg % a.Hkv, b = bg / a.Hkv;
+    const int P = P_next;
+    if (id + 1 < last) P_next = __ldg(a.prefix_len + (id + 1) / ntile / a.Hkv);
+    if ((P < 0 || pages_of(P) > a.nblk_max) && t == 0 && g == 0 && x == 0)
+      flag_status(a.status, VSD_DEV_BAD_LENGTH);
+    if (!has_work(id, P)) continue;  // CTA-uniform; nothing was fetched for it
+    if (t == 0 && !in_flight) {
+      fetch(id);
+      in_flight = true;
     }
-    ptx::fence_proxy_async_smem();
-    __syncthreads();
+    if (bg != staged_bg) {
+      // the group's query rows r = tr * G + hl as fp32, zero past R * G (the previous
+      // tile's product, the last reader of this block, is complete)
+      uint4 qv[QL];
+#pragma unroll
+      for (int u = 0; u < QL; ++u) {
+        const int i = t + u * kTcScoreThreads, r = i / (D / 8), c8 = i % (D / 8);
+        qv[u] = make_uint4(0, 0, 0, 0);
+        if (r < RG)
+          qv[u] = __ldg(reinterpret_cast<const uint4*>(
+              qb + ((static_cast<size_t>(b) * a.R + r / G) * a.Hq + g * G + r % G) * D + c8 * 8));
+      }
+#pragma unroll
+      for (int u = 0; u < QL; ++u) {
+        const int i = t + u * kTcScoreThreads, r = i / (D / 8), c8 = i % (D / 8);
+        const int c = c8 >> 2;            // 32-dim box
+        const int u0 = (c8 & 3) * 2;      // first 16-byte unit of the 128-byte row
+        uint8_t* row = q_s + c * NQ * 128 + r * 128;
+        const uint4 v = qv[u];
+        *reinterpret_cast<float4*>(row + ((u0 ^ (r & 7)) << 4)) =
+            make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+        *reinterpret_cast<float4*>(row + (((u0 + 1) ^ (r & 7)) << 4)) =
+            make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+      }
+      ptx::fence_proxy_async_smem();
+      staged_bg = bg;
+    }
+    ptx::tc_fence_before();
+    // the query block is staged and the previous tile's TMEM reads are done
+    if (__syncthreads_or(timed_out)) break;
     if (t == 0) {
-      if (!ptx::mbar_wait(bar_a, 0)) timed_out = true;
+      if (ptx::mbar_wait(bar_a, a_phase)) {
+        a_phase ^= 1;
+        in_flight = false;
+      } else {
+        timed_out = true;
+      }
       ptx::tc_fence_after();
       constexpr uint32_t idesc = ptx::idesc_tf32_f32(128, NQ, 0, 0);
       const uint32_t aa = ptx::smem_u32(a_s), qa = ptx::smem_u32(q_s);
@@ -218,27 +249,42 @@ __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
       }
       ptx::umma_commit(bar_s);
     }
-    if (!ptx::mbar_wait(bar_s, 0)) timed_out = true;
+    if (!ptx::mbar_wait(bar_s, s_phase)) timed_out = true;
+    s_phase ^= 1;
     ptx::tc_fence_after();
+    // the product has read the buffer: it takes the next tile's copy now
+    if (t == 0 && !timed_out && id + 1 < last && has_work(id + 1, P_next)) {
+      fetch(id + 1);
+      in_flight = true;
+    }
     float sv[NQ];
     ptx::tmem_ld_cols<NQ>(tmem + (static_cast<uint32_t>(warp * 32) << 16),
                           reinterpret_cast<uint32_t*>(sv));
     ptx::tmem_wait_ld();
-    const int beta = beta0 + t;  // TMEM lane t = page beta0 + t
-    if (beta < nblk) {
+    const int beta = x * kTcPages + t;  // TMEM lane t = page beta
+    if (beta < pages_of(P)) {
+      // column c = tr * G + hl is query row (b, tr, g * G + hl): consecutive columns step
+      // one head, and past the group's last head to the next draft position's first
+      const size_t step_h = static_cast<size_t>(a.nblk_max);
+      const size_t step_r = static_cast<size_t>(a.Hq - G + 1) * a.nblk_max;
+      float* dst = a.scores + (static_cast<size_t>(b) * a.R * a.Hq + g * G) * a.nblk_max + beta;
+      int hl = 0;
 #pragma unroll
       for (int c = 0; c < NQ; ++c) {
         if (c < RG) {
-          const int tr = c / G, h = g * G + c % G;
-          a.scores[((static_cast<size_t>(b) * a.R + tr) * a.Hq + h) * a.nblk_max + beta] =
-              sv[c] * a.scale + 0.f;  // + 0 turns -0 into +0: equal scores compare equal as keys
+          *dst = sv[c] * a.scale + 0.f;  // + 0 turns -0 into +0: equal scores compare equal as keys
+          if (++hl == G) {
+            hl = 0;
+            dst += step_r;
+          } else {
+            dst += step_h;
+          }
         }
       }
     }
-  } else if (t == 0) {
-    // no MMA reads this tile, but its copy must land before the CTA leaves
-    if (!ptx::mbar_wait(bar_a, 0)) timed_out = true;
   }
+  // a copy still in flight lands before the CTA leaves
+  if (t == 0 && in_flight && !ptx::mbar_wait(bar_a, a_phase)) timed_out = true;
   if (timed_out) flag_status(a.status, VSD_DEV_TIMEOUT);
   ptx::tc_fence_before();
   __syncthreads();
@@ -537,14 +583,29 @@ cudaError_t launch_scores_dn(const CUtensorMap& map, const BlockTopkArgs& a, cud
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // persistent CTAs: as many as fit at once, each with a contiguous run of tiles
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTcScoreThreads, smem);
+    if (e != cudaSuccess) return e;
+    per_sm = per_sm > 0 ? per_sm : 1;
+  }
+  int dev = 0, sm_count = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long tiles =
+      static_cast<long long>(a.B) * a.Hkv * ((a.nblk_max + kTcPages - 1) / kTcPages);
+  const long long slots = static_cast<long long>(per_sm) * sm_count;
+  const int per_cta = static_cast<int>((tiles + slots - 1) / slots);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.nblk_max + kTcPages - 1) / kTcPages, a.Hkv, a.B);
+  cfg.gridDim = dim3(static_cast<unsigned>((tiles + per_cta - 1) / per_cta), 1, 1);
   cfg.blockDim = dim3(kTcScoreThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, map, a);
+  return cudaLaunchKernelEx(&cfg, kern, map, a, per_cta);
 }
 
 template <int D>
