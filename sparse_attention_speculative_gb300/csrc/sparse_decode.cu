@@ -528,6 +528,8 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
   using Sm = TcSmem<D>;
   constexpr int LPR = D / 8;        // 16-byte chunks per row
   constexpr int RPI = 32 / LPR;     // rows per warp instruction
+  constexpr int QPT = kTcNQ * LPR / kTcThreads;  // query chunks per thread
+  static_assert(kTcNQ * LPR % kTcThreads == 0, "query staging");
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -569,6 +571,15 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
   const int ns_raw = a.n_sel != nullptr ? __ldg(a.n_sel + b) : 0;
   const int t0_raw = __ldg(a.tail_start + b);
   const int t1 = __ldg(a.seq_len + b);
+  uint4 qv[QPT];
+#pragma unroll
+  for (int u = 0; u < QPT; ++u) {
+    const int i = t + u * kTcThreads, r = i / LPR, c = i % LPR;
+    qv[u] = make_uint4(0, 0, 0, 0);
+    if (r < G)
+      qv[u] = *reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + g * G + r) * D +
+                                              c * 8);
+  }
   const SList L = attended_list(ns_raw, t0_raw, t1, a, split == 0 && g == 0 && t == 0);
   const bool work = lo < L.total || (split == 0 && L.total == 0);
   const int n_splits = (L.total + a.split_len - 1) / a.split_len;
@@ -605,12 +616,12 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
       ptx::cp_async16(v_s + off, a.v_cache + src, cr >= 0 ? 16u : 0u);
     }
     ptx::cp_async_commit();
-    // ---- the group's query rows, padded with zeros to 16
-    for (int i = t; i < kTcNQ * LPR; i += kTcThreads) {
-      const int r = i / LPR, c = i % LPR;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < G) v = *reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + g * G + r) * D + c * 8);
-      *reinterpret_cast<uint4*>(q_s + (c >> 3) * (kTcNQ * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+    // ---- the group's query rows (loaded with the indices), padded with zeros to 16
+#pragma unroll
+    for (int u = 0; u < QPT; ++u) {
+      const int i = t + u * kTcThreads, r = i / LPR, c = i % LPR;
+      *reinterpret_cast<uint4*>(q_s + (c >> 3) * (kTcNQ * 128) + r * 128 +
+                                (((c & 7) ^ (r & 7)) << 4)) = qv[u];
     }
     ptx::cp_async_wait_all();
     ptx::fence_proxy_async_smem();  // make the copies and stores visible to the tensor cores
@@ -756,9 +767,20 @@ cudaError_t launch_tc(const SParams& p, int B, int Hkv, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  constexpr int smem = TcSmem<D>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(sparse_tc_kernel<D, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // When the splits fit one wave at one CTA per SM, each CTA reserves more than half of
+  // an SM's shared memory, so that no two share an SM (its load/store pipe and issue
+  // slots); beyond that, as many CTAs per SM as fit (three), in waves.
+  int dev = 0, sm_count = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long ctas = static_cast<long long>(p.max_splits) * Hkv * B;
+  constexpr int kSpreadSmem = 120 * 1024;
+  static_assert(TcSmem<D>::kBytes <= kSpreadSmem && 2 * kSpreadSmem > 228 * 1024,
+                "one CTA per SM at the spread reservation");
+  const int smem = ctas <= sm_count ? kSpreadSmem : TcSmem<D>::kBytes;
+  e = cudaFuncSetAttribute(sparse_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.max_splits, Hkv, B);
