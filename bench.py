@@ -613,6 +613,273 @@ def run_e2e(args, w, batch, vsd, dev, stream, workspace, prefix, total_bytes):
                     "-> pinned host results, one CUDA-graph replay per step" % gamma}
 
 
+# ------------------------------------------------------------------ multi-layer loop
+
+def run_gpu_loop(args, world, rank, local):
+    """One decode iteration of a multi-layer model's attention: every layer's
+    verification + Collect-2-Query with the fused aggregation, one selection launch for
+    all layers x sequences, then gamma draft steps, each over every layer.  Each layer
+    has its own seeded cache; the step's queries sit in one device arena (filled from
+    pinned host memory in the end-to-end variant)."""
+    import sparse_attention_speculative_gb300 as vsd
+    from sparse_attention_speculative_gb300 import build as pkg_build
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import ALL
+
+    if rank == 0 or not pkg_build.up_to_date():
+        pkg_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    vsd.load()
+    w = ALL[args.workload]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    NL = w.layers
+    B, R, Hq, d, gamma = w.B, w.R, w.Hq, w.d, w.gamma
+    batches = [make_batch(w, dev, layer=l) for l in range(NL)]
+    prefix = list(w.prefix())
+    P_max = w.P_max
+    pl = batches[0].prefix_len
+    rows_pl = pl.repeat(NL)
+    geom = vsd.geom_for(B, Hq, batches[0].k_cache, batches[0].block_table)
+    ws_bytes = vsd.vsd_verify_workspace_size(geom, R, P_max)
+    workspace = torch.zeros(max(ws_bytes, 1) + 256, dtype=torch.uint8, device=dev)
+    workspace = workspace[(-workspace.data_ptr()) % 256:][:ws_bytes] if ws_bytes else None
+    max_tail = 2 * gamma + 1
+    sws_bytes = vsd.vsd_sparse_workspace_size(geom, w.k, max_tail)
+    sws = torch.zeros(max(sws_bytes, 1) + 256, dtype=torch.uint8, device=dev)
+    sws = sws[(-sws.data_ptr()) % 256:][:sws_bytes] if sws_bytes else None
+    # the step's inputs (queries of every layer, draft lengths) and results (draft outputs)
+    q_all = torch.stack([bt.q for bt in batches])              # [NL, B, R, Hq, d]
+    qd_all = torch.stack([bt.q_draft for bt in batches])       # [NL, gamma, B, Hq, d]
+    seq_len = torch.empty((gamma, B), dtype=torch.int32, device=dev)
+    d_out = torch.empty((gamma, NL, B, Hq, d), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((B, R, Hq, d), dtype=torch.bfloat16, device=dev)
+    logits = torch.empty((B, 2, Hq, P_max), dtype=torch.float32, device=dev)
+    partial = torch.empty((B, w.Hkv, P_max), dtype=torch.float32, device=dev)
+    score = torch.empty((NL * B, P_max), dtype=torch.float32, device=dev)
+    hist = torch.empty((NL * B, vsd.HIST_BINS), dtype=torch.int32, device=dev)
+    idx = torch.empty((NL * B, w.k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty((NL * B,), dtype=torch.int32, device=dev)
+    tail_start = pl.clone()
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    rng = np.random.default_rng(w.seed + 77)
+
+    def draw_seq_len():
+        a = rng.integers(0, gamma + 1, size=B)
+        return np.array([[prefix[b] + a[b] + 2 + i for b in range(B)] for i in range(gamma)],
+                        dtype=np.int32)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def step(events=False):
+        for l, bt in enumerate(batches):
+            rows = slice(l * B, (l + 1) * B)
+            vsd.vsd_verify_attn_collect_scored(q_all[l], bt.k_cache, bt.v_cache, bt.block_table,
+                                               pl, P_max=P_max, scale=w.scale, row0=0,
+                                               row1=R - 1, logits=logits, partial=partial,
+                                               score=score[rows], score_hist=hist[rows],
+                                               out=out, workspace=workspace)
+        if events:
+            ev[1].record(stream)
+        vsd.vsd_select_topk_scored(score, hist, rows_pl, k=w.k, n_sink=w.n_sink,
+                                   n_recent=w.n_recent, idx=idx, n_sel=n_sel)
+        if events:
+            ev[2].record(stream)
+        for i in range(gamma):
+            for l, bt in enumerate(batches):
+                rows = slice(l * B, (l + 1) * B)
+                vsd.vsd_sparse_decode_attn(qd_all[l, i], bt.k_cache, bt.v_cache, bt.block_table,
+                                           idx[rows], n_sel[rows], tail_start, seq_len[i],
+                                           scale=w.scale, max_tail=max_tail, out=d_out[i, l],
+                                           workspace=sws)
+        if events:
+            ev[3].record(stream)
+
+    launches_per_step = 2 * NL + 1 + gamma * NL
+    sleep_cycles = 8_000_000
+    for _ in range(max(args.warmup, 1)):
+        seq_len.copy_(torch.from_numpy(draw_seq_len()))
+        step()
+    torch.cuda.synchronize()
+    status = vsd.vsd_read_device_status()
+    if status:
+        raise RuntimeError("device status 0x%x during warm-up" % status)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def graph_step(sl):
+        seq_len.copy_(torch.from_numpy(sl))
+        flush_l2(flush_w, flush_r)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(sleep_cycles)
+        g0.record(stream)
+        graph.replay()
+        g1.record(stream)
+
+    for _ in range(args.warmup):
+        graph_step(draw_seq_len())
+    torch.cuda.synchronize()
+    per = {"graph": [], "verify": [], "select": [], "sparse": []}
+    tails_seen = []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for _ in range(args.steps):
+            sl = draw_seq_len()
+            tails_seen.append([[int(sl[i, b] - prefix[b]) for b in range(B)]
+                               for i in range(gamma)])
+            graph_step(sl)
+            torch.cuda.synchronize()
+            per["graph"].append(g0.elapsed_time(g1) * 1e-3)
+        # per-phase breakdown: the same iteration launched eagerly, events between phases
+        for _ in range(args.steps):
+            seq_len.copy_(torch.from_numpy(draw_seq_len()))
+            flush_l2(flush_w, flush_r)
+            torch.cuda.synchronize()
+            torch.cuda._sleep(sleep_cycles)
+            ev[0].record(stream)
+            step(events=True)
+            torch.cuda.synchronize()
+            per["verify"].append(ev[0].elapsed_time(ev[1]) * 1e-3)
+            per["select"].append(ev[1].elapsed_time(ev[2]) * 1e-3)
+            per["sparse"].append(ev[2].elapsed_time(ev[3]) * 1e-3)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    status = vsd.vsd_read_device_status()
+    if status:
+        raise RuntimeError("device status 0x%x in the timed region" % status)
+    n_sel_host = n_sel.cpu().tolist()
+    mean_tails = [[statistics.mean(t[i][b] for t in tails_seen) for b in range(B)]
+                  for i in range(gamma)]
+    vb = sb = 0
+    spb = [0] * gamma
+    for l in range(NL):
+        v_l, s_l, sp_l = iteration_bytes(w, prefix, n_sel_host[l * B:(l + 1) * B], mean_tails)
+        vb, sb = vb + v_l, sb + s_l
+        spb = [x + y for x, y in zip(spb, sp_l)]
+    total_bytes = vb + sb + sum(spb)
+    t_step = sum(per["graph"])
+    t_tensor = torch.tensor([t_step], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_tensor, op=torch.distributed.ReduceOp.MAX)
+    t_max = float(t_tensor.item())
+    value = world * total_bytes * args.steps / t_max / 1e9
+    peak, peak_kind = measured_peaks()
+    t_v = statistics.median(per["verify"])
+    t_s = statistics.median(per["select"])
+    t_sp = statistics.median(per["sparse"])
+    nominal = NOMINAL_HBM_GBS
+
+    def entry(t, nbytes, calls):
+        return {"us": t * 1e6, "calls": calls, "us_per_call": t * 1e6 / calls, "bytes": nbytes,
+                "GB_s": nbytes / t / 1e9, "frac_of_%s_hbm" % peak_kind: nbytes / t / 1e9 / peak,
+                "frac_of_nominal_8tbs": nbytes / t / 1e9 / nominal}
+
+    # the verification calls of the layers run back to back (K/V of each layer larger
+    # than L2): the roofline of the dominant kernel from their phase, per call
+    achieved = vb / t_v / 1e9
+    clk = clocks.summary()
+    result = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
+        "us_per_iter": t_max / args.steps * 1e6, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "layers": NL, "B": B, "P": w.P, "Hq": Hq, "Hkv": w.Hkv,
+                   "d": d, "gamma": gamma, "k": w.k, "n_sink": w.n_sink,
+                   "n_recent": w.n_recent, "page": w.page,
+                   "prefix": "fixed at P (the accept draws vary the draft tails only)",
+                   "l2": "flushed before every timed iteration (512 MB write, then 512 MB "
+                         "read so no dirty lines remain)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "timing": "value: one CUDA-graph replay of the whole iteration (%d kernels) per step; "
+                  "phases: medians of the same iteration launched eagerly with events "
+                  "between the phases" % launches_per_step,
+        "phases": {"verify_collect": entry(t_v, vb, NL), "select_topk": entry(t_s, sb, 1),
+                   "sparse_draft_steps": entry(t_sp, sum(spb), gamma * NL)},
+        "select_over_verify_call": t_s / (t_v / NL),
+        "roofline": {"bound": "hbm", "kernel": "vsd_verify_attn_collect_scored",
+                     "timing": "the %d layers' verification calls back to back (eager phase "
+                               "between two events), per-call mean; bytes = algorithmic bytes "
+                               "of one call" % NL,
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": None},
+        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches_per_step": launches_per_step,
+        "clocks": clk,
+    }
+    if args.e2e:
+        # the same iteration with the step's inputs copied in from pinned host memory and
+        # the draft outputs copied back, all in one graph
+        h_q = q_all.cpu().pin_memory()
+        h_qd = qd_all.cpu().pin_memory()
+        h_sl = torch.empty((gamma, B), dtype=torch.int32).pin_memory()
+        h_out = torch.empty(d_out.shape, dtype=d_out.dtype).pin_memory()
+        h_nsel = torch.empty(n_sel.shape, dtype=n_sel.dtype).pin_memory()
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2):
+            q_all.copy_(h_q, non_blocking=True)
+            qd_all.copy_(h_qd, non_blocking=True)
+            seq_len.copy_(h_sl, non_blocking=True)
+            step()
+            h_out.copy_(d_out, non_blocking=True)
+            h_nsel.copy_(n_sel, non_blocking=True)
+        torch.cuda.synchronize()
+        times = []
+        for s in range(args.warmup + args.steps):
+            h_sl.copy_(torch.from_numpy(draw_seq_len()))
+            flush_l2(flush_w, flush_r)
+            torch.cuda.synchronize()
+            torch.cuda._sleep(2_000_000)
+            g0.record(stream)
+            g2.replay()
+            g1.record(stream)
+            torch.cuda.synchronize()
+            if s >= args.warmup:
+                times.append(g0.elapsed_time(g1) * 1e-3)
+        t = statistics.mean(times)
+        h2d = h_q.numel() * 2 + h_qd.numel() * 2 + h_sl.numel() * 4
+        d2h = h_out.numel() * 2 + h_nsel.numel() * 4
+        result["e2e"] = {"value": total_bytes / t / 1e9, "unit": "GB/s", "us_per_iter": t * 1e6,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "path": "one CUDA graph per step: every layer's queries and the draft "
+                                 "lengths copied in from pinned host memory, the iteration, "
+                                 "every draft output and the selection counts copied back"}
+    return result, batches
+
+
+def run_cpu_baseline_loop(w, batches, layers_sample=4):
+    """The fp64 oracle on a sample of the loop's layers (one iteration each), the time
+    scaled to all layers."""
+    import oracle
+    from sparse_attention_speculative_gb300.synth import host_arrays
+    oracle.build()
+    prefix = list(w.prefix())
+    n = min(layers_sample, w.layers)
+    hs = [host_arrays(batches[l]) for l in range(n)]
+    t0 = time.perf_counter()
+    vb = sb = 0
+    spb_total = 0
+    for l in range(n):
+        n_sel, tails = cpu_oracle_iteration(w, hs[l], prefix, 1234 + l)
+        v_l, s_l, sp_l = iteration_bytes(w, prefix, n_sel, tails)
+        vb, sb, spb_total = vb + v_l, sb + s_l, spb_total + sum(sp_l)
+    dt = time.perf_counter() - t0
+    return {"value": (vb + sb + spb_total) / dt / 1e9, "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "seconds_per_iter": dt * w.layers / n,
+            "sample": "%d of the %d layers of one iteration of %s (each: verify+collect2, "
+                      "select, %d draft steps), fp64 C oracle; seconds_per_iter scales the "
+                      "sample to all layers" % (n, w.layers, w.name, w.gamma)}
+
+
 # ------------------------------------------------------------------ oracle (CPU) arm
 
 def cpu_oracle_iteration(w, h, prefix, steps_seed):
@@ -685,7 +952,11 @@ def run_reference(args, world, rank):
                    "gamma": w.gamma, "k": w.k, "n_sink": w.n_sink, "n_recent": w.n_recent},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
-                         "sample": "each step one full iteration of %s on the host" % w.name},
+                         "sample": ("each step one full iteration of %s on the host" % w.name
+                                    if w.layers == 1 else
+                                    "each step one layer (of %d, the rate is the same for "
+                                    "every layer) of one iteration of %s on the host"
+                                    % (w.layers, w.name))},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -710,11 +981,16 @@ def main():
     if world > 1:
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    res, batch = run_gpu(args, world, rank, local)
+    from sparse_attention_speculative_gb300.workloads import ALL
+    w = ALL[args.workload]
+    if w.layers > 1:
+        res, batches = run_gpu_loop(args, world, rank, local)
+    else:
+        res, batch = run_gpu(args, world, rank, local)
     if rank == 0:
         if args.cpu_baseline:
-            from sparse_attention_speculative_gb300.workloads import ALL
-            res["cpu_baseline"] = run_cpu_baseline(ALL[args.workload], batch)
+            res["cpu_baseline"] = (run_cpu_baseline_loop(w, batches) if w.layers > 1
+                                   else run_cpu_baseline(w, batch))
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.barrier()
