@@ -114,22 +114,32 @@ __device__ __forceinline__ SList attended_list(int ns, int t0, int t1, const SPa
   return L;
 }
 
+// One split's partial (m, l, o) in the workspace: the G heads' running max and sum,
+// padded so that the G output rows (read as float4 by the merge) start on a 16-byte
+// boundary, then the rows.
+template <int D, int G>
+struct SSlot {
+  static constexpr int kO = (2 * G + 3) / 4 * 4;  // floats before the output rows
+  static constexpr int kFloats = kO + G * D;
+  static_assert(kFloats % 4 == 0 && D % 4 == 0, "16-byte slots");
+};
+
 // Combine the n partial (m, l, o) of one pair's splits and write its G output rows.
-// Thread = (float4 group of (head, dims), part); part p takes splits p, p + kParts,
-// ... with all loads of a round in flight; the parts then combine in shared memory.
+// Thread t of the kSThreads that run it (`sync` is their barrier) = (float4 group of
+// (head, dims), part); part p takes splits p, p + kParts, ... with all loads of a round
+// in flight; the parts then combine in shared memory.
 // kRound: splits per load round when a thread holds one output group.
-template <int D, int G, int kSThreads, int kRound = 16>
-__device__ __forceinline__ void merge_splits(const SParams& a, float* scratch, int pair, int b,
-                                             int g, int n) {
+template <int D, int G, int kSThreads, int kRound, typename Sync>
+__device__ __forceinline__ void merge_splits_by(const SParams& a, float* scratch, int pair, int b,
+                                                int g, int n, const int t, Sync sync) {
   constexpr int kQ = D / 4;
   constexpr int NG = G * kQ;                              // float4 groups of the output
   constexpr int kGPT = NG > kSThreads ? NG / kSThreads : 1;  // groups per thread
   constexpr int kParts = NG >= kSThreads ? 1 : kSThreads / NG;
   constexpr int kU = kGPT == 1 ? kRound : (16 / kGPT > 1 ? 16 / kGPT : 1);  // per load round
   static_assert(NG * kParts / kGPT == kSThreads || NG >= kSThreads, "merge layout");
-  const int t = threadIdx.x;
   const int part = kParts > 1 ? t / NG : 0;
-  const size_t stride = static_cast<size_t>(G) * (D + 2);
+  const size_t stride = SSlot<D, G>::kFloats;
   const float* base = a.ws + static_cast<size_t>(pair) * a.max_splits * stride;
   float M[kGPT], L[kGPT];
   float4 O[kGPT];
@@ -153,7 +163,7 @@ __device__ __forceinline__ void merge_splits(const SParams& a, float* scratch, i
           const float* sl = base + k * stride;
           mk[i][u] = __ldcg(sl + hh);
           lk[i][u] = __ldcg(sl + G + hh);
-          ok[i][u] = __ldcg(reinterpret_cast<const float4*>(sl + 2 * G + hh * D) + q4);
+          ok[i][u] = __ldcg(reinterpret_cast<const float4*>(sl + SSlot<D, G>::kO + hh * D) + q4);
         } else {
           mk[i][u] = -INFINITY;
           lk[i][u] = 0.f;
@@ -193,7 +203,7 @@ __device__ __forceinline__ void merge_splits(const SParams& a, float* scratch, i
     pm[part * NG + gi] = M[0];
     pl[part * NG + gi] = L[0];
     po[part * NG + gi] = O[0];
-    __syncthreads();
+    sync();
     if (part == 0) {
       float mn = -INFINITY;
 #pragma unroll
@@ -227,6 +237,14 @@ __device__ __forceinline__ void merge_splits(const SParams& a, float* scratch, i
     *reinterpret_cast<uint2*>(a.out + (static_cast<size_t>(b) * a.Hq + g * G + hh) * D +
                               q4 * 4) = pk;
   }
+}
+
+template <int D, int G, int kSThreads, int kRound = 16>
+__device__ __forceinline__ void merge_splits(const SParams& a, float* scratch, int pair, int b,
+                                             int g, int n) {
+  merge_splits_by<D, G, kSThreads, kRound>(a, scratch, pair, b, g, n,
+                                           static_cast<int>(threadIdx.x),
+                                           [] { __syncthreads(); });
 }
 
 template <int D, int G>
@@ -439,7 +457,7 @@ __global__ void __launch_bounds__(SCfg<G>::kThreads, 1) sparse_decode_kernel(con
   const bool direct = n_splits <= 1;
   const int pair = b * a.Hkv + g;
   const size_t slot = static_cast<size_t>(pair) * a.max_splits + split;
-  float* wsl = direct ? nullptr : a.ws + slot * G * (D + 2);
+  float* wsl = direct ? nullptr : a.ws + slot * SSlot<D, G>::kFloats;
   for (int i = threadIdx.x; i < G * D; i += kSThreads) {
     const int hh = i / D, dim = i % D;
     float M = -INFINITY;
@@ -459,7 +477,7 @@ __global__ void __launch_bounds__(SCfg<G>::kThreads, 1) sparse_decode_kernel(con
       a.out[(static_cast<size_t>(b) * a.Hq + g * G + hh) * D + dim] =
           *reinterpret_cast<const uint16_t*>(&bv);
     } else {
-      wsl[2 * G + hh * D + dim] = o;
+      wsl[SSlot<D, G>::kO + hh * D + dim] = o;
       if (dim == 0) {
         wsl[hh] = M;
         wsl[G + hh] = Lh;
@@ -722,9 +740,9 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
               *reinterpret_cast<const uint16_t*>(&bv);
         }
       } else {
-        float* wsl = a.ws + (static_cast<size_t>(pair) * a.max_splits + split) * G * (D + 2);
+        float* wsl = a.ws + (static_cast<size_t>(pair) * a.max_splits + split) * SSlot<D, G>::kFloats;
 #pragma unroll
-        for (int h = 0; h < G; ++h) wsl[2 * G + h * D + dim] = o[h];
+        for (int h = 0; h < G; ++h) wsl[SSlot<D, G>::kO + h * D + dim] = o[h];
         if (dim < G) {
           // m and l of head `dim` (every thread holds all heads' values)
 #pragma unroll
@@ -762,6 +780,394 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
   merge_splits<D, G, kTcThreads, 24>(a, scratch, pair, b, g, n_splits);
 }
 
+// ---------------------------------------------------------------- warp-specialised step
+// An item's position in the launch and its pair's attended list (CTA-uniform).
+struct TcItem {
+  int pair, b, g, split, lo;
+  SList L;
+};
+
+// For launches with more splits than one wave of the one-split kernel holds: persistent
+// CTAs (one per SM) over contiguous runs of the (pair, split) items, numbered pair-major
+// as that kernel's grid.  A producer warpgroup resolves each item's positions (one item
+// ahead) and gathers its K / V rows into a ring of three stages; its copies and the
+// item's metadata (which rows are present, the list length) complete the stage's `full`
+// barrier.  Two consumer warpgroups take alternate items through the one-split kernel's
+// tensor-core steps, each with its own TMEM columns, barriers, query block and merge
+// scratch, and hand the stage back through its `empty` barrier when the PV product has
+// read it.  One item's gather and two items' products are in flight per SM.  A
+// consumer counts its run of splits of one pair in one arrival; the pair's last arrival
+// merges.
+constexpr int kWsStages = 3;
+constexpr int kWsThreads = 3 * kTcThreads;
+
+template <int D>
+struct WsSmem {
+  static constexpr int kHalf = kBatch * 128;
+  static constexpr int kTile = kBatch * D * 2;  // one K or V tile; stage s: K at 2 s kTile
+  static constexpr int kQBytes = kTcNQ * D * 2 < 2048 ? 2048 : kTcNQ * D * 2;
+  static constexpr int kOffQ = 2 * kWsStages * kTile;              // [2] query blocks
+  static constexpr int kOffRed = kOffQ + 2 * kQBytes;              // [2][2][4][16] floats
+  static constexpr int kOffScratch = kOffRed + 2 * 2 * 4 * kTcNQ * 4;  // [2][128 * 6] floats
+  static constexpr int kOffMeta = kOffScratch + 2 * kTcThreads * 6 * 4;  // [S][8] words
+  static constexpr int kOffBar = kOffMeta + kWsStages * 8 * 4;
+  static constexpr int kBarBytes = (2 * kWsStages + 4) * 8 + 16;  // full, empty, s[2], o[2], slot
+  // with D = 64 the PV MMA reads 16 KB past a V tile (rows never read back)
+  static constexpr int kUsedA = kOffBar + kBarBytes;
+  static constexpr int kUsedB = (2 * kWsStages - 1) * kTile + 2 * kHalf;
+  static constexpr int kBytes = (kUsedA > kUsedB ? kUsedA : kUsedB) + 1024;
+  static_assert(kTile % 1024 == 0 && kOffQ % 1024 == 0 && kQBytes % 1024 == 0,
+                "swizzle atoms need 1 KB alignment");
+  static_assert(kBatch * 128 <= kTile, "P^T fits in the K tile");
+  static_assert(kOffScratch % 16 == 0 && kOffBar % 8 == 0, "layout");
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kWsThreads, 1)
+    sparse_ws_kernel(const SParams a, const int items_per_cta, const int n_items) {
+  using Sm = WsSmem<D>;
+  constexpr int LPR = D / 8;        // 16-byte chunks per row
+  constexpr int RPI = 32 / LPR;     // rows per warp instruction
+  constexpr int QPT = kTcNQ * LPR / kTcThreads;  // query chunks per consumer thread
+  static_assert(kTcNQ * LPR % kTcThreads == 0, "query staging");
+  extern __shared__ uint8_t ws_smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(ws_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint32_t* meta = reinterpret_cast<uint32_t*>(base + Sm::kOffMeta);  // [s][0..3] rows, [s][4] length
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + Sm::kOffBar);
+  uint64_t* empty = full + kWsStages;
+  uint64_t* bar_s = empty + kWsStages;  // [2]
+  uint64_t* bar_o = bar_s + 2;          // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o + 2);
+  __shared__ int s_last[2];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wg = warp >> 2;  // 0: producer; 1, 2: consumers
+  const int first = blockIdx.x * items_per_cta;
+  const int n = min(n_items, first + items_per_cta) - first;
+  if (tid == 0) {
+    for (int s = 0; s < kWsStages; ++s) {
+      ptx::mbar_init(&full[s], kTcThreads + 1);  // every producer's copies + the metadata
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int c = 0; c < 2; ++c) {
+      ptx::mbar_init(&bar_s[c], 1);
+      ptx::mbar_init(&bar_o[c], 1);
+    }
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 4) {
+    ptx::tmem_alloc(tmem_slot, 64);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait_primary();  // idx / n_sel come from the preceding kernel
+
+  const auto item_of = [&](int it) {
+    TcItem w;
+    w.pair = it / a.max_splits;
+    w.split = it - w.pair * a.max_splits;
+    w.b = w.pair / a.Hkv;
+    w.g = w.pair - w.b * a.Hkv;
+    w.lo = w.split * a.split_len;
+    w.L = SList{0, 0, 0};
+    return w;
+  };
+  const auto has_work = [&](const TcItem& w) {
+    return w.lo < w.L.total || (w.split == 0 && w.L.total == 0);
+  };
+  bool timed_out = false;
+
+  if (wg == 0) {
+    // ---------------------------------------------------------------- producer
+    struct Loads {
+      int j_spec, ns, t0, t1;
+    };
+    const auto load = [&](const TcItem& w) {
+      Loads l;
+      l.j_spec = (a.idx != nullptr && w.lo + tid < a.k_max)
+                     ? __ldg(a.idx + static_cast<size_t>(w.b) * a.k_max + w.lo + tid)
+                     : 0;
+      l.ns = a.n_sel != nullptr ? __ldg(a.n_sel + w.b) : 0;
+      l.t0 = __ldg(a.tail_start + w.b);
+      l.t1 = __ldg(a.seq_len + w.b);
+      return l;
+    };
+    TcItem nxt = item_of(first);
+    Loads ln = n > 0 ? load(nxt) : Loads{0, 0, 0, 0};
+    for (int j = 0; j < n; ++j) {
+      TcItem cur = nxt;
+      const Loads lc = ln;
+      // position tid of the item -> cache row (-1: absent, zero-filled)
+      cur.L = attended_list(lc.ns, lc.t0, lc.t1, a, cur.split == 0 && cur.g == 0 && tid == 0);
+      int crow = -1;
+      const int pos = cur.lo + tid;
+      if (pos < cur.L.total && pos < cur.lo + kBatch) {
+        const int jj = pos >= cur.L.ns ? cur.L.t0 + (pos - cur.L.ns) : lc.j_spec;
+        if (jj < 0 || jj >= lc.t1) {
+          flag_status(a.status, VSD_DEV_BAD_INDEX);
+        } else {
+          const int blk =
+              __ldg(a.block_table + static_cast<size_t>(cur.b) * a.max_blocks + jj / kPageS);
+          if (blk < 0 || blk >= a.num_blocks)
+            flag_status(a.status, VSD_DEV_BAD_BLOCK);
+          else
+            crow = (blk * a.Hkv + cur.g) * kPageS + (jj % kPageS);
+        }
+      }
+      if (j + 1 < n) {  // the next item's loads go out under this one's
+        nxt = item_of(first + j + 1);
+        ln = load(nxt);
+      }
+      const int s = j % kWsStages;
+      const uint32_t use = static_cast<uint32_t>(j / kWsStages);
+      if (use > 0 && !ptx::mbar_wait(&empty[s], (use - 1) & 1u)) timed_out = true;
+      if (has_work(cur)) {
+        // warp w copies rows 32 w .. 32 w + 31, RPI whole rows per instruction
+        uint8_t* k_s = base + s * 2 * Sm::kTile;
+        uint8_t* v_s = k_s + Sm::kTile;
+        const int ch = lane % LPR;
+#pragma unroll
+        for (int u = 0; u < 32 / RPI; ++u) {
+          const int rl = u * RPI + lane / LPR;
+          const int r = warp * 32 + rl;
+          const int cr = __shfl_sync(0xffffffffu, crow, rl);
+          const size_t src = cr >= 0 ? static_cast<size_t>(cr) * D + ch * 8 : 0;
+          const int off = (ch >> 3) * Sm::kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+          ptx::cp_async16(k_s + off, a.k_cache + src, cr >= 0 ? 16u : 0u);
+          ptx::cp_async16(v_s + off, a.v_cache + src, cr >= 0 ? 16u : 0u);
+        }
+      }
+      ptx::cp_async_mbar_arrive_noinc(&full[s]);
+      const unsigned rows = __ballot_sync(0xffffffffu, crow >= 0);
+      if (lane == 0) meta[s * 8 + warp] = rows;
+      if (tid == 0) meta[s * 8 + 4] = static_cast<uint32_t>(cur.L.total);
+      ptx::named_barrier_sync(3, kTcThreads);
+      if (tid == 0) ptx::mbar_arrive(&full[s]);  // releases the metadata
+    }
+    ptx::cp_async_wait_all();
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int c = wg - 1;
+    const int ct = tid - wg * kTcThreads;  // key of the item = TMEM lane
+    const int cw = ct >> 5;                // lane quarter
+    const uint32_t tm = tmem + 32 * c;     // S^T: columns [0, 16); O^T: [16, 32)
+    uint8_t* q_s = base + Sm::kOffQ + c * Sm::kQBytes;
+    float* red = reinterpret_cast<float*>(base + Sm::kOffRed) + c * (2 * 4 * kTcNQ);
+    float* scratch = reinterpret_cast<float*>(base + Sm::kOffScratch) + c * (kTcThreads * 6);
+    const uint32_t bar_id = 1 + c;
+    const auto csync = [bar_id] { ptx::named_barrier_sync(bar_id, kTcThreads); };
+    int staged_pair = -1;
+    int pend_pair = -1, pend_splits = 0, pend_count = 0;  // partials not yet counted
+    uint32_t phase = 0;
+    const auto flush = [&]() {
+      // the barrier orders every thread's partial stores before the acquire-release
+      // count; the last arrival of the pair combines its splits
+      ptx::tc_fence_before();
+      csync();
+      if (ct == 0) {
+        const unsigned old =
+            ptx::atom_add_acq_rel_gpu(a.counters + pend_pair, static_cast<unsigned>(pend_count));
+        const int lst =
+            old + static_cast<unsigned>(pend_count) == static_cast<unsigned>(pend_splits);
+        if (lst) ptx::st_relaxed_gpu(a.counters + pend_pair, 0u);
+        s_last[c] = lst;
+      }
+      csync();
+      if (s_last[c]) {
+        const int pb = pend_pair / a.Hkv;
+        merge_splits_by<D, G, kTcThreads, 24>(a, scratch, pend_pair, pb, pend_pair - pb * a.Hkv,
+                                              pend_splits, ct, csync);
+      }
+      pend_count = 0;
+    };
+    for (int j = c; j < n; j += 2) {
+      const int s = j % kWsStages;
+      const uint32_t use = static_cast<uint32_t>(j / kWsStages);
+      if (!ptx::mbar_wait(&full[s], use & 1u)) timed_out = true;
+      TcItem cur = item_of(first + j);
+      cur.L.total = static_cast<int>(meta[s * 8 + 4]);
+      const bool valid = (meta[s * 8 + cw] >> (ct & 31)) & 1u;
+      const bool work = has_work(cur);
+      const int n_splits = (cur.L.total + a.split_len - 1) / a.split_len;
+      const bool direct = n_splits <= 1;
+      // every consumer thread has read the stage's metadata past this barrier
+      if (pend_count > 0 && (cur.pair != pend_pair || !work || direct)) flush();
+      if (!work) {
+        csync();
+        if (ct == 0) ptx::mbar_arrive(&empty[s]);
+        continue;
+      }
+      uint8_t* k_s = base + s * 2 * Sm::kTile;
+      uint8_t* v_s = k_s + Sm::kTile;
+      uint8_t* p_s = k_s;
+      if (cur.pair != staged_pair) {
+        // the group's query rows, padded with zeros to 16 (this consumer's previous QK
+        // product, the block's last reader, has completed)
+#pragma unroll
+        for (int u = 0; u < QPT; ++u) {
+          const int i = ct + u * kTcThreads, r = i / LPR, cc = i % LPR;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (r < G)
+            v = *reinterpret_cast<const uint4*>(
+                a.q + (static_cast<size_t>(cur.b) * a.Hq + cur.g * G + r) * D + cc * 8);
+          *reinterpret_cast<uint4*>(q_s + (cc >> 3) * (kTcNQ * 128) + r * 128 +
+                                    (((cc & 7) ^ (r & 7)) << 4)) = v;
+        }
+        staged_pair = cur.pair;
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      csync();
+      // ---- S^T = K Q^T
+      if (ct == 0) {
+        ptx::tc_fence_after();
+        constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTcNQ, 0, 0);
+        const uint32_t ka = ptx::smem_u32(k_s), qa = ptx::smem_u32(q_s);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int hh = kk >> 2, w = kk & 3;
+          const uint64_t ad = ptx::sdesc_sw128(ka + hh * Sm::kHalf + w * 32, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(qa + hh * kTcNQ * 128 + w * 32, 16, 1024);
+          ptx::umma_bf16(tm, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        ptx::umma_commit(&bar_s[c]);
+      }
+      if (!ptx::mbar_wait(&bar_s[c], phase)) timed_out = true;
+      ptx::tc_fence_after();
+      float sv[kTcNQ];
+      ptx::tmem_ld16(tm + (static_cast<uint32_t>(cw * 32) << 16),
+                     reinterpret_cast<uint32_t(&)[16]>(sv));
+      ptx::tmem_wait_ld();
+      // ---- softmax over the item's keys, per head (log2 units)
+      float z[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        z[h] = valid ? sv[h] * a.scale_log2 : -INFINITY;
+        float mx = z[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) red[cw * kTcNQ + h] = mx;
+      }
+      csync();
+      float m[G], psum[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        m[h] = fmaxf(fmaxf(red[h], red[kTcNQ + h]), fmaxf(red[2 * kTcNQ + h], red[3 * kTcNQ + h]));
+        const float pv = (z[h] == -INFINITY) ? 0.f : exp2f(z[h] - m[h]);
+        z[h] = pv;
+        float sp = pv;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(0xffffffffu, sp, o);
+        if (lane == 0) red[4 * kTcNQ + cw * kTcNQ + h] = sp;
+      }
+      // row ct of P^T: 16 bf16 (heads >= G are zero) in two swizzled 16-byte chunks
+      float pr[kTcNQ];
+#pragma unroll
+      for (int cc = 0; cc < kTcNQ; ++cc) pr[cc] = cc < G ? z[cc < G ? cc : 0] : 0.f;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint4 pk;
+        pk.x = pack_bf16x2(pr[k * 8 + 0], pr[k * 8 + 1]);
+        pk.y = pack_bf16x2(pr[k * 8 + 2], pr[k * 8 + 3]);
+        pk.z = pack_bf16x2(pr[k * 8 + 4], pr[k * 8 + 5]);
+        pk.w = pack_bf16x2(pr[k * 8 + 6], pr[k * 8 + 7]);
+        *reinterpret_cast<uint4*>(p_s + ct * 128 + ((k ^ (ct & 7)) << 4)) = pk;
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      csync();
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        psum[h] = red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
+      // ---- O^T = V^T P^T; its completion also hands the stage back to the producer
+      if (ct == 0) {
+        ptx::tc_fence_after();
+        constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTcNQ, 1, 1);
+        const uint32_t va = ptx::smem_u32(v_s), pa = ptx::smem_u32(p_s);
+#pragma unroll
+        for (int kk = 0; kk < kBatch / 16; ++kk) {
+          const uint64_t ad = ptx::sdesc_sw128(va + kk * 2048, Sm::kHalf, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(pa + kk * 2048, Sm::kHalf, 1024);
+          ptx::umma_bf16(tm + 16, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        ptx::umma_commit(&bar_o[c]);
+        ptx::umma_commit(&empty[s]);
+      }
+      if (!ptx::mbar_wait(&bar_o[c], phase)) timed_out = true;
+      ptx::tc_fence_after();
+      phase ^= 1u;
+      if (cw < D / 32) {  // TMEM lanes 0 .. D-1 hold the output dimensions
+        float o[kTcNQ];
+        ptx::tmem_ld16(tm + (static_cast<uint32_t>(cw * 32) << 16) + 16,
+                       reinterpret_cast<uint32_t(&)[16]>(o));
+        ptx::tmem_wait_ld();
+        const int dim = ct;
+        if (direct) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float val = psum[h] > 0.f ? o[h] / psum[h] : 0.f;
+            const __nv_bfloat16 bv = __float2bfloat16_rn(val);
+            a.out[(static_cast<size_t>(cur.b) * a.Hq + cur.g * G + h) * D + dim] =
+                *reinterpret_cast<const uint16_t*>(&bv);
+          }
+        } else {
+          float* wsl =
+              a.ws + (static_cast<size_t>(cur.pair) * a.max_splits + cur.split) * SSlot<D, G>::kFloats;
+#pragma unroll
+          for (int h = 0; h < G; ++h) wsl[SSlot<D, G>::kO + h * D + dim] = o[h];
+          if (dim < G) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              if (h == dim) {
+                wsl[h] = m[h];
+                wsl[G + h] = psum[h];
+              }
+            }
+          }
+        }
+      }
+      if (!direct) {
+        pend_pair = cur.pair;
+        pend_splits = n_splits;
+        ++pend_count;
+      }
+    }
+    if (pend_count > 0) flush();
+  }
+  if (timed_out) flag_status(a.status, VSD_DEV_TIMEOUT);
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 64);
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_ws(const SParams& p, long long items, int sm_count, cudaStream_t stream) {
+  constexpr int smem = WsSmem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(sparse_ws_kernel<D, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  const int per_cta = static_cast<int>((items + sm_count - 1) / sm_count);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((items + per_cta - 1) / per_cta), 1, 1);
+  cfg.blockDim = dim3(kWsThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sparse_ws_kernel<D, G>, p, per_cta, static_cast<int>(items));
+}
+
 template <int D, int G>
 cudaError_t launch_tc(const SParams& p, int B, int Hkv, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
@@ -775,6 +1181,8 @@ cudaError_t launch_tc(const SParams& p, int B, int Hkv, cudaStream_t stream) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long ctas = static_cast<long long>(p.max_splits) * Hkv * B;
+  // more splits than one wave holds at three CTAs per SM: the warp-specialised kernel
+  if (ctas > 3LL * sm_count && ctas <= 0x7fffffffLL) return launch_ws<D, G>(p, ctas, sm_count, stream);
   constexpr int kSpreadSmem = 120 * 1024;
   static_assert(TcSmem<D>::kBytes <= kSpreadSmem && 2 * kSpreadSmem > 228 * 1024,
                 "one CTA per SM at the spread reservation");
@@ -834,7 +1242,8 @@ size_t sparse_counter_bytes(const SparsePlan& plan, int B, int Hkv) {
 size_t sparse_workspace_bytes(const SparsePlan& plan, int B, int Hkv, int G, int head_dim) {
   if (plan.max_splits <= 1) return 0;
   return sparse_counter_bytes(plan, B, Hkv) +
-         static_cast<size_t>(B) * Hkv * plan.max_splits * G * (head_dim + 2) * sizeof(float);
+         static_cast<size_t>(B) * Hkv * plan.max_splits * ((2 * G + 3) / 4 * 4 + G * head_dim) *
+             sizeof(float);
 }
 
 cudaError_t launch_sparse(const SparseArgs& sa, cudaStream_t stream) {

@@ -270,6 +270,32 @@ def test_sparse_edge_cases():
     check_sparse(batch, w, idx2, n_sel, tail, seq_len)
 
 
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (128, 64, 8), (128, 8, 8), (64, 16, 8)])
+def test_sparse_many_splits_one_launch(d, Hq, Hkv):
+    """More splits than one wave of the one-split kernel holds (8 sequences x 8 KV heads x
+    33 splits), with lists of every shape in the same launch: long (many splits, merged),
+    one batch and just over it, a single short split (direct output), the tail alone, and
+    an empty list."""
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    prefix = (6000, 5000, 4500, 300, 129, 128, 17, 0)
+    w = Workload("spws", B=8, P=6000, Hq=Hq, Hkv=Hkv, d=d, gamma=3, k=4096, n_sink=0,
+                 n_recent=0, seed=12, prefix_lens=prefix)
+    batch = make_batch(w, "cuda")
+    dev = "cuda"
+    n_per = [4096, 2000, 129, 128, 100, 0, 5, 0]
+    idx = torch.full((w.B, 4096), -1, dtype=torch.int32, device=dev)
+    n_sel = torch.tensor(n_per, dtype=torch.int32, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(1)
+    for b, (P, n) in enumerate(zip(prefix, n_per)):
+        if n:
+            idx[b, :n] = torch.sort(torch.randperm(P, generator=g)[:n]).values.to(torch.int32).to(dev)
+    tail = batch.prefix_len.clone()
+    seq_len = batch.prefix_len + torch.tensor([3, 1, 2, 0, 4, 2, 1, 3], dtype=torch.int32,
+                                              device=dev)
+    check_sparse(batch, w, idx, n_sel, tail, seq_len, max_tail=4)
+
+
 def test_sparse_bad_index_is_flagged():
     from sparse_attention_speculative_gb300.synth import make_batch
     from sparse_attention_speculative_gb300.workloads import Workload
