@@ -98,3 +98,24 @@ def test_collect_all_rejects_wide_groups(lib):
                                          1024, ctypes.c_float(0.1), None, None, None, None, 0,
                                          None)
     assert rc == -2
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+def test_sparse_workspace_holds_aligned_split_slots(lib, d, G):
+    """The draft step's workspace: per-(sequence, KV head) counters, then one partial
+    (m, l, o) slot per split -- the G maxima and sums padded to a multiple of four
+    floats, then the G output rows of d floats -- so that every slot and every output
+    row starts on a 16-byte boundary (the merge reads them as float4)."""
+    B, Hkv = 3, 8
+    g = _geom(B=B, Hq=Hkv * G, Hkv=Hkv, head_dim=d)
+    k_max, max_tail = 2048, 9  # 2057 positions: 17 splits of 128
+    size = ctypes.c_size_t(0)
+    assert lib.vsd_sparse_workspace_size(ctypes.byref(g), k_max, max_tail,
+                                         ctypes.byref(size)) == 0
+    splits = -(-(k_max + max_tail) // 128)
+    header = -(-2 * G // 4) * 4
+    slot = header + G * d
+    assert header * 4 % 16 == 0 and slot * 4 % 16 == 0
+    counters = -(-B * Hkv * 4 // 256) * 256
+    assert size.value == counters + B * Hkv * splits * slot * 4
