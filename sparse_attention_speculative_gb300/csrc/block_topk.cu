@@ -345,8 +345,10 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // NT threads per row; the boundary bucket's candidates are ranked directly up to NT
 constexpr int kBins = 256;
 
+// The 256-thread form runs when rows are plentiful: capped at 40 registers so that six
+// CTAs (six rows) are resident per SM instead of five.
 template <int ITEMS, int NT>
-__global__ void __launch_bounds__(NT) block_select_kernel(const BlockTopkArgs a) {
+__global__ void __launch_bounds__(NT, NT == 256 ? 6 : 1) block_select_kernel(const BlockTopkArgs a) {
   constexpr int kSelThreads = NT, kMaxCand = NT;
   static_assert(kSelThreads >= kBins && ITEMS <= 32, "one bin per thread; keep mask in 32 bits");
   __shared__ int hist[2][kBins];
