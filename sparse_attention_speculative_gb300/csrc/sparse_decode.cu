@@ -5,31 +5,31 @@
 // (paged attention with page size 1 whose page indices are the selected token
 // indices) plus the tokens appended after the selection (dense tail).
 //
-// How (GB300 design).  The step moves a few MB of randomly placed 256-byte rows, so it
-// is bound by the latency of its dependent loads (index -> block table -> K and V
-// rows), not by bandwidth.  The design therefore issues every load of a CTA at once
-// and spreads the list over the SMs in splits of 128 positions:
-//   * The attended list of one (sequence, KV head) pair, idx[0 .. n_sel) followed by
-//     [tail_start, seq_len), is cut into splits of 128 positions (more per split
-//     only when the list is very long); one CTA takes one split: sixteen warps of 8
-//     positions for up to 4 query heads per KV head, eight warps of 16 beyond.  The work of a warp is a short dependent chain (loads, dot
-//     products, shuffles, softmax, P.V), so the split is spread over many warps: the
-//     SM hides one warp's latencies behind the others'.
-//   * A row of K or V is read by head_dim/8 adjacent lanes, 16 bytes each, so one
-//     warp instruction fetches whole rows of 2 (head_dim 128) or 4 (64) keys and the
-//     8 (16) keys of a warp take 4 or 2 (8 or 4) instructions for K and as many for V, all in
-//     flight together (the first index loads are issued speculatively, before the
-//     list lengths are known).
-//   * Each lane forms partial dot products of its 8 dims with the G queries of the
-//     group (fp32, q in shared memory); a shuffle tree over the row's lanes
-//     completes the logits.  The warp softmax over its keys and the P.V product
-//     on the lane's 8 dims follow in registers.
-//   * The warps merge in shared memory in a fixed order.  A pair with a single
-//     split writes its output directly; otherwise each split writes (m, l, o) to the
-//     workspace and the split that finishes last (a per-pair counter in the
-//     workspace, reset to zero by that split) combines them with all its threads,
-//     every load of a round in flight at once, in split order.  Results are
-//     bit-reproducible; the only atomics are the counters.
+// How (GB300 design).  The step moves a few MB to tens of MB of randomly placed
+// 256-byte rows; at one sequence it is bound by the latency of its dependent loads
+// (index -> block table -> K and V rows), at large batches by how many gathers stay in
+// flight.  The attended list of one (sequence, KV head) pair, idx[0 .. n_sel) followed
+// by [tail_start, seq_len), is cut into splits of 128 positions (more per split only
+// when the list is very long).  A pair with a single split writes its output directly;
+// otherwise each split writes (m, l, o) to the workspace and the pair's last split (a
+// per-pair counter in the workspace, reset to zero by that split) combines them, every
+// load of a round in flight at once, in split order.  Results are bit-reproducible;
+// the only atomics are the counters.  Three kernels:
+//   * sparse_tc_kernel (splits of one 128-position batch, the common case): one split
+//     per CTA of four warps on the 5th-generation tensor cores (below); one CTA per SM
+//     when the splits fit one wave, three per SM otherwise.
+//   * sparse_ws_kernel (more splits than one wave of it holds): persistent CTAs with a
+//     producer warpgroup gathering into three stages and two consumer warpgroups
+//     running the same tensor-core steps (below).
+//   * sparse_decode_kernel (splits longer than one batch: lists beyond 1024 batches),
+//     on the CUDA cores: sixteen warps of 8 positions for up to 4 query heads per KV
+//     head, eight warps of 16 beyond; a row of K or V is read by head_dim/8 adjacent
+//     lanes, 16 bytes each, all of a warp's loads in flight together (the first index
+//     loads issued speculatively, before the list lengths are known); each lane forms
+//     partial dot products of its 8 dims with the G queries of the group (fp32, q in
+//     shared memory), a shuffle tree over the row's lanes completes the logits, the
+//     warp softmax and the P.V product on the lane's 8 dims follow in registers, and
+//     the warps merge in shared memory in a fixed order.
 #include <cfloat>
 
 #include "common.cuh"
