@@ -53,3 +53,29 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, r.stdout
     res = json.loads(lines[0])
     assert res["impl"] == "reference" and res["value"] > 0
+
+
+def test_algorithmic_bytes_match_the_configuration_table():
+    """The bytes the benchmark divides by, against the figures the configurations are
+    stated with: the Qwen3-8B 32K layer (verification 142.7 MB: K/V 134.2 + logits 8.4 +
+    q/out, plus the 1 MB of partials it also writes; one draft step 8.4 MB) and the
+    36-layer loop (per iteration 41.1 GB of verification, 0.30 GB of selection, 2.42 GB
+    per draft step)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from sparse_attention_speculative_gb300.workloads import LOOP_36L, QWEN3_8B_32K
+
+    w = QWEN3_8B_32K
+    prefix = list(w.prefix())
+    vb, sb, spb = bench.iteration_bytes(w, prefix, [w.k] * w.B,
+                                        [[2 + i] * w.B for i in range(w.gamma)])
+    assert abs(vb / 1e6 - (142.7 + 1.05)) < 0.5
+    assert all(abs(x / 1e6 - 8.4) < 0.1 for x in spb)
+    w = LOOP_36L
+    prefix = list(w.prefix())
+    vb, sb, spb = bench.iteration_bytes(w, prefix, [w.k] * w.B,
+                                        [[2 + i] * w.B for i in range(w.gamma)])
+    L = w.layers
+    assert abs(L * vb / 1e9 - 41.1) / 41.1 < 0.01
+    assert abs(L * sb / 1e9 - 0.30) / 0.30 < 0.02
+    assert all(abs(L * x / 1e9 - 2.42) / 2.42 < 0.01 for x in spb)
