@@ -68,25 +68,30 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic(workload: str):
-    """DRAM bytes per launch recorded by ncu for the verification kernel, if the
-    kernel sources have not changed since the counters were taken."""
-    prof = os.path.join(ROOT, "profiles", "verify_attn_collect_%s.md" % workload)
-    try:
-        text = open(prof).read()
-    except OSError:
-        return None
+def verify_sources_digest():
+    """Digest of the sources the verification kernel compiles from."""
     csrc = os.path.join(ROOT, "sparse_attention_speculative_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.startswith("verify_attn") or name in ("ptx.cuh", "common.cuh"):
-            h.update(open(os.path.join(csrc, name), "rb").read())
-    digest = h.hexdigest()[:16]
-    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if m_src and m_tr and m_src.group(1) == digest:
-        return int(m_tr.group(1))
-    return None
+    for name in ("verify_attn.cuh", "verify_attn.cu", "verify_attn_d128.cu", "verify_attn_d64.cu",
+                 "ptx.cuh", "common.cuh", "launch.h"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "vsd.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(workload: str, bytes_per_call: float):
+    """DRAM bytes per launch of the verification call, from the committed ncu record
+    (profiles/verify_traffic.json: read + write bytes of the main and merge kernels of one
+    call on a captured workload, with that call's algorithmic bytes), scaled to a call of
+    `bytes_per_call` algorithmic bytes; None when the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", "verify_traffic.json")
+    try:
+        rec = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    if rec.get("sources_digest") != verify_sources_digest():
+        return None
+    return rec["dram_bytes_per_call"] * bytes_per_call / rec["algorithmic_bytes_per_call"]
 
 
 class ClockSampler:
@@ -556,7 +561,7 @@ def run_gpu(args, world, rank, local):
                                "bytes = algorithmic bytes of one call" % B2B_CALLS,
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": profile_traffic(w.name)},
+                     "traffic": profile_traffic(w.name, vb)},
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_all_timed_loops": (2 * launches_per_step * args.steps +
                                          (6 if per["verify_all_b2b"] else 3) * B2B_CALLS *
@@ -615,15 +620,40 @@ def run_e2e(args, w, batch, vsd, dev, stream, workspace, prefix, total_bytes):
 
 # ------------------------------------------------------------------ multi-layer loop
 
+def append_bytes(w):
+    """Algorithmic bytes of one iteration's cache appends for one layer: the R verify
+    rows and the gamma draft-step rows of every sequence and KV head, K and V, read from
+    the input arena and written into the cache."""
+    return 2 * 2 * w.B * (w.R + w.gamma) * w.Hkv * w.d * 2
+
+
+def loop_run_bytes(w, accepted):
+    """Algorithmic bytes of a decode run (one entry per iteration: verification,
+    selection, draft steps and appends over every layer) for the accepted counts
+    `accepted` [iterations][B]; the prefixes grow by accepted + 1 per iteration."""
+    prefix = list(w.prefix())
+    per_iter = []
+    for acc in accepted:
+        n_sel = [min(w.k, P) for P in prefix]
+        tails = [[int(acc[b]) + 2 + i for b in range(w.B)] for i in range(w.gamma)]
+        vb, sb, spb = iteration_bytes(w, prefix, n_sel, tails)
+        per_iter.append({"verify": w.layers * vb, "select": w.layers * sb,
+                         "sparse": w.layers * sum(spb), "append": w.layers * append_bytes(w),
+                         "prefix": list(prefix)})
+        prefix = [P + int(a) + 1 for P, a in zip(prefix, acc)]
+    return per_iter
+
+
 def run_gpu_loop(args, world, rank, local):
-    """One decode iteration of a multi-layer model's attention: every layer's
-    verification + Collect-2-Query with the fused aggregation, one selection launch for
-    all layers x sequences, then gamma draft steps, each over every layer.  Each layer
-    has its own seeded cache; the step's queries sit in one device arena (filled from
-    pinned host memory in the end-to-end variant)."""
+    """Decode runs of a multi-layer model's attention (`DecodeLoop`): every iteration
+    appends the verify block's K/V of every layer, runs each layer's scored verification,
+    one selection over all layers x sequences, advances the prefixes by the accepted
+    counts, and runs gamma draft steps over every layer, each appending its input token's
+    K/V first.  One step = one run of `w.iterations` iterations from the initial prefix
+    (one CUDA-graph replay); the caches (tens of GB) exceed L2, so no flush is needed."""
     import sparse_attention_speculative_gb300 as vsd
     from sparse_attention_speculative_gb300 import build as pkg_build
-    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.synth import make_batch, seeded_bf16
     from sparse_attention_speculative_gb300.workloads import ALL
 
     if rank == 0 or not pkg_build.up_to_date():
@@ -634,148 +664,104 @@ def run_gpu_loop(args, world, rank, local):
     w = ALL[args.workload]
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream()
-    NL = w.layers
-    B, R, Hq, d, gamma = w.B, w.R, w.Hq, w.d, w.gamma
-    batches = [make_batch(w, dev, layer=l) for l in range(NL)]
-    prefix = list(w.prefix())
-    P_max = w.P_max
-    pl = batches[0].prefix_len
-    rows_pl = pl.repeat(NL)
-    geom = vsd.geom_for(B, Hq, batches[0].k_cache, batches[0].block_table)
-    ws_bytes = vsd.vsd_verify_workspace_size(geom, R, P_max)
-    workspace = torch.zeros(max(ws_bytes, 1) + 256, dtype=torch.uint8, device=dev)
-    workspace = workspace[(-workspace.data_ptr()) % 256:][:ws_bytes] if ws_bytes else None
-    max_tail = 2 * gamma + 1
-    sws_bytes = vsd.vsd_sparse_workspace_size(geom, w.k, max_tail)
-    sws = torch.zeros(max(sws_bytes, 1) + 256, dtype=torch.uint8, device=dev)
-    sws = sws[(-sws.data_ptr()) % 256:][:sws_bytes] if sws_bytes else None
-    # the step's inputs (queries of every layer, draft lengths) and results (draft outputs)
-    q_all = torch.stack([bt.q for bt in batches])              # [NL, B, R, Hq, d]
-    qd_all = torch.stack([bt.q_draft for bt in batches])       # [NL, gamma, B, Hq, d]
-    seq_len = torch.empty((gamma, B), dtype=torch.int32, device=dev)
-    d_out = torch.empty((gamma, NL, B, Hq, d), dtype=torch.bfloat16, device=dev)
-    out = torch.empty((B, R, Hq, d), dtype=torch.bfloat16, device=dev)
-    logits = torch.empty((B, 2, Hq, P_max), dtype=torch.float32, device=dev)
-    partial = torch.empty((B, w.Hkv, P_max), dtype=torch.float32, device=dev)
-    score = torch.empty((NL * B, P_max), dtype=torch.float32, device=dev)
-    hist = torch.empty((NL * B, vsd.HIST_BINS), dtype=torch.int32, device=dev)
-    idx = torch.empty((NL * B, w.k), dtype=torch.int32, device=dev)
-    n_sel = torch.empty((NL * B,), dtype=torch.int32, device=dev)
-    tail_start = pl.clone()
-    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    NL, B, R, Hq, Hkv, d, gamma = w.layers, w.B, w.R, w.Hq, w.Hkv, w.d, w.gamma
+    iters = w.iterations
+    P_max = (max(w.prefix()) + iters * R + 3) // 4 * 4
+    batches = [make_batch(w, dev, layer=l, extra_capacity=iters * R + 2 * R)
+               for l in range(NL)]
+    loop = vsd.DecodeLoop([bt.k_cache for bt in batches], [bt.v_cache for bt in batches],
+                          [bt.block_table for bt in batches], list(w.prefix()), Hq=Hq,
+                          gamma=gamma, k=w.k, n_sink=w.n_sink, n_recent=w.n_recent,
+                          P_max=P_max, scale=w.scale)
+    # the iteration's inputs: each layer's seeded queries and the seeded K/V of the new
+    # tokens (the same every iteration; the positions they go to move with the prefix)
+    for l, bt in enumerate(batches):
+        loop.q[l].copy_(bt.q)
+        loop.q_draft[l].copy_(bt.q_draft)
+    loop.k_verify.copy_(seeded_bf16((NL, B, R, Hkv, d), w.seed * 31 + 1, dev))
+    loop.v_verify.copy_(seeded_bf16((NL, B, R, Hkv, d), w.seed * 31 + 2, dev))
+    loop.k_draft.copy_(seeded_bf16((NL, gamma, B, Hkv, d), w.seed * 31 + 3, dev))
+    loop.v_draft.copy_(seeded_bf16((NL, gamma, B, Hkv, d), w.seed * 31 + 4, dev))
     rng = np.random.default_rng(w.seed + 77)
-
-    def draw_seq_len():
-        a = rng.integers(0, gamma + 1, size=B)
-        return np.array([[prefix[b] + a[b] + 2 + i for b in range(B)] for i in range(gamma)],
-                        dtype=np.int32)
-
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-
-    def step(events=False):
-        for l, bt in enumerate(batches):
-            rows = slice(l * B, (l + 1) * B)
-            vsd.vsd_verify_attn_collect_scored(q_all[l], bt.k_cache, bt.v_cache, bt.block_table,
-                                               pl, P_max=P_max, scale=w.scale, row0=0,
-                                               row1=R - 1, logits=logits, partial=partial,
-                                               score=score[rows], score_hist=hist[rows],
-                                               out=out, workspace=workspace)
-        if events:
-            ev[1].record(stream)
-        vsd.vsd_select_topk_scored(score, hist, rows_pl, k=w.k, n_sink=w.n_sink,
-                                   n_recent=w.n_recent, idx=idx, n_sel=n_sel)
-        if events:
-            ev[2].record(stream)
-        for i in range(gamma):
-            for l, bt in enumerate(batches):
-                rows = slice(l * B, (l + 1) * B)
-                vsd.vsd_sparse_decode_attn(qd_all[l, i], bt.k_cache, bt.v_cache, bt.block_table,
-                                           idx[rows], n_sel[rows], tail_start, seq_len[i],
-                                           scale=w.scale, max_tail=max_tail, out=d_out[i, l],
-                                           workspace=sws)
-        if events:
-            ev[3].record(stream)
-
-    launches_per_step = 2 * NL + 1 + gamma * NL
-    sleep_cycles = 8_000_000
-    for _ in range(max(args.warmup, 1)):
-        seq_len.copy_(torch.from_numpy(draw_seq_len()))
-        step()
-    torch.cuda.synchronize()
+    n_runs = args.warmup + args.steps
+    acc_all = rng.integers(0, gamma + 1, size=(n_runs, iters, B)).astype(np.int32)
+    acc_dev = torch.from_numpy(acc_all).to(dev)
+    stream = loop.stream
+    # one graph of a whole run; each run's accepted draws are copied into its input rows
+    # just before its replay (800 bytes, stream-ordered)
+    acc_rows = torch.empty((iters, B), dtype=torch.int32, device=dev)
+    acc_rows.copy_(acc_dev[0])
+    t_cap = time.perf_counter()
+    run_graph = loop.record_run(acc_rows)
+    t_cap = time.perf_counter() - t_cap
+    status = vsd.vsd_read_device_status()
+    if status:
+        raise RuntimeError("device status 0x%x after capture" % status)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for r in range(args.warmup):
+            acc_rows.copy_(acc_dev[r])
+            run_graph.replay()
+    stream.synchronize()
     status = vsd.vsd_read_device_status()
     if status:
         raise RuntimeError("device status 0x%x during warm-up" % status)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
-    torch.cuda.synchronize()
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
-    def graph_step(sl):
-        seq_len.copy_(torch.from_numpy(sl))
-        flush_l2(flush_w, flush_r)
-        torch.cuda.synchronize()
-        torch.cuda._sleep(sleep_cycles)
-        g0.record(stream)
-        graph.replay()
-        g1.record(stream)
-
-    for _ in range(args.warmup):
-        graph_step(draw_seq_len())
-    torch.cuda.synchronize()
-    per = {"graph": [], "verify": [], "select": [], "sparse": []}
-    tails_seen = []
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        for _ in range(args.steps):
-            sl = draw_seq_len()
-            tails_seen.append([[int(sl[i, b] - prefix[b]) for b in range(B)]
-                               for i in range(gamma)])
-            graph_step(sl)
-            torch.cuda.synchronize()
-            per["graph"].append(g0.elapsed_time(g1) * 1e-3)
-        # per-phase breakdown: the same iteration launched eagerly, events between phases
-        for _ in range(args.steps):
-            seq_len.copy_(torch.from_numpy(draw_seq_len()))
-            flush_l2(flush_w, flush_r)
-            torch.cuda.synchronize()
-            torch.cuda._sleep(sleep_cycles)
-            ev[0].record(stream)
-            step(events=True)
-            torch.cuda.synchronize()
-            per["verify"].append(ev[0].elapsed_time(ev[1]) * 1e-3)
-            per["select"].append(ev[1].elapsed_time(ev[2]) * 1e-3)
-            per["sparse"].append(ev[2].elapsed_time(ev[3]) * 1e-3)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(8_000_000)  # the first replays are queued before the GPU gets to them
+            e0.record(stream)
+            for r in range(args.warmup, n_runs):
+                acc_rows.copy_(acc_dev[r])
+                run_graph.replay()
+            e1.record(stream)
+        stream.synchronize()
     torch.cuda.synchronize()
+    t_total = e0.elapsed_time(e1) * 1e-3
     if world > 1:
         torch.distributed.barrier()
     status = vsd.vsd_read_device_status()
     if status:
         raise RuntimeError("device status 0x%x in the timed region" % status)
-    n_sel_host = n_sel.cpu().tolist()
-    mean_tails = [[statistics.mean(t[i][b] for t in tails_seen) for b in range(B)]
-                  for i in range(gamma)]
-    vb = sb = 0
-    spb = [0] * gamma
-    for l in range(NL):
-        v_l, s_l, sp_l = iteration_bytes(w, prefix, n_sel_host[l * B:(l + 1) * B], mean_tails)
-        vb, sb = vb + v_l, sb + s_l
-        spb = [x + y for x, y in zip(spb, sp_l)]
-    total_bytes = vb + sb + sum(spb)
-    t_step = sum(per["graph"])
-    t_tensor = torch.tensor([t_step], dtype=torch.float64, device=dev)
+    del run_graph
+    run_bytes = [loop_run_bytes(w, acc_all[r]) for r in range(args.warmup, n_runs)]
+    total_bytes = sum(sum(it["verify"] + it["select"] + it["sparse"] + it["append"]
+                          for it in rb) for rb in run_bytes)
+    t_tensor = torch.tensor([t_total], dtype=torch.float64, device=dev)
     if world > 1:
         torch.distributed.all_reduce(t_tensor, op=torch.distributed.ReduceOp.MAX)
     t_max = float(t_tensor.item())
-    value = world * total_bytes * args.steps / t_max / 1e9
+    value = world * total_bytes / t_max / 1e9
     peak, peak_kind = measured_peaks()
-    t_v = statistics.median(per["verify"])
-    t_s = statistics.median(per["select"])
-    t_sp = statistics.median(per["sparse"])
+    clk = clocks.summary()
+
+    # per-phase breakdown: one run of iterations from a graph with external event
+    # records at the phase boundaries (verify = the layers' appends + verifications;
+    # select = the selection + the advance; draft = the draft steps with their appends)
+    marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    g_marked = loop.record_marked({"verified": lambda: marks[1].record(stream),
+                                   "selected": lambda: marks[2].record(stream),
+                                   "drafted": lambda: marks[3].record(stream)},
+                                  first=lambda: marks[0].record(stream))
+    phase = {"verify": [], "select": [], "sparse": []}
+    acc_ph = acc_all[args.warmup]
+    with torch.cuda.stream(stream):
+        loop.reset()
+        for it in range(iters):
+            loop.accepted.copy_(acc_dev[args.warmup, it])
+            g_marked.replay()
+            stream.synchronize()
+            phase["verify"].append(marks[0].elapsed_time(marks[1]) * 1e-3)
+            phase["select"].append(marks[1].elapsed_time(marks[2]) * 1e-3)
+            phase["sparse"].append(marks[2].elapsed_time(marks[3]) * 1e-3)
+    del g_marked
+    ph_bytes = loop_run_bytes(w, acc_ph)
+    t_v, t_s, t_sp = (statistics.mean(phase[k]) for k in ("verify", "select", "sparse"))
+    b_v = statistics.mean(it["verify"] + it["append"] * R / (R + gamma) for it in ph_bytes)
+    b_s = statistics.mean(it["select"] for it in ph_bytes)
+    b_sp = statistics.mean(it["sparse"] + it["append"] * gamma / (R + gamma) for it in ph_bytes)
     nominal = NOMINAL_HBM_GBS
 
     def entry(t, nbytes, calls):
@@ -783,76 +769,226 @@ def run_gpu_loop(args, world, rank, local):
                 "GB_s": nbytes / t / 1e9, "frac_of_%s_hbm" % peak_kind: nbytes / t / 1e9 / peak,
                 "frac_of_nominal_8tbs": nbytes / t / 1e9 / nominal}
 
-    # the verification calls of the layers run back to back (K/V of each layer larger
-    # than L2): the roofline of the dominant kernel from their phase, per call
-    achieved = vb / t_v / 1e9
-    clk = clocks.summary()
+    # the dominant kernel: the layers' verification calls inside the iteration (their
+    # phase between two event records in the graph, the 36 small verify-block appends
+    # included), algorithmic bytes of the calls / phase time
+    verify_call_bytes = statistics.mean(it["verify"] for it in ph_bytes) / NL
+    achieved = statistics.mean(it["verify"] for it in ph_bytes) / t_v / 1e9
+    us_iter = t_max / (args.steps * iters) * 1e6
     result = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
-        "us_per_iter": t_max / args.steps * 1e6, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "layers": NL, "B": B, "P": w.P, "Hq": Hq, "Hkv": w.Hkv,
+        "us_per_iter": us_iter, "iterations_per_step": iters,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "layers": NL, "B": B, "P": w.P, "Hq": Hq, "Hkv": Hkv,
                    "d": d, "gamma": gamma, "k": w.k, "n_sink": w.n_sink,
-                   "n_recent": w.n_recent, "page": w.page,
-                   "prefix": "fixed at P (the accept draws vary the draft tails only)",
-                   "l2": "flushed before every timed iteration (512 MB write, then 512 MB "
-                         "read so no dirty lines remain)",
+                   "n_recent": w.n_recent, "page": w.page, "iterations": iters,
+                   "prefix": "starts at P and grows by accepted + 1 every iteration "
+                             "(accepted ~ uniform{0..gamma}, seeded); the verify block's "
+                             "and every draft token's K/V are appended inside the graph",
+                   "l2": "no flush: every iteration streams %.1f GB from %.1f GB of caches "
+                         "(far larger than the 126 MB L2)"
+                         % (total_bytes / (args.steps * iters) / 1e9,
+                            2 * NL * batches[0].k_cache.numel() * 2 / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "timing": "value: one CUDA-graph replay of the whole iteration (%d kernels) per step; "
-                  "phases: medians of the same iteration launched eagerly with events "
-                  "between the phases" % launches_per_step,
-        "phases": {"verify_collect": entry(t_v, vb, NL), "select_topk": entry(t_s, sb, 1),
-                   "sparse_draft_steps": entry(t_sp, sum(spb), gamma * NL)},
+        "timing": "value: %d runs of %d iterations, each run one CUDA-graph replay (%d libvsd "
+                  "kernels per iteration), device events around all runs; phases: one run "
+                  "from a graph with event records at the phase boundaries"
+                  % (args.steps, iters, loop.launches_per_iteration),
+        "graph_capture_s": t_cap,
+        "phases": {"verify_collect": entry(t_v, b_v, NL),
+                   "select_topk": entry(t_s, b_s, 1),
+                   "sparse_draft_steps": entry(t_sp, b_sp, gamma * NL)},
         "select_over_verify_call": t_s / (t_v / NL),
         "roofline": {"bound": "hbm", "kernel": "vsd_verify_attn_collect_scored",
-                     "timing": "the %d layers' verification calls back to back (eager phase "
-                               "between two events), per-call mean; bytes = algorithmic bytes "
-                               "of one call" % NL,
+                     "timing": "the %d layers' verification calls inside the iteration (their "
+                               "phase between event records in the iteration graph, the "
+                               "verify-block appends included), per call; bytes = "
+                               "algorithmic bytes of one call at the run's prefixes" % NL,
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": None},
-        "gpu_launches": launches_per_step * args.steps,
-        "gpu_launches_per_step": launches_per_step,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "bytes_per_call": verify_call_bytes,
+                     "traffic": profile_traffic("qwen3_8b_loop_layer", verify_call_bytes)},
+        "gpu_launches": loop.launches_per_iteration * iters * args.steps + args.steps,
+        "gpu_launches_per_iteration": loop.launches_per_iteration,
         "clocks": clk,
     }
     if args.e2e:
-        # the same iteration with the step's inputs copied in from pinned host memory and
-        # the draft outputs copied back, all in one graph
-        h_q = q_all.cpu().pin_memory()
-        h_qd = qd_all.cpu().pin_memory()
-        h_sl = torch.empty((gamma, B), dtype=torch.int32).pin_memory()
-        h_out = torch.empty(d_out.shape, dtype=d_out.dtype).pin_memory()
-        h_nsel = torch.empty(n_sel.shape, dtype=n_sel.dtype).pin_memory()
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2):
-            q_all.copy_(h_q, non_blocking=True)
-            qd_all.copy_(h_qd, non_blocking=True)
-            seq_len.copy_(h_sl, non_blocking=True)
-            step()
-            h_out.copy_(d_out, non_blocking=True)
-            h_nsel.copy_(n_sel, non_blocking=True)
-        torch.cuda.synchronize()
-        times = []
-        for s in range(args.warmup + args.steps):
-            h_sl.copy_(torch.from_numpy(draw_seq_len()))
+        # the same runs through the public API as a caller drives it: per iteration the
+        # host fills the pinned input arena (its accepted counts), DecodeLoop.run(sync=True)
+        # copies the inputs in, runs the iteration and copies every result back, and the
+        # host waits for it; host wall clock around every call, no GPU sleep in front
+        for name in ("q", "q_draft", "k_verify", "v_verify", "k_draft", "v_draft"):
+            getattr(loop, "h_" + name).copy_(getattr(loop, name))
+        walls = []
+        for r in range(n_runs):
+            loop.reset()
+            loop.synchronize()
+            for it in range(iters):
+                loop.h_accepted.copy_(torch.from_numpy(acc_all[r, it]))
+                t0 = time.perf_counter()
+                loop.run(sync=True)
+                t1 = time.perf_counter()
+                if r >= args.warmup:
+                    walls.append(t1 - t0)
+        status = vsd.vsd_read_device_status()
+        if status:
+            raise RuntimeError("device status 0x%x in the end-to-end runs" % status)
+        t_wall = sum(walls)
+        result["e2e"] = {"value": total_bytes / t_wall / 1e9, "unit": "GB/s",
+                         "wall_us_per_iter": t_wall / len(walls) * 1e6,
+                         "h2d_bytes_per_step": loop.h2d_bytes * iters,
+                         "d2h_bytes_per_step": loop.d2h_bytes * iters,
+                         "path": "DecodeLoop.run(sync=True) per iteration (host wall clock): "
+                                 "pinned host inputs (queries, new K/V, accepted counts) -> "
+                                 "the iteration -> every output, selection and the loop "
+                                 "state back to pinned host memory; %d iterations per step"
+                                 % iters}
+    if rank == 0 and args.cpu_baseline:
+        result["cpu_baseline"] = run_cpu_baseline_loop(w, batches)
+    if args.configs and rank == 0:
+        # the single-layer configurations' per-call figures, from the same run
+        del loop, batches
+        torch.cuda.empty_cache()
+        result["configs"] = {}
+        for name in ("qwen3_8b_32k", "qwen25_72b_b16_32k", "qwen3_8b_128k_bursts"):
+            result["configs"][name] = layer_figures(ALL[name], dev, peak, peak_kind)
+    return result
+
+
+def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
+    """Per-call figures of one single-layer configuration, three ways, each from CUDA
+    graphs replayed with L2 flushed before every replay (512 MB written, then 512 MB
+    read) and a GPU sleep in front so the replay is queued before the GPU reaches it:
+      iteration   verify (main + merge/aggregation kernel) -> select -> gamma draft
+                  steps, device events around the replay;
+      in_iteration the same graph with external event records between the calls: each
+                  call's share of it (the verification's share includes the start of the
+                  replay, the other calls lose their overlap with their predecessor);
+      chained     `chain` calls of one kind back to back in one graph (each a
+                  programmatic dependent of the previous one), time / chain."""
+    import sparse_attention_speculative_gb300 as vsd
+    from sparse_attention_speculative_gb300.synth import make_batch
+    batch = make_batch(w, dev)
+    B, R, Hq, d, gamma = w.B, w.R, w.Hq, w.d, w.gamma
+    P_max = w.P_max
+    prefix = list(w.prefix())
+    stream = torch.cuda.current_stream()
+    geom = vsd.geom_for(B, Hq, batch.k_cache, batch.block_table)
+    nb = vsd.vsd_verify_workspace_size(geom, R, P_max)
+    ws = torch.zeros(nb + 256, dtype=torch.uint8, device=dev)
+    ws = ws[(-ws.data_ptr()) % 256:][:nb] if nb else None
+    max_tail = 2 * gamma + 1
+    nb = vsd.vsd_sparse_workspace_size(geom, w.k, max_tail)
+    sws = torch.zeros(nb + 256, dtype=torch.uint8, device=dev)
+    sws = sws[(-sws.data_ptr()) % 256:][:nb] if nb else None
+    out = torch.empty_like(batch.q)
+    logits = torch.empty((B, 2, Hq, P_max), dtype=torch.float32, device=dev)
+    partial = torch.empty((B, w.Hkv, P_max), dtype=torch.float32, device=dev)
+    score = torch.empty((B, P_max), dtype=torch.float32, device=dev)
+    hist = torch.empty((B, vsd.HIST_BINS), dtype=torch.int32, device=dev)
+    idx = torch.empty((B, w.k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty((B,), dtype=torch.int32, device=dev)
+    d_out = torch.empty((gamma, B, Hq, d), dtype=torch.bfloat16, device=dev)
+    tail_start = batch.prefix_len.clone()
+    a = np.random.default_rng(w.seed + 77).integers(0, gamma + 1, size=B)
+    seq_len = torch.tensor([[prefix[b] + int(a[b]) + 2 + i for b in range(B)]
+                            for i in range(gamma)], dtype=torch.int32, device=dev)
+
+    def verify():
+        vsd.vsd_verify_attn_collect_scored(batch.q, batch.k_cache, batch.v_cache,
+                                           batch.block_table, batch.prefix_len, P_max=P_max,
+                                           scale=w.scale, row0=0, row1=R - 1, logits=logits,
+                                           partial=partial, score=score, score_hist=hist,
+                                           out=out, workspace=ws)
+
+    def select():
+        vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                   n_recent=w.n_recent, idx=idx, n_sel=n_sel)
+
+    def draft(i):
+        vsd.vsd_sparse_decode_attn(batch.q_draft[i], batch.k_cache, batch.v_cache,
+                                   batch.block_table, idx, n_sel, tail_start, seq_len[i],
+                                   scale=w.scale, max_tail=max_tail, out=d_out[i],
+                                   workspace=sws)
+
+    marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3 + gamma)]
+
+    def iteration(marked=False):
+        cur = torch.cuda.current_stream()  # the capturing stream inside a capture
+        if marked:
+            marks[0].record(cur)
+        verify()
+        if marked:
+            marks[1].record(cur)
+        select()
+        if marked:
+            marks[2].record(cur)
+        for i in range(gamma):
+            draft(i)
+            if marked:
+                marks[3 + i].record(cur)
+
+    iteration()
+    torch.cuda.synchronize()
+    graphs = {}
+    for name, fn in (("iteration", iteration), ("in_iteration", lambda: iteration(True)),
+                     ("verify", lambda: [verify() for _ in range(chain)]),
+                     ("select", lambda: [select() for _ in range(chain)]),
+                     ("draft", lambda: [draft(i % gamma) for i in range(chain)])):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs[name] = g
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = {k: [] for k in graphs}
+    phases = []
+    for rep in range(reps + 2):
+        for name, g in graphs.items():
             flush_l2(flush_w, flush_r)
             torch.cuda.synchronize()
             torch.cuda._sleep(2_000_000)
-            g0.record(stream)
-            g2.replay()
-            g1.record(stream)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
             torch.cuda.synchronize()
-            if s >= args.warmup:
-                times.append(g0.elapsed_time(g1) * 1e-3)
-        t = statistics.mean(times)
-        h2d = h_q.numel() * 2 + h_qd.numel() * 2 + h_sl.numel() * 4
-        d2h = h_out.numel() * 2 + h_nsel.numel() * 4
-        result["e2e"] = {"value": total_bytes / t / 1e9, "unit": "GB/s", "us_per_iter": t * 1e6,
-                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                         "path": "one CUDA graph per step: every layer's queries and the draft "
-                                 "lengths copied in from pinned host memory, the iteration, "
-                                 "every draft output and the selection counts copied back"}
-    return result, batches
+            if rep >= 2:
+                times[name].append(e0.elapsed_time(e1) * 1e-3)
+                if name == "in_iteration":
+                    phases.append([marks[i].elapsed_time(marks[i + 1]) * 1e-3
+                                   for i in range(2 + gamma)])
+    status = vsd.vsd_read_device_status()
+    if status:
+        raise RuntimeError("device status 0x%x in the per-call figures of %s" % (status, w.name))
+    n_sel_host = n_sel.cpu().tolist()
+    tails = [[int(a[b]) + 2 + i for b in range(B)] for i in range(gamma)]
+    vb, sb, spb = iteration_bytes(w, prefix, n_sel_host, tails)
+    t = {k: statistics.median(v) for k, v in times.items()}
+    ph = [statistics.median(p[i] for p in phases) for i in range(2 + gamma)]
+
+    def fig(tt, nbytes):
+        return {"us": tt * 1e6, "bytes": nbytes, "GB_s": nbytes / tt / 1e9,
+                "frac_of_%s_hbm" % peak_kind: nbytes / tt / 1e9 / peak}
+
+    res = {"iteration": fig(t["iteration"], vb + sb + sum(spb)),
+           "in_iteration": {"verify_collect_scored": fig(ph[0], vb),
+                            "select_topk_scored_us": ph[1] * 1e6,
+                            "select_over_verify": ph[1] / ph[0],
+                            "draft_steps": [fig(ph[2 + i], spb[i]) for i in range(gamma)]},
+           "chained": {"verify_collect_scored": fig(t["verify"] / chain, vb),
+                       "select_topk_scored_us": t["select"] / chain * 1e6,
+                       "select_over_verify": t["select"] / t["verify"],
+                       "sparse_draft_step": fig(t["draft"] / chain, statistics.mean(spb))},
+           "timing": "CUDA graphs, L2 flushed before every replay, medians of %d replays; "
+                     "in_iteration: event records between the calls of the iteration graph; "
+                     "chained: %d calls of one kind in one graph" % (reps, chain),
+           "shape": {"B": B, "P": w.P, "Hq": Hq, "Hkv": w.Hkv, "d": d, "gamma": gamma,
+                     "k": w.k}}
+    del graphs
+    return res
 
 
 def run_cpu_baseline_loop(w, batches, layers_sample=4):
@@ -962,17 +1098,66 @@ def run_reference(args, world, rank):
     }
 
 
+def profile_call(args):
+    """One libvsd call of a single-layer workload, --warmup untimed then --steps more
+    times, nothing else: the command an ncu capture runs (few launches, few GB)."""
+    import sparse_attention_speculative_gb300 as vsd
+    from sparse_attention_speculative_gb300 import build as pkg_build
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import ALL
+    pkg_build.build()
+    vsd.load()
+    w = ALL[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    batch = make_batch(w, dev)
+    B, R, gamma = w.B, w.R, w.gamma
+    out, logits, partial, score, hist = vsd.vsd_verify_attn_collect_scored(
+        batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+        P_max=w.P_max, scale=w.scale)
+    idx, n_sel = vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k,
+                                            n_sink=w.n_sink, n_recent=w.n_recent)
+    seq_len = batch.prefix_len + R
+    for _ in range(args.warmup + args.steps):
+        if args.profile_call == "verify":
+            vsd.vsd_verify_attn_collect_scored(batch.q, batch.k_cache, batch.v_cache,
+                                               batch.block_table, batch.prefix_len,
+                                               P_max=w.P_max, scale=w.scale, logits=logits,
+                                               partial=partial, score=score, score_hist=hist,
+                                               out=out)
+        elif args.profile_call == "select":
+            vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                       n_recent=w.n_recent, idx=idx, n_sel=n_sel)
+        else:
+            vsd.vsd_sparse_decode_attn(batch.q_draft[0], batch.k_cache, batch.v_cache,
+                                       batch.block_table, idx, n_sel, batch.prefix_len,
+                                       seq_len, scale=w.scale, max_tail=2 * gamma + 1)
+    torch.cuda.synchronize()
+    status = vsd.vsd_read_device_status()
+    if status:
+        raise RuntimeError("device status 0x%x" % status)
+    print("profile-call %s on %s: %d calls" % (args.profile_call, w.name,
+                                               args.warmup + args.steps))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="qwen3_8b_32k")
+    ap.add_argument("--workload", default="qwen3_8b_36layer_loop")
     ap.add_argument("--impl", default="vsd", choices=["vsd", "reference"])
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--profile-call", choices=["verify", "select", "draft"], default=None,
+                    help="run one call of the workload --steps times and exit (for ncu)")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the single-layer configurations' per-call figures (loop only)")
     args = ap.parse_args()
     world, rank, local = dist_env()
+    if args.profile_call:
+        profile_call(args)
+        return
     if args.impl == "reference":
         res = run_reference(args, world, rank)
         if res is not None:
@@ -984,13 +1169,12 @@ def main():
     from sparse_attention_speculative_gb300.workloads import ALL
     w = ALL[args.workload]
     if w.layers > 1:
-        res, batches = run_gpu_loop(args, world, rank, local)
+        res = run_gpu_loop(args, world, rank, local)
     else:
         res, batch = run_gpu(args, world, rank, local)
+        if rank == 0 and args.cpu_baseline:
+            res["cpu_baseline"] = run_cpu_baseline(w, batch)
     if rank == 0:
-        if args.cpu_baseline:
-            res["cpu_baseline"] = (run_cpu_baseline_loop(w, batches) if w.layers > 1
-                                   else run_cpu_baseline(w, batch))
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.barrier()

@@ -397,6 +397,53 @@ vsd_status vsd_block_topk(const vsd_geom* geom, int R, const void* q, const floa
                           float* scores, int32_t* blocks, void* stream);
 
 /* ------------------------------------------------------------------------------
+ * Cache bookkeeping of a decode iteration (Vegas summary, sec. 2 core mechanism: each
+ * iteration verifies the drafts with a full forward pass, selects from it and drafts
+ * from the selection; sec. 3 integration: the drafts come from repeated forward passes
+ * of the target model).  Every forward pass stores the keys and values of the tokens
+ * it processes in the paged cache before their attention reads them, and the number of
+ * drafts a verification accepts moves each sequence's prefix forward.
+ *
+ * vsd_append_kv: for every sequence b, token t < n_new and KV head g,
+ *   K[b, p, g, :] = k_new[b][t][g][:],  V[b, p, g, :] = v_new[b][t][g][:],
+ *   p = pos_base[b] + pos_offset + t   (stored through the block table)
+ *   k_new, v_new  bf16 [B][n_new][Hkv][head_dim]
+ *   pos_base      int32 [B] (device); pos_offset a host integer (e.g. 0 with
+ *                 pos_base = prefix_len for the verify block, or -1 with pos_base =
+ *                 seq_len for the newest token of a draft step)
+ *   k_cache, v_cache written in place; nothing else is read or written
+ * A position outside [0, max_blocks_per_seq * page_size) is skipped and flagged
+ * VSD_DEV_BAD_LENGTH; a block-table entry outside [0, num_blocks), VSD_DEV_BAD_BLOCK.
+ *
+ * vsd_advance_lengths: after a verification that accepted a_b = accepted[b] of the
+ * gamma drafts of sequence b (0 <= a_b <= gamma), with P = prefix_len[b]:
+ *   prefix_len[b]        = P + a_b + 1   (the verify block's first token and the
+ *                                          accepted drafts join the prefix)
+ *   tail_start[b]        = P
+ *   seq_len[i * B + b]   = P + a_b + 2 + i   for draft step i < gamma (the attended
+ *                          dense tail of step i: the accepted tokens, the bonus token
+ *                          and the inputs of steps 0 .. i)
+ *   prefix_copies[r * B + b] = P + a_b + 1   for r < n_copies (e.g. the per-(layer,
+ *                          sequence) prefix lengths of a multi-layer selection)
+ *   accepted int32 [B]; prefix_len, tail_start int32 [B]; seq_len int32 [gamma][B];
+ *   prefix_copies int32 [n_copies][B] or NULL when n_copies == 0 (all device memory)
+ * A count outside [0, gamma], a negative prefix or a new prefix above max_prefix
+ * (a host integer: the longest prefix the caches can take) is flagged
+ * VSD_DEV_BAD_LENGTH and that sequence keeps its prefix (tail_start = P, seq_len
+ * P + 1 + i, prefix_len and its copies P).
+ *
+ * Both are programmatic dependents of the preceding kernel on the stream: they wait
+ * for its results before reading or writing anything.
+ * ------------------------------------------------------------------------------ */
+vsd_status vsd_append_kv(const vsd_geom* geom, int n_new, const void* k_new, const void* v_new,
+                         const int32_t* block_table, const int32_t* pos_base, int pos_offset,
+                         void* k_cache, void* v_cache, void* stream);
+
+vsd_status vsd_advance_lengths(int B, int gamma, const int32_t* accepted, int max_prefix,
+                               int32_t* prefix_len, int32_t* tail_start, int32_t* seq_len,
+                               int n_copies, int32_t* prefix_copies, void* stream);
+
+/* ------------------------------------------------------------------------------
  * vsd_copy: dst <- src as a kernel on `stream` (a programmatic dependent of the
  * preceding kernel).  Either pointer may be pinned host memory, which the device
  * addresses directly; a decode loop moves its inputs in and its results out this way.

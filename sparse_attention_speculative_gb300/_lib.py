@@ -82,6 +82,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_select_topk_scored.argtypes = [I, P, P, P, I, I, I, I, P, P, P]
         lib.vsd_page_key_means.argtypes = [GP, P, P, P, P, I, P, P]
         lib.vsd_copy.argtypes = [P, P, SZ, P]
+        lib.vsd_append_kv.argtypes = [GP, I, P, P, P, P, I, P, P, P]
+        lib.vsd_advance_lengths.argtypes = [I, I, P, I, P, P, P, I, P, P]
         lib.vsd_block_topk.argtypes = [GP, I, P, P, P, I, I, F, P, P, P]
         lib.vsd_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
         lib.vsd_get_error_string.argtypes = [I]
@@ -96,6 +98,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                      "vsd_select_workspace_size", "vsd_select_topk", "vsd_sparse_workspace_size",
                      "vsd_sparse_decode_attn", "vsd_page_key_means", "vsd_block_topk",
                      "vsd_verify_attn_collect_scored", "vsd_select_topk_scored", "vsd_copy",
+                     "vsd_append_kv", "vsd_advance_lengths",
                      "vsd_read_device_status", "vsd_last_cuda_error"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -532,3 +535,42 @@ def vsd_copy(dst, src, stream=None):
         raise ValueError("vsd_copy: size mismatch")
     _check(lib.vsd_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "vsd_copy")
     return dst
+
+
+def vsd_append_kv(k_new, v_new, k_cache, v_cache, block_table, pos_base, *, pos_offset: int = 0,
+                  stream=None):
+    """Store K/V rows k_new, v_new: bf16 [B, n_new, Hkv, d] at positions
+    pos_base[b] + pos_offset + t of each sequence (through the block table)."""
+    lib = load()
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(v_new, torch.bfloat16, "v_new")
+    _need(pos_base, torch.int32, "pos_base")
+    B, n_new = int(k_new.shape[0]), int(k_new.shape[1])
+    if tuple(v_new.shape) != tuple(k_new.shape):
+        raise ValueError("k_new and v_new shapes differ")
+    geom = geom_for(B, int(k_cache.shape[1]), k_cache, block_table)
+    rc = lib.vsd_append_kv(ctypes.byref(geom), n_new, _ptr(k_new), _ptr(v_new), _ptr(block_table),
+                           _ptr(pos_base), int(pos_offset), _ptr(k_cache), _ptr(v_cache),
+                           _stream(stream))
+    _check(rc, "vsd_append_kv")
+
+
+def vsd_advance_lengths(accepted, prefix_len, tail_start, seq_len, *, max_prefix: int,
+                        prefix_copies=None, stream=None):
+    """After a verification that accepted accepted[b] drafts: prefix_len += accepted + 1,
+    tail_start = the old prefix, seq_len[i] = old prefix + accepted + 2 + i, and every row
+    of prefix_copies ([n_copies, B]) = the new prefix.  All int32 device tensors."""
+    lib = load()
+    for t, name in ((accepted, "accepted"), (prefix_len, "prefix_len"),
+                    (tail_start, "tail_start"), (seq_len, "seq_len")):
+        _need(t, torch.int32, name)
+    B = int(prefix_len.shape[0])
+    gamma = int(seq_len.shape[0])
+    n_copies = 0
+    if prefix_copies is not None:
+        _need(prefix_copies, torch.int32, "prefix_copies")
+        n_copies = prefix_copies.numel() // max(B, 1)
+    rc = lib.vsd_advance_lengths(B, gamma, _ptr(accepted), int(max_prefix), _ptr(prefix_len),
+                                 _ptr(tail_start), _ptr(seq_len), n_copies, _ptr(prefix_copies),
+                                 _stream(stream))
+    _check(rc, "vsd_advance_lengths")

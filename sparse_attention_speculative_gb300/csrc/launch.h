@@ -121,6 +121,35 @@ struct SparseVerifyArgs {
 int sparse_verify_pages(int k_max, int R);
 cudaError_t launch_sparse_verify_gather(const SparseVerifyArgs& a, cudaStream_t stream);
 
+// ---------------------------------------------------------------- cache bookkeeping
+// K/V rows [B][n_new][Hkv][d] stored at positions pos_base[b] + pos_offset + t.
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  const int32_t* block_table;
+  const int32_t* pos_base;
+  void* k_cache;
+  void* v_cache;
+  unsigned* status;
+  int B, n_new, Hkv, d, max_blocks, num_blocks, pos_offset;
+};
+
+cudaError_t launch_append_kv(const AppendArgs& a, cudaStream_t stream);
+
+// prefix_len[b] += accepted[b] + 1; tail_start[b] = old prefix; seq_len[i][b] = old
+// prefix + accepted[b] + 2 + i; prefix_copies[r][b] = new prefix.
+struct AdvanceArgs {
+  const int32_t* accepted;
+  int32_t* prefix_len;
+  int32_t* tail_start;
+  int32_t* seq_len;
+  int32_t* prefix_copies;
+  unsigned* status;
+  int B, gamma, max_prefix, n_copies;
+};
+
+cudaError_t launch_advance(const AdvanceArgs& a, cudaStream_t stream);
+
 // ---------------------------------------------------------------- copies
 // dst <- src, `bytes` a multiple of 16, both 16-byte aligned; either may be pinned host
 // memory (addressable from the device).

@@ -668,6 +668,71 @@ vsd_status vsd_copy(void* dst, const void* src, size_t bytes, void* stream) {
   return VSD_OK;
 }
 
+vsd_status vsd_append_kv(const vsd_geom* geom, int n_new, const void* k_new, const void* v_new,
+                         const int32_t* block_table, const int32_t* pos_base, int pos_offset,
+                         void* k_cache, void* v_cache, void* stream) {
+  vsd_status st = check_geom(geom);
+  if (st != VSD_OK) return st;
+  if (n_new < 0) return VSD_ERR_INVALID_ARG;
+  if (geom->B == 0 || n_new == 0) return VSD_OK;
+  if (!k_new || !v_new || !block_table || !pos_base || !k_cache || !v_cache)
+    return VSD_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(block_table, 4) || !aligned(pos_base, 4))
+    return VSD_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  st = device_info(&status, nullptr);
+  if (st != VSD_OK) return st;
+  vsd::AppendArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.block_table = block_table;
+  a.pos_base = pos_base;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.status = status;
+  a.B = geom->B;
+  a.n_new = n_new;
+  a.Hkv = geom->Hkv;
+  a.d = geom->head_dim;
+  a.max_blocks = geom->max_blocks_per_seq;
+  a.num_blocks = geom->num_blocks;
+  a.pos_offset = pos_offset;
+  cudaError_t e = vsd::launch_append_kv(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
+vsd_status vsd_advance_lengths(int B, int gamma, const int32_t* accepted, int max_prefix,
+                               int32_t* prefix_len, int32_t* tail_start, int32_t* seq_len,
+                               int n_copies, int32_t* prefix_copies, void* stream) {
+  if (B < 0 || gamma < 0 || n_copies < 0 || max_prefix < 0) return VSD_ERR_INVALID_ARG;
+  if (B == 0) return VSD_OK;
+  if (!accepted || !prefix_len || !tail_start || (gamma > 0 && !seq_len) ||
+      (n_copies > 0 && !prefix_copies))
+    return VSD_ERR_INVALID_ARG;
+  if (!aligned(accepted, 4) || !aligned(prefix_len, 4) || !aligned(tail_start, 4) ||
+      !aligned(seq_len, 4) || !aligned(prefix_copies, 4))
+    return VSD_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  vsd_status st = device_info(&status, nullptr);
+  if (st != VSD_OK) return st;
+  vsd::AdvanceArgs a;
+  a.accepted = accepted;
+  a.prefix_len = prefix_len;
+  a.tail_start = tail_start;
+  a.seq_len = seq_len;
+  a.prefix_copies = n_copies > 0 ? prefix_copies : nullptr;
+  a.status = status;
+  a.B = B;
+  a.gamma = gamma;
+  a.max_prefix = max_prefix;
+  a.n_copies = n_copies;
+  cudaError_t e = vsd::launch_advance(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return VSD_OK;
+}
+
 vsd_status vsd_page_key_means(const vsd_geom* geom, const void* k_cache,
                               const int32_t* block_table, const int32_t* prefix_len,
                               const int32_t* page_begin, int page_blocks_max,

@@ -92,4 +92,10 @@ LOOP_36L = Workload("qwen3_8b_36layer_loop", B=4, P=65536, Hq=32, Hkv=8, d=128, 
                     k=4096, n_sink=16, n_recent=256, planted_frac=0.01, seed=5, layers=36,
                     iterations=50)
 
-ALL = {w.name: w for w in (TINY, QWEN3_8B_32K, QWEN25_72B_B16_32K, LONG_128K, LOOP_36L)}
+# One layer of that loop at its initial prefix (the shape of one verification call of the
+# loop; a few GB, small enough for profiler captures).
+LOOP_LAYER = Workload("qwen3_8b_loop_layer", B=4, P=65536, Hq=32, Hkv=8, d=128, gamma=5,
+                      k=4096, n_sink=16, n_recent=256, planted_frac=0.01, seed=5)
+
+ALL = {w.name: w for w in (TINY, QWEN3_8B_32K, QWEN25_72B_B16_32K, LONG_128K, LOOP_36L,
+                           LOOP_LAYER)}

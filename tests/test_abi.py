@@ -119,3 +119,29 @@ def test_sparse_workspace_holds_aligned_split_slots(lib, d, G):
     assert header * 4 % 16 == 0 and slot * 4 % 16 == 0
     counters = -(-B * Hkv * 4 // 256) * 256
     assert size.value == counters + B * Hkv * splits * slot * 4
+
+
+def test_append_rejects_bad_arguments(lib):
+    g = _geom()
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    # a missing cache pointer, a negative row count, a misaligned row buffer
+    assert lib.vsd_append_kv(ctypes.byref(g), 4, p, p, p, p, 0, None, p, None) == -1
+    assert lib.vsd_append_kv(ctypes.byref(g), -1, p, p, p, p, 0, p, p, None) == -1
+    q = ctypes.c_void_p(p.value + 4)
+    assert lib.vsd_append_kv(ctypes.byref(g), 4, q, p, p, p, 0, p, p, None) == -1
+    # nothing to store: no launch, no device needed
+    assert lib.vsd_append_kv(ctypes.byref(g), 0, None, None, None, None, 0, None, None,
+                             None) == 0
+    assert lib.vsd_append_kv(ctypes.byref(_geom(head_dim=96)), 4, p, p, p, p, 0, p, p,
+                             None) == -2
+
+
+def test_advance_rejects_bad_arguments(lib):
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    assert lib.vsd_advance_lengths(4, 5, None, 100, p, p, p, 0, None, None) == -1
+    assert lib.vsd_advance_lengths(4, 5, p, 100, p, p, p, 3, None, None) == -1
+    assert lib.vsd_advance_lengths(-1, 5, p, 100, p, p, p, 0, None, None) == -1
+    assert lib.vsd_advance_lengths(4, -1, p, 100, p, p, p, 0, None, None) == -1
+    assert lib.vsd_advance_lengths(0, 5, None, 100, None, None, None, 0, None, None) == 0

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def test_bench_calls_only_exported_names():
     import sparse_attention_speculative_gb300 as vsd
     src = open(os.path.join(ROOT, "bench.py")).read()
-    names = set(re.findall(r"\bvsd\.(\w+)", src))
+    names = set(re.findall(r"(?<![/\w\"])vsd\.(\w+)", src))
     missing = sorted(n for n in names if not hasattr(vsd, n))
     assert not missing, "bench.py uses names the package does not export: %s" % missing
 
@@ -79,3 +79,30 @@ def test_algorithmic_bytes_match_the_configuration_table():
     assert abs(L * vb / 1e9 - 41.1) / 41.1 < 0.01
     assert abs(L * sb / 1e9 - 0.30) / 0.30 < 0.02
     assert all(abs(L * x / 1e9 - 2.42) / 2.42 < 0.01 for x in spb)
+
+
+def test_loop_run_bytes_follow_the_growing_prefix():
+    """A decode run's bytes: the first iteration is the configuration's iteration at P
+    (plus the appends), and every iteration's prefix is the previous one plus the
+    accepted drafts plus one."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from sparse_attention_speculative_gb300.workloads import LOOP_36L as w
+    acc = [[(i + b) % (w.gamma + 1) for b in range(w.B)] for i in range(w.iterations)]
+    run = bench.loop_run_bytes(w, acc)
+    assert len(run) == w.iterations
+    vb, sb, spb = bench.iteration_bytes(w, list(w.prefix()), [w.k] * w.B,
+                                        [[acc[0][b] + 2 + i for b in range(w.B)]
+                                         for i in range(w.gamma)])
+    assert run[0]["verify"] == w.layers * vb and run[0]["select"] == w.layers * sb
+    assert run[0]["sparse"] == w.layers * sum(spb)
+    # appends: (R + gamma) rows of K and V per sequence and KV head, read and written
+    assert run[0]["append"] == w.layers * 4 * w.B * (w.R + w.gamma) * w.Hkv * w.d * 2
+    for i in range(1, w.iterations):
+        assert run[i]["prefix"] == [p + a + 1 for p, a in zip(run[i - 1]["prefix"], acc[i - 1])]
+    assert run[-1]["verify"] > run[0]["verify"]
+
+
+def test_bench_defaults_to_the_decode_loop():
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    assert 'default="qwen3_8b_36layer_loop"' in src
