@@ -666,7 +666,7 @@ def run_gpu_loop(args, world, rank, local):
     torch.cuda.set_device(dev)
     NL, B, R, Hq, Hkv, d, gamma = w.layers, w.B, w.R, w.Hq, w.Hkv, w.d, w.gamma
     iters = w.iterations
-    P_max = (max(w.prefix()) + iters * R + 3) // 4 * 4
+    P_max = max(w.prefix()) + iters * R  # the longest prefix of a run
     batches = [make_batch(w, dev, layer=l, extra_capacity=iters * R + 2 * R)
                for l in range(NL)]
     loop = vsd.DecodeLoop([bt.k_cache for bt in batches], [bt.v_cache for bt in batches],

@@ -97,7 +97,11 @@ typedef struct vsd_geom {
  *   prefix_len     int32 [B]; 0 <= P_b <= P_max and P_b + R <= max_blocks*page_size
  *   collect_row0/1 verify rows whose logits are collected (0 and R-1 = gamma for
  *                  the first draft token and the bonus token); in [0, R)
- *   P_max          row stride of logits / partial_scores (upper bound of P_b)
+ *   P_max          row stride of logits / partial_scores (upper bound of P_b); a
+ *                  multiple of 32 keeps every row on a 128-byte boundary, which the
+ *                  stores need to cover whole 32-byte sectors (rows that start inside
+ *                  a sector cost DRAM read-modify-writes: about 15 % of the call on a
+ *                  64K-position batch of 4)
  *   scale          softmax scale (1/sqrt(head_dim) normally)
  *   logits         fp32 [B][2][Hq][P_max] or NULL; only j < P_b are written
  *   partial_scores fp32 [B][Hkv][P_max] or NULL; only j < P_b are written
@@ -317,6 +321,57 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
                                   const int32_t* tail_start, const int32_t* seq_len,
                                   int max_tail, float scale, void* out, void* workspace,
                                   size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * A draft step of a decode loop (Vegas summary, sec. 2 drafting phase and sec. 3
+ * integration: the drafts come from repeated forward passes of the target model with
+ * sparse attention; each pass processes one new token, whose keys and values join the
+ * cache before its attention reads them).
+ *
+ * The same attention as vsd_sparse_decode_attn, with these options:
+ *   k_new, v_new   bf16 [B][Hkv][head_dim] or both NULL: the keys and values of the
+ *                  step's input token, stored at position seq_len[b] - 1 of the cache
+ *                  (the last position of the dense tail, so tail_start[b] < seq_len[b]
+ *                  is required for it) and attended from these buffers; the result is
+ *                  the call on the cache after the store.  k_cache / v_cache are
+ *                  written at that position only.
+ *   sel_rows       int32 [B][k_max] (device) or NULL; with flags:
+ *     VSD_STEP_RECORD_ROWS  the call also writes, for every selected position
+ *                  i < n_sel[b], the cache row base of idx[b][i] (block * Hkv *
+ *                  page_size + offset within the page; -1 for an invalid index or block)
+ *     VSD_STEP_REUSE_ROWS   the call reads those row bases instead of resolving idx
+ *                  through the block table: the later steps of one selection (the same
+ *                  idx, n_sel and block table as the recording call); an entry outside
+ *                  the cache is skipped and flagged VSD_DEV_BAD_INDEX
+ *   flags          also:
+ *     VSD_STEP_EARLY_GATHER  the selection and the tail are resolved and gathered before
+ *                  the call waits for the preceding kernel on the stream (which hides the
+ *                  gather behind that kernel's last microseconds).  The caller promises
+ *                  that the preceding kernel writes none of idx, n_sel, tail_start,
+ *                  seq_len, block_table and sel_rows, nor any cache row this call reads
+ *                  except at seq_len[b] - 1, and that it is a kernel of this library or a
+ *                  kernel launched without programmatic dependent launch.  (Every kernel
+ *                  of this library lets its dependents start only after its own wait for
+ *                  its predecessor, so anything written two launches earlier is complete.)
+ *                  q, k_new / v_new, the workspace and out are always touched after the
+ *                  wait.
+ * Every other argument, result and rule as vsd_sparse_decode_attn (the workspace may be
+ * shared with it).  Supported: as vsd_sparse_decode_attn, with num_blocks * Hkv *
+ * page_size < 2^31 (VSD_ERR_UNSUPPORTED otherwise); RECORD and REUSE together, or an
+ * unknown flag, are VSD_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------------ */
+#define VSD_STEP_RECORD_ROWS 0x1u
+#define VSD_STEP_REUSE_ROWS 0x2u
+#define VSD_STEP_EARLY_GATHER 0x4u
+
+vsd_status vsd_sparse_decode_attn_step(const vsd_geom* geom, const void* q, const void* k_new,
+                                       const void* v_new, void* k_cache, void* v_cache,
+                                       const int32_t* block_table, const int32_t* idx,
+                                       const int32_t* n_sel, int k_max,
+                                       const int32_t* tail_start, const int32_t* seq_len,
+                                       int max_tail, int32_t* sel_rows, unsigned flags,
+                                       float scale, void* out, void* workspace,
+                                       size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------
  * Sparse verification (Dustin summary, "Verification workflow", steps 3-4: a

@@ -10,6 +10,7 @@ device (``decode_loop.py``), the workload
 table (``workloads.py``) and the seeded input generators (``synth.py``).
 """
 from ._lib import (DEV_BAD_BLOCK, DEV_BAD_INDEX, DEV_BAD_LENGTH, DEV_TIMEOUT, Geom,  # noqa: F401
+                   STEP_EARLY_GATHER, STEP_RECORD_ROWS, STEP_REUSE_ROWS,
                    VsdError, geom_for, load, vsd_read_device_status, vsd_select_topk,
                    vsd_sparse_decode_attn, vsd_sparse_workspace_size, vsd_verify_attn_collect,
                    vsd_select_topk_hybrid, vsd_sparse_verify_attn,
@@ -18,6 +19,6 @@ from ._lib import (DEV_BAD_BLOCK, DEV_BAD_INDEX, DEV_BAD_LENGTH, DEV_TIMEOUT, Ge
                    vsd_verify_attn_collect_noalloc, vsd_verify_workspace_size,
                    page_blocks, vsd_page_key_means, vsd_block_topk,
                    vsd_verify_attn_collect_scored, vsd_select_topk_scored, HIST_BINS,
-                   vsd_copy, vsd_append_kv, vsd_advance_lengths)
+                   vsd_copy, vsd_append_kv, vsd_advance_lengths, vsd_sparse_decode_attn_step)
 from .decode_loop import DecodeLoop  # noqa: F401
 from .iteration import IterationGraph  # noqa: F401

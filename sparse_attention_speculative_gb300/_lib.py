@@ -31,6 +31,9 @@ DEV_BAD_BLOCK = 0x1
 DEV_BAD_INDEX = 0x2
 DEV_BAD_LENGTH = 0x4
 DEV_TIMEOUT = 0x8
+STEP_RECORD_ROWS = 0x1
+STEP_REUSE_ROWS = 0x2
+STEP_EARLY_GATHER = 0x4
 
 
 class VsdError(RuntimeError):
@@ -83,6 +86,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_page_key_means.argtypes = [GP, P, P, P, P, I, P, P]
         lib.vsd_copy.argtypes = [P, P, SZ, P]
         lib.vsd_append_kv.argtypes = [GP, I, P, P, P, P, I, P, P, P]
+        lib.vsd_sparse_decode_attn_step.argtypes = [GP, P, P, P, P, P, P, P, P, I, P, P, I, P,
+                                                    ctypes.c_uint, F, P, P, SZ, P]
         lib.vsd_advance_lengths.argtypes = [I, I, P, I, P, P, P, I, P, P]
         lib.vsd_block_topk.argtypes = [GP, I, P, P, P, I, I, F, P, P, P]
         lib.vsd_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
@@ -98,7 +103,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                      "vsd_select_workspace_size", "vsd_select_topk", "vsd_sparse_workspace_size",
                      "vsd_sparse_decode_attn", "vsd_page_key_means", "vsd_block_topk",
                      "vsd_verify_attn_collect_scored", "vsd_select_topk_scored", "vsd_copy",
-                     "vsd_append_kv", "vsd_advance_lengths",
+                     "vsd_append_kv", "vsd_advance_lengths", "vsd_sparse_decode_attn_step",
                      "vsd_read_device_status", "vsd_last_cuda_error"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -574,3 +579,40 @@ def vsd_advance_lengths(accepted, prefix_len, tail_start, seq_len, *, max_prefix
                                  _ptr(tail_start), _ptr(seq_len), n_copies, _ptr(prefix_copies),
                                  _stream(stream))
     _check(rc, "vsd_advance_lengths")
+
+
+def vsd_sparse_decode_attn_step(q, k_cache, v_cache, block_table, idx, n_sel, tail_start, seq_len,
+                                *, scale: float, max_tail: int, k_new=None, v_new=None,
+                                sel_rows=None, flags: int = 0, out=None, workspace=None,
+                                stream=None):
+    """A draft step of a decode loop: the step's input token (k_new, v_new: bf16
+    [B, Hkv, d]) is stored at seq_len - 1 and attended; sel_rows (int32 [B, k_max]) caches
+    the selection's cache rows (STEP_RECORD_ROWS writes them, STEP_REUSE_ROWS reads
+    them); STEP_EARLY_GATHER gathers before waiting for the preceding kernel (see
+    include/vsd.h for what the caller promises with it)."""
+    lib = load()
+    B, Hq, d = q.shape
+    _need(q, torch.bfloat16, "q")
+    _need(tail_start, torch.int32, "tail_start")
+    _need(seq_len, torch.int32, "seq_len")
+    if k_new is not None:
+        _need(k_new, torch.bfloat16, "k_new")
+        _need(v_new, torch.bfloat16, "v_new")
+    if sel_rows is not None:
+        _need(sel_rows, torch.int32, "sel_rows")
+    geom = geom_for(B, Hq, k_cache, block_table)
+    k_max = 0 if idx is None else int(idx.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = _workspace(vsd_sparse_workspace_size(geom, k_max, max_tail), q.device,
+                               "sparse")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.vsd_sparse_decode_attn_step(ctypes.byref(geom), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                         _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                         _ptr(idx), _ptr(n_sel), k_max, _ptr(tail_start),
+                                         _ptr(seq_len), int(max_tail), _ptr(sel_rows),
+                                         int(flags), float(scale), _ptr(out), _ptr(workspace),
+                                         ws_bytes, _stream(stream))
+    _check(rc, "vsd_sparse_decode_attn_step")
+    return out

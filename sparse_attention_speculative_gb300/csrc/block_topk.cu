@@ -54,21 +54,21 @@ __global__ void __launch_bounds__(kMeanWarps * 32) page_mean_kernel(const BlockT
   const int beta = blockIdx.x * kMeanWarps + w;
   ptx::pdl_launch_dependents();
   ptx::pdl_wait_primary();  // the cache and the lengths may come from the preceding kernel
-  const int P = __ldg(a.prefix_len + b);
+  const int P = __ldcg(a.prefix_len + b);
   const int nblk = (P + kPageB - 1) / kPageB;
   if (P < 0 || static_cast<long long>(P) > static_cast<long long>(a.max_blocks) * kPageB ||
       nblk > a.nblk_max) {
     if (threadIdx.x == 0 && g == 0 && blockIdx.x == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
     return;
   }
-  int first = a.page_begin != nullptr ? __ldg(a.page_begin + b) : 0;
+  int first = a.page_begin != nullptr ? __ldcg(a.page_begin + b) : 0;
   if (first < 0) {
     if (threadIdx.x == 0 && g == 0 && blockIdx.x == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
     return;
   }
   if (beta < first || beta >= nblk) return;
   const int n_rows = min(kPageB, P - beta * kPageB);
-  const int blk = __ldg(a.block_table + static_cast<size_t>(b) * a.max_blocks + beta);
+  const int blk = __ldcg(a.block_table + static_cast<size_t>(b) * a.max_blocks + beta);
   float* dst = a.kbar + ((static_cast<size_t>(b) * a.Hkv + g) * a.nblk_max + beta) * D;
   const int col = lane % CPR, row0 = lane / CPR;
   float acc[8];
@@ -188,11 +188,11 @@ __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
   bool in_flight = false;  // thread 0: a copy into the buffer has not been waited for
   bool timed_out = false;
   int staged_bg = -1;
-  int P_next = first < last ? __ldg(a.prefix_len + first / ntile / a.Hkv) : 0;
+  int P_next = first < last ? __ldcg(a.prefix_len + first / ntile / a.Hkv) : 0;
   for (int id = first; id < last; ++id) {
     const int x = id % ntile, bg = id / ntile, g = bg % a.Hkv, b = bg / a.Hkv;
     const int P = P_next;
-    if (id + 1 < last) P_next = __ldg(a.prefix_len + (id + 1) / ntile / a.Hkv);
+    if (id + 1 < last) P_next = __ldcg(a.prefix_len + (id + 1) / ntile / a.Hkv);
     if ((P < 0 || pages_of(P) > a.nblk_max) && t == 0 && g == 0 && x == 0)
       flag_status(a.status, VSD_DEV_BAD_LENGTH);
     if (!has_work(id, P)) continue;  // CTA-uniform; nothing was fetched for it
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
         const int i = t + u * kTcScoreThreads, r = i / (D / 8), c8 = i % (D / 8);
         qv[u] = make_uint4(0, 0, 0, 0);
         if (r < RG)
-          qv[u] = __ldg(reinterpret_cast<const uint4*>(
+          qv[u] = __ldcg(reinterpret_cast<const uint4*>(
               qb + ((static_cast<size_t>(b) * a.R + r / G) * a.Hq + g * G + r % G) * D + c8 * 8));
       }
 #pragma unroll
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 6 : 1) block_select_kernel(con
   int32_t* out = a.blocks + static_cast<size_t>(row) * a.kb;
   ptx::pdl_launch_dependents();
   ptx::pdl_wait_primary();  // the scores come from the preceding kernel
-  const int P = __ldg(a.prefix_len + b);
+  const int P = __ldcg(a.prefix_len + b);
   int nblk = (P + kPageB - 1) / kPageB;
   if (P < 0 || nblk > a.nblk_max) nblk = 0;  // flagged by the score kernel
   if (nblk <= a.kb) {  // every page is kept
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 6 : 1) block_select_kernel(con
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
   for (int m = 0; m < ITEMS; ++m) {
-    key[m] = m < n_mine ? order_key(__ldg(sc + j0 + m)) : 0u;
+    key[m] = m < n_mine ? order_key(__ldcg(sc + j0 + m)) : 0u;
     if (m < n_mine) {
       kmin = min(kmin, key[m]);
       kmax = max(kmax, key[m]);

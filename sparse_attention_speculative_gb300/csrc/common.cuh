@@ -31,26 +31,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
-// Streaming 16-byte load that skips L1 allocation (data used once).
+// Loads of anything a preceding kernel may have written.  Every kernel here is a
+// programmatic dependent of its predecessor, so such data is read only after the wait
+// for it, and never through the non-coherent read-only path: a load the compiler treats
+// as read-only for the kernel's lifetime may be moved above that wait.  These go to L2
+// (the data is used once or is small).
 __device__ __forceinline__ uint4 ldg_stream16(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "l"(p)
+               : "memory");
   return v;
 }
 
 __device__ __forceinline__ uint2 ldg_stream8(const void* p) {
   uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-               : "=r"(v.x), "=r"(v.y)
-               : "l"(p));
+  asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
   return v;
 }
 
 __device__ __forceinline__ uint32_t ldg_stream4(const void* p) {
   uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 

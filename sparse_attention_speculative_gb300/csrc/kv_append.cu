@@ -48,12 +48,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const AppendP
     const long long bt = row / a.Hkv;
     const int t = static_cast<int>(bt % a.n_new);
     const int b = static_cast<int>(bt / a.n_new);
-    const long long pos = static_cast<long long>(__ldg(a.pos_base + b)) + a.pos_offset + t;
+    const long long pos = static_cast<long long>(__ldcg(a.pos_base + b)) + a.pos_offset + t;
     if (pos < 0 || pos >= static_cast<long long>(a.max_blocks) * kPageA) {
       if (c == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
       continue;
     }
-    const int blk = __ldg(a.block_table + static_cast<size_t>(b) * a.max_blocks +
+    const int blk = __ldcg(a.block_table + static_cast<size_t>(b) * a.max_blocks +
                           static_cast<int>(pos / kPageA));
     if (blk < 0 || blk >= a.num_blocks) {
       if (c == 0) flag_status(a.status, VSD_DEV_BAD_BLOCK);
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kAppendThreads) advance_kernel(const AdvancePa
   for (int b = blockIdx.x * kAppendThreads + threadIdx.x; b < a.B;
        b += gridDim.x * kAppendThreads) {
     const int P = a.prefix_len[b];
-    const int acc = __ldg(a.accepted + b);
+    const int acc = __ldcg(a.accepted + b);
     // the accepted drafts and the verify block's first token join the prefix; a count
     // outside [0, gamma] or a prefix past max_prefix is refused (lengths unchanged)
     const bool ok = acc >= 0 && acc <= a.gamma && P >= 0 &&

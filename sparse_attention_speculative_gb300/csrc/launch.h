@@ -74,6 +74,13 @@ struct SparseArgs {
   const void* q;
   const void* k_cache;
   const void* v_cache;
+  const void* k_new = nullptr;  // [B][Hkv][d] the step's input token, or null
+  const void* v_new = nullptr;
+  void* k_store = nullptr;      // the caches, written at position seq_len - 1
+  void* v_store = nullptr;
+  int32_t* sel_rows = nullptr;  // [B][k_max] cache row bases of the selection
+  int rows_mode = 0;            // 0 unused, 1 resolve and write, 2 read
+  int early = 0;                // gather before waiting for the preceding kernel
   const int32_t* block_table;
   const int32_t* idx;
   const int32_t* n_sel;

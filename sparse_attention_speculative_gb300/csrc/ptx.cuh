@@ -11,6 +11,12 @@
 #ifndef VSD_WAIT_LIMIT_NS
 #define VSD_WAIT_LIMIT_NS 2000000000ull  // 2 s: far beyond any legitimate wait here
 #endif
+// Limit of the waits that drain a kernel's own asynchronous operations before it exits
+// (after a wait above gave up): these complete unless the hardware stops, so they keep
+// the full limit even in builds that shorten VSD_WAIT_LIMIT_NS.
+#ifndef VSD_DRAIN_LIMIT_NS
+#define VSD_DRAIN_LIMIT_NS 2000000000ull
+#endif
 
 namespace vsd {
 namespace ptx {
@@ -82,6 +88,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
       if (abort != nullptr && *abort) return false;
       if (global_timer_ns() - t0 > VSD_WAIT_LIMIT_NS) return false;
     }
+  }
+}
+
+// The same wait with the drain limit and no abort flag.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > VSD_DRAIN_LIMIT_NS) return false;
   }
 }
 

@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
         float4 x[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          x[u] = __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g + u) * a.P_max + j));
+          x[u] = __ldcg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g + u) * a.P_max + j));
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           s[0] += x[u].x;
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
       }
       for (; g < a.Hkv; ++g) {
         const float4 x =
-            __ldg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g) * a.P_max + j));
+            __ldcg(reinterpret_cast<const float4*>(base + static_cast<size_t>(g) * a.P_max + j));
         s[0] += x.x;
         s[1] += x.y;
         s[2] += x.z;
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
       for (int g = 0; g < a.Hkv; ++g)
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          if (j + u < a.P_max) s[u] += __ldg(base + static_cast<size_t>(g) * a.P_max + j + u);
+          if (j + u < a.P_max) s[u] += __ldcg(base + static_cast<size_t>(g) * a.P_max + j + u);
     }
   };
   const int my0 = rank * chunk + t * KPT;  // this thread's positions [my0, my0 + KPT)
@@ -352,10 +352,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   if (a.hist != nullptr) {
 #pragma unroll
     for (int i = 0; i < kHistPerThread; ++i)
-      h_pre[i] = __ldg(a.hist + static_cast<size_t>(row) * kBins0 + t + i * kSelThreads);
+      h_pre[i] = __ldcg(a.hist + static_cast<size_t>(row) * kBins0 + t + i * kSelThreads);
   }
 
-  int P = __ldg(a.prefix_len + row);
+  int P = __ldcg(a.prefix_len + row);
   if (P < 0 || P > a.P_max) {
     if (t == 0 && rank == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);
     P = 0;
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   uint32_t prot_key = 0u;
   if (a.hist != nullptr && t < n_prot) {
     const int j = t < sink_end ? t : rb + (t - sink_end);
-    prot_key = order_key(__ldg(base + j));
+    prot_key = order_key(__ldcg(base + j));
   }
   // candidates chosen beforehand (first pass of the hybrid budget) are always taken
   // and not ranked; this thread's KPT positions sit in one word of that bitmap
@@ -379,10 +379,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   if (a.pre_bitmap != nullptr) {
     const int wi = my0 >> 5;
     if (wi < a.bm_words) {
-      const uint32_t wv = __ldg(a.pre_bitmap + static_cast<size_t>(row) * a.bm_words + wi);
+      const uint32_t wv = __ldcg(a.pre_bitmap + static_cast<size_t>(row) * a.bm_words + wi);
       pre_bits = (wv >> (my0 & 31)) & (KPT >= 32 ? 0xFFFFFFFFu : ((1u << KPT) - 1u));
     }
-    n_pre = __ldg(a.pre_count + row);
+    n_pre = __ldcg(a.pre_count + row);
   }
   const int n_cand = rb - sink_end - n_pre;  // rankable candidates
   int r_need = n - (P - (rb - sink_end)) - n_pre;
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
         if (t < n_prot) atomicSub(&gh_local[prot_key >> 20], 1u);
         for (int i = t + kSelThreads; i < n_prot; i += kSelThreads) {
           const int j = i < sink_end ? i : rb + (i - sink_end);
-          atomicSub(&gh_local[order_key(__ldg(base + j)) >> 20], 1u);
+          atomicSub(&gh_local[order_key(__ldcg(base + j)) >> 20], 1u);
         }
         __syncthreads();
         find_bin(gh_local, nb, r_rem, sh);

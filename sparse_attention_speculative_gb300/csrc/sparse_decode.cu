@@ -11,10 +11,18 @@
 // flight.  The attended list of one (sequence, KV head) pair, idx[0 .. n_sel) followed
 // by [tail_start, seq_len), is cut into splits of 128 positions (more per split only
 // when the list is very long).  A pair with a single split writes its output directly;
-// otherwise each split writes (m, l, o) to the workspace and the pair's last split (a
-// per-pair counter in the workspace, reset to zero by that split) combines them, every
-// load of a round in flight at once, in split order.  Results are bit-reproducible;
-// the only atomics are the counters.  Three kernels:
+// otherwise each split (or run of splits) writes (m, l, o) to the workspace and the
+// pair's last arrival (a per-pair counter in the workspace, reset to zero by that
+// arrival) combines them, every load of a round in flight at once, in a fixed order.
+// Results are bit-reproducible; the only atomics are the counters.
+//
+// Two options serve a decode loop.  (1) The step's input token: its K/V rows (k_new,
+// v_new) are stored at position seq_len - 1, the last of the dense tail, and attended
+// from k_new / v_new directly (no other position of the call reads that cache row).
+// (2) The selection's cache rows: the first draft step after a selection writes the
+// resolved cache row of every selected position (rows_mode 1) and the later steps read
+// them (rows_mode 2), one dependent load (index -> block table) fewer per position.
+// Three kernels:
 //   * sparse_tc_kernel (splits of one 128-position batch, the common case): one split
 //     per CTA of four warps on the 5th-generation tensor cores (below); one CTA per SM
 //     when the splits fit one wave, three per SM otherwise.
@@ -57,14 +65,21 @@ struct SParams {
   const uint16_t* q;
   const uint16_t* k_cache;
   const uint16_t* v_cache;
+  const uint16_t* k_new;  // [B][Hkv][D]: K of the step's input token, or null
+  const uint16_t* v_new;
+  uint16_t* k_store;      // the caches, written at the input token's position
+  uint16_t* v_store;
   const int32_t* block_table;
   const int32_t* idx;
   const int32_t* n_sel;
   const int32_t* tail_start;
   const int32_t* seq_len;
+  int32_t* sel_rows;  // [B][k_max]: cache row base of each selected position, or null
+  int rows_mode;      // 0: sel_rows unused, 1: resolved and written, 2: read
+  int early;          // gather the list before waiting for the preceding kernel
   uint16_t* out;
   float* ws;
-  unsigned* counters;  // per pair: splits that have written their partial
+  unsigned* counters;  // per pair: splits whose partials are complete
   unsigned* status;
   int Hq, Hkv, max_blocks, num_blocks, k_max;
   int split_len;   // positions per split (a multiple of kBatch)
@@ -114,6 +129,93 @@ __device__ __forceinline__ SList attended_list(int ns, int t0, int t1, const SPa
   return L;
 }
 
+// Where list position `pos` of pair (b, g) reads its K / V row: `row` is the cache row
+// ((block * Hkv + g) * 16 + offset) or -1 (absent: zero-filled and masked); `fresh`
+// marks the step's input token, gathered from k_new / v_new and stored at `row`.
+struct SRow {
+  int row;
+  bool fresh;
+};
+
+constexpr int kEntryBadIndex = -2147483647 - 1;  // a selected index outside its sequence
+
+// Resolution of a position is split in two so that a persistent kernel can keep the
+// block-table load of its next item in flight: position_entry issues the one global
+// load a position needs (its block-table entry; with rows_mode 2 the row base an earlier
+// step recorded, which `spec` already is), position_row checks and completes it.
+// `spec` is the value loaded ahead for a selected position: idx[b][pos], or with
+// rows_mode 2 the recorded row base.
+__device__ __forceinline__ int position_entry(const SParams& a, const SList& L, int b, int pos,
+                                              int t1, int spec) {
+  int j;
+  if (pos < L.ns) {
+    if (a.rows_mode == 2) return spec;
+    if (spec < 0 || spec >= t1) return kEntryBadIndex;
+    j = spec;
+  } else {
+    j = L.t0 + (pos - L.ns);
+  }
+  return __ldcg(a.block_table + static_cast<size_t>(b) * a.max_blocks + j / kPageS);
+}
+
+// Checks flag what is wrong (VSD_DEV_BAD_INDEX, VSD_DEV_BAD_BLOCK); with rows_mode 1
+// the pairs of KV head 0 record the row base of every selected position (-1 if none).
+__device__ __forceinline__ SRow position_row(const SParams& a, const SList& L, int b, int g,
+                                             int pos, int spec, int entry) {
+  SRow r{-1, false};
+  int base = -1;
+  if (pos < L.ns && a.rows_mode == 2) {
+    const long long lim = static_cast<long long>(a.num_blocks) * a.Hkv * kPageS;
+    if (entry >= 0 && entry < lim && (entry / kPageS) % a.Hkv == 0)
+      base = entry;
+    else
+      flag_status(a.status, VSD_DEV_BAD_INDEX);
+  } else {
+    if (entry == kEntryBadIndex) {
+      flag_status(a.status, VSD_DEV_BAD_INDEX);
+    } else if (entry < 0 || entry >= a.num_blocks) {
+      flag_status(a.status, VSD_DEV_BAD_BLOCK);
+    } else {
+      const int j = pos < L.ns ? spec : L.t0 + (pos - L.ns);
+      base = entry * a.Hkv * kPageS + (j % kPageS);
+    }
+    if (pos < L.ns && a.rows_mode == 1 && g == 0)
+      a.sel_rows[static_cast<size_t>(b) * a.k_max + pos] = base;
+    if (pos >= L.ns) r.fresh = a.k_new != nullptr && pos == L.total - 1;
+  }
+  if (base >= 0)
+    r.row = base + g * kPageS;
+  else
+    r.fresh = false;
+  return r;
+}
+
+__device__ __forceinline__ SRow resolve_position(const SParams& a, const SList& L, int b, int g,
+                                                 int pos, int t1, int spec) {
+  return position_row(a, L, b, g, pos, spec, position_entry(a, L, b, pos, t1, spec));
+}
+
+// The value a selected position's resolution starts from (see position_entry).
+__device__ __forceinline__ const int32_t* spec_source(const SParams& a) {
+  return a.rows_mode == 2 ? a.sel_rows : a.idx;
+}
+
+// Store the step's input token, already gathered into row r of a 128-byte-swizzled K / V
+// tile pair in shared memory (kHalf bytes per 64-column half), into cache row `row`:
+// D / 8 16-byte chunks of K and V by one thread, no global load on its path.
+template <int D, int kHalf>
+__device__ __forceinline__ void store_fresh_from_tile(const SParams& a, const uint8_t* k_s,
+                                                      const uint8_t* v_s, int r, int row) {
+  uint4* kd = reinterpret_cast<uint4*>(a.k_store + static_cast<size_t>(row) * D);
+  uint4* vd = reinterpret_cast<uint4*>(a.v_store + static_cast<size_t>(row) * D);
+#pragma unroll
+  for (int ch = 0; ch < D / 8; ++ch) {
+    const int off = (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+    kd[ch] = *reinterpret_cast<const uint4*>(k_s + off);
+    vd[ch] = *reinterpret_cast<const uint4*>(v_s + off);
+  }
+}
+
 // One split's partial (m, l, o) in the workspace: the G heads' running max and sum,
 // padded so that the G output rows (read as float4 by the merge) start on a 16-byte
 // boundary, then the rows.
@@ -124,19 +226,21 @@ struct SSlot {
   static_assert(kFloats % 4 == 0 && D % 4 == 0, "16-byte slots");
 };
 
-// Combine the n partial (m, l, o) of one pair's splits and write its G output rows.
-// Thread t of the kSThreads that run it (`sync` is their barrier) = (float4 group of
-// (head, dims), part); part p takes splits p, p + kParts, ... with all loads of a round
-// in flight; the parts then combine in shared memory.
-// kRound: splits per load round when a thread holds one output group.
-template <int D, int G, int kSThreads, int kRound, typename Sync>
+// Combine the n partials (m, l, o) of one pair and write its G output rows: partial k
+// (k < n) is in workspace slot slot_of(k), or absent when that is negative.  Thread t
+// of the kSThreads that run it (`sync` is their barrier) = (float4 group of (head,
+// dims), part); part p takes partials p, p + kParts, ... with all loads of a round in
+// flight; the parts then combine in shared memory.
+// kRound: partials per load round when a thread holds one output group.
+template <int D, int G, int kSThreads, int kRound, typename Sync, typename SlotOf>
 __device__ __forceinline__ void merge_splits_by(const SParams& a, float* scratch, int pair, int b,
-                                                int g, int n, const int t, Sync sync) {
+                                                int g, int n, const int t, Sync sync,
+                                                SlotOf slot_of) {
   constexpr int kQ = D / 4;
   constexpr int NG = G * kQ;                              // float4 groups of the output
   constexpr int kGPT = NG > kSThreads ? NG / kSThreads : 1;  // groups per thread
   constexpr int kParts = NG >= kSThreads ? 1 : kSThreads / NG;
-  constexpr int kU = kGPT == 1 ? kRound : (16 / kGPT > 1 ? 16 / kGPT : 1);  // per load round
+  constexpr int kU = kGPT == 1 ? kRound : (kRound / kGPT > 1 ? kRound / kGPT : 1);  // per round
   static_assert(NG * kParts / kGPT == kSThreads || NG >= kSThreads, "merge layout");
   const int part = kParts > 1 ? t / NG : 0;
   const size_t stride = SSlot<D, G>::kFloats;
@@ -159,8 +263,9 @@ __device__ __forceinline__ void merge_splits_by(const SParams& a, float* scratch
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int k = k0 + u * kParts;
-        if (k < n) {
-          const float* sl = base + k * stride;
+        const int sk = k < n ? slot_of(k) : -1;
+        if (sk >= 0) {
+          const float* sl = base + static_cast<size_t>(sk) * stride;
           mk[i][u] = __ldcg(sl + hh);
           lk[i][u] = __ldcg(sl + G + hh);
           ok[i][u] = __ldcg(reinterpret_cast<const float4*>(sl + SSlot<D, G>::kO + hh * D) + q4);
@@ -244,7 +349,7 @@ __device__ __forceinline__ void merge_splits(const SParams& a, float* scratch, i
                                              int g, int n) {
   merge_splits_by<D, G, kSThreads, kRound>(a, scratch, pair, b, g, n,
                                            static_cast<int>(threadIdx.x),
-                                           [] { __syncthreads(); });
+                                           [] { __syncthreads(); }, [](int k) { return k; });
 }
 
 template <int D, int G>
@@ -262,20 +367,21 @@ __global__ void __launch_bounds__(SCfg<G>::kThreads, 1) sparse_decode_kernel(con
   const int sub = lane / LPR;  // which row of an instruction
   const int lr = lane % LPR;   // which 8 dims of the row
 
-  ptx::pdl_launch_dependents();  // the next kernel on the stream may become resident
   ptx::pdl_wait_primary();       // idx / n_sel come from the preceding kernel
+  ptx::pdl_launch_dependents();  // after the wait: see kv_append.cu
 
   // First round of loads, independent of one another: the list lengths, the first
-  // batch's indices (speculatively: used only for positions that turn out to be
-  // selected ones) and the queries.
+  // batch's indices or row bases (speculatively: used only for positions that turn out
+  // to be selected ones) and the queries.
   const int lo = split * a.split_len;
   const int wbase0 = lo + warp * kKeysPerWarp;
+  const int32_t* spec_src = spec_source(a);
   int j_spec[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int pos = wbase0 + u * KPI + sub;
-    j_spec[u] = (a.idx != nullptr && pos < a.k_max)
-                    ? __ldg(a.idx + static_cast<size_t>(b) * a.k_max + pos)
+    j_spec[u] = (spec_src != nullptr && pos < a.k_max)
+                    ? __ldcg(spec_src + static_cast<size_t>(b) * a.k_max + pos)
                     : 0;
   }
   constexpr int kQLoads = (G * D / 8 + kSThreads - 1) / kSThreads;
@@ -289,9 +395,9 @@ __global__ void __launch_bounds__(SCfg<G>::kThreads, 1) sparse_decode_kernel(con
           a.q + (static_cast<size_t>(b) * a.Hq + g * G + hh) * D + c8 * 8);
     }
   }
-  const int ns_raw = a.n_sel != nullptr ? __ldg(a.n_sel + b) : 0;
-  const int t0_raw = __ldg(a.tail_start + b);
-  const int t1 = __ldg(a.seq_len + b);
+  const int ns_raw = a.n_sel != nullptr ? __ldcg(a.n_sel + b) : 0;
+  const int t0_raw = __ldcg(a.tail_start + b);
+  const int t1 = __ldcg(a.seq_len + b);
   const SList L = attended_list(ns_raw, t0_raw, t1, a, split == 0 && g == 0 && threadIdx.x == 0);
   if (lo >= L.total && !(split == 0 && L.total == 0)) return;  // no work in this split
   const int hi = min(lo + a.split_len, L.total);
@@ -330,32 +436,35 @@ __global__ void __launch_bounds__(SCfg<G>::kThreads, 1) sparse_decode_kernel(con
   for (int wbase = wbase0; wbase < hi; wbase += kBatch) {
     // ---- list position -> token -> cache row, for each slot of this lane's row group
     int row[U];
+    bool fresh[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int pos = wbase + u * KPI + sub;
       row[u] = -1;
+      fresh[u] = false;
       if (pos < hi) {
-        const int j = pos >= L.ns ? L.t0 + (pos - L.ns)
-                      : wbase == wbase0 ? j_spec[u]
-                                        : __ldg(a.idx + static_cast<size_t>(b) * a.k_max + pos);
-        if (j < 0 || j >= t1) {
-          if (lr == 0) flag_status(a.status, VSD_DEV_BAD_INDEX);
-        } else {
-          const int blk =
-              __ldg(a.block_table + static_cast<size_t>(b) * a.max_blocks + j / kPageS);
-          if (blk < 0 || blk >= a.num_blocks) {
-            if (lr == 0) flag_status(a.status, VSD_DEV_BAD_BLOCK);
-          } else {
-            row[u] = (blk * a.Hkv + g) * kPageS + (j % kPageS);
-          }
-        }
+        const int spec = pos >= L.ns ? 0
+                         : wbase == wbase0
+                             ? j_spec[u]
+                             : __ldcg(spec_src + static_cast<size_t>(b) * a.k_max + pos);
+        const SRow r = resolve_position(a, L, b, g, pos, t1, spec);
+        row[u] = r.row;
+        fresh[u] = r.fresh;
       }
     }
-    // ---- every K and V load of the batch in flight: 16 bytes of each row per lane
+    // ---- every K and V load of the batch in flight: 16 bytes of each row per lane (the
+    // step's input token from k_new / v_new, each lane also storing its 16 bytes of it)
     uint4 kr[U], vr[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (row[u] >= 0) {
+      if (fresh[u]) {
+        const size_t src = (static_cast<size_t>(b) * a.Hkv + g) * D + lr * 8;
+        kr[u] = *reinterpret_cast<const uint4*>(a.k_new + src);
+        vr[u] = *reinterpret_cast<const uint4*>(a.v_new + src);
+        const size_t dst = static_cast<size_t>(row[u]) * D + lr * 8;
+        *reinterpret_cast<uint4*>(a.k_store + dst) = kr[u];
+        *reinterpret_cast<uint4*>(a.v_store + dst) = vr[u];
+      } else if (row[u] >= 0) {
         const size_t off = static_cast<size_t>(row[u]) * D + lr * 8;
         kr[u] = ldg_stream16(a.k_cache + off);
         vr[u] = ldg_stream16(a.v_cache + off);
@@ -577,64 +686,83 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // S^T: columns [0, 16); O^T: columns [16, 32)
-  ptx::pdl_launch_dependents();
-  ptx::pdl_wait_primary();  // idx / n_sel come from the preceding kernel
-
-  // this thread's index is loaded together with the list lengths (every position
-  // below k_max is valid memory; it is used only if the position is a selected one)
-  const int lo = split * a.split_len;
-  const int j_spec = (a.idx != nullptr && lo + t < a.k_max)
-                         ? __ldg(a.idx + static_cast<size_t>(b) * a.k_max + lo + t)
-                         : 0;
-  const int ns_raw = a.n_sel != nullptr ? __ldg(a.n_sel + b) : 0;
-  const int t0_raw = __ldg(a.tail_start + b);
-  const int t1 = __ldg(a.seq_len + b);
-  uint4 qv[QPT];
-#pragma unroll
-  for (int u = 0; u < QPT; ++u) {
-    const int i = t + u * kTcThreads, r = i / LPR, c = i % LPR;
-    qv[u] = make_uint4(0, 0, 0, 0);
-    if (r < G)
-      qv[u] = *reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + g * G + r) * D +
-                                              c * 8);
+  // In the early mode the list is resolved and gathered before the wait for the
+  // preceding kernel, unless this split holds the step's input token (read from k_new);
+  // the queries, the workspace and the outputs always come after it.
+  bool waited = a.early == 0;
+  if (waited) {
+    ptx::pdl_wait_primary();  // idx / n_sel come from the preceding kernel
+    ptx::pdl_launch_dependents();
   }
+
+  // this thread's index (or row base) is loaded together with the list lengths (every
+  // position below k_max is valid memory; it is used only if the position is a
+  // selected one)
+  const int lo = split * a.split_len;
+  const int32_t* spec_src = spec_source(a);
+  const int j_spec = (spec_src != nullptr && lo + t < a.k_max)
+                         ? __ldcg(spec_src + static_cast<size_t>(b) * a.k_max + lo + t)
+                         : 0;
+  const int ns_raw = a.n_sel != nullptr ? __ldcg(a.n_sel + b) : 0;
+  const int t0_raw = __ldcg(a.tail_start + b);
+  const int t1 = __ldcg(a.seq_len + b);
   const SList L = attended_list(ns_raw, t0_raw, t1, a, split == 0 && g == 0 && t == 0);
   const bool work = lo < L.total || (split == 0 && L.total == 0);
   const int n_splits = (L.total + a.split_len - 1) / a.split_len;
   const bool direct = n_splits <= 1;
   const int pair = b * a.Hkv + g;
   bool timed_out = false;
+  bool drain_s = false, drain_o = false;  // an MMA whose completion wait gave up
+  const bool holds_fresh = a.k_new != nullptr && L.total > L.ns && L.total - 1 >= lo &&
+                           L.total - 1 < lo + kBatch;
+  if (!waited && (holds_fresh || !work)) {
+    ptx::pdl_wait_primary();
+    ptx::pdl_launch_dependents();
+    waited = true;
+  }
 
   if (work) {
     // ---- this thread's position -> cache row (-1: absent, zero-filled)
     const int pos = lo + t;
-    int crow = -1;
-    if (pos < L.total && pos < lo + kBatch) {
-      const int j = pos >= L.ns ? L.t0 + (pos - L.ns) : j_spec;
-      if (j < 0 || j >= t1) {
-        flag_status(a.status, VSD_DEV_BAD_INDEX);
-      } else {
-        const int blk = __ldg(a.block_table + static_cast<size_t>(b) * a.max_blocks + j / kPageS);
-        if (blk < 0 || blk >= a.num_blocks)
-          flag_status(a.status, VSD_DEV_BAD_BLOCK);
-        else
-          crow = (blk * a.Hkv + g) * kPageS + (j % kPageS);
-      }
-    }
+    SRow rr{-1, false};
+    if (pos < L.total && pos < lo + kBatch) rr = resolve_position(a, L, b, g, pos, t1, j_spec);
+    const int crow = rr.row;
     // ---- gather: warp w copies rows 32 w .. 32 w + 31, RPI whole rows per instruction
+    // (the step's input token from k_new / v_new)
     const int ch = lane % LPR;
+    const unsigned fresh_bits = __ballot_sync(0xffffffffu, rr.fresh);
+    const size_t fresh_off = (static_cast<size_t>(b) * a.Hkv + g) * D;
+    const uint16_t* k_fresh = a.k_new != nullptr ? a.k_new + fresh_off : a.k_cache;
+    const uint16_t* v_fresh = a.v_new != nullptr ? a.v_new + fresh_off : a.v_cache;
 #pragma unroll
     for (int u = 0; u < 32 / RPI; ++u) {
       const int rl = u * RPI + lane / LPR;  // row within the warp
       const int r = warp * 32 + rl;
       const int cr = __shfl_sync(0xffffffffu, crow, rl);
+      const bool fr = (fresh_bits >> rl) & 1u;
       const size_t src = cr >= 0 ? static_cast<size_t>(cr) * D + ch * 8 : 0;
+      const uint16_t* ks = fr ? k_fresh + ch * 8 : a.k_cache + src;
+      const uint16_t* vs = fr ? v_fresh + ch * 8 : a.v_cache + src;
       const int off = (ch >> 3) * Sm::kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-      ptx::cp_async16(k_s + off, a.k_cache + src, cr >= 0 ? 16u : 0u);
-      ptx::cp_async16(v_s + off, a.v_cache + src, cr >= 0 ? 16u : 0u);
+      ptx::cp_async16(k_s + off, ks, cr >= 0 ? 16u : 0u);
+      ptx::cp_async16(v_s + off, vs, cr >= 0 ? 16u : 0u);
     }
     ptx::cp_async_commit();
-    // ---- the group's query rows (loaded with the indices), padded with zeros to 16
+    if (!waited) {
+      ptx::pdl_wait_primary();
+      ptx::pdl_launch_dependents();
+      waited = true;
+    }
+    uint4 qv[QPT];
+#pragma unroll
+    for (int u = 0; u < QPT; ++u) {
+      const int i = t + u * kTcThreads, r = i / LPR, c = i % LPR;
+      qv[u] = make_uint4(0, 0, 0, 0);
+      if (r < G)
+        qv[u] = *reinterpret_cast<const uint4*>(
+            a.q + (static_cast<size_t>(b) * a.Hq + g * G + r) * D + c * 8);
+    }
+    // ---- the group's query rows (loaded after the wait), padded with zeros to 16
 #pragma unroll
     for (int u = 0; u < QPT; ++u) {
       const int i = t + u * kTcThreads, r = i / LPR, c = i % LPR;
@@ -644,6 +772,9 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
     ptx::cp_async_wait_all();
     ptx::fence_proxy_async_smem();  // make the copies and stores visible to the tensor cores
     __syncthreads();
+    // the step's input token joins the cache from its gathered row (P^T overwrites the
+    // K tile only after the QK product below has read it)
+    if (rr.fresh) store_fresh_from_tile<D, Sm::kHalf>(a, k_s, v_s, t, crow);
 
     // ---- S^T = K Q^T
     if (t == 0) {
@@ -659,10 +790,13 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
       }
       ptx::umma_commit(bar_s);
     }
-    if (!ptx::mbar_wait(bar_s, 0)) timed_out = true;
+    if (!ptx::mbar_wait(bar_s, 0)) {
+      timed_out = true;
+      drain_s = true;
+    }
     ptx::tc_fence_after();
-    float sv[kTcNQ];
-    ptx::tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16), reinterpret_cast<uint32_t(&)[16]>(sv));
+    float sv[G];  // the G real query columns (the rest are zero padding)
+    ptx::tmem_ld<G>(tmem + (static_cast<uint32_t>(warp * 32) << 16), reinterpret_cast<uint32_t*>(sv));
     ptx::tmem_wait_ld();
     // ---- softmax over the CTA's keys, per head (log2 units)
     const bool valid = crow >= 0;
@@ -707,8 +841,10 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
     for (int h = 0; h < G; ++h)
       psum[h] = red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
 
-    // ---- O^T = V^T P^T
-    if (t == 0) {
+    // ---- O^T = V^T P^T (not issued by a thread whose QK wait gave up: the QK product
+    // may still be running, and the output is flagged anyway)
+    bool issued_o = false;
+    if (t == 0 && !drain_s) {
       ptx::tc_fence_after();
       // M = 128 for either head dimension: with D = 64 the upper 64 rows of A are the
       // next 16 KB of this CTA's shared memory and land in TMEM lanes 64-127, never read
@@ -722,13 +858,19 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
         ptx::umma_bf16(tmem + 16, ad, bd, idesc, kk > 0 ? 1u : 0u);
       }
       ptx::umma_commit(bar_o);
+      issued_o = true;
     }
-    if (!ptx::mbar_wait(bar_o, 0)) timed_out = true;
+    // every thread learns whether the PV product was issued (one CTA-wide vote)
+    issued_o = __syncthreads_or(issued_o);
+    if (issued_o && !ptx::mbar_wait(bar_o, 0)) {
+      timed_out = true;
+      drain_o = true;
+    }
     ptx::tc_fence_after();
     if (warp < D / 32) {  // TMEM lanes 0 .. D-1 hold the output dimensions
-      float o[kTcNQ];
-      ptx::tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 16,
-                     reinterpret_cast<uint32_t(&)[16]>(o));
+      float o[G];
+      ptx::tmem_ld<G>(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 16,
+                      reinterpret_cast<uint32_t*>(o));
       ptx::tmem_wait_ld();
       const int dim = t;
       if (direct) {
@@ -757,6 +899,10 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
     }
     if (timed_out) flag_status(a.status, VSD_DEV_TIMEOUT);
   }
+  // never free TMEM under a running MMA: a product whose wait gave up is waited for
+  // again (bounded) before the columns go back
+  if (drain_s) ptx::mbar_wait_drain(bar_s, 0);
+  if (drain_o) ptx::mbar_wait_drain(bar_o, 0);
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -789,15 +935,17 @@ struct TcItem {
 
 // For launches with more splits than one wave of the one-split kernel holds: persistent
 // CTAs (one per SM) over contiguous runs of the (pair, split) items, numbered pair-major
-// as that kernel's grid.  A producer warpgroup resolves each item's positions (one item
-// ahead) and gathers its K / V rows into a ring of three stages; its copies and the
-// item's metadata (which rows are present, the list length) complete the stage's `full`
-// barrier.  Two consumer warpgroups take alternate items through the one-split kernel's
-// tensor-core steps, each with its own TMEM columns, barriers, query block and merge
-// scratch, and hand the stage back through its `empty` barrier when the PV product has
-// read it.  One item's gather and two items' products are in flight per SM.  A
-// consumer counts its run of splits of one pair in one arrival; the pair's last arrival
-// merges.
+// as that kernel's grid.  A producer warpgroup resolves each item's positions one item
+// ahead of its gather (the indices or row bases two items ahead) and gathers its K / V
+// rows into a ring of three stages; its copies and the item's metadata (which rows are
+// present, the list length) complete the stage's `full` barrier.  Two consumer
+// warpgroups take alternate items through the one-split kernel's tensor-core steps,
+// each with its own TMEM columns, barriers, query block and merge scratch, and hand the
+// stage back through its `empty` barrier when the PV product has read it.  A consumer
+// folds its items of one pair into one running (m, l, o) in registers and writes a
+// single partial per run (to the slot of the run's first split); the pair's last
+// arrival merges the runs' partials, whose slots follow from the launch geometry
+// (ws_slot), in a fixed order.
 constexpr int kWsStages = 3;
 constexpr int kWsThreads = 3 * kTcThreads;
 
@@ -809,8 +957,10 @@ struct WsSmem {
   static constexpr int kOffQ = 2 * kWsStages * kTile;              // [2] query blocks
   static constexpr int kOffRed = kOffQ + 2 * kQBytes;              // [2][2][4][16] floats
   static constexpr int kOffScratch = kOffRed + 2 * 2 * 4 * kTcNQ * 4;  // [2][128 * 6] floats
-  static constexpr int kOffMeta = kOffScratch + 2 * kTcThreads * 6 * 4;  // [S][8] words
-  static constexpr int kOffBar = kOffMeta + kWsStages * 8 * 4;
+  static constexpr int kOffMeta = kOffScratch + 2 * kTcThreads * 6 * 4;  // [S][16] words
+  static constexpr int kOffCtl = kOffMeta + kWsStages * 16 * 4;  // abort flag
+  static constexpr int kCtlBytes = 64;
+  static constexpr int kOffBar = kOffCtl + kCtlBytes;
   static constexpr int kBarBytes = (2 * kWsStages + 4) * 8 + 16;  // full, empty, s[2], o[2], slot
   // with D = 64 the PV MMA reads 16 KB past a V tile (rows never read back)
   static constexpr int kUsedA = kOffBar + kBarBytes;
@@ -821,6 +971,50 @@ struct WsSmem {
   static_assert(kBatch * 128 <= kTile, "P^T fits in the K tile");
   static_assert(kOffScratch % 16 == 0 && kOffBar % 8 == 0, "layout");
 };
+
+// Workspace slot of partial k (k < ws_partials) of a pair whose items are
+// [i0, i0 + n): partial k belongs to consumer k & 1 of CTA i0 / ipc + k / 2, which
+// writes it at the split of its first item in the pair; -1 when that consumer has no
+// item of the pair.
+__device__ __forceinline__ int ws_slot(int k, long long i0, int n, int ipc) {
+  const long long i1 = i0 + n;
+  const long long cs = (i0 / ipc + (k >> 1)) * static_cast<long long>(ipc);
+  long long lo = cs > i0 ? cs : i0;
+  if (((lo - cs) & 1) != (k & 1)) ++lo;
+  const long long hi = cs + ipc < i1 ? cs + ipc : i1;
+  return lo < hi ? static_cast<int>(lo - i0) : -1;
+}
+
+__device__ __forceinline__ int ws_partials(long long i0, int n, int ipc) {
+  return 2 * static_cast<int>((i0 + n - 1) / ipc - i0 / ipc + 1);
+}
+
+// OR of `pred` over the `nthreads` threads of named barrier `id` (a barrier too).
+__device__ __forceinline__ bool named_vote_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// The list lengths of one sequence as every thread of the kernel reads them.
+struct SLen {
+  int ns, t0, t1;
+};
+
+__device__ __forceinline__ SLen load_len(const SParams& a, int b) {
+  SLen l;
+  l.ns = a.n_sel != nullptr ? __ldcg(a.n_sel + b) : 0;
+  l.t0 = __ldcg(a.tail_start + b);
+  l.t1 = __ldcg(a.seq_len + b);
+  return l;
+}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kWsThreads, 1)
@@ -833,7 +1027,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   extern __shared__ uint8_t ws_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(ws_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint32_t* meta = reinterpret_cast<uint32_t*>(base + Sm::kOffMeta);  // [s][0..3] rows, [s][4] length
+  // per stage: [0..3] present rows (one word per producer warp), [4] list length,
+  // [8..11] per warp the lane holding the step's input token (or -1), [12..15] its row
+  uint32_t* meta = reinterpret_cast<uint32_t*>(base + Sm::kOffMeta);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + Sm::kOffCtl);
   uint64_t* full = reinterpret_cast<uint64_t*>(base + Sm::kOffBar);
   uint64_t* empty = full + kWsStages;
   uint64_t* bar_s = empty + kWsStages;  // [2]
@@ -854,6 +1051,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       ptx::mbar_init(&bar_s[c], 1);
       ptx::mbar_init(&bar_o[c], 1);
     }
+    *abort_flag = 0;
     ptx::fence_mbarrier_init();
   }
   if (warp == 4) {
@@ -864,8 +1062,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  ptx::pdl_launch_dependents();
-  ptx::pdl_wait_primary();  // idx / n_sel come from the preceding kernel
 
   const auto item_of = [&](int it) {
     TcItem w;
@@ -880,78 +1076,139 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   const auto has_work = [&](const TcItem& w) {
     return w.lo < w.L.total || (w.split == 0 && w.L.total == 0);
   };
-  bool timed_out = false;
+  // A wait that gave up raises the CTA's abort flag (and the status bit once): from
+  // then on no copy or MMA is issued, and the products already issued are waited for
+  // again before the TMEM columns are freed.  No named barrier depends on the flag or
+  // on anything a failed wait leaves unfinished, so every warpgroup runs to its end.
+  const auto set_abort = [&]() {
+    if (!*abort_flag) {
+      *abort_flag = 1;
+      flag_status(a.status, VSD_DEV_TIMEOUT);
+    }
+  };
 
   if (wg == 0) {
     // ---------------------------------------------------------------- producer
-    struct Loads {
-      int j_spec, ns, t0, t1;
+    // Position tid of each item is resolved in three stages, one item apart, so that no
+    // load is waited for on the way to an item's copies: the index (or recorded row
+    // base) and the list lengths two items ahead, the block-table entry one item ahead,
+    // the checks and the row for the item being gathered.  In the early mode the first
+    // stages' items (those without the step's input token) are resolved and gathered
+    // before the wait for the preceding kernel.
+    struct Pre {
+      int spec;
+      SLen len;
     };
-    const auto load = [&](const TcItem& w) {
-      Loads l;
-      l.j_spec = (a.idx != nullptr && w.lo + tid < a.k_max)
-                     ? __ldg(a.idx + static_cast<size_t>(w.b) * a.k_max + w.lo + tid)
-                     : 0;
-      l.ns = a.n_sel != nullptr ? __ldg(a.n_sel + w.b) : 0;
-      l.t0 = __ldg(a.tail_start + w.b);
-      l.t1 = __ldg(a.seq_len + w.b);
+    struct Mid {
+      int spec, entry;
+    };
+    const int32_t* spec_src = spec_source(a);
+    const auto pre_load = [&](const TcItem& w) {
+      Pre l;
+      l.spec = (spec_src != nullptr && w.lo + tid < a.k_max)
+                   ? __ldcg(spec_src + static_cast<size_t>(w.b) * a.k_max + w.lo + tid)
+                   : 0;
+      l.len = load_len(a, w.b);
       return l;
     };
-    TcItem nxt = item_of(first);
-    Loads ln = n > 0 ? load(nxt) : Loads{0, 0, 0, 0};
+    const auto pos_in = [&](const TcItem& w) {
+      const int pos = w.lo + tid;
+      return pos < w.L.total && pos < w.lo + kBatch;
+    };
+    // sets w.L and issues the entry load (not waited for here)
+    const auto mid_of = [&](TcItem& w, const Pre& l) {
+      w.L = attended_list(l.len.ns, l.len.t0, l.len.t1, a, w.split == 0 && w.g == 0 && tid == 0);
+      Mid m{l.spec, 0};
+      if (pos_in(w)) m.entry = position_entry(a, w.L, w.b, w.lo + tid, l.len.t1, l.spec);
+      return m;
+    };
+    // the item holds the step's input token (read from k_new, which the preceding kernel
+    // may write)
+    const auto holds_fresh = [&](const TcItem& w) {
+      return a.k_new != nullptr && w.L.total > w.L.ns && w.L.total - 1 >= w.lo &&
+             w.L.total - 1 < w.lo + kBatch;
+    };
+    bool waited = a.early == 0;
+    if (waited) {
+      ptx::pdl_wait_primary();  // idx / n_sel come from the preceding kernel
+      ptx::pdl_launch_dependents();
+    }
+    TcItem cur = item_of(first), nxt = item_of(first + 1);
+    Mid mcur{0, 0};
+    Pre pnxt{0, {0, 0, 0}};
+    if (n > 0) {
+      const Pre p0 = pre_load(cur);
+      if (n > 1) pnxt = pre_load(nxt);
+      mcur = mid_of(cur, p0);
+    }
     for (int j = 0; j < n; ++j) {
-      TcItem cur = nxt;
-      const Loads lc = ln;
-      // position tid of the item -> cache row (-1: absent, zero-filled)
-      cur.L = attended_list(lc.ns, lc.t0, lc.t1, a, cur.split == 0 && cur.g == 0 && tid == 0);
-      int crow = -1;
-      const int pos = cur.lo + tid;
-      if (pos < cur.L.total && pos < cur.lo + kBatch) {
-        const int jj = pos >= cur.L.ns ? cur.L.t0 + (pos - cur.L.ns) : lc.j_spec;
-        if (jj < 0 || jj >= lc.t1) {
-          flag_status(a.status, VSD_DEV_BAD_INDEX);
-        } else {
-          const int blk =
-              __ldg(a.block_table + static_cast<size_t>(cur.b) * a.max_blocks + jj / kPageS);
-          if (blk < 0 || blk >= a.num_blocks)
-            flag_status(a.status, VSD_DEV_BAD_BLOCK);
-          else
-            crow = (blk * a.Hkv + cur.g) * kPageS + (jj % kPageS);
-        }
+      // a stage is reused only after the consumers (which wait for the preceding kernel)
+      // hand it back, and k_new is read only after the wait
+      if (!waited && (j >= kWsStages || holds_fresh(cur))) {
+        ptx::pdl_wait_primary();
+        ptx::pdl_launch_dependents();
+        waited = true;
       }
-      if (j + 1 < n) {  // the next item's loads go out under this one's
-        nxt = item_of(first + j + 1);
-        ln = load(nxt);
+      // this item's row (its entry load was issued one item ago), then the next item's
+      // entry load and the loads of the item after it, all before this item's stage wait
+      const SRow rcur = pos_in(cur) ? position_row(a, cur.L, cur.b, cur.g, cur.lo + tid,
+                                                   mcur.spec, mcur.entry)
+                                    : SRow{-1, false};
+      Mid mnxt{0, 0};
+      if (j + 1 < n) {
+        const Pre pl = pnxt;
+        if (j + 2 < n) pnxt = pre_load(item_of(first + j + 2));
+        mnxt = mid_of(nxt, pl);
       }
       const int s = j % kWsStages;
       const uint32_t use = static_cast<uint32_t>(j / kWsStages);
-      if (use > 0 && !ptx::mbar_wait(&empty[s], (use - 1) & 1u)) timed_out = true;
-      if (has_work(cur)) {
-        // warp w copies rows 32 w .. 32 w + 31, RPI whole rows per instruction
+      if (use > 0 && !ptx::mbar_wait(&empty[s], (use - 1) & 1u, abort_flag)) set_abort();
+      const int crow = rcur.row;
+      const unsigned fresh_bits = __ballot_sync(0xffffffffu, rcur.fresh);
+      if (has_work(cur) && !*abort_flag) {
+        // warp w copies rows 32 w .. 32 w + 31, RPI whole rows per instruction (the
+        // step's input token from k_new / v_new)
         uint8_t* k_s = base + s * 2 * Sm::kTile;
         uint8_t* v_s = k_s + Sm::kTile;
         const int ch = lane % LPR;
+        const size_t fresh_off = (static_cast<size_t>(cur.b) * a.Hkv + cur.g) * D + ch * 8;
 #pragma unroll
         for (int u = 0; u < 32 / RPI; ++u) {
           const int rl = u * RPI + lane / LPR;
           const int r = warp * 32 + rl;
           const int cr = __shfl_sync(0xffffffffu, crow, rl);
+          const bool fr = (fresh_bits >> rl) & 1u;
           const size_t src = cr >= 0 ? static_cast<size_t>(cr) * D + ch * 8 : 0;
+          const uint16_t* ks = fr ? a.k_new + fresh_off : a.k_cache + src;
+          const uint16_t* vs = fr ? a.v_new + fresh_off : a.v_cache + src;
           const int off = (ch >> 3) * Sm::kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-          ptx::cp_async16(k_s + off, a.k_cache + src, cr >= 0 ? 16u : 0u);
-          ptx::cp_async16(v_s + off, a.v_cache + src, cr >= 0 ? 16u : 0u);
+          ptx::cp_async16(k_s + off, ks, cr >= 0 ? 16u : 0u);
+          ptx::cp_async16(v_s + off, vs, cr >= 0 ? 16u : 0u);
         }
       }
       ptx::cp_async_mbar_arrive_noinc(&full[s]);
       const unsigned rows = __ballot_sync(0xffffffffu, crow >= 0);
-      if (lane == 0) meta[s * 8 + warp] = rows;
-      if (tid == 0) meta[s * 8 + 4] = static_cast<uint32_t>(cur.L.total);
+      if (lane == 0) {
+        meta[s * 16 + warp] = rows;
+        meta[s * 16 + 8 + warp] = fresh_bits ? static_cast<uint32_t>(__ffs(fresh_bits) - 1) : 0xFFFFFFFFu;
+      }
+      if (rcur.fresh) meta[s * 16 + 12 + warp] = static_cast<uint32_t>(crow);
+      if (tid == 0) meta[s * 16 + 4] = static_cast<uint32_t>(cur.L.total);
       ptx::named_barrier_sync(3, kTcThreads);
       if (tid == 0) ptx::mbar_arrive(&full[s]);  // releases the metadata
+      cur = nxt;
+      nxt = item_of(first + j + 2);
+      mcur = mnxt;
+    }
+    if (!waited) {
+      ptx::pdl_wait_primary();
+      ptx::pdl_launch_dependents();
     }
     ptx::cp_async_wait_all();
   } else {
     // ---------------------------------------------------------------- consumers
+    ptx::pdl_wait_primary();  // the workspace, q and the outputs: after the preceding kernel
+    ptx::pdl_launch_dependents();
     const int c = wg - 1;
     const int ct = tid - wg * kTcThreads;  // key of the item = TMEM lane
     const int cw = ct >> 5;                // lane quarter
@@ -961,70 +1218,129 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     float* scratch = reinterpret_cast<float*>(base + Sm::kOffScratch) + c * (kTcThreads * 6);
     const uint32_t bar_id = 1 + c;
     const auto csync = [bar_id] { ptx::named_barrier_sync(bar_id, kTcThreads); };
+    // the query rows of a (sequence, KV group), padded with zeros to 16 rows, and the
+    // list lengths of an item's sequence: loaded one item of this consumer ahead
+    const auto load_q = [&](const TcItem& w, uint4 (&qv)[QPT]) {
+#pragma unroll
+      for (int u = 0; u < QPT; ++u) {
+        const int i = ct + u * kTcThreads, r = i / LPR, cc = i % LPR;
+        qv[u] = make_uint4(0, 0, 0, 0);
+        if (r < G)
+          qv[u] = *reinterpret_cast<const uint4*>(
+              a.q + (static_cast<size_t>(w.b) * a.Hq + w.g * G + r) * D + cc * 8);
+      }
+    };
+    uint4 qcur[QPT], qnext[QPT];
+    SLen lcur{0, 0, 0}, lnext{0, 0, 0};
+    int qnext_pair = -1;
+    if (c < n) {
+      const TcItem w0 = item_of(first + c);
+      lnext = load_len(a, w0.b);
+      load_q(w0, qnext);
+      qnext_pair = w0.pair;
+    }
     int staged_pair = -1;
-    int pend_pair = -1, pend_splits = 0, pend_count = 0;  // partials not yet counted
+    // the running partial of this consumer's current run of one pair's splits
+    int run_pair = -1, run_first = 0, run_count = 0, run_splits = 0;
+    float m_run[G], l_run[G], o_run[G];
     uint32_t phase = 0;
+    bool drain_s = false, drain_o = false;
+    uint32_t drain_s_par = 0, drain_o_par = 0;
     const auto flush = [&]() {
-      // the barrier orders every thread's partial stores before the acquire-release
-      // count; the last arrival of the pair combines its splits
-      ptx::tc_fence_before();
+      // the run's partial at the slot of its first split; the barrier orders every
+      // thread's stores before the acquire-release count, whose last arrival merges
+      float* wsl = a.ws + (static_cast<size_t>(run_pair) * a.max_splits + run_first) *
+                              SSlot<D, G>::kFloats;
+      if (ct < D) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) wsl[SSlot<D, G>::kO + h * D + ct] = o_run[h];
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        if (h == ct) {
+          wsl[h] = m_run[h];
+          wsl[G + h] = l_run[h];
+        }
+      }
       csync();
       if (ct == 0) {
         const unsigned old =
-            ptx::atom_add_acq_rel_gpu(a.counters + pend_pair, static_cast<unsigned>(pend_count));
+            ptx::atom_add_acq_rel_gpu(a.counters + run_pair, static_cast<unsigned>(run_count));
         const int lst =
-            old + static_cast<unsigned>(pend_count) == static_cast<unsigned>(pend_splits);
-        if (lst) ptx::st_relaxed_gpu(a.counters + pend_pair, 0u);
+            old + static_cast<unsigned>(run_count) == static_cast<unsigned>(run_splits);
+        if (lst) ptx::st_relaxed_gpu(a.counters + run_pair, 0u);
         s_last[c] = lst;
       }
       csync();
       if (s_last[c]) {
-        const int pb = pend_pair / a.Hkv;
-        merge_splits_by<D, G, kTcThreads, 24>(a, scratch, pend_pair, pb, pend_pair - pb * a.Hkv,
-                                              pend_splits, ct, csync);
+        const int pb = run_pair / a.Hkv;
+        const long long i0 = static_cast<long long>(run_pair) * a.max_splits;
+        const int ns = run_splits, ipc = items_per_cta;
+        // a pair has two partials per CTA it spans (about a dozen in a 36-layer decode
+        // loop): a load round of 12 (8 for wider groups) keeps the merge's registers
+        // within the consumer's
+        merge_splits_by<D, G, kTcThreads, (G <= 4 ? 12 : 8)>(
+            a, scratch, run_pair, pb, run_pair - pb * a.Hkv, ws_partials(i0, ns, ipc), ct, csync,
+            [i0, ns, ipc](int k) { return ws_slot(k, i0, ns, ipc); });
       }
-      pend_count = 0;
+      run_count = 0;
     };
     for (int j = c; j < n; j += 2) {
-      const int s = j % kWsStages;
-      const uint32_t use = static_cast<uint32_t>(j / kWsStages);
-      if (!ptx::mbar_wait(&full[s], use & 1u)) timed_out = true;
       TcItem cur = item_of(first + j);
-      cur.L.total = static_cast<int>(meta[s * 8 + 4]);
-      const bool valid = (meta[s * 8 + cw] >> (ct & 31)) & 1u;
+      lcur = lnext;
+      if (cur.pair != staged_pair) {
+#pragma unroll
+        for (int u = 0; u < QPT; ++u) qcur[u] = qnext[u];
+      }
+      // the next item's lengths and (for a new pair) query rows go out now
+      if (j + 2 < n) {
+        const TcItem wn = item_of(first + j + 2);
+        lnext = load_len(a, wn.b);
+        if (wn.pair != cur.pair && wn.pair != qnext_pair) {
+          load_q(wn, qnext);
+          qnext_pair = wn.pair;
+        }
+      }
+      // every thread computes the same list from the same lengths: the control flow of
+      // the warpgroup never depends on what a wait left behind
+      cur.L = attended_list(lcur.ns, lcur.t0, lcur.t1, a, false);
       const bool work = has_work(cur);
       const int n_splits = (cur.L.total + a.split_len - 1) / a.split_len;
       const bool direct = n_splits <= 1;
-      // every consumer thread has read the stage's metadata past this barrier
-      if (pend_count > 0 && (cur.pair != pend_pair || !work || direct)) flush();
+      if (run_count > 0 && (cur.pair != run_pair || !work || direct)) flush();
+      const int s = j % kWsStages;
+      const uint32_t use = static_cast<uint32_t>(j / kWsStages);
+      if (!ptx::mbar_wait(&full[s], use & 1u, abort_flag)) set_abort();
+      const bool stop = *abort_flag != 0;
       if (!work) {
-        csync();
-        if (ct == 0) ptx::mbar_arrive(&empty[s]);
+        if (ct == 0) ptx::mbar_arrive(&empty[s]);  // nothing of this stage is read
         continue;
       }
+      const bool valid = (meta[s * 16 + cw] >> (ct & 31)) & 1u;
       uint8_t* k_s = base + s * 2 * Sm::kTile;
       uint8_t* v_s = k_s + Sm::kTile;
       uint8_t* p_s = k_s;
+      // the step's input token joins the cache from its gathered row (P^T overwrites the
+      // K tile only after the QK product below has read it)
+      if (!stop && static_cast<int>(meta[s * 16 + 8 + cw]) == (ct & 31))
+        store_fresh_from_tile<D, Sm::kHalf>(a, k_s, v_s, ct,
+                                            static_cast<int>(meta[s * 16 + 12 + cw]));
       if (cur.pair != staged_pair) {
-        // the group's query rows, padded with zeros to 16 (this consumer's previous QK
-        // product, the block's last reader, has completed)
+        // the group's query rows (this consumer's previous QK product, the block's last
+        // reader, has completed)
 #pragma unroll
         for (int u = 0; u < QPT; ++u) {
           const int i = ct + u * kTcThreads, r = i / LPR, cc = i % LPR;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (r < G)
-            v = *reinterpret_cast<const uint4*>(
-                a.q + (static_cast<size_t>(cur.b) * a.Hq + cur.g * G + r) * D + cc * 8);
           *reinterpret_cast<uint4*>(q_s + (cc >> 3) * (kTcNQ * 128) + r * 128 +
-                                    (((cc & 7) ^ (r & 7)) << 4)) = v;
+                                    (((cc & 7) ^ (r & 7)) << 4)) = qcur[u];
         }
         staged_pair = cur.pair;
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        csync();
       }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      csync();
-      // ---- S^T = K Q^T
-      if (ct == 0) {
+      // ---- S^T = K Q^T (the stage has landed: this thread waited for it)
+      if (ct == 0 && !stop) {
         ptx::tc_fence_after();
         constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTcNQ, 0, 0);
         const uint32_t ka = ptx::smem_u32(k_s), qa = ptx::smem_u32(q_s);
@@ -1037,11 +1353,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         ptx::umma_commit(&bar_s[c]);
       }
-      if (!ptx::mbar_wait(&bar_s[c], phase)) timed_out = true;
+      bool s_failed = false;
+      if (!stop && !ptx::mbar_wait(&bar_s[c], phase, abort_flag)) {
+        set_abort();
+        s_failed = true;
+        if (!drain_s) {
+          drain_s = true;
+          drain_s_par = phase;
+        }
+      }
       ptx::tc_fence_after();
-      float sv[kTcNQ];
-      ptx::tmem_ld16(tm + (static_cast<uint32_t>(cw * 32) << 16),
-                     reinterpret_cast<uint32_t(&)[16]>(sv));
+      float sv[G];  // the G real query columns (the rest are zero padding)
+      ptx::tmem_ld<G>(tm + (static_cast<uint32_t>(cw * 32) << 16),
+                      reinterpret_cast<uint32_t*>(sv));
       ptx::tmem_wait_ld();
       // ---- softmax over the item's keys, per head (log2 units)
       float z[G];
@@ -1080,66 +1404,88 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
-      csync();
+      // a barrier that also tells every thread whether some QK wait gave up: the PV
+      // product is issued only when the QK product is known to be complete
+      const bool skip_pv = named_vote_or(bar_id, kTcThreads, stop || s_failed);
 #pragma unroll
       for (int h = 0; h < G; ++h)
         psum[h] = red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
       // ---- O^T = V^T P^T; its completion also hands the stage back to the producer
       if (ct == 0) {
-        ptx::tc_fence_after();
-        constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTcNQ, 1, 1);
-        const uint32_t va = ptx::smem_u32(v_s), pa = ptx::smem_u32(p_s);
+        if (!skip_pv) {
+          ptx::tc_fence_after();
+          constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, kTcNQ, 1, 1);
+          const uint32_t va = ptx::smem_u32(v_s), pa = ptx::smem_u32(p_s);
 #pragma unroll
-        for (int kk = 0; kk < kBatch / 16; ++kk) {
-          const uint64_t ad = ptx::sdesc_sw128(va + kk * 2048, Sm::kHalf, 1024);
-          const uint64_t bd = ptx::sdesc_sw128(pa + kk * 2048, Sm::kHalf, 1024);
-          ptx::umma_bf16(tm + 16, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kBatch / 16; ++kk) {
+            const uint64_t ad = ptx::sdesc_sw128(va + kk * 2048, Sm::kHalf, 1024);
+            const uint64_t bd = ptx::sdesc_sw128(pa + kk * 2048, Sm::kHalf, 1024);
+            ptx::umma_bf16(tm + 16, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          }
+          ptx::umma_commit(&bar_o[c]);
+          ptx::umma_commit(&empty[s]);
+        } else {
+          ptx::mbar_arrive(&empty[s]);
         }
-        ptx::umma_commit(&bar_o[c]);
-        ptx::umma_commit(&empty[s]);
       }
-      if (!ptx::mbar_wait(&bar_o[c], phase)) timed_out = true;
+      if (!skip_pv && !ptx::mbar_wait(&bar_o[c], phase, abort_flag)) {
+        set_abort();
+        if (!drain_o) {
+          drain_o = true;
+          drain_o_par = phase;
+        }
+      }
       ptx::tc_fence_after();
-      phase ^= 1u;
+      // both barriers completed a phase when both products ran; after an abort the
+      // phases no longer matter (no product is issued and the drain keeps its parity)
+      if (!skip_pv) phase ^= 1u;
+      float o[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) o[h] = 0.f;
       if (cw < D / 32) {  // TMEM lanes 0 .. D-1 hold the output dimensions
-        float o[kTcNQ];
-        ptx::tmem_ld16(tm + (static_cast<uint32_t>(cw * 32) << 16) + 16,
-                       reinterpret_cast<uint32_t(&)[16]>(o));
+        ptx::tmem_ld<G>(tm + (static_cast<uint32_t>(cw * 32) << 16) + 16,
+                        reinterpret_cast<uint32_t*>(o));
         ptx::tmem_wait_ld();
-        const int dim = ct;
-        if (direct) {
+      }
+      if (direct) {
+        if (ct < D) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             const float val = psum[h] > 0.f ? o[h] / psum[h] : 0.f;
             const __nv_bfloat16 bv = __float2bfloat16_rn(val);
-            a.out[(static_cast<size_t>(cur.b) * a.Hq + cur.g * G + h) * D + dim] =
+            a.out[(static_cast<size_t>(cur.b) * a.Hq + cur.g * G + h) * D + ct] =
                 *reinterpret_cast<const uint16_t*>(&bv);
           }
-        } else {
-          float* wsl =
-              a.ws + (static_cast<size_t>(cur.pair) * a.max_splits + cur.split) * SSlot<D, G>::kFloats;
-#pragma unroll
-          for (int h = 0; h < G; ++h) wsl[SSlot<D, G>::kO + h * D + dim] = o[h];
-          if (dim < G) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              if (h == dim) {
-                wsl[h] = m[h];
-                wsl[G + h] = psum[h];
-              }
-            }
-          }
         }
-      }
-      if (!direct) {
-        pend_pair = cur.pair;
-        pend_splits = n_splits;
-        ++pend_count;
+      } else if (run_count == 0) {
+        run_pair = cur.pair;
+        run_first = cur.split;
+        run_splits = n_splits;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          m_run[h] = m[h];
+          l_run[h] = psum[h];
+          o_run[h] = o[h];
+        }
+        run_count = 1;
+      } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float mn = fmaxf(m_run[h], m[h]);
+          const float f0 = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - mn);
+          const float f1 = (m[h] == -INFINITY) ? 0.f : exp2f(m[h] - mn);
+          l_run[h] = l_run[h] * f0 + psum[h] * f1;
+          o_run[h] = o_run[h] * f0 + o[h] * f1;
+          m_run[h] = mn;
+        }
+        ++run_count;
       }
     }
-    if (pend_count > 0) flush();
+    if (run_count > 0) flush();
+    // products whose wait gave up are waited for again before the columns are freed
+    if (drain_s) ptx::mbar_wait_drain(&bar_s[c], drain_s_par);
+    if (drain_o) ptx::mbar_wait_drain(&bar_o[c], drain_o_par);
   }
-  if (timed_out) flag_status(a.status, VSD_DEV_TIMEOUT);
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 4) {
@@ -1253,6 +1599,13 @@ cudaError_t launch_sparse(const SparseArgs& sa, cudaStream_t stream) {
   p.q = static_cast<const uint16_t*>(sa.q);
   p.k_cache = static_cast<const uint16_t*>(sa.k_cache);
   p.v_cache = static_cast<const uint16_t*>(sa.v_cache);
+  p.k_new = static_cast<const uint16_t*>(sa.k_new);
+  p.v_new = static_cast<const uint16_t*>(sa.v_new);
+  p.k_store = static_cast<uint16_t*>(sa.k_store);
+  p.v_store = static_cast<uint16_t*>(sa.v_store);
+  p.sel_rows = sa.sel_rows;
+  p.rows_mode = sa.sel_rows != nullptr && sa.k_max > 0 ? sa.rows_mode : 0;
+  p.early = sa.early;
   p.block_table = sa.block_table;
   p.idx = sa.idx;
   p.n_sel = sa.n_sel;

@@ -44,8 +44,8 @@ __global__ void __launch_bounds__(kGThreads) sparse_verify_gather_kernel(const S
   uint16_t* ck = a.compact_k;
   uint16_t* cv = a.compact_v;
 
-  int ns = a.n_sel != nullptr ? __ldg(a.n_sel + b) : 0;
-  const int P = __ldg(a.prefix_len + b);
+  int ns = a.n_sel != nullptr ? __ldcg(a.n_sel + b) : 0;
+  const int P = __ldcg(a.prefix_len + b);
   const bool ok = ns >= 0 && ns <= a.k_max && P >= 0 &&
                   static_cast<long long>(P) + a.R <= static_cast<long long>(a.max_blocks) * kPageG;
   if (!ok) {
@@ -69,11 +69,11 @@ __global__ void __launch_bounds__(kGThreads) sparse_verify_gather_kernel(const S
     kv[u] = vv[u] = make_uint4(0, 0, 0, 0);
     dst[u] = 0;
     if (p < n_used) {
-      const int j = p < ns ? __ldg(a.idx + static_cast<size_t>(b) * a.k_max + p) : P + (p - ns);
+      const int j = p < ns ? __ldcg(a.idx + static_cast<size_t>(b) * a.k_max + p) : P + (p - ns);
       if (j < 0 || j >= P + a.R) {
         if (ch == 0) flag_status(a.status, VSD_DEV_BAD_INDEX);
       } else {
-        const int blk = __ldg(a.block_table + static_cast<size_t>(b) * a.max_blocks + j / kPageG);
+        const int blk = __ldcg(a.block_table + static_cast<size_t>(b) * a.max_blocks + j / kPageG);
         if (blk < 0 || blk >= a.num_blocks) {
           if (ch == 0) flag_status(a.status, VSD_DEV_BAD_BLOCK);
         } else {

@@ -130,7 +130,7 @@ __device__ __forceinline__ Seg segment_at(long long v, long long v1, const VPara
   s.next_v = e;
   s.b = s.p / a.Hkv;
   s.g = s.p - s.b * a.Hkv;
-  const int P = __ldg(a.prefix_len + s.b);
+  const int P = __ldcg(a.prefix_len + s.b);
   const bool ok = P >= 0 && P <= a.P_max &&
                   static_cast<long long>(P) + a.R <= static_cast<long long>(a.max_blocks) * kPage;
   s.bad_len = !ok;
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* bt_row = a.block_table + static_cast<size_t>(b0) * a.max_blocks;
       auto raw_entry = [&](int tile_base) {
         const int lp = (tile_base + (lane >> 3)) * kPagesPerTile + (lane & 7);
-        return lp < a.max_blocks ? __ldg(bt_row + lp) : a.num_blocks;
+        return lp < a.max_blocks ? __ldcg(bt_row + lp) : a.num_blocks;
       };
       int ent_cur = raw_entry(tb0);
       int ent_nxt = raw_entry(tb0 + 4);
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int lp0 = (tb0 * kTile + row) / kPage;
       const int entry_first =
-          lp0 < a.max_blocks ? __ldg(a.block_table + static_cast<size_t>(b0) * a.max_blocks + lp0)
+          lp0 < a.max_blocks ? __ldcg(a.block_table + static_cast<size_t>(b0) * a.max_blocks + lp0)
                              : 0;
       const Seg s = segment_at(v, v1, a);
       v = s.next_v;
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         gmask = 0u;
 #pragma unroll
         for (int hl = 0; hl < G; ++hl)
-          gmask |= (__ldg(a.head_mask + s.g * G + hl) != 0 ? 1u : 0u) << hl;
+          gmask |= (__ldcg(a.head_mask + s.g * G + hl) != 0 ? 1u : 0u) << hl;
       }
       const bool all_heads = gmask == kAllHeads;
       const long long first_v = static_cast<long long>(s.p) * a.t_max;
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto page_entry = [&](int tile) {
         const int jj = tile * kTile + row;
         return (tile < s.t_end && jj < s.L)
-                   ? __ldg(a.block_table + static_cast<size_t>(s.b) * a.max_blocks + jj / kPage)
+                   ? __ldcg(a.block_table + static_cast<size_t>(s.b) * a.max_blocks + jj / kPage)
                    : 0;
       };
       int entry_next =
@@ -817,7 +817,7 @@ __device__ __forceinline__ void aggregate_scores(const VParams& a, int blk) {
           if (j0 + u < a.P_max) s[u] += __ldcg(base + static_cast<size_t>(g) * a.P_max + u);
     }
   }
-  const int P = __ldg(a.prefix_len + b);
+  const int P = __ldcg(a.prefix_len + b);
   const bool ok = P >= 0 && P <= a.P_max;  // else flagged by the verification kernel
   __syncthreads();
   if (ok) {

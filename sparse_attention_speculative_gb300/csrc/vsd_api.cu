@@ -600,17 +600,32 @@ vsd_status vsd_sparse_workspace_size(const vsd_geom* geom, int k_max, int max_ta
   return VSD_OK;
 }
 
-vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const void* k_cache,
-                                  const void* v_cache, const int32_t* block_table,
-                                  const int32_t* idx, const int32_t* n_sel, int k_max,
-                                  const int32_t* tail_start, const int32_t* seq_len,
-                                  int max_tail, float scale, void* out, void* workspace,
-                                  size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The draft step with its options (see vsd_sparse_decode_attn_step); the plain call
+// passes none of them.
+vsd_status sparse_step(const vsd_geom* geom, const void* q, const void* k_new, const void* v_new,
+                       const void* k_cache, const void* v_cache, void* k_store, void* v_store,
+                       const int32_t* block_table, const int32_t* idx, const int32_t* n_sel,
+                       int k_max, const int32_t* tail_start, const int32_t* seq_len,
+                       int max_tail, int32_t* sel_rows, unsigned flags, float scale, void* out,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  const unsigned kKnown = VSD_STEP_RECORD_ROWS | VSD_STEP_REUSE_ROWS | VSD_STEP_EARLY_GATHER;
+  if ((flags & ~kKnown) != 0u) return VSD_ERR_INVALID_ARG;
+  const int rows_mode = (flags & VSD_STEP_RECORD_ROWS) ? 1 : (flags & VSD_STEP_REUSE_ROWS) ? 2 : 0;
+  if ((flags & VSD_STEP_RECORD_ROWS) && (flags & VSD_STEP_REUSE_ROWS)) return VSD_ERR_INVALID_ARG;
   vsd_status st = check_geom(geom);
   if (st != VSD_OK) return st;
   if (geom->Hq / geom->Hkv > 16) return VSD_ERR_UNSUPPORTED;
   if (k_max < 0 || max_tail < 0) return VSD_ERR_INVALID_ARG;
   if (geom->B > 65535) return VSD_ERR_UNSUPPORTED;
+  // cache rows are 32-bit: block * Hkv * page_size + offset
+  if (static_cast<long long>(geom->num_blocks) * geom->Hkv * geom->page_size > 0x7FFFFFFFll)
+    return VSD_ERR_UNSUPPORTED;
+  if ((k_new == nullptr) != (v_new == nullptr)) return VSD_ERR_INVALID_ARG;
+  if (rows_mode != 0 && k_max > 0 && sel_rows == nullptr) return VSD_ERR_INVALID_ARG;
   if (geom->B == 0) return VSD_OK;
   const vsd::SparsePlan splan = vsd::plan_sparse(k_max, max_tail);
   const size_t need = vsd::sparse_workspace_bytes(splan, geom->B, geom->Hkv,
@@ -622,7 +637,8 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
   if (k_max > 0 && (!idx || !n_sel)) return VSD_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(idx, 4) || !aligned(n_sel, 4) || !aligned(block_table, 4) ||
-      !aligned(tail_start, 4) || !aligned(seq_len, 4))
+      !aligned(tail_start, 4) || !aligned(seq_len, 4) || !aligned(k_new, 16) ||
+      !aligned(v_new, 16) || !aligned(sel_rows, 4))
     return VSD_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return VSD_ERR_INVALID_ARG;
   unsigned* status = nullptr;
@@ -632,6 +648,13 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
   sa.q = q;
   sa.k_cache = k_cache;
   sa.v_cache = v_cache;
+  sa.k_new = k_new;
+  sa.v_new = v_new;
+  sa.k_store = k_store;
+  sa.v_store = v_store;
+  sa.sel_rows = k_max > 0 ? sel_rows : nullptr;
+  sa.rows_mode = k_max > 0 ? rows_mode : 0;
+  sa.early = (flags & VSD_STEP_EARLY_GATHER) ? 1 : 0;
   sa.block_table = block_table;
   sa.idx = k_max > 0 ? idx : nullptr;
   sa.n_sel = k_max > 0 ? n_sel : nullptr;
@@ -657,6 +680,34 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
   cudaError_t e = vsd::launch_sparse(sa, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return VSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table,
+                                  const int32_t* idx, const int32_t* n_sel, int k_max,
+                                  const int32_t* tail_start, const int32_t* seq_len,
+                                  int max_tail, float scale, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return sparse_step(geom, q, nullptr, nullptr, k_cache, v_cache, nullptr, nullptr, block_table,
+                     idx, n_sel, k_max, tail_start, seq_len, max_tail, nullptr, 0u, scale, out,
+                     workspace, workspace_bytes, stream);
+}
+
+vsd_status vsd_sparse_decode_attn_step(const vsd_geom* geom, const void* q, const void* k_new,
+                                       const void* v_new, void* k_cache, void* v_cache,
+                                       const int32_t* block_table, const int32_t* idx,
+                                       const int32_t* n_sel, int k_max,
+                                       const int32_t* tail_start, const int32_t* seq_len,
+                                       int max_tail, int32_t* sel_rows, unsigned flags,
+                                       float scale, void* out, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  return sparse_step(geom, q, k_new, v_new, k_cache, v_cache, k_cache, v_cache, block_table, idx,
+                     n_sel, k_max, tail_start, seq_len, max_tail, sel_rows, flags, scale, out,
+                     workspace, workspace_bytes, stream);
 }
 
 vsd_status vsd_copy(void* dst, const void* src, size_t bytes, void* stream) {

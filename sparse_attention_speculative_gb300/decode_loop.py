@@ -12,10 +12,11 @@ layers, every kernel libvsd's:
   once:                the protected top-k of every (layer, sequence) row
                                                              (vsd_select_topk_scored)
                        the accepted counts move every prefix     (vsd_advance_lengths)
-  for draft step i:    for every layer l: the step's input token keys/values join the
-                       cache at seq_len_i - 1, then the sparse draft attention over the
-                       selection plus the dense tail     (vsd_append_kv,
-                                                          vsd_sparse_decode_attn)
+  for draft step i:    for every layer l: the sparse draft attention over the selection
+                       plus the dense tail, which also stores the step's input token
+                       keys/values at seq_len_i - 1; the first step records the
+                       selection's cache rows for the later ones
+                                                        (vsd_sparse_decode_attn_step)
 
 The prefix lengths, the draft tails and the per-row prefixes of the selection live on
 the device and advance inside the graph, so consecutive replays are consecutive decode
@@ -87,8 +88,11 @@ class DecodeLoop:
                    ("k_verify", (L, B, R, Hkv, d), bf), ("v_verify", (L, B, R, Hkv, d), bf),
                    ("k_draft", (L, gamma, B, Hkv, d), bf), ("v_draft", (L, gamma, B, Hkv, d), bf),
                    ("accepted", (B,), i32))
-        if P_max % 4:
-            raise ValueError("P_max must be a multiple of 4 (16-byte score rows)")
+        # row stride of the logits, partial-score and score buffers: a multiple of 32
+        # positions, so every row starts on a 128-byte boundary (the verification writes
+        # 32 consecutive positions per warp store; rows that start inside a 32-byte
+        # sector leave partly written sectors that cost DRAM read-modify-writes)
+        self.row_stride = (P_max + 31) // 32 * 32
         self._h_in, self._d_in = _arena(self, in_spec, dev)
 
         def dbuf(shape, dtype):
@@ -114,12 +118,14 @@ class DecodeLoop:
             setattr(self, "h_%s_out" % name, base[t0:t0 + n.numel() * 4].view(torch.int32)
                     .view(n.shape))
         # device-only intermediates, shared by the layers
-        self.logits = dbuf((B, 2, Hq, P_max), torch.float32) if collect_logits else None
-        self.partial = dbuf((B, Hkv, P_max), torch.float32)
-        self.score = dbuf((L * B, P_max), torch.float32)
+        rs = self.row_stride
+        self.logits = dbuf((B, 2, Hq, rs), torch.float32) if collect_logits else None
+        self.partial = dbuf((B, Hkv, rs), torch.float32)
+        self.score = dbuf((L * B, rs), torch.float32)
         self.score_hist = dbuf((L * B, _lib.HIST_BINS), torch.int32)
+        self.sel_rows = dbuf((L * B, k), torch.int32)  # the selection's cache rows
         geom = _lib.geom_for(B, Hq, kc0, self.block_tables[0])
-        nb = _lib.vsd_verify_workspace_size(geom, R, P_max)
+        nb = _lib.vsd_verify_workspace_size(geom, R, self.row_stride)
         self.verify_ws = _aligned(dbuf((nb + 256,), torch.uint8), nb) if nb else None
         nb = _lib.vsd_sparse_workspace_size(geom, k, self.max_tail)
         self.sparse_ws = _aligned(dbuf((nb + 256,), torch.uint8), nb) if nb else None
@@ -156,7 +162,7 @@ class DecodeLoop:
             _lib.vsd_append_kv(self.k_verify[l], self.v_verify[l], kc, vc, bt, self.prefix_len,
                                pos_offset=0, stream=s)
             _lib.vsd_verify_attn_collect_scored(
-                self.q[l], kc, vc, bt, self.prefix_len, P_max=self.P_max, scale=self.scale,
+                self.q[l], kc, vc, bt, self.prefix_len, P_max=self.row_stride, scale=self.scale,
                 row0=0, row1=self.R - 1, logits=self.logits, partial=self.partial,
                 score=self.score[rows], score_hist=self.score_hist[rows], out=self.out[l],
                 workspace=self.verify_ws, stream=s)
@@ -175,13 +181,22 @@ class DecodeLoop:
             for l in range(L):
                 kc, vc, bt = self.k_caches[l], self.v_caches[l], self.block_tables[l]
                 rows = slice(l * B, (l + 1) * B)
-                _lib.vsd_append_kv(self.k_draft[l, i].unsqueeze(1), self.v_draft[l, i].unsqueeze(1),
-                                   kc, vc, bt, self.seq_len[i], pos_offset=-1, stream=s)
-                _lib.vsd_sparse_decode_attn(self.q_draft[l, i], kc, vc, bt, self.idx[rows],
-                                            self.n_sel[rows], self.tail_start, self.seq_len[i],
-                                            scale=self.scale, max_tail=self.max_tail,
-                                            out=self.draft_out[i, l], workspace=self.sparse_ws,
-                                            stream=s)
+                # the step's input token joins the cache inside the draft call; the first
+                # step records the selection's cache rows, the later steps reuse them.  A
+                # call whose predecessor is the draft call of another layer (which writes
+                # none of the inputs this one gathers from) gathers before waiting for it;
+                # the first call after the advance (which writes the tails), and with one
+                # layer every call (its predecessor wrote this layer's previous token and
+                # recorded rows), wait first
+                flags = _lib.STEP_RECORD_ROWS if i == 0 else _lib.STEP_REUSE_ROWS
+                if l > 0 or (i > 0 and L > 1):
+                    flags |= _lib.STEP_EARLY_GATHER
+                _lib.vsd_sparse_decode_attn_step(
+                    self.q_draft[l, i], kc, vc, bt, self.idx[rows], self.n_sel[rows],
+                    self.tail_start, self.seq_len[i], scale=self.scale, max_tail=self.max_tail,
+                    k_new=self.k_draft[l, i], v_new=self.v_draft[l, i],
+                    sel_rows=self.sel_rows[rows], flags=flags, out=self.draft_out[i, l],
+                    workspace=self.sparse_ws, stream=s)
         if marks and "drafted" in marks:
             marks["drafted"]()
         _lib.vsd_copy(self.state_out, self._d_state, stream=s)
@@ -193,8 +208,9 @@ class DecodeLoop:
     def launches_per_iteration(self) -> int:
         """libvsd kernel launches of one device iteration (no host copies): per layer an
         append, the verification and its merge kernel; the selection and the advance;
-        per draft step and layer an append and the draft kernel; the state copy."""
-        return self.L * 3 + 2 + self.gamma * self.L * 2 + 1
+        per draft step and layer the draft kernel (it stores its input token's K/V
+        itself); the state copy."""
+        return self.L * 3 + 2 + self.gamma * self.L + 1
 
     @property
     def h2d_bytes(self) -> int:

@@ -145,3 +145,18 @@ def test_advance_rejects_bad_arguments(lib):
     assert lib.vsd_advance_lengths(-1, 5, p, 100, p, p, p, 0, None, None) == -1
     assert lib.vsd_advance_lengths(4, -1, p, 100, p, p, p, 0, None, None) == -1
     assert lib.vsd_advance_lengths(0, 5, None, 100, None, None, None, 0, None, None) == 0
+
+
+def test_draft_step_rejects_bad_flags(lib):
+    g = _geom()
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+
+    def call(flags, rows=p, k_new=None, v_new=None):
+        return lib.vsd_sparse_decode_attn_step(ctypes.byref(g), p, k_new, v_new, p, p, p, p, p,
+                                               16, p, p, 4, rows, ctypes.c_uint(flags),
+                                               ctypes.c_float(0.088), p, None, 0, None)
+    assert call(0x8) == -1            # unknown flag
+    assert call(0x1 | 0x2) == -1      # record and reuse together
+    assert call(0x2, rows=None) == -1  # reuse without the rows
+    assert call(0x0, k_new=p) == -1   # k_new without v_new

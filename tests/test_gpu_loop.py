@@ -42,7 +42,7 @@ def _run_loop(w, layers, iterations, seed):
     dev = torch.device("cuda", 0)
     B, R, Hq, Hkv, d, gamma = w.B, w.R, w.Hq, w.Hkv, w.d, w.gamma
     prefix = list(w.prefix())
-    P_max = (max(prefix) + iterations * R + 3) // 4 * 4
+    P_max = max(prefix) + iterations * R
     batches = [make_batch(w, dev, layer=l, extra_capacity=4 * R + iterations * R)
                for l in range(layers)]
     host = [host_arrays(bt) for bt in batches]
@@ -74,7 +74,8 @@ def _run_loop(w, layers, iterations, seed):
                             range(prefix[b], prefix[b] + R), _bits(loop.h_k_verify[l, b]),
                             _bits(loop.h_v_verify[l, b]))
             o_ref, l_ref, _ = oracle.verify(_bits(loop.h_q[l]), h["k_cache"], h["v_cache"],
-                                            h["block_table"], pl, scale=w.scale, P_max=P_max)
+                                            h["block_table"], pl, scale=w.scale,
+                                            P_max=loop.row_stride)
             assert_attn_close(loop.h_out[l].float().numpy(), o_ref, "loop verify output")
             s_rows.append(oracle.score_from_logits(l_ref, pl))
         s_ref = np.concatenate(s_rows, axis=0)

@@ -483,7 +483,10 @@ def test_results_do_not_depend_on_the_split():
     """The split of the work is not part of the result: a sequence verified alone and
     inside a batch (different CTA ranges and split-K merges) agree within the attention
     tolerance with identical collected logits; a draft step planned for a longer tail
-    (more, emptier splits) gives the same output."""
+    (more, emptier splits) gives the same output bit for bit while the same one-split
+    kernel runs, and within the attention tolerance once the plan moves to the
+    persistent kernel (which folds each consumer's run of splits into one partial, so
+    its additions come in another order)."""
     from sparse_attention_speculative_gb300.synth import make_batch
     from sparse_attention_speculative_gb300.workloads import Workload
     vsd = _vsd()
@@ -511,8 +514,9 @@ def test_results_do_not_depend_on_the_split():
                                        scale=w.scale, max_tail=mt) for mt in (3, 200, 2000)]
     torch.cuda.synchronize()
     assert vsd.vsd_read_device_status() == 0
-    for o in outs[1:]:
-        assert torch.equal(o, outs[0])
+    assert torch.equal(outs[1], outs[0])  # 5 and 6 splits per pair: one split per CTA
+    assert_attn_close(outs[2].float().cpu().numpy(), outs[0].float().cpu().numpy(),
+                      "draft output, persistent plan")  # 20 splits per pair x 24 pairs
 
 
 @pytest.mark.parametrize("d,Hq,Hkv,gamma,prefix,k", [
