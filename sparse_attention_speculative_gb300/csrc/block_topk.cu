@@ -144,7 +144,8 @@ __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
   uint8_t* q_s = base + Sm::kOffQ;
   uint64_t* bar_a = reinterpret_cast<uint64_t*>(base + Sm::kOffBar);
   uint64_t* bar_s = bar_a + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_a + 2);
+  uint64_t* bar_fin = bar_a + 2;  // every product of this CTA complete (before TMEM goes back)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_a + 3);
   const int t = threadIdx.x, warp = t >> 5;
   const int G = a.G, RG = a.R * a.G;
   const int ntile = (a.nblk_max + kTcPages - 1) / kTcPages;
@@ -153,6 +154,7 @@ __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
   if (t == 0) {
     ptx::mbar_init(bar_a, 1);
     ptx::mbar_init(bar_s, 1);
+    ptx::mbar_init(bar_fin, 1);
     ptx::fence_mbarrier_init();
     ptx::tma_prefetch_desc(&kbar_map);
   }
@@ -237,6 +239,10 @@ __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
       } else {
         timed_out = true;
       }
+    }
+    // no product on a tile whose copy has not landed (the loop ends at the next vote)
+    if (__syncthreads_or(timed_out)) break;
+    if (t == 0) {
       ptx::tc_fence_after();
       constexpr uint32_t idesc = ptx::idesc_tf32_f32(128, NQ, 0, 0);
       const uint32_t aa = ptx::smem_u32(a_s), qa = ptx::smem_u32(q_s);
@@ -283,8 +289,13 @@ __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
       }
     }
   }
-  // a copy still in flight lands before the CTA leaves
-  if (t == 0 && in_flight && !ptx::mbar_wait(bar_a, a_phase)) timed_out = true;
+  // a copy still in flight lands and every product issued completes before the CTA
+  // leaves and frees its TMEM (waits with the drain limit)
+  if (t == 0) {
+    if (in_flight && !ptx::mbar_wait_drain(bar_a, a_phase)) timed_out = true;
+    ptx::umma_commit(bar_fin);  // arrives once every earlier product of this thread is done
+    if (!ptx::mbar_wait_drain(bar_fin, 0)) timed_out = true;
+  }
   if (timed_out) flag_status(a.status, VSD_DEV_TIMEOUT);
   ptx::tc_fence_before();
   __syncthreads();

@@ -11,6 +11,16 @@
 #ifndef VSD_WAIT_LIMIT_NS
 #define VSD_WAIT_LIMIT_NS 2000000000ull  // 2 s: far beyond any legitimate wait here
 #endif
+// Test builds of the library (VSD_TEST_STALLED_WAIT defined) make one wait of each
+// waiting kernel wait for a barrier that nothing completes before that kernel's end,
+// so that its time limit runs out (the failure path without a GPU fault); regular
+// builds never take this path.
+#ifdef VSD_TEST_STALLED_WAIT
+#define VSD_STALL(first) (first)
+#else
+#define VSD_STALL(first) false
+#endif
+
 // Limit of the waits that drain a kernel's own asynchronous operations before it exits
 // (after a wait above gave up): these complete unless the hardware stops, so they keep
 // the full limit even in builds that shorten VSD_WAIT_LIMIT_NS.

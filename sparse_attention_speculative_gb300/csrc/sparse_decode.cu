@@ -668,7 +668,8 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
   float* scratch = reinterpret_cast<float*>(base + Sm::kOffScratch);
   uint64_t* bar_s = reinterpret_cast<uint64_t*>(base + Sm::kOffBar);
   uint64_t* bar_o = bar_s + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 2);
+  uint64_t* bar_fin = bar_s + 2;  // every product of this CTA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 3);
   __shared__ int s_last;
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -676,6 +677,7 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
   if (t == 0) {
     ptx::mbar_init(bar_s, 1);
     ptx::mbar_init(bar_o, 1);
+    ptx::mbar_init(bar_fin, 1);
     ptx::fence_mbarrier_init();
   }
   if (warp == 0) {
@@ -790,7 +792,8 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
       }
       ptx::umma_commit(bar_s);
     }
-    if (!ptx::mbar_wait(bar_s, 0)) {
+    // (a test build waits on the end-of-kernel barrier here, which nothing completes yet)
+    if (!ptx::mbar_wait(VSD_STALL(true) ? bar_fin : bar_s, 0)) {
       timed_out = true;
       drain_s = true;
     }
@@ -899,10 +902,12 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
     }
     if (timed_out) flag_status(a.status, VSD_DEV_TIMEOUT);
   }
-  // never free TMEM under a running MMA: a product whose wait gave up is waited for
-  // again (bounded) before the columns go back
-  if (drain_s) ptx::mbar_wait_drain(bar_s, 0);
-  if (drain_o) ptx::mbar_wait_drain(bar_o, 0);
+  // never free TMEM under a running MMA: one more commit by the issuing thread arrives
+  // once every product it issued is done (waited for with the drain limit)
+  if (t == 0 && (drain_s || drain_o || work)) {
+    ptx::umma_commit(bar_fin);
+    ptx::mbar_wait_drain(bar_fin, 0);
+  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -961,7 +966,8 @@ struct WsSmem {
   static constexpr int kOffCtl = kOffMeta + kWsStages * 16 * 4;  // abort flag
   static constexpr int kCtlBytes = 64;
   static constexpr int kOffBar = kOffCtl + kCtlBytes;
-  static constexpr int kBarBytes = (2 * kWsStages + 4) * 8 + 16;  // full, empty, s[2], o[2], slot
+  // full, empty, s[2], o[2], fin[2], TMEM slot
+  static constexpr int kBarBytes = (2 * kWsStages + 6) * 8 + 16;
   // with D = 64 the PV MMA reads 16 KB past a V tile (rows never read back)
   static constexpr int kUsedA = kOffBar + kBarBytes;
   static constexpr int kUsedB = (2 * kWsStages - 1) * kTile + 2 * kHalf;
@@ -1035,7 +1041,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   uint64_t* empty = full + kWsStages;
   uint64_t* bar_s = empty + kWsStages;  // [2]
   uint64_t* bar_o = bar_s + 2;          // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o + 2);
+  uint64_t* bar_fin = bar_o + 2;        // [2] every product of a consumer complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_fin + 2);
   __shared__ int s_last[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1050,6 +1057,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     for (int c = 0; c < 2; ++c) {
       ptx::mbar_init(&bar_s[c], 1);
       ptx::mbar_init(&bar_o[c], 1);
+      ptx::mbar_init(&bar_fin[c], 1);
     }
     *abort_flag = 0;
     ptx::fence_mbarrier_init();
@@ -1244,8 +1252,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     int run_pair = -1, run_first = 0, run_count = 0, run_splits = 0;
     float m_run[G], l_run[G], o_run[G];
     uint32_t phase = 0;
-    bool drain_s = false, drain_o = false;
-    uint32_t drain_s_par = 0, drain_o_par = 0;
     const auto flush = [&]() {
       // the run's partial at the slot of its first split; the barrier orders every
       // thread's stores before the acquire-release count, whose last arrival merges
@@ -1310,7 +1316,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (run_count > 0 && (cur.pair != run_pair || !work || direct)) flush();
       const int s = j % kWsStages;
       const uint32_t use = static_cast<uint32_t>(j / kWsStages);
-      if (!ptx::mbar_wait(&full[s], use & 1u, abort_flag)) set_abort();
+      // (a test build waits on the end-of-kernel barrier for the first item, which
+      // nothing completes yet)
+      if (!(VSD_STALL(j == c) ? ptx::mbar_wait(&bar_fin[c], 0u, abort_flag)
+                              : ptx::mbar_wait(&full[s], use & 1u, abort_flag)))
+        set_abort();
       const bool stop = *abort_flag != 0;
       if (!work) {
         if (ct == 0) ptx::mbar_arrive(&empty[s]);  // nothing of this stage is read
@@ -1357,10 +1367,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (!stop && !ptx::mbar_wait(&bar_s[c], phase, abort_flag)) {
         set_abort();
         s_failed = true;
-        if (!drain_s) {
-          drain_s = true;
-          drain_s_par = phase;
-        }
       }
       ptx::tc_fence_after();
       float sv[G];  // the G real query columns (the rest are zero padding)
@@ -1428,13 +1434,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           ptx::mbar_arrive(&empty[s]);
         }
       }
-      if (!skip_pv && !ptx::mbar_wait(&bar_o[c], phase, abort_flag)) {
-        set_abort();
-        if (!drain_o) {
-          drain_o = true;
-          drain_o_par = phase;
-        }
-      }
+      if (!skip_pv && !ptx::mbar_wait(&bar_o[c], phase, abort_flag)) set_abort();
       ptx::tc_fence_after();
       // both barriers completed a phase when both products ran; after an abort the
       // phases no longer matter (no product is issued and the drain keeps its parity)
@@ -1482,9 +1482,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
     }
     if (run_count > 0) flush();
-    // products whose wait gave up are waited for again before the columns are freed
-    if (drain_s) ptx::mbar_wait_drain(&bar_s[c], drain_s_par);
-    if (drain_o) ptx::mbar_wait_drain(&bar_o[c], drain_o_par);
+    // one more commit by the issuing thread arrives once every product it issued is
+    // done (waited for with the drain limit) before the TMEM columns are freed
+    if (ct == 0) {
+      ptx::umma_commit(&bar_fin[c]);
+      ptx::mbar_wait_drain(&bar_fin[c], 0);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();

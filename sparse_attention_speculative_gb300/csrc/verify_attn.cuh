@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_empty + 2;     // [2]
   uint64_t* pv_done = p_full + 2;     // [2]
   uint64_t* q_ready = pv_done + 2;
+  uint64_t* mma_fin = q_ready + 1;    // every product of the issuer complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
   float* m2s = reinterpret_cast<float*>(misc + 320);              // [64] new running max
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(q_ready, kSoftmaxThreads);
+    mbar_init(mma_fin, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -323,10 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = it + 1;
       }
     }
-    // Never leave a copy in flight: wait (bounded) for the last stages issued.
+    // Never leave a copy in flight: wait (with the drain limit) for the last stages.
     if (lane == 0) {
       const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0;
-      for (uint32_t i = first; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1);
+      for (uint32_t i = first; i < issued; ++i) mbar_wait_drain(&full[i % S], (i / S) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -422,8 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Never leave an MMA in flight: wait (bounded) for the last PV issued.
-      if (pi > 0) mbar_wait(&pv_done[(pi - 1) % PB], ((pi - 1) / PB) & 1);
+      // Never leave an MMA in flight: one more commit arrives once every product this
+      // thread issued (QK ones after the last PV included) is done; wait for it with the
+      // drain limit before the TMEM columns go back.
+      umma_commit(mma_fin);
+      mbar_wait_drain(mma_fin, 0);
     }
     __syncwarp();
   } else {
@@ -531,7 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pb = it % PB;
         const int entry = entry_next;
         entry_next = page_entry(tile + 1);
-        if (!mbar_wait(&s_full[buf], (it >> 1) & 1, abort_flag)) set_abort();
+        // (a test build waits on the issuer's end-of-kernel barrier for the first tile,
+        // which nothing completes yet)
+        if (!(VSD_STALL(it == 0) ? mbar_wait(mma_fin, 0, abort_flag)
+                                 : mbar_wait(&s_full[buf], (it >> 1) & 1, abort_flag)))
+          set_abort();
         const int j = tile * kTile + row;
         const bool want_collect = collect && !split_collect && half == 0 && j < s.P;
         tc_fence_after();
