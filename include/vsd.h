@@ -43,6 +43,10 @@
  *     masked) and a bit is set in the device status word, read with
  *     vsd_read_device_status.  Every wait inside a kernel is bounded; a wait that
  *     gives up sets VSD_DEV_TIMEOUT and the kernel returns.
+ *   - The library looks up the device addresses of its own device variables (the
+ *     status word, the no-alloc scratch) once per device and keeps them: do not use it
+ *     across a cudaDeviceReset or anything else that destroys and recreates the
+ *     device's primary context (the kept addresses would be stale).
  */
 #ifndef VSD_H_
 #define VSD_H_

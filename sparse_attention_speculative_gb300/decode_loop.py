@@ -266,6 +266,13 @@ class DecodeLoop:
         self.stream.synchronize()
         return g
 
+    def reset_workspaces(self) -> None:
+        """Zero the draft step's workspace (its per-pair counters): needed after a call
+        whose status word showed VSD_DEV_TIMEOUT, which may leave counters behind."""
+        if self.sparse_ws is not None:
+            with torch.cuda.stream(self.stream):
+                self.sparse_ws.zero_()
+
     def synchronize(self) -> None:
         self.stream.synchronize()
 

@@ -85,3 +85,37 @@ def test_noalloc_rejects_geometry_beyond_its_scratch():
                                              None, None)
     assert rc == -4  # VSD_ERR_WORKSPACE
     np.testing.assert_equal(rc, -4)
+
+
+def test_noalloc_near_its_scratch_bound():
+    """A geometry whose partial-result scratch fills the fixed array almost to its end
+    (the last slots are where an offset error would first write past it): the same
+    results as the regular entry point."""
+    import sparse_attention_speculative_gb300 as vsd
+    from sparse_attention_speculative_gb300 import build
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    build.build()
+    torch.cuda.set_device(0)
+    lib = vsd.load()
+    limit = 16 << 20
+    chosen = None
+    for B in range(1, 200):  # 8 verify rows x 8 query heads per KV head: 33 KB slots
+        geom = vsd.Geom(B, 64, 8, 128, 16, 64, 64 * B)
+        need = ctypes.c_size_t(0)
+        assert lib.vsd_verify_workspace_size(ctypes.byref(geom), 8, 1000,
+                                             ctypes.byref(need)) == 0
+        if need.value > limit:
+            break
+        chosen = (B, need.value)
+    assert chosen is not None and chosen[1] > limit - (1 << 20), chosen
+    B = chosen[0]
+    w = Workload("noalloc_edge", B=B, P=1000, Hq=64, Hkv=8, d=128, gamma=7, k=64, n_sink=4,
+                 n_recent=16, seed=13, prefix_lens=tuple(1000 - (b * 37) % 600 for b in range(B)))
+    batch = make_batch(w, "cuda")
+    w = w.with_(prefix_lens=tuple(int(x) for x in batch.prefix_len.cpu()))
+    ref = _regular(vsd, batch, w)
+    got = _noalloc_c_abi(vsd, batch, w)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    _compare(got, ref, list(w.prefix()))
