@@ -68,14 +68,39 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments and blank-space runs (string literals are
+    kept as they are), so that edits to comments leave the digest alone."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def verify_sources_digest():
-    """Digest of the sources the verification kernel compiles from."""
+    """Digest of the code (comments left out) the verification kernels compile from."""
     csrc = os.path.join(ROOT, "sparse_attention_speculative_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("verify_attn.cuh", "verify_attn.cu", "verify_attn_d128.cu", "verify_attn_d64.cu",
-                 "ptx.cuh", "common.cuh", "launch.h"):
-        h.update(open(os.path.join(csrc, name), "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "vsd.h"), "rb").read())
+    for path in [os.path.join(csrc, name) for name in (
+            "verify_attn.cuh", "verify_attn.cu", "verify_attn_d128.cu", "verify_attn_d64.cu",
+            "ptx.cuh", "common.cuh", "launch.h")] + [os.path.join(ROOT, "include", "vsd.h")]:
+        h.update(_code_only(open(path).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -100,7 +100,10 @@ typedef struct vsd_geom {
  *   block_table    int32 [B][max_blocks_per_seq]
  *   prefix_len     int32 [B]; 0 <= P_b <= P_max and P_b + R <= max_blocks*page_size
  *   collect_row0/1 verify rows whose logits are collected (0 and R-1 = gamma for
- *                  the first draft token and the bonus token); in [0, R)
+ *                  the first draft token and the bonus token); in [0, R).  They may
+ *                  be equal: with R = 1 (no drafts) both are row 0 and the scores are
+ *                  twice that row's logits, which ranks positions exactly as the one
+ *                  row does
  *   P_max          row stride of logits / partial_scores (upper bound of P_b); a
  *                  multiple of 32 keeps every row on a 128-byte boundary, which the
  *                  stores need to cover whole 32-byte sectors (rows that start inside
