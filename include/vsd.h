@@ -246,10 +246,14 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
  *
  * vsd_select_topk_scored: vsd_select_topk on n_rows = B rows of such a score
  * (Hkv = 1) and its histogram -- the same index sets, bit for bit, as
- * vsd_select_topk on the partial scores; the kernel skips the aggregation and its
- * first two cluster rounds.  A histogram that does not match the scores (fewer
- * candidates than the budget needs) raises VSD_DEV_BAD_LENGTH and the row's selection
- * is unspecified.  Supported sizes as vsd_select_topk.
+ * vsd_select_topk on the partial scores (NaN scores excepted: their order among
+ * themselves is unspecified).  Its own kernel: a cluster of up to 16 CTAs per row,
+ * each holding a slice of the row in registers; the boundary bin's keys are exchanged
+ * once between the CTAs.  A histogram that does not match the scores (its counts are
+ * not the scores') raises VSD_DEV_BAD_LENGTH and the row's selection is unspecified;
+ * a prefix length outside [0, P_max] raises it too and leaves the row empty
+ * (n_sel = 0, all -1).  Supported: P_max <= 524288, n_rows <= 65535
+ * (VSD_ERR_UNSUPPORTED otherwise).
  * ------------------------------------------------------------------------------ */
 vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const void* q,
                                           const void* k_cache, const void* v_cache,

@@ -65,6 +65,11 @@ struct SelectArgs {
   const uint32_t* hist = nullptr;
 };
 
+// Scored input (select_scored.cu; Hkv = 1, hist given): CTAs per row for P_max, or -1
+// above 16 x 32768 positions.
+int select_scored_cluster(int P_max);
+cudaError_t launch_select_scored(const SelectArgs& a, cudaStream_t stream);
+
 int select_cluster_size(int P_max, int n_rows);
 int select_chunk(int P_max, int cs);  // prefix positions per CTA, or -1 if unsupported
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream);

@@ -486,8 +486,7 @@ vsd_status vsd_select_topk_scored(int n_rows, const float* score, const uint32_t
   if (n_rows < 0 || P_max < 0 || k < 1 || n_sink < 0 || n_recent < 0)
     return VSD_ERR_INVALID_ARG;
   if (static_cast<long long>(n_sink) + n_recent > k) return VSD_ERR_INVALID_ARG;
-  if (vsd::select_chunk(P_max, vsd::select_cluster_size(P_max, n_rows)) < 0)
-    return VSD_ERR_UNSUPPORTED;
+  if (vsd::select_scored_cluster(P_max) < 0 || n_rows > 65535) return VSD_ERR_UNSUPPORTED;
   if (n_rows == 0) return VSD_OK;
   if (!score || !score_hist || !prefix_len || !idx || !n_sel) return VSD_ERR_INVALID_ARG;
   if (!aligned(score, 16) || !aligned(score_hist, 4) || !aligned(idx, 4) ||
@@ -510,7 +509,7 @@ vsd_status vsd_select_topk_scored(int n_rows, const float* score, const uint32_t
   sa.n_sink = n_sink;
   sa.n_recent = n_recent;
   sa.hist = score_hist;
-  cudaError_t e = vsd::launch_select(sa, static_cast<cudaStream_t>(stream));
+  cudaError_t e = vsd::launch_select_scored(sa, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return VSD_OK;
 }

@@ -124,3 +124,90 @@ def test_scored_select_flags_a_foreign_histogram():
     torch.cuda.synchronize()
     assert vsd.vsd_read_device_status() == vsd.DEV_BAD_LENGTH
     assert int(n_sel[0]) == 100  # the selection itself is unspecified
+
+
+@pytest.mark.parametrize("P_max,prefix,k,ns,nr,ties", [
+    (5000, (5000, 4999, 17, 0, 300), 512, 4, 64, True),        # 8K slices, one CTA a row
+    (12001, (12001, 9000, 12000), 1024, 16, 256, False),       # 16K slices, P_max % 4 != 0
+    (32768, (32768, 32767, 2049), 2048, 16, 256, True),        # one full 32K slice
+    (70001, (70001, 65536, 32769, 100), 4096, 16, 256, True),  # 3-CTA clusters
+    (131072, (131072,), 8192, 16, 512, False),                 # 4-CTA cluster
+    (300000, (300000, 200001), 8192, 4, 64, True),             # 10-CTA clusters (beyond 8)
+])
+def test_scored_select_against_oracle(P_max, prefix, k, ns, nr, ties):
+    """The scored selection at every slice size and cluster width, ragged prefixes,
+    scores with many exact ties (small integers) or none, against the oracle's selection
+    on the same fp32 scores: identical index rows."""
+    vsd = _vsd()
+    rng = np.random.default_rng(P_max)
+    B = len(prefix)
+    if ties:
+        s = rng.integers(-20, 21, size=(B, P_max)).astype(np.float32)
+    else:
+        s = rng.normal(size=(B, P_max)).astype(np.float32)
+    pl = np.array(prefix, np.int32)
+    hist = np.zeros((B, vsd.HIST_BINS), np.uint32)
+    for b in range(B):
+        hist[b] = np.bincount(_keys(s[b, :pl[b]]) >> 20, minlength=vsd.HIST_BINS)
+    score = torch.tensor(s, device="cuda")
+    idx, n_sel = vsd.vsd_select_topk_scored(score, torch.tensor(hist.view(np.int32), device="cuda"),
+                                            torch.tensor(pl, device="cuda"), k=k, n_sink=ns,
+                                            n_recent=nr)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    want_i, want_n = oracle.select(s, pl, k=k, n_sink=ns, n_recent=nr)
+    np.testing.assert_array_equal(n_sel.cpu().numpy(), want_n)
+    np.testing.assert_array_equal(idx.cpu().numpy(), want_i)
+
+
+def test_scored_select_many_rows_and_a_bad_prefix():
+    """144 rows of a 64K prefix (one launch of 2-CTA clusters, as a 36-layer loop selects);
+    a row whose prefix length is past P_max is flagged and left empty."""
+    vsd = _vsd()
+    rng = np.random.default_rng(144)
+    n_rows, P_max = 144, 65600
+    pl = rng.integers(60000, P_max + 1, size=n_rows).astype(np.int32)
+    s = rng.normal(size=(n_rows, P_max)).astype(np.float32)
+    hist = np.zeros((n_rows, vsd.HIST_BINS), np.uint32)
+    for b in range(n_rows):
+        hist[b] = np.bincount(_keys(s[b, :pl[b]]) >> 20, minlength=vsd.HIST_BINS)
+    score = torch.tensor(s, device="cuda")
+    th = torch.tensor(hist.view(np.int32), device="cuda")
+    idx, n_sel = vsd.vsd_select_topk_scored(score, th, torch.tensor(pl, device="cuda"), k=4096,
+                                            n_sink=16, n_recent=256)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    want_i, want_n = oracle.select(s, pl, k=4096, n_sink=16, n_recent=256)
+    np.testing.assert_array_equal(idx.cpu().numpy(), want_i)
+    np.testing.assert_array_equal(n_sel.cpu().numpy(), want_n)
+    bad = pl.copy()
+    bad[3] = P_max + 1
+    idx, n_sel = vsd.vsd_select_topk_scored(score, th, torch.tensor(bad, device="cuda"), k=4096,
+                                            n_sink=16, n_recent=256)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == vsd.DEV_BAD_LENGTH
+    assert int(n_sel[3]) == 0 and bool((idx[3] == -1).all())
+    np.testing.assert_array_equal(idx.cpu().numpy()[4:], want_i[4:])
+
+
+def test_scored_select_boundary_bin_held_by_one_slice():
+    """A boundary bin of 3000 near-equal scores all in the first slice of a 32K row (more
+    than that slice's share of the exchanged list): the other route to the cut, same
+    rows as the oracle; and a bin of exactly equal scores there (ties by position)."""
+    vsd = _vsd()
+    rng = np.random.default_rng(77)
+    P = 32768
+    for equal in (False, True):
+        s = rng.uniform(-4.0, 4.0, size=(1, P)).astype(np.float32)
+        s[0, 16:3016] = 5.0 if equal else 5.0 + np.arange(3000, dtype=np.float32) * 1e-6
+        pl = np.array([P], np.int32)
+        hist = np.bincount(_keys(s[0]) >> 20, minlength=vsd.HIST_BINS).astype(np.uint32)[None]
+        idx, n_sel = vsd.vsd_select_topk_scored(torch.tensor(s, device="cuda"),
+                                                torch.tensor(hist.view(np.int32), device="cuda"),
+                                                torch.tensor(pl, device="cuda"), k=2048,
+                                                n_sink=16, n_recent=256)
+        torch.cuda.synchronize()
+        assert vsd.vsd_read_device_status() == 0
+        want_i, want_n = oracle.select(s, pl, k=2048, n_sink=16, n_recent=256)
+        np.testing.assert_array_equal(idx.cpu().numpy(), want_i)
+        np.testing.assert_array_equal(n_sel.cpu().numpy(), want_n)
