@@ -94,13 +94,19 @@ def _code_only(text: str) -> str:
 
 
 def verify_sources_digest():
-    """Digest of the code (comments left out) the verification kernels compile from."""
+    """Digest of the code (comments left out) the verification kernels compile from: their
+    own files, the PTX and common helpers, the public header and the verification part of
+    the internal launch interface."""
     csrc = os.path.join(ROOT, "sparse_attention_speculative_gb300", "csrc")
     h = hashlib.sha256()
-    for path in [os.path.join(csrc, name) for name in (
-            "verify_attn.cuh", "verify_attn.cu", "verify_attn_d128.cu", "verify_attn_d64.cu",
-            "ptx.cuh", "common.cuh", "launch.h")] + [os.path.join(ROOT, "include", "vsd.h")]:
-        h.update(_code_only(open(path).read()).encode())
+    for name in ("verify_attn.cuh", "verify_attn.cu", "verify_attn_d128.cu", "verify_attn_d64.cu",
+                 "ptx.cuh", "common.cuh"):
+        h.update(_code_only(open(os.path.join(csrc, name)).read()).encode())
+    h.update(_code_only(open(os.path.join(ROOT, "include", "vsd.h")).read()).encode())
+    launch = open(os.path.join(csrc, "launch.h")).read()
+    i = launch.index("// " + "-" * 64 + " verify")
+    j = launch.index("// " + "-" * 64, i + 10)
+    h.update(_code_only(launch[i:j]).encode())
     return h.hexdigest()[:16]
 
 
@@ -932,11 +938,20 @@ def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
         vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k, n_sink=w.n_sink,
                                    n_recent=w.n_recent, idx=idx, n_sel=n_sel)
 
-    def draft(i):
-        vsd.vsd_sparse_decode_attn(batch.q_draft[i], batch.k_cache, batch.v_cache,
-                                   batch.block_table, idx, n_sel, tail_start, seq_len[i],
-                                   scale=w.scale, max_tail=max_tail, out=d_out[i],
-                                   workspace=sws)
+    # the draft steps run as a decode loop runs them: the first step after the
+    # selection records the selected positions' cache rows, the later ones reuse them,
+    # and those whose inputs were all written two or more launches back gather before
+    # waiting for their predecessor
+    rows = torch.zeros((B, w.k), dtype=torch.int32, device=dev)
+
+    def draft(i, flags=None):
+        if flags is None:
+            flags = (vsd.STEP_RECORD_ROWS if i == 0 else
+                     vsd.STEP_REUSE_ROWS | (vsd.STEP_EARLY_GATHER if i >= 2 else 0))
+        vsd.vsd_sparse_decode_attn_step(batch.q_draft[i], batch.k_cache, batch.v_cache,
+                                        batch.block_table, idx, n_sel, tail_start, seq_len[i],
+                                        scale=w.scale, max_tail=max_tail, sel_rows=rows,
+                                        flags=flags, out=d_out[i], workspace=sws)
 
     marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3 + gamma)]
 
@@ -961,7 +976,8 @@ def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
     for name, fn in (("iteration", iteration), ("in_iteration", lambda: iteration(True)),
                      ("verify", lambda: [verify() for _ in range(chain)]),
                      ("select", lambda: [select() for _ in range(chain)]),
-                     ("draft", lambda: [draft(i % gamma) for i in range(chain)])):
+                     ("draft", lambda: [draft(i % gamma, vsd.STEP_REUSE_ROWS |
+                                              vsd.STEP_EARLY_GATHER) for i in range(chain)])):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fn()
@@ -1010,6 +1026,10 @@ def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
            "timing": "CUDA graphs, L2 flushed before every replay, medians of %d replays; "
                      "in_iteration: event records between the calls of the iteration graph; "
                      "chained: %d calls of one kind in one graph" % (reps, chain),
+           "draft_calls": "vsd_sparse_decode_attn_step as a decode loop calls it: step 0 "
+                          "records the selection's cache rows, later steps reuse them, steps "
+                          ">= 2 (chained: every call) gather before waiting for their "
+                          "predecessor",
            "shape": {"B": B, "P": w.P, "Hq": Hq, "Hkv": w.Hkv, "d": d, "gamma": gamma,
                      "k": w.k}}
     del graphs
