@@ -178,6 +178,13 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload bytes
 
+def sparse_verify_bytes(w, n_sel):
+    """Algorithmic bytes of one sparse verification: K and V of the selected positions
+    and the verify block, q in and out."""
+    kv_row = w.d * 2
+    return sum(2 * w.Hkv * (n + w.R) * kv_row + 2 * w.R * w.Hq * w.d * 2 for n in n_sel)
+
+
 def iteration_bytes(w, prefix, n_sel, tail_lens):
     """Algorithmic bytes of one iteration (per kernel), from the shapes."""
     d, Hq, Hkv, R = w.d, w.Hq, w.Hkv, w.R
@@ -953,6 +960,18 @@ def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
                                         scale=w.scale, max_tail=max_tail, sel_rows=rows,
                                         flags=flags, out=d_out[i], workspace=sws)
 
+    # Dustin's sparse verification over the selection (the fused kernel where R * G <= 32)
+    sv_geom = vsd.geom_for(B, Hq, batch.k_cache, batch.block_table)
+    nb = vsd.vsd_sparse_verify_workspace_size(sv_geom, R, w.k)
+    sv_ws = torch.zeros(nb + 256, dtype=torch.uint8, device=dev)
+    sv_ws = sv_ws[(-sv_ws.data_ptr()) % 256:][:nb]
+    sv_out = torch.empty_like(batch.q)
+
+    def sparse_verify():
+        vsd.vsd_sparse_verify_attn(batch.q, batch.k_cache, batch.v_cache, batch.block_table,
+                                   batch.prefix_len, idx, n_sel, scale=w.scale, out=sv_out,
+                                   workspace=sv_ws)
+
     marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3 + gamma)]
 
     def iteration(marked=False):
@@ -977,7 +996,8 @@ def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
                      ("verify", lambda: [verify() for _ in range(chain)]),
                      ("select", lambda: [select() for _ in range(chain)]),
                      ("draft", lambda: [draft(i % gamma, vsd.STEP_REUSE_ROWS |
-                                              vsd.STEP_EARLY_GATHER) for i in range(chain)])):
+                                              vsd.STEP_EARLY_GATHER) for i in range(chain)]),
+                     ("sparse_verify", lambda: [sparse_verify() for _ in range(chain)])):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fn()
@@ -1022,7 +1042,9 @@ def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
            "chained": {"verify_collect_scored": fig(t["verify"] / chain, vb),
                        "select_topk_scored_us": t["select"] / chain * 1e6,
                        "select_over_verify": t["select"] / t["verify"],
-                       "sparse_draft_step": fig(t["draft"] / chain, statistics.mean(spb))},
+                       "sparse_draft_step": fig(t["draft"] / chain, statistics.mean(spb)),
+                       "sparse_verify": fig(t["sparse_verify"] / chain,
+                                            sparse_verify_bytes(w, n_sel_host))},
            "timing": "CUDA graphs, L2 flushed before every replay, medians of %d replays; "
                      "in_iteration: event records between the calls of the iteration graph; "
                      "chained: %d calls of one kind in one graph" % (reps, chain),

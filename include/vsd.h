@@ -392,9 +392,13 @@ vsd_status vsd_sparse_decode_attn_step(const vsd_geom* geom, const void* q, cons
  * For sequence b with prefix length P_b, verify row t in [0, R) attends
  *   J_bt = idx[b, 0 .. n_sel[b])  followed by  P_b .. P_b + t
  *   out[b,t,h,:] = sum_{j in J_bt} softmax_j(scale * <q[b,t,h,:], K[b,j,h/G,:]>) V[b,j,h/G,:]
- * The cache must hold the verify block (positions P_b .. P_b + R - 1).  The call
- * writes the compressed cache into the workspace and runs the verification kernel on
- * it; no logits are collected.
+ * The cache must hold the verify block (positions P_b .. P_b + R - 1).  No logits are
+ * collected.  When R * G <= 32 (and the list k_max + R spans at most 1024 batches of
+ * 128) one kernel gathers the attended rows straight into shared memory, a split of
+ * 128 list positions per CTA with the R * G verify rows of a KV group as the tensor-core
+ * product's N side, the verify block masked causally, and a second kernel merges the
+ * splits; otherwise the call writes the compressed cache into the workspace and runs
+ * the verification kernel on it.
  *
  *   q          bf16 [B][R][Hq][head_dim]
  *   prefix_len int32 [B]; P_b + R <= max_blocks_per_seq * page_size
@@ -403,8 +407,9 @@ vsd_status vsd_sparse_decode_attn_step(const vsd_geom* geom, const void* q, cons
  *              VSD_DEV_BAD_INDEX and that sequence's output is unspecified
  *   out        bf16 [B][R][Hq][head_dim]
  *   workspace  >= vsd_sparse_verify_workspace_size(...) bytes, 256-byte aligned
- *              (holds the compressed cache: about 2 * B * Hkv * (k_max + R) *
- *              head_dim * 2 bytes); contents on entry are ignored
+ *              (the compressed cache, about 2 * B * Hkv * (k_max + R) * head_dim * 2
+ *              bytes, or the fused kernel's split partials, B * Hkv * splits *
+ *              R * G * (head_dim + 2) floats); contents on entry are ignored
  * Supported: as vsd_verify_attn_collect with P_max = k_max.
  * ------------------------------------------------------------------------------ */
 vsd_status vsd_sparse_verify_workspace_size(const vsd_geom* geom, int R, int k_max,

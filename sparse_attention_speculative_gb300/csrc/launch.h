@@ -133,6 +133,15 @@ struct SparseVerifyArgs {
 int sparse_verify_pages(int k_max, int R);
 cudaError_t launch_sparse_verify_gather(const SparseVerifyArgs& a, cudaStream_t stream);
 
+// Fused sparse verification (sparse_decode.cu): the draft step's tensor-core kernel with
+// the R * G verify rows of a group as its queries, when R * G <= 32 (power-of-two G) and
+// the list (k_max + R) fits 1024 batches; 0 / no bytes otherwise.  SparseArgs as for the
+// draft step with tail_start = the prefix lengths, seq_len and counters unused,
+// max_tail = R; ws holds the split partials (a second kernel merges them).
+int sparse_verify_fused_nq(int R, int G, int k_max);
+size_t sparse_verify_fused_bytes(int B, int Hkv, int R, int G, int k_max, int head_dim);
+cudaError_t launch_sparse_verify_fused(const SparseArgs& a, int R, cudaStream_t stream);
+
 // ---------------------------------------------------------------- cache bookkeeping
 // K/V rows [B][n_new][Hkv][d] stored at positions pos_base[b] + pos_offset + t.
 struct AppendArgs {

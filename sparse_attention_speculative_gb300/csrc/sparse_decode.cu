@@ -85,6 +85,8 @@ struct SParams {
   int split_len;   // positions per split (a multiple of kBatch)
   int max_splits;  // workspace slots per pair
   float scale_log2;
+  // fused sparse verification: R verify rows per sequence, log2 of the group size
+  int vrows = 0, gshift = 0;
 };
 
 // Thread layout of one warp's batch for head dimension D: a K / V row is read by
@@ -232,10 +234,12 @@ struct SSlot {
 // dims), part); part p takes partials p, p + kParts, ... with all loads of a round in
 // flight; the parts then combine in shared memory.
 // kRound: partials per load round when a thread holds one output group.
-template <int D, int G, int kSThreads, int kRound, typename Sync, typename SlotOf>
-__device__ __forceinline__ void merge_splits_by(const SParams& a, float* scratch, int pair, int b,
-                                                int g, int n, const int t, Sync sync,
-                                                SlotOf slot_of) {
+// `out_row(hh)` is where output row hh goes (null: a padding row, not written).
+template <int D, int G, int kSThreads, int kRound, typename Sync, typename SlotOf,
+          typename OutRow>
+__device__ __forceinline__ void merge_splits_rows(const SParams& a, float* scratch, int pair,
+                                                  int n, const int t, Sync sync, SlotOf slot_of,
+                                                  OutRow out_row) {
   constexpr int kQ = D / 4;
   constexpr int NG = G * kQ;                              // float4 groups of the output
   constexpr int kGPT = NG > kSThreads ? NG / kSThreads : 1;  // groups per thread
@@ -339,9 +343,20 @@ __device__ __forceinline__ void merge_splits_by(const SParams& a, float* scratch
     uint2 pk;
     pk.x = pack_bf16x2(O[i].x * inv, O[i].y * inv);
     pk.y = pack_bf16x2(O[i].z * inv, O[i].w * inv);
-    *reinterpret_cast<uint2*>(a.out + (static_cast<size_t>(b) * a.Hq + g * G + hh) * D +
-                              q4 * 4) = pk;
+    uint16_t* row = out_row(hh);
+    if (row != nullptr) *reinterpret_cast<uint2*>(row + q4 * 4) = pk;
   }
+}
+
+// The draft step's merge: output row hh of pair (b, g) is query head g * G + hh.
+template <int D, int G, int kSThreads, int kRound, typename Sync, typename SlotOf>
+__device__ __forceinline__ void merge_splits_by(const SParams& a, float* scratch, int pair, int b,
+                                                int g, int n, const int t, Sync sync,
+                                                SlotOf slot_of) {
+  merge_splits_rows<D, G, kSThreads, kRound>(
+      a, scratch, pair, n, t, sync, slot_of, [&a, b, g](int hh) {
+        return a.out + (static_cast<size_t>(b) * a.Hq + g * G + hh) * D;
+      });
 }
 
 template <int D, int G, int kSThreads, int kRound = 16>
@@ -929,6 +944,367 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
   // 24 splits per round: a head's 2048 selected positions plus its tail (17 splits)
   // merge in one round of loads
   merge_splits<D, G, kTcThreads, 24>(a, scratch, pair, b, g, n_splits);
+}
+
+// ---------------------------------------------------------------- fused sparse verification
+// Dustin's sparse verification (summary, "Verification workflow", steps 3-4) without
+// materialising the compressed cache: the tensor-core step above with the R * G verify
+// rows of a KV group on the MMA's N side (row r = t * G + h, padded to NQ = 16 or 32)
+// over the list idx[b, 0 .. n_sel) followed by the verify block P_b .. P_b + R - 1.
+// The block is masked causally: verify row t attends block position u only for u <= t.
+// One split of up to 128 list positions per CTA; a pair of more than one split writes
+// the splits' (m, l, o) to the workspace and a merge kernel (one block per output row)
+// combines them: one CTA merging all 32 rows of 17-65 splits took 9-35 us.
+template <int D, int NQ>
+struct TcvSmem {
+  static constexpr int kHalf = kBatch * 128;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kBatch * D * 2;
+  static constexpr int kQBytes = NQ * D * 2 < 2048 ? 2048 : NQ * D * 2;
+  static constexpr int kOffQ = kOffV + kBatch * D * 2;
+  static constexpr int kOffRed = kOffQ + kQBytes;         // [2][4][NQ] floats
+  static constexpr int kOffBar = kOffRed + 2 * 4 * NQ * 4;
+  static constexpr int kOffP = kOffK;  // P^T in the K tile (after its QK product)
+  static constexpr int kUsed = kOffBar + 64 > kOffV + 2 * kHalf ? kOffBar + 64 : kOffV + 2 * kHalf;
+  static constexpr int kBytes = kUsed + 1024;
+  static_assert(kOffQ % 1024 == 0 && kQBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+  static_assert(NQ * 2 <= 128, "a P^T row holds the NQ probabilities of one key");
+};
+
+// Reduce v[0 .. NQ) (NQ = 16 or 32 columns) over the warp's 32 lanes with `op`, every
+// column at once: butterfly steps that halve the columns a lane keeps (lanes with the
+// step's bit set keep the upper half), NQ - 1 shuffles plus 16 for NQ = 16, all of a
+// step independent.  Afterwards lane L holds column L % NQ.
+template <int NQ, typename Op>
+__device__ __forceinline__ float warp_reduce_columns(float (&v)[NQ], Op op) {
+  const int lane = threadIdx.x & 31;
+  if constexpr (NQ == 16) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = op(v[i], __shfl_xor_sync(0xffffffffu, v[i], 16));
+  }
+#pragma unroll
+  for (int m = NQ / 2; m >= 1; m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float send = upper ? v[i] : v[i + m];
+      const float keep = upper ? v[i + m] : v[i];
+      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, m));
+    }
+  }
+  return v[0];
+}
+
+// TMEM columns [c0, c0 + NQ) of this warp's lane quarter.
+template <int NQ>
+__device__ __forceinline__ void tmem_ld_nq(uint32_t taddr, float (&v)[NQ]) {
+  ptx::tmem_ld<16>(taddr, reinterpret_cast<uint32_t*>(v));
+  if constexpr (NQ == 32) ptx::tmem_ld<16>(taddr + 16, reinterpret_cast<uint32_t*>(v) + 16);
+  ptx::tmem_wait_ld();
+}
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SParams a) {
+  using Sm = TcvSmem<D, NQ>;
+  constexpr int LPR = D / 8;                  // 16-byte chunks per row
+  constexpr int RPI = 32 / LPR;               // rows per warp instruction
+  constexpr int QPT = NQ * LPR / kTcThreads;  // query chunks per thread
+  static_assert(NQ * LPR % kTcThreads == 0, "query staging");
+  extern __shared__ uint8_t tcv_smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(tcv_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* k_s = base + Sm::kOffK;
+  uint8_t* v_s = base + Sm::kOffV;
+  uint8_t* q_s = base + Sm::kOffQ;
+  uint8_t* p_s = base + Sm::kOffP;
+  float* red = reinterpret_cast<float*>(base + Sm::kOffRed);
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(base + Sm::kOffBar);
+  uint64_t* bar_o = bar_s + 1;
+  uint64_t* bar_fin = bar_s + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 3);
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int G = 1 << a.gshift;
+  const int NR = a.vrows << a.gshift;  // real verify rows of the group (<= NQ)
+  if (t == 0) {
+    ptx::mbar_init(bar_s, 1);
+    ptx::mbar_init(bar_o, 1);
+    ptx::mbar_init(bar_fin, 1);
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(tmem_slot, 2 * NQ);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S^T: columns [0, NQ); O^T: [NQ, 2 NQ)
+  ptx::pdl_wait_primary();  // idx / n_sel / the prefix lengths may come from the preceding kernel
+  ptx::pdl_launch_dependents();
+
+  const int lo = split * a.split_len;
+  const int j_spec = (a.idx != nullptr && lo + t < a.k_max)
+                         ? __ldcg(a.idx + static_cast<size_t>(b) * a.k_max + lo + t)
+                         : 0;
+  const int ns_raw = a.n_sel != nullptr ? __ldcg(a.n_sel + b) : 0;
+  const int P = __ldcg(a.tail_start + b);  // the prefix length: the verify block starts there
+  const SList L = attended_list(ns_raw, P, P + a.vrows, a, split == 0 && g == 0 && t == 0);
+  const bool work = lo < L.total || (split == 0 && L.total == 0);
+  const int n_splits = (L.total + a.split_len - 1) / a.split_len;
+  const bool direct = n_splits <= 1;
+  const int pair = b * a.Hkv + g;
+  bool timed_out = false, drain_s = false, drain_o = false;
+  // output row r of the pair: verify row r >> gshift, query head g * G + (r & (G - 1))
+  const auto out_row = [&](int r) -> uint16_t* {
+    if (r >= NR) return nullptr;
+    return a.out + ((static_cast<size_t>(b) * a.vrows + (r >> a.gshift)) * a.Hq + g * G +
+                    (r & (G - 1))) * D;
+  };
+
+  if (work) {
+    // ---- this thread's position -> cache row (-1: absent, zero-filled and masked)
+    const int pos = lo + t;
+    SRow rr{-1, false};
+    if (pos < L.total && pos < lo + kBatch) rr = resolve_position(a, L, b, g, pos, P + a.vrows, j_spec);
+    const int crow = rr.row;
+    const int ch = lane % LPR;
+#pragma unroll
+    for (int u = 0; u < 32 / RPI; ++u) {
+      const int rl = u * RPI + lane / LPR;
+      const int r = warp * 32 + rl;
+      const int cr = __shfl_sync(0xffffffffu, crow, rl);
+      const size_t src = cr >= 0 ? static_cast<size_t>(cr) * D + ch * 8 : 0;
+      const int off = (ch >> 3) * Sm::kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+      ptx::cp_async16(k_s + off, a.k_cache + src, cr >= 0 ? 16u : 0u);
+      ptx::cp_async16(v_s + off, a.v_cache + src, cr >= 0 ? 16u : 0u);
+    }
+    ptx::cp_async_commit();
+    // ---- the group's verify rows, padded with zeros to NQ, K-major and swizzled
+#pragma unroll
+    for (int u = 0; u < QPT; ++u) {
+      const int i = t + u * kTcThreads, r = i / LPR, c = i % LPR;
+      uint4 qv = make_uint4(0, 0, 0, 0);
+      if (r < NR)
+        qv = *reinterpret_cast<const uint4*>(
+            a.q + ((static_cast<size_t>(b) * a.vrows + (r >> a.gshift)) * a.Hq + g * G +
+                   (r & (G - 1))) * D + c * 8);
+      *reinterpret_cast<uint4*>(q_s + (c >> 3) * (NQ * 128) + r * 128 +
+                                (((c & 7) ^ (r & 7)) << 4)) = qv;
+    }
+    ptx::cp_async_wait_all();
+    ptx::fence_proxy_async_smem();
+    __syncthreads();
+
+    // ---- S^T = K Q^T  (M = 128 keys, N = NQ rows, K = head_dim)
+    if (t == 0) {
+      ptx::tc_fence_after();
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, NQ, 0, 0);
+      const uint32_t ka = ptx::smem_u32(k_s), qa = ptx::smem_u32(q_s);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int hh = kk >> 2, w = kk & 3;
+        const uint64_t ad = ptx::sdesc_sw128(ka + hh * Sm::kHalf + w * 32, 16, 1024);
+        const uint64_t bd = ptx::sdesc_sw128(qa + hh * NQ * 128 + w * 32, 16, 1024);
+        ptx::umma_bf16(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      ptx::umma_commit(bar_s);
+    }
+    if (!ptx::mbar_wait(bar_s, 0)) {
+      timed_out = true;
+      drain_s = true;
+    }
+    ptx::tc_fence_after();
+    float z[NQ];  // this key's logits for the NQ rows
+    tmem_ld_nq<NQ>(tmem + (static_cast<uint32_t>(warp * 32) << 16), z);
+    // ---- softmax per row over the CTA's keys (log2 units), the verify block masked
+    // causally: a block key at u = pos - n_sel is seen by the rows of verify row >= u
+    const bool valid = crow >= 0;
+    const int u_blk = pos - L.ns;  // < 0: a selected position, seen by every row
+#pragma unroll
+    for (int c = 0; c < NQ; ++c) {
+      const bool seen = valid && c < NR && (u_blk < 0 || u_blk <= (c >> a.gshift));
+      z[c] = seen ? z[c] * a.scale_log2 : -INFINITY;
+    }
+    // per-row maxima: one column-wise reduction over the warp's keys, the warps meet in
+    // shared memory, lane c of every warp then holds row c's maximum
+    {
+      float v[NQ];
+#pragma unroll
+      for (int c = 0; c < NQ; ++c) v[c] = z[c];
+      const float wm = warp_reduce_columns<NQ>(v, [](float x, float y) { return fmaxf(x, y); });
+      if (lane < NQ) red[warp * NQ + lane] = wm;
+    }
+    __syncthreads();
+    const int cl = lane % NQ;
+    const float m_lane =
+        fmaxf(fmaxf(red[cl], red[NQ + cl]), fmaxf(red[2 * NQ + cl], red[3 * NQ + cl]));
+    {
+      float v[NQ];
+#pragma unroll
+      for (int c = 0; c < NQ; ++c) {
+        const float m = __shfl_sync(0xffffffffu, m_lane, c);
+        const float p = (z[c] == -INFINITY) ? 0.f : exp2f(z[c] - m);
+        z[c] = p;
+        v[c] = p;
+      }
+      const float ws = warp_reduce_columns<NQ>(v, [](float x, float y) { return x + y; });
+      if (lane < NQ) red[4 * NQ + warp * NQ + lane] = ws;
+    }
+    // row t of P^T: NQ bf16 in NQ / 8 swizzled 16-byte chunks
+#pragma unroll
+    for (int k = 0; k < NQ / 8; ++k) {
+      uint4 pk;
+      pk.x = pack_bf16x2(z[k * 8 + 0], z[k * 8 + 1]);
+      pk.y = pack_bf16x2(z[k * 8 + 2], z[k * 8 + 3]);
+      pk.z = pack_bf16x2(z[k * 8 + 4], z[k * 8 + 5]);
+      pk.w = pack_bf16x2(z[k * 8 + 6], z[k * 8 + 7]);
+      *reinterpret_cast<uint4*>(p_s + t * 128 + ((k ^ (t & 7)) << 4)) = pk;
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+
+    // ---- O^T = V^T P^T  (M = 128, N = NQ, K = 128 keys); not issued after a QK wait
+    // that gave up (that product may still be running)
+    bool issued_o = false;
+    if (t == 0 && !drain_s) {
+      ptx::tc_fence_after();
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, NQ, 1, 1);
+      const uint32_t va = ptx::smem_u32(v_s), pa = ptx::smem_u32(p_s);
+#pragma unroll
+      for (int kk = 0; kk < kBatch / 16; ++kk) {
+        const uint64_t ad = ptx::sdesc_sw128(va + kk * 2048, Sm::kHalf, 1024);
+        const uint64_t bd = ptx::sdesc_sw128(pa + kk * 2048, Sm::kHalf, 1024);
+        ptx::umma_bf16(tmem + NQ, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      ptx::umma_commit(bar_o);
+      issued_o = true;
+    }
+    issued_o = __syncthreads_or(issued_o);
+    if (issued_o && !ptx::mbar_wait(bar_o, 0)) {
+      timed_out = true;
+      drain_o = true;
+    }
+    ptx::tc_fence_after();
+    if (warp < D / 32) {  // TMEM lanes 0 .. D-1 hold the output dimensions
+      float o[NQ];
+      tmem_ld_nq<NQ>(tmem + (static_cast<uint32_t>(warp * 32) << 16) + NQ, o);
+      const int dim = t;
+      if (direct) {
+#pragma unroll
+        for (int r = 0; r < NQ; ++r) {
+          uint16_t* row = out_row(r);
+          if (row == nullptr) continue;
+          const float l = red[4 * NQ + r] + red[5 * NQ + r] + red[6 * NQ + r] + red[7 * NQ + r];
+          const __nv_bfloat16 bv = __float2bfloat16_rn(l > 0.f ? o[r] / l : 0.f);
+          row[dim] = *reinterpret_cast<const uint16_t*>(&bv);
+        }
+      } else {
+        float* wsl = a.ws + (static_cast<size_t>(pair) * a.max_splits + split) * SSlot<D, NQ>::kFloats;
+#pragma unroll
+        for (int r = 0; r < NQ; ++r) wsl[SSlot<D, NQ>::kO + r * D + dim] = o[r];
+        if (dim < NQ) {  // m and l of row `dim`
+          wsl[dim] = fmaxf(fmaxf(red[dim], red[NQ + dim]), fmaxf(red[2 * NQ + dim], red[3 * NQ + dim]));
+          wsl[NQ + dim] = red[4 * NQ + dim] + red[5 * NQ + dim] + red[6 * NQ + dim] + red[7 * NQ + dim];
+        }
+      }
+    }
+    if (timed_out) flag_status(a.status, VSD_DEV_TIMEOUT);
+  }
+  // never free TMEM under a running MMA: one more commit arrives once every product this
+  // CTA issued is done (waited for with the drain limit)
+  if (t == 0 && (drain_s || drain_o || work)) {
+    ptx::umma_commit(bar_fin);
+    ptx::mbar_wait_drain(bar_fin, 0);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 2 * NQ);
+  }
+}
+
+// The splits' partials of one output row of one pair: block (row, KV head, sequence)
+// of kSvParts * D threads, thread (part, dimension); part p combines splits p,
+// p + kSvParts, ... (every load of a round in flight), then the parts combine in shared
+// memory in part order.  One part for up to 32 splits, four beyond (a 32K row's 17
+// splits: 8.8 us per call with one part, 10.1 us with four; 128K's 65 splits: 19.5 us
+// with one, 18.4 us with four).  A programmatic dependent of the kernel above (waits
+// for all its partials).
+template <int D, int NQ, int kSvParts>
+__global__ void __launch_bounds__(kSvParts * D) sparse_verify_merge_kernel(const SParams a) {
+  __shared__ float pm[kSvParts][D], pl[kSvParts][D], po[kSvParts][D];
+  const int r = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int dim = threadIdx.x % D, part = threadIdx.x / D;
+  ptx::pdl_wait_primary();
+  ptx::pdl_launch_dependents();
+  const int ns_raw = a.n_sel != nullptr ? __ldcg(a.n_sel + b) : 0;
+  const int P = __ldcg(a.tail_start + b);
+  const SList L = attended_list(ns_raw, P, P + a.vrows, a, false);
+  const int n = (L.total + a.split_len - 1) / a.split_len;
+  if (n <= 1) return;  // one split wrote its rows itself
+  constexpr int kU = kSvParts == 1 ? 32 : 16;
+  const size_t stride = SSlot<D, NQ>::kFloats;
+  const float* base = a.ws + static_cast<size_t>(b * a.Hkv + g) * a.max_splits * stride;
+  float M = -INFINITY, Ls = 0.f, O = 0.f;
+  for (int k0 = part; k0 < n; k0 += kU * kSvParts) {
+    float mk[kU], lk[kU], ok[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int k = k0 + u * kSvParts;
+      if (k < n) {
+        const float* sl = base + static_cast<size_t>(k) * stride;
+        mk[u] = __ldcg(sl + r);
+        lk[u] = __ldcg(sl + NQ + r);
+        ok[u] = __ldcg(sl + SSlot<D, NQ>::kO + r * D + dim);
+      } else {
+        mk[u] = -INFINITY;
+        lk[u] = 0.f;
+        ok[u] = 0.f;
+      }
+    }
+    float mn = M;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) mn = fmaxf(mn, mk[u]);
+    const float sc = (M == -INFINITY) ? 0.f : exp2f(M - mn);
+    Ls *= sc;
+    O *= sc;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const float w = (mk[u] == -INFINITY) ? 0.f : exp2f(mk[u] - mn);
+      Ls += w * lk[u];
+      O += w * ok[u];
+    }
+    M = mn;
+  }
+  if constexpr (kSvParts > 1) {
+    pm[part][dim] = M;
+    pl[part][dim] = Ls;
+    po[part][dim] = O;
+    __syncthreads();
+  }
+  if (part != 0) return;
+  float Lt = Ls, Ot = O;
+  if constexpr (kSvParts > 1) {
+    float mn = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kSvParts; ++q) mn = fmaxf(mn, pm[q][dim]);
+    Lt = 0.f;
+    Ot = 0.f;
+#pragma unroll
+    for (int q = 0; q < kSvParts; ++q) {
+      const float w = (pm[q][dim] == -INFINITY) ? 0.f : exp2f(pm[q][dim] - mn);
+      Lt += w * pl[q][dim];
+      Ot += w * po[q][dim];
+    }
+  }
+  const int G = 1 << a.gshift;
+  const __nv_bfloat16 bv = __float2bfloat16_rn(Lt > 0.f ? Ot / Lt : 0.f);
+  a.out[((static_cast<size_t>(b) * a.vrows + (r >> a.gshift)) * a.Hq + g * G + (r & (G - 1))) * D +
+        dim] = *reinterpret_cast<const uint16_t*>(&bv);
 }
 
 // ---------------------------------------------------------------- warp-specialised step
@@ -1549,6 +1925,42 @@ cudaError_t launch_tc(const SParams& p, int B, int Hkv, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, sparse_tc_kernel<D, G>, p);
 }
 
+template <int D, int NQ>
+cudaError_t launch_tcv(const SParams& p, int B, int Hkv, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int dev = 0, sm_count = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // as the draft step: one CTA per SM when the splits fit one wave, else as many as fit
+  const long long ctas = static_cast<long long>(p.max_splits) * Hkv * B;
+  constexpr int kSpreadSmem = 120 * 1024;
+  static_assert(TcvSmem<D, NQ>::kBytes <= kSpreadSmem, "spread reservation");
+  const int smem = ctas <= sm_count ? kSpreadSmem : TcvSmem<D, NQ>::kBytes;
+  e = cudaFuncSetAttribute(sparse_verify_tc_kernel<D, NQ>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.max_splits, Hkv, B);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, sparse_verify_tc_kernel<D, NQ>, p);
+  if (e != cudaSuccess || p.max_splits <= 1) return e;
+  cfg.gridDim = dim3(p.vrows << p.gshift, Hkv, B);
+  cfg.dynamicSmemBytes = 0;
+  if (p.max_splits <= 32) {
+    cfg.blockDim = dim3(D, 1, 1);
+    return cudaLaunchKernelEx(&cfg, sparse_verify_merge_kernel<D, NQ, 1>, p);
+  }
+  cfg.blockDim = dim3(4 * D, 1, 1);
+  return cudaLaunchKernelEx(&cfg, sparse_verify_merge_kernel<D, NQ, 4>, p);
+}
+
 template <int D, int G>
 cudaError_t launch_dg(const SParams& p, int B, int Hkv, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
@@ -1644,6 +2056,65 @@ cudaError_t launch_sparse(const SparseArgs& sa, cudaStream_t stream) {
   VSD_SPARSE_CASE(64, 8)
   VSD_SPARSE_CASE(64, 16)
 #undef VSD_SPARSE_CASE
+  return cudaErrorInvalidValue;
+}
+
+int sparse_verify_fused_nq(int R, int G, int k_max) {
+  const int nr = R * G;
+  if (nr < 1 || nr > 32 || (G & (G - 1)) != 0) return 0;
+  if (plan_sparse(k_max, R).split_len != kBatch) return 0;  // lists beyond 1024 batches
+  return nr <= 16 ? 16 : 32;
+}
+
+size_t sparse_verify_fused_bytes(int B, int Hkv, int R, int G, int k_max, int head_dim) {
+  const int nq = sparse_verify_fused_nq(R, G, k_max);
+  if (nq == 0) return 0;
+  const SparsePlan plan = plan_sparse(k_max, R);
+  return static_cast<size_t>(B) * Hkv * plan.max_splits * ((2 * nq + 3) / 4 * 4 + nq * head_dim) *
+         sizeof(float);
+}
+
+cudaError_t launch_sparse_verify_fused(const SparseArgs& sa, int R, cudaStream_t stream) {
+  if (sa.B == 0) return cudaSuccess;
+  const int nq = sparse_verify_fused_nq(R, sa.G, sa.k_max);
+  if (nq == 0) return cudaErrorInvalidValue;
+  const SparsePlan plan = plan_sparse(sa.k_max, R);
+  SParams p;
+  p.q = static_cast<const uint16_t*>(sa.q);
+  p.k_cache = static_cast<const uint16_t*>(sa.k_cache);
+  p.v_cache = static_cast<const uint16_t*>(sa.v_cache);
+  p.k_new = nullptr;
+  p.v_new = nullptr;
+  p.k_store = nullptr;
+  p.v_store = nullptr;
+  p.sel_rows = nullptr;
+  p.rows_mode = 0;
+  p.early = 0;
+  p.block_table = sa.block_table;
+  p.idx = sa.idx;
+  p.n_sel = sa.n_sel;
+  p.tail_start = sa.tail_start;  // the prefix lengths
+  p.seq_len = nullptr;
+  p.out = static_cast<uint16_t*>(sa.out);
+  p.ws = sa.ws;
+  p.counters = sa.counters;
+  p.status = sa.status;
+  p.Hq = sa.Hq;
+  p.Hkv = sa.Hkv;
+  p.max_blocks = sa.max_blocks;
+  p.num_blocks = sa.num_blocks;
+  p.k_max = sa.k_max;
+  p.split_len = plan.split_len;
+  p.max_splits = plan.max_splits;
+  p.scale_log2 = sa.scale * kLog2e;
+  p.vrows = R;
+  int gs = 0;
+  while ((1 << gs) < sa.G) ++gs;
+  p.gshift = gs;
+  if (sa.d == 128) return nq == 16 ? launch_tcv<128, 16>(p, sa.B, sa.Hkv, stream)
+                                   : launch_tcv<128, 32>(p, sa.B, sa.Hkv, stream);
+  if (sa.d == 64) return nq == 16 ? launch_tcv<64, 16>(p, sa.B, sa.Hkv, stream)
+                                  : launch_tcv<64, 32>(p, sa.B, sa.Hkv, stream);
   return cudaErrorInvalidValue;
 }
 

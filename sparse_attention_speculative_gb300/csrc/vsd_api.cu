@@ -305,9 +305,12 @@ namespace {
 
 // Workspace of sparse verification: compact K, compact V, compact block table and
 // prefix lengths, then the verification kernel's own workspace (all 256-byte aligned).
+// The workspace of a sparse verification: the compressed cache and the verification
+// kernel's partials (gather path), or the split partials (fused path).
 struct SparseVerifyLayout {
   size_t off_k, off_v, off_table, off_prefix, off_verify, total;
   int pages;
+  int fused_nq;  // > 0: the fused kernel runs
   vsd::VerifyPlan plan;
 };
 
@@ -324,7 +327,12 @@ vsd_status sparse_verify_layout(const vsd_geom* geom, int R, int k_max, int sms,
   L->off_prefix = L->off_table + round256(static_cast<size_t>(geom->B) * L->pages * 4);
   L->off_verify = L->off_prefix + round256(static_cast<size_t>(geom->B) * 4);
   L->plan = vsd::plan_verify(geom->B, geom->Hkv, R, geom->Hq / geom->Hkv, k_max, sms);
-  L->total = L->off_verify + round256(vsd::verify_workspace_bytes(L->plan, geom->head_dim));
+  const size_t gathered = L->off_verify + round256(vsd::verify_workspace_bytes(L->plan, geom->head_dim));
+  const int G = geom->Hq / geom->Hkv;
+  L->fused_nq = vsd::sparse_verify_fused_nq(R, G, k_max);
+  const size_t fused = round256(vsd::sparse_verify_fused_bytes(geom->B, geom->Hkv, R, G, k_max,
+                                                              geom->head_dim));
+  L->total = L->fused_nq > 0 ? fused : gathered;
   return VSD_OK;
 }
 
@@ -378,6 +386,35 @@ vsd_status vsd_sparse_verify_attn(const vsd_geom* geom, int R, const void* q,
   sparse_verify_layout(geom, R, k_max, sms, &L);
   if (workspace_bytes < L.total || !aligned(workspace, 256)) return VSD_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
+  if (L.fused_nq > 0) {
+    // the draft step's tensor-core kernel with the verify rows as its queries
+    vsd::SparseArgs sa;
+    sa.q = q;
+    sa.k_cache = k_cache;
+    sa.v_cache = v_cache;
+    sa.block_table = block_table;
+    sa.idx = k_max > 0 ? idx : nullptr;
+    sa.n_sel = k_max > 0 ? n_sel : nullptr;
+    sa.tail_start = prefix_len;
+    sa.seq_len = nullptr;
+    sa.out = out;
+    sa.ws = reinterpret_cast<float*>(ws);
+    sa.counters = nullptr;
+    sa.status = status;
+    sa.B = geom->B;
+    sa.Hq = geom->Hq;
+    sa.Hkv = geom->Hkv;
+    sa.G = geom->Hq / geom->Hkv;
+    sa.d = geom->head_dim;
+    sa.max_blocks = geom->max_blocks_per_seq;
+    sa.num_blocks = geom->num_blocks;
+    sa.k_max = k_max;
+    sa.max_tail = R;
+    sa.scale = scale;
+    cudaError_t e = vsd::launch_sparse_verify_fused(sa, R, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return VSD_OK;
+  }
   vsd::SparseVerifyArgs ga;
   ga.k_cache = k_cache;
   ga.v_cache = v_cache;
