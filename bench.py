@@ -1195,6 +1195,9 @@ def profile_call(args):
         elif args.profile_call == "select":
             vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k, n_sink=w.n_sink,
                                        n_recent=w.n_recent, idx=idx, n_sel=n_sel)
+        elif args.profile_call == "sparse_verify":
+            vsd.vsd_sparse_verify_attn(batch.q, batch.k_cache, batch.v_cache, batch.block_table,
+                                       batch.prefix_len, idx, n_sel, scale=w.scale)
         else:
             vsd.vsd_sparse_decode_attn(batch.q_draft[0], batch.k_cache, batch.v_cache,
                                        batch.block_table, idx, n_sel, batch.prefix_len,
@@ -1216,7 +1219,8 @@ def main():
     ap.add_argument("--impl", default="vsd", choices=["vsd", "reference"])
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
-    ap.add_argument("--profile-call", choices=["verify", "select", "draft"], default=None,
+    ap.add_argument("--profile-call", choices=["verify", "select", "draft", "sparse_verify"],
+                    default=None,
                     help="run one call of the workload --steps times and exit (for ncu)")
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip the single-layer configurations' per-call figures (loop only)")
