@@ -259,7 +259,8 @@ def run_gpu(args, world, rank, local):
                                            batch.block_table, batch.prefix_len, P_max=P_max,
                                            scale=w.scale, row0=0, row1=R - 1, logits=logits,
                                            partial=partial, score=score, score_hist=score_hist,
-                                           out=out, workspace=workspace)
+                                           n_sink=w.n_sink, n_recent=w.n_recent, out=out,
+                                           workspace=workspace)
         if events:
             ev[1].record(stream)
         vsd.vsd_select_topk_scored(score, score_hist, batch.prefix_len, k=w.k, n_sink=w.n_sink,
@@ -366,8 +367,8 @@ def run_gpu(args, world, rank, local):
                 vsd.vsd_verify_attn_collect_scored(
                     batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
                     P_max=P_max, scale=w.scale, row0=0, row1=R - 1, logits=logits,
-                    partial=partial, score=score, score_hist=score_hist, out=out,
-                    workspace=workspace)
+                    partial=partial, score=score, score_hist=score_hist, n_sink=w.n_sink,
+                    n_recent=w.n_recent, out=out, workspace=workspace)
             v1.record(stream)
             torch.cuda.synchronize()
             per["verify_scored_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
@@ -939,7 +940,8 @@ def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
                                            batch.block_table, batch.prefix_len, P_max=P_max,
                                            scale=w.scale, row0=0, row1=R - 1, logits=logits,
                                            partial=partial, score=score, score_hist=hist,
-                                           out=out, workspace=ws)
+                                           n_sink=w.n_sink, n_recent=w.n_recent, out=out,
+                                           workspace=ws)
 
     def select():
         vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k, n_sink=w.n_sink,
@@ -1181,7 +1183,7 @@ def profile_call(args):
     B, R, gamma = w.B, w.R, w.gamma
     out, logits, partial, score, hist = vsd.vsd_verify_attn_collect_scored(
         batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
-        P_max=w.P_max, scale=w.scale)
+        P_max=w.P_max, scale=w.scale, n_sink=w.n_sink, n_recent=w.n_recent)
     idx, n_sel = vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k,
                                             n_sink=w.n_sink, n_recent=w.n_recent)
     seq_len = batch.prefix_len + R
@@ -1191,7 +1193,7 @@ def profile_call(args):
                                                batch.block_table, batch.prefix_len,
                                                P_max=w.P_max, scale=w.scale, logits=logits,
                                                partial=partial, score=score, score_hist=hist,
-                                               out=out)
+                                               n_sink=w.n_sink, n_recent=w.n_recent, out=out)
         elif args.profile_call == "select":
             vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k, n_sink=w.n_sink,
                                        n_recent=w.n_recent, idx=idx, n_sel=n_sel)

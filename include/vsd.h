@@ -237,7 +237,10 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
  * be NULL, partial_scores may not) that also writes, for every sequence b,
  *   score[b][j] = sum_g partial_scores[b][g][j]   (fp32, groups in order from zero;
  *                                                  j < P_b; later entries not written)
- *   score_hist[b][i] = #{ j < P_b : key(score[b][j]) >> 20 == i },  i < 4096
+ *   score_hist[b][i] = #{ j in C_b : key(score[b][j]) >> 20 == i },  i < 4096
+ * over the selection's candidates C_b = [s, max(P_b - n_recent, s)), s = min(n_sink,
+ * P_b): the selection's protected sinks and recent window are left out (n_sink =
+ * n_recent = 0 counts every prefix position).
  * where key(x) maps the fp32 bits order-preservingly to uint32 (sign bit set for
  * x >= +0: bits | 0x80000000; else ~bits).  score fp32 [B][P_max] and score_hist
  * uint32 [B][4096] are caller-owned (4-byte aligned; the rows of several calls may
@@ -245,7 +248,9 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
  * reads a score buffer with 16-byte loads: its base must be 16-byte aligned.
  *
  * vsd_select_topk_scored: vsd_select_topk on n_rows = B rows of such a score
- * (Hkv = 1) and its histogram -- the same index sets, bit for bit, as
+ * (Hkv = 1) and its histogram (of the candidates for the same n_sink and n_recent, or
+ * of every prefix position, whose protected positions the kernel then takes out itself
+ * at the cost of one more round trip) -- the same index sets, bit for bit, as
  * vsd_select_topk on the partial scores (NaN scores excepted: their order among
  * themselves is unspecified).  Its own kernel: a cluster of up to 16 CTAs per row,
  * each holding a slice of the row in registers; the boundary bin's keys are exchanged
@@ -260,9 +265,9 @@ vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const voi
                                           const int32_t* block_table, const int32_t* prefix_len,
                                           int collect_row0, int collect_row1, int P_max,
                                           float scale, float* logits, float* partial_scores,
-                                          float* score, uint32_t* score_hist, void* out,
-                                          void* workspace, size_t workspace_bytes,
-                                          void* stream);
+                                          float* score, uint32_t* score_hist, int n_sink,
+                                          int n_recent, void* out, void* workspace,
+                                          size_t workspace_bytes, void* stream);
 
 vsd_status vsd_select_topk_scored(int n_rows, const float* score, const uint32_t* score_hist,
                                   const int32_t* prefix_len, int P_max, int k, int n_sink,

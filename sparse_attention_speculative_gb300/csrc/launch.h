@@ -40,6 +40,8 @@ struct VerifyArgs {
   // keys of those scores (zeroed by the call)
   float* score = nullptr;
   uint32_t* hist = nullptr;
+  // the histogram counts positions [min(hist_sink, P), max(P - hist_recent, that)) only
+  int hist_sink = 0, hist_recent = 0;
   float scale;
 };
 

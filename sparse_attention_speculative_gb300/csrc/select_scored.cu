@@ -13,11 +13,13 @@
 // rounds.  A row is split into slices of 4K-32K positions, one CTA (512 threads) each,
 // the CTAs of a row forming one cluster; a slice stays in registers as order-preserving
 // keys for the whole kernel.
-//   1. Every CTA loads its slice and the row's level-0 histogram (top 12 key bits),
-//      takes the sinks and the recent window out of it and finds the boundary bin, the
-//      one holding the r-th largest candidate key (r = the budget left after the
-//      protected positions).  Every CTA reaches the same bin without an exchange.
-//      Rank 0 writes the protected part of the row and its padding meanwhile.
+//   1. Every CTA loads its slice and the row's level-0 histogram (top 12 key bits) of
+//      the candidates (the verification call leaves the sinks and the recent window
+//      out of it; a histogram of every prefix position has them taken out here, from
+//      the scores) and finds the boundary bin, the one holding the r-th largest
+//      candidate key (r = the budget left after the protected positions).  Every CTA
+//      reaches the same bin without an exchange.  Rank 0 writes the protected part of
+//      the row and its padding after the exchange.
 //   2. Common case (the boundary bin holds at most 4096 keys): every CTA appends its
 //      boundary-bin keys, with their positions, to every CTA's list and posts its count
 //      of keys above the bin -- one cluster barrier -- and then resolves the cut on the
@@ -417,25 +419,15 @@ __global__ void __launch_bounds__(kScThreads, (NG <= 4 ? 2 : 1))
   __syncthreads();  // h0 copied
 
   // Candidate keys become >= 1, every other position 0 (never taken: the cut is >= 1).
-  // A single-CTA row takes its protected keys out of the histogram from registers.
 #pragma unroll
   for (int i = 0; i < NG; ++i) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int j = cb + (i * kScThreads + t) * 4 + e;
       const bool cand = j >= sink_end && j < rb;
-      if (thresh && CS == 1 && !cand && j < P) atomicSub(&h0[key[i][e] >> 20], 1u);
       key[i][e] = cand ? (key[i][e] > 1u ? key[i][e] : 1u) : 0u;
     }
   }
-  if (thresh && CS > 1) {  // protected positions of the whole row, from the scores
-    const int n_prot = sink_end + (P - rb);
-    for (int q = t; q < n_prot; q += kScThreads) {
-      const int j = q < sink_end ? q : rb + (q - sink_end);
-      atomicSub(&h0[sc_key(__ldcg(srow + j)) >> 20], 1u);
-    }
-  }
-  __syncthreads();
 
   // The cut.  List rule: taken iff key > T, or key == T at a position <= cut.
   uint32_t T = 0u;
@@ -447,6 +439,18 @@ __global__ void __launch_bounds__(kScThreads, (NG <= 4 ? 2 : 1))
   int need = 0, cnt0 = 0;
   if (thresh) {
     sc_find_bin<true>(h0, kScBins0, static_cast<uint32_t>(r), sh);
+    if (sh.f_tot != static_cast<uint32_t>(n_cand) && sh.f_tot == static_cast<uint32_t>(P)) {
+      // a histogram of every prefix position (a verification call told no sink or
+      // recent window): take the protected positions out, from the scores, and search
+      // again
+      const int n_prot = sink_end + (P - rb);
+      for (int q = t; q < n_prot; q += kScThreads) {
+        const int j = q < sink_end ? q : rb + (q - sink_end);
+        atomicSub(&h0[sc_key(__ldcg(srow + j)) >> 20], 1u);
+      }
+      __syncthreads();
+      sc_find_bin<true>(h0, kScBins0, static_cast<uint32_t>(r), sh);
+    }
     if (sh.f_bin < 0 || sh.f_tot != static_cast<uint32_t>(n_cand)) {
       // a histogram that does not count these scores: the row is unspecified
       if (rank == 0 && t == 0) flag_status(a.status, VSD_DEV_BAD_LENGTH);

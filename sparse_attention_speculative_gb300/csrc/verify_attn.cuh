@@ -103,6 +103,7 @@ struct VParams {
   const uint8_t* head_mask;  // [Hq] or NULL: only heads with a non-zero byte are collected
   float* score;              // fused aggregation outputs, or NULL (see VerifyArgs)
   uint32_t* hist;
+  int hist_sink, hist_recent;  // the histogram skips the first / last positions
   int pairs, t_max, max_chunks;
   float scale;
 };
@@ -830,6 +831,10 @@ __device__ __forceinline__ void aggregate_scores(const VParams& a, int blk) {
   const bool ok = P >= 0 && P <= a.P_max;  // else flagged by the verification kernel
   __syncthreads();
   if (ok) {
+    // the histogram counts the selection's candidates only: the sinks and the recent
+    // window (as the selection clamps them) are left out
+    const int c_lo = a.hist_sink < P ? a.hist_sink : P;
+    const int c_hi = P - a.hist_recent > c_lo ? P - a.hist_recent : c_lo;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int j = j0 + u;
@@ -837,7 +842,7 @@ __device__ __forceinline__ void aggregate_scores(const VParams& a, int blk) {
         a.score[static_cast<size_t>(b) * a.P_max + j] = s[u];
         const uint32_t bits = __float_as_uint(s[u]);
         const uint32_t key = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
-        atomicAdd(&h[key >> 20], 1u);
+        if (j >= c_lo && j < c_hi) atomicAdd(&h[key >> 20], 1u);
       }
     }
   }
@@ -969,6 +974,8 @@ inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {
   p.head_mask = va.head_mask;
   p.score = va.score;
   p.hist = va.hist;
+  p.hist_sink = va.hist_sink;
+  p.hist_recent = va.hist_recent;
   p.pairs = plan.pairs;
   p.t_max = plan.t_max;
   p.max_chunks = plan.max_chunks;

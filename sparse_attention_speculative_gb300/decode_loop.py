@@ -164,8 +164,8 @@ class DecodeLoop:
             _lib.vsd_verify_attn_collect_scored(
                 self.q[l], kc, vc, bt, self.prefix_len, P_max=self.row_stride, scale=self.scale,
                 row0=0, row1=self.R - 1, logits=self.logits, partial=self.partial,
-                score=self.score[rows], score_hist=self.score_hist[rows], out=self.out[l],
-                workspace=self.verify_ws, stream=s)
+                score=self.score[rows], score_hist=self.score_hist[rows], n_sink=self.n_sink,
+                n_recent=self.n_recent, out=self.out[l], workspace=self.verify_ws, stream=s)
         if marks and "verified" in marks:
             marks["verified"]()
         _lib.vsd_select_topk_scored(self.score, self.score_hist, self.rows_prefix, k=self.k,

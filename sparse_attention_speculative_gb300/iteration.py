@@ -111,7 +111,8 @@ class IterationGraph:
                                             self.prefix_len, P_max=self.P_max, scale=self.scale,
                                             row0=self.row0, row1=self.row1, logits=self.logits,
                                             partial=self.partial, score=self.score,
-                                            score_hist=self.score_hist, out=self.out,
+                                            score_hist=self.score_hist, n_sink=self.n_sink,
+                                            n_recent=self.n_recent, out=self.out,
                                             workspace=self.verify_ws, stream=s)
         _lib.vsd_select_topk_scored(self.score, self.score_hist, self.prefix_len, k=self.k,
                                     n_sink=self.n_sink, n_recent=self.n_recent, idx=self.idx,

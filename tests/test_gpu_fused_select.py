@@ -98,21 +98,59 @@ def test_scored_select_matches_plain_select():
 
 
 def test_fused_path_end_to_end():
-    """verify (scored) -> select (scored) selects what verify -> select selects."""
+    """verify (scored) -> select (scored) selects what verify -> select selects, with the
+    histogram of the candidates (the verification told the protected budget) and with
+    the histogram of every prefix position (the selection takes the protected ones out)."""
     from sparse_attention_speculative_gb300.synth import make_batch
     from sparse_attention_speculative_gb300.workloads import QWEN3_8B_32K as w
     vsd = _vsd()
     batch = make_batch(w, "cuda")
-    _, _, partial, score, hist = vsd.vsd_verify_attn_collect_scored(
+    i1 = n1 = None
+    for ns, nr in ((w.n_sink, w.n_recent), (0, 0)):
+        _, _, partial, score, hist = vsd.vsd_verify_attn_collect_scored(
+            batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+            P_max=w.P_max, scale=w.scale, n_sink=ns, n_recent=nr)
+        if i1 is None:
+            i1, n1 = vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
+                                         n_recent=w.n_recent)[:2]
+        i2, n2 = vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k,
+                                            n_sink=w.n_sink, n_recent=w.n_recent)
+        torch.cuda.synchronize()
+        assert vsd.vsd_read_device_status() == 0
+        assert torch.equal(i1, i2) and torch.equal(n1, n2), (ns, nr)
+
+
+@pytest.mark.parametrize("ns,nr", [(4, 32), (0, 100), (7000, 0), (16, 9000)])
+def test_candidate_histogram(ns, nr):
+    """With a protected budget the verification counts only the selection's candidates
+    [min(n_sink, P), max(P - n_recent, that)): an exact bincount of those keys, and the
+    scored selection from it equals the oracle's, on ragged prefixes (one shorter than
+    the sinks, one covered by the recent window)."""
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    prefix = (6001, 0, 1, 511, 40000)
+    w = Workload("cand", B=len(prefix), P=max(prefix), Hq=32, Hkv=8, d=128, gamma=4, k=10000,
+                 n_sink=ns, n_recent=nr, planted_frac=0.01, seed=83, prefix_lens=prefix)
+    batch = make_batch(w, "cuda")
+    score = torch.zeros((w.B, w.P_max), dtype=torch.float32, device="cuda")  # past P_b: 0
+    _, _, _, score, hist = vsd.vsd_verify_attn_collect_scored(
         batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
-        P_max=w.P_max, scale=w.scale)
-    i1, n1 = vsd.vsd_select_topk(partial, batch.prefix_len, k=w.k, n_sink=w.n_sink,
-                                 n_recent=w.n_recent)[:2]
-    i2, n2 = vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k, n_sink=w.n_sink,
-                                        n_recent=w.n_recent)
+        P_max=w.P_max, scale=w.scale, score=score, n_sink=ns, n_recent=nr)
+    idx, n_sel = vsd.vsd_select_topk_scored(score, hist, batch.prefix_len, k=w.k, n_sink=ns,
+                                            n_recent=nr)
     torch.cuda.synchronize()
     assert vsd.vsd_read_device_status() == 0
-    assert torch.equal(i1, i2) and torch.equal(n1, n2)
+    sc = score.cpu().numpy()
+    hs = hist.cpu().numpy().view(np.uint32)
+    for b, P in enumerate(prefix):
+        lo = min(ns, P)
+        hi = max(P - nr, lo)
+        np.testing.assert_array_equal(hs[b], np.bincount(_keys(sc[b, lo:hi]) >> 20,
+                                                         minlength=vsd.HIST_BINS))
+    want_i, want_n = oracle.select(sc, np.array(prefix, np.int32), k=w.k, n_sink=ns, n_recent=nr)
+    np.testing.assert_array_equal(n_sel.cpu().numpy(), want_n)
+    np.testing.assert_array_equal(idx.cpu().numpy(), want_i)
 
 
 def test_scored_select_flags_a_foreign_histogram():
