@@ -645,6 +645,63 @@ __global__ void __launch_bounds__(SCfg<G>::kThreads, 1) sparse_decode_kernel(con
 constexpr int kTcThreads = 128;
 constexpr int kTcNQ = 16;  // MMA N: query heads of the group, padded
 
+// Reduce v[0 .. G) (G a power of two up to 16) over the warp's 32 lanes with `op`, every
+// column at once: butterfly steps on the low lane bits that halve the columns a lane
+// keeps (G - 1 shuffles), then plain steps on the other bits (5 - log2 G shuffles), all
+// shuffles of a step independent.  Afterwards lane L holds column L % G.  (One shuffle
+// chain per column with a shared-memory store after each, 5 G dependent shuffles, took
+// 0.55 us of a 128-key tile's softmax at G = 4 and 1.2 us at G = 8.)
+template <int G, typename Op>
+__device__ __forceinline__ float warp_reduce_heads(float (&v)[G], Op op) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = G / 2; m >= 1; m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float send = upper ? v[i] : v[i + m];
+      const float keep = upper ? v[i + m] : v[i];
+      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, m));
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int m = 16; m >= G; m >>= 1) r = op(r, __shfl_xor_sync(0xffffffffu, r, m));
+  return r;
+}
+
+// Softmax of one 128-key tile for the G heads of a group (log2 units): the thread of
+// key t (warp `qw` of the tile's four) holds its logits sv[] (G columns of S^T), `valid`
+// false for an absent key; `red` is [2][4][kTcNQ] floats of the 128 threads, `sync`
+// their barrier.  Returns the heads' maxima in m[] and key t's probabilities in p[];
+// each warp's per-head sums are stored in red[1][qw][.] (added up by the caller after
+// its next barrier).
+template <int G, typename Sync>
+__device__ __forceinline__ void tile_softmax(const float (&sv)[G], bool valid, float scale_log2,
+                                             float* red, int qw, Sync sync, float (&m)[G],
+                                             float (&p)[G]) {
+  const int lane = threadIdx.x & 31;
+  float v[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    p[h] = valid ? sv[h] * scale_log2 : -INFINITY;
+    v[h] = p[h];
+  }
+  const float wmax = warp_reduce_heads<G>(v, [](float x, float y) { return fmaxf(x, y); });
+  if (lane < G) red[qw * kTcNQ + lane] = wmax;
+  sync();
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+    m[h] = fmaxf(fmaxf(red[h], red[kTcNQ + h]), fmaxf(red[2 * kTcNQ + h], red[3 * kTcNQ + h]));
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    p[h] = (p[h] == -INFINITY) ? 0.f : exp2f(p[h] - m[h]);
+    v[h] = p[h];
+  }
+  const float wsum = warp_reduce_heads<G>(v, [](float x, float y) { return x + y; });
+  if (lane < G) red[4 * kTcNQ + qw * kTcNQ + lane] = wsum;
+}
+
 template <int D>
 struct TcSmem {
   static constexpr int kHalf = kBatch * 128;       // one 64-column half of a K/V tile
@@ -817,28 +874,8 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
     ptx::tmem_ld<G>(tmem + (static_cast<uint32_t>(warp * 32) << 16), reinterpret_cast<uint32_t*>(sv));
     ptx::tmem_wait_ld();
     // ---- softmax over the CTA's keys, per head (log2 units)
-    const bool valid = crow >= 0;
-    float z[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      z[h] = valid ? sv[h] * a.scale_log2 : -INFINITY;
-      float mx = z[h];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      if (lane == 0) red[warp * kTcNQ + h] = mx;
-    }
-    __syncthreads();
-    float m[G], psum[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = fmaxf(fmaxf(red[h], red[kTcNQ + h]), fmaxf(red[2 * kTcNQ + h], red[3 * kTcNQ + h]));
-      const float p = (z[h] == -INFINITY) ? 0.f : exp2f(z[h] - m[h]);
-      z[h] = p;
-      float sp = p;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(0xffffffffu, sp, o);
-      if (lane == 0) red[4 * kTcNQ + warp * kTcNQ + h] = sp;
-    }
+    float m[G], z[G], psum[G];
+    tile_softmax<G>(sv, crow >= 0, a.scale_log2, red, warp, [] { __syncthreads(); }, m, z);
     // row t of P^T: 16 bf16 (heads >= G are zero) in two swizzled 16-byte chunks
     float pr[kTcNQ];
 #pragma unroll
@@ -855,9 +892,6 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-      psum[h] = red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
 
     // ---- O^T = V^T P^T (not issued by a thread whose QK wait gave up: the QK product
     // may still be running, and the output is flagged anyway)
@@ -878,6 +912,10 @@ __global__ void __launch_bounds__(kTcThreads) sparse_tc_kernel(const SParams a) 
       ptx::umma_commit(bar_o);
       issued_o = true;
     }
+    // the heads' sums while the product runs
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      psum[h] = red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
     // every thread learns whether the PV product was issued (one CTA-wide vote)
     issued_o = __syncthreads_or(issued_o);
     if (issued_o && !ptx::mbar_wait(bar_o, 0)) {
@@ -1752,27 +1790,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                       reinterpret_cast<uint32_t*>(sv));
       ptx::tmem_wait_ld();
       // ---- softmax over the item's keys, per head (log2 units)
-      float z[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        z[h] = valid ? sv[h] * a.scale_log2 : -INFINITY;
-        float mx = z[h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) red[cw * kTcNQ + h] = mx;
-      }
-      csync();
-      float m[G], psum[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        m[h] = fmaxf(fmaxf(red[h], red[kTcNQ + h]), fmaxf(red[2 * kTcNQ + h], red[3 * kTcNQ + h]));
-        const float pv = (z[h] == -INFINITY) ? 0.f : exp2f(z[h] - m[h]);
-        z[h] = pv;
-        float sp = pv;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(0xffffffffu, sp, o);
-        if (lane == 0) red[4 * kTcNQ + cw * kTcNQ + h] = sp;
-      }
+      float m[G], z[G], psum[G];
+      tile_softmax<G>(sv, valid, a.scale_log2, red, cw, csync, m, z);
       // row ct of P^T: 16 bf16 (heads >= G are zero) in two swizzled 16-byte chunks
       float pr[kTcNQ];
 #pragma unroll
@@ -1791,9 +1810,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       // a barrier that also tells every thread whether some QK wait gave up: the PV
       // product is issued only when the QK product is known to be complete
       const bool skip_pv = named_vote_or(bar_id, kTcThreads, stop || s_failed);
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-        psum[h] = red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
       // ---- O^T = V^T P^T; its completion also hands the stage back to the producer
       if (ct == 0) {
         if (!skip_pv) {
@@ -1812,6 +1828,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           ptx::mbar_arrive(&empty[s]);
         }
       }
+      // the heads' sums while the product runs
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        psum[h] = red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
       if (!skip_pv && !ptx::mbar_wait(&bar_o[c], phase, abort_flag)) set_abort();
       ptx::tc_fence_after();
       // both barriers completed a phase when both products ran; after an abort the
