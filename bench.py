@@ -386,7 +386,8 @@ def run_gpu(args, world, rank, local):
             for _ in range(B2B_CALLS):
                 vsd.vsd_sparse_verify_attn(batch.q, batch.k_cache, batch.v_cache,
                                            batch.block_table, batch.prefix_len, idx, n_sel,
-                                           scale=w.scale, out=sv_out, workspace=sv_ws)
+                                           scale=w.scale, flags=vsd.SPARSE_VERIFY_EARLY_GATHER,
+                                           out=sv_out, workspace=sv_ws)
             v1.record(stream)
             torch.cuda.synchronize()
             per["sparse_verify_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
@@ -969,10 +970,10 @@ def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
     sv_ws = sv_ws[(-sv_ws.data_ptr()) % 256:][:nb]
     sv_out = torch.empty_like(batch.q)
 
-    def sparse_verify():
+    def sparse_verify(flags=0):
         vsd.vsd_sparse_verify_attn(batch.q, batch.k_cache, batch.v_cache, batch.block_table,
-                                   batch.prefix_len, idx, n_sel, scale=w.scale, out=sv_out,
-                                   workspace=sv_ws)
+                                   batch.prefix_len, idx, n_sel, scale=w.scale, flags=flags,
+                                   out=sv_out, workspace=sv_ws)
 
     marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3 + gamma)]
 
@@ -999,7 +1000,10 @@ def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
                      ("select", lambda: [select() for _ in range(chain)]),
                      ("draft", lambda: [draft(i % gamma, vsd.STEP_REUSE_ROWS |
                                               vsd.STEP_EARLY_GATHER) for i in range(chain)]),
-                     ("sparse_verify", lambda: [sparse_verify() for _ in range(chain)])):
+                     # (back-to-back calls write nothing another call reads: the
+                     # selected rows are gathered before the dependency wait)
+                     ("sparse_verify", lambda: [sparse_verify(vsd.SPARSE_VERIFY_EARLY_GATHER)
+                                                for _ in range(chain)])):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fn()

@@ -365,10 +365,11 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
  *                  gather behind that kernel's last microseconds).  The caller promises
  *                  that the preceding kernel writes none of idx, n_sel, tail_start,
  *                  seq_len, block_table and sel_rows, nor any cache row this call reads
- *                  except at seq_len[b] - 1, and that it is a kernel of this library or a
- *                  kernel launched without programmatic dependent launch.  (Every kernel
- *                  of this library lets its dependents start only after its own wait for
- *                  its predecessor, so anything written two launches earlier is complete.)
+ *                  except at seq_len[b] - 1, and that it is a draft-step,
+ *                  sparse-verification, append or advance kernel of this library (these
+ *                  let their dependents start only after their own wait for their
+ *                  predecessor, so anything written two launches earlier is complete) or a
+ *                  kernel launched without programmatic dependent launch.
  *                  q, k_new / v_new, the workspace and out are always touched after the
  *                  wait.
  * Every other argument, result and rule as vsd_sparse_decode_attn (the workspace may be
@@ -406,6 +407,16 @@ vsd_status vsd_sparse_decode_attn_step(const vsd_geom* geom, const void* q, cons
  * the verification kernel on it.
  *
  *   q          bf16 [B][R][Hq][head_dim]
+ *   flags      0 or VSD_SPARSE_VERIFY_EARLY_GATHER (any other bit: VSD_ERR_INVALID_ARG):
+ *              the fused kernel resolves and gathers the selected positions' rows before
+ *              it waits for the preceding kernel on the stream, and the verify block's
+ *              rows and q after the wait.  The caller promises that the preceding kernel
+ *              writes none of idx, n_sel, prefix_len and block_table, nor the selected
+ *              positions' cache rows, and that it is a draft-step, sparse-verification,
+ *              append or advance kernel of this library (these let their dependents start
+ *              only after their own wait, so what was written two launches earlier is
+ *              complete) or a kernel launched without programmatic dependent launch.  The
+ *              gathered path ignores the flag.
  *   prefix_len int32 [B]; P_b + R <= max_blocks_per_seq * page_size
  *   idx        int32 [B][k_max] selected prefix positions (< P_b), n_sel int32 [B]
  *              (0 <= n_sel[b] <= k_max); a position outside [0, P_b + R) is flagged
@@ -420,11 +431,13 @@ vsd_status vsd_sparse_decode_attn_step(const vsd_geom* geom, const void* q, cons
 vsd_status vsd_sparse_verify_workspace_size(const vsd_geom* geom, int R, int k_max,
                                             size_t* bytes);
 
+#define VSD_SPARSE_VERIFY_EARLY_GATHER 0x4u
+
 vsd_status vsd_sparse_verify_attn(const vsd_geom* geom, int R, const void* q,
                                   const void* k_cache, const void* v_cache,
                                   const int32_t* block_table, const int32_t* prefix_len,
                                   const int32_t* idx, const int32_t* n_sel, int k_max,
-                                  float scale, void* out, void* workspace,
+                                  unsigned flags, float scale, void* out, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------

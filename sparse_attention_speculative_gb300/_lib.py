@@ -34,6 +34,7 @@ DEV_TIMEOUT = 0x8
 STEP_RECORD_ROWS = 0x1
 STEP_REUSE_ROWS = 0x2
 STEP_EARLY_GATHER = 0x4
+SPARSE_VERIFY_EARLY_GATHER = 0x4
 
 
 class VsdError(RuntimeError):
@@ -71,7 +72,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_verify_attn_collect_all.argtypes = [GP, I, P, P, P, P, P, I, F, P, P, P, P, SZ,
                                                     P]
         lib.vsd_sparse_verify_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
-        lib.vsd_sparse_verify_attn.argtypes = [GP, I, P, P, P, P, P, P, P, I, F, P, P, SZ, P]
+        lib.vsd_sparse_verify_attn.argtypes = [GP, I, P, P, P, P, P, P, P, I, ctypes.c_uint, F, P,
+                                                P, SZ, P]
         lib.vsd_verify_attn_collect_srh.argtypes = [GP, I, P, P, P, P, P, I, I, P, I, F, P, P, P,
                                                     P, SZ, P]
         lib.vsd_select_hybrid_workspace_size.argtypes = [I, I, ctypes.POINTER(SZ)]
@@ -334,9 +336,10 @@ def vsd_sparse_verify_workspace_size(geom: Geom, R: int, k_max: int) -> int:
 
 
 def vsd_sparse_verify_attn(q, k_cache, v_cache, block_table, prefix_len, idx, n_sel, *,
-                           scale: float, out=None, workspace=None, stream=None):
+                           scale: float, flags: int = 0, out=None, workspace=None, stream=None):
     """Sparse verification: verify row t attends idx[b, :n_sel[b]] and the verify block
-    positions P_b .. P_b + t.  q: bf16 [B, R, Hq, d]; idx: int32 [B, k_max].  Returns out."""
+    positions P_b .. P_b + t.  q: bf16 [B, R, Hq, d]; idx: int32 [B, k_max].  flags: 0 or
+    SPARSE_VERIFY_EARLY_GATHER.  Returns out."""
     lib = load()
     B, R, Hq, d = q.shape
     _need(q, torch.bfloat16, "q")
@@ -353,8 +356,8 @@ def vsd_sparse_verify_attn(q, k_cache, v_cache, block_table, prefix_len, idx, n_
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.vsd_sparse_verify_attn(ctypes.byref(geom), R, _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(block_table), _ptr(prefix_len), _ptr(idx), _ptr(n_sel),
-                                    k_max, float(scale), _ptr(out), _ptr(workspace), ws_bytes,
-                                    _stream(stream))
+                                    k_max, int(flags), float(scale), _ptr(out), _ptr(workspace),
+                                    ws_bytes, _stream(stream))
     _check(rc, "vsd_sparse_verify_attn")
     return out
 

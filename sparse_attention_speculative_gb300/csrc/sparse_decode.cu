@@ -674,9 +674,9 @@ __device__ __forceinline__ float warp_reduce_heads(float (&v)[G], Op op) {
 // key t (warp `qw` of the tile's four) holds its logits sv[] (G columns of S^T), `valid`
 // false for an absent key; `red` is [2][4][kTcNQ] floats of the 128 threads, `sync`
 // their barrier.  Returns the heads' maxima in m[] and key t's probabilities in p[];
-// each warp's per-head sums are stored in red[1][qw][.] (added up by the caller after
-// its next barrier).
-template <int G, typename Sync>
+// with kSums each warp's per-head sums are stored in red[1][qw][.] (added up by the
+// caller after its next barrier).
+template <int G, bool kSums = true, typename Sync>
 __device__ __forceinline__ void tile_softmax(const float (&sv)[G], bool valid, float scale_log2,
                                              float* red, int qw, Sync sync, float (&m)[G],
                                              float (&p)[G]) {
@@ -698,8 +698,10 @@ __device__ __forceinline__ void tile_softmax(const float (&sv)[G], bool valid, f
     p[h] = (p[h] == -INFINITY) ? 0.f : exp2f(p[h] - m[h]);
     v[h] = p[h];
   }
-  const float wsum = warp_reduce_heads<G>(v, [](float x, float y) { return x + y; });
-  if (lane < G) red[4 * kTcNQ + qw * kTcNQ + lane] = wsum;
+  if constexpr (kSums) {
+    const float wsum = warp_reduce_heads<G>(v, [](float x, float y) { return x + y; });
+    if (lane < G) red[4 * kTcNQ + qw * kTcNQ + lane] = wsum;
+  }
 }
 
 template <int D>
@@ -1079,8 +1081,13 @@ __global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SPar
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // S^T: columns [0, NQ); O^T: [NQ, 2 NQ)
-  ptx::pdl_wait_primary();  // idx / n_sel / the prefix lengths may come from the preceding kernel
-  ptx::pdl_launch_dependents();
+  // idx / n_sel / the prefix lengths may come from the preceding kernel; in the early
+  // mode they do not (nor the selected positions' cache rows): those rows are resolved
+  // and gathered before the wait, the verify block's rows and the queries after it
+  if (!a.early) {
+    ptx::pdl_wait_primary();
+    ptx::pdl_launch_dependents();
+  }
 
   const int lo = split * a.split_len;
   const int j_spec = (a.idx != nullptr && lo + t < a.k_max)
@@ -1107,17 +1114,30 @@ __global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SPar
     SRow rr{-1, false};
     if (pos < L.total && pos < lo + kBatch) rr = resolve_position(a, L, b, g, pos, P + a.vrows, j_spec);
     const int crow = rr.row;
+    const bool in_block = pos >= L.ns && pos < L.total;  // a verify-block row
     const int ch = lane % LPR;
+    // the selected (and absent) rows, or the verify block's rows
+    const auto gather = [&](bool block_rows) {
 #pragma unroll
-    for (int u = 0; u < 32 / RPI; ++u) {
-      const int rl = u * RPI + lane / LPR;
-      const int r = warp * 32 + rl;
-      const int cr = __shfl_sync(0xffffffffu, crow, rl);
-      const size_t src = cr >= 0 ? static_cast<size_t>(cr) * D + ch * 8 : 0;
-      const int off = (ch >> 3) * Sm::kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-      ptx::cp_async16(k_s + off, a.k_cache + src, cr >= 0 ? 16u : 0u);
-      ptx::cp_async16(v_s + off, a.v_cache + src, cr >= 0 ? 16u : 0u);
+      for (int u = 0; u < 32 / RPI; ++u) {
+        const int rl = u * RPI + lane / LPR;
+        const int r = warp * 32 + rl;
+        const int cr = __shfl_sync(0xffffffffu, crow, rl);
+        const bool blk = __shfl_sync(0xffffffffu, in_block, rl);
+        const size_t src = cr >= 0 ? static_cast<size_t>(cr) * D + ch * 8 : 0;
+        const int off = (ch >> 3) * Sm::kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+        if (blk == block_rows) {
+          ptx::cp_async16(k_s + off, a.k_cache + src, cr >= 0 ? 16u : 0u);
+          ptx::cp_async16(v_s + off, a.v_cache + src, cr >= 0 ? 16u : 0u);
+        }
+      }
+    };
+    gather(false);
+    if (a.early) {
+      ptx::pdl_wait_primary();
+      ptx::pdl_launch_dependents();
     }
+    gather(true);
     ptx::cp_async_commit();
     // ---- the group's verify rows, padded with zeros to NQ, K-major and swizzled
 #pragma unroll
@@ -1367,6 +1387,7 @@ struct TcItem {
 // (ws_slot), in a fixed order.
 constexpr int kWsStages = 3;
 constexpr int kWsThreads = 3 * kTcThreads;
+constexpr float kDraftTau = 8.0f;  // slack of a run's reference maximum, log2 units
 
 template <int D>
 struct WsSmem {
@@ -1460,6 +1481,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   uint64_t* bar_fin = bar_o + 2;        // [2] every product of a consumer complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_fin + 2);
   __shared__ int s_last[2];
+  __shared__ int s_raised[2];  // per consumer: the item whose logits raised the maximum
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = warp >> 2;  // 0: producer; 1, 2: consumers
@@ -1476,6 +1498,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       ptx::mbar_init(&bar_fin[c], 1);
     }
     *abort_flag = 0;
+    s_raised[0] = s_raised[1] = -1;
     ptx::fence_mbarrier_init();
   }
   if (warp == 4) {
@@ -1664,11 +1687,28 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       qnext_pair = w0.pair;
     }
     int staged_pair = -1;
-    // the running partial of this consumer's current run of one pair's splits
+    // The running partial of this consumer's current run of one pair's splits.  The
+    // run's items share one reference maximum per head, m_ref, set by the run's first
+    // item: a later item's probabilities are exp2(z - m_ref) unless one of its logits
+    // exceeds m_ref by more than kDraftTau, which the barrier before the PV product
+    // reports (and m_ref is raised, o_run and l_part rescaled).  So a later item reduces
+    // neither maxima nor sums across threads: each thread adds up the probabilities of
+    // its keys in l_part, and the run's sums are reduced once, when the run is written.
+    // (With per-item maxima and sums the two cross-warp reductions took a quarter of an
+    // item's time.)  Pairs of a single split keep the exact per-item softmax.
     int run_pair = -1, run_first = 0, run_count = 0, run_splits = 0;
-    float m_run[G], l_run[G], o_run[G];
+    float m_ref[G], l_part[G], o_run[G];
     uint32_t phase = 0;
     const auto flush = [&]() {
+      // the run's sums over every thread's keys (the first barrier: the sums' area may
+      // still be read for an earlier item)
+      float v[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) v[h] = l_part[h];
+      const float wsum = warp_reduce_heads<G>(v, [](float x, float y) { return x + y; });
+      csync();
+      if (lane < G) red[4 * kTcNQ + cw * kTcNQ + lane] = wsum;
+      csync();
       // the run's partial at the slot of its first split; the barrier orders every
       // thread's stores before the acquire-release count, whose last arrival merges
       float* wsl = a.ws + (static_cast<size_t>(run_pair) * a.max_splits + run_first) *
@@ -1680,8 +1720,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         if (h == ct) {
-          wsl[h] = m_run[h];
-          wsl[G + h] = l_run[h];
+          wsl[h] = m_ref[h];
+          wsl[G + h] =
+              red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
         }
       }
       csync();
@@ -1789,27 +1830,71 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       ptx::tmem_ld<G>(tm + (static_cast<uint32_t>(cw * 32) << 16),
                       reinterpret_cast<uint32_t*>(sv));
       ptx::tmem_wait_ld();
-      // ---- softmax over the item's keys, per head (log2 units)
-      float m[G], z[G], psum[G];
-      tile_softmax<G>(sv, valid, a.scale_log2, red, cw, csync, m, z);
-      // row ct of P^T: 16 bf16 (heads >= G are zero) in two swizzled 16-byte chunks
-      float pr[kTcNQ];
+      // ---- probabilities over the item's keys, per head (log2 units)
+      const auto write_p = [&](const float (&pv)[G]) {
+        // row ct of P^T: 16 bf16 (heads >= G are zero) in two swizzled 16-byte chunks
+        float pr[kTcNQ];
 #pragma unroll
-      for (int cc = 0; cc < kTcNQ; ++cc) pr[cc] = cc < G ? z[cc < G ? cc : 0] : 0.f;
+        for (int cc = 0; cc < kTcNQ; ++cc) pr[cc] = cc < G ? pv[cc < G ? cc : 0] : 0.f;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        uint4 pk;
-        pk.x = pack_bf16x2(pr[k * 8 + 0], pr[k * 8 + 1]);
-        pk.y = pack_bf16x2(pr[k * 8 + 2], pr[k * 8 + 3]);
-        pk.z = pack_bf16x2(pr[k * 8 + 4], pr[k * 8 + 5]);
-        pk.w = pack_bf16x2(pr[k * 8 + 6], pr[k * 8 + 7]);
-        *reinterpret_cast<uint4*>(p_s + ct * 128 + ((k ^ (ct & 7)) << 4)) = pk;
+        for (int k = 0; k < 2; ++k) {
+          uint4 pk;
+          pk.x = pack_bf16x2(pr[k * 8 + 0], pr[k * 8 + 1]);
+          pk.y = pack_bf16x2(pr[k * 8 + 2], pr[k * 8 + 3]);
+          pk.z = pack_bf16x2(pr[k * 8 + 4], pr[k * 8 + 5]);
+          pk.w = pack_bf16x2(pr[k * 8 + 6], pr[k * 8 + 7]);
+          *reinterpret_cast<uint4*>(p_s + ct * 128 + ((k ^ (ct & 7)) << 4)) = pk;
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+      };
+      float z[G], p[G], psum[G];
+      bool over = false;
+      if (direct) {
+        float m[G];
+        tile_softmax<G, true>(sv, valid, a.scale_log2, red, cw, csync, m, p);
+      } else if (run_count == 0) {
+        tile_softmax<G, false>(sv, valid, a.scale_log2, red, cw, csync, m_ref, p);
+      } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          z[h] = valid ? sv[h] * a.scale_log2 : -INFINITY;
+          over |= z[h] > m_ref[h] + kDraftTau;
+          p[h] = (z[h] == -INFINITY) ? 0.f : exp2f(z[h] - m_ref[h]);
+        }
       }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      // a barrier that also tells every thread whether some QK wait gave up: the PV
-      // product is issued only when the QK product is known to be complete
-      const bool skip_pv = named_vote_or(bar_id, kTcThreads, stop || s_failed);
+      write_p(p);
+      if (over) s_raised[c] = j;
+      // a barrier that also tells every thread whether some QK wait gave up (the PV
+      // product is issued only when the QK product is known to be complete) or some
+      // logit raised the maximum
+      bool skip_pv = named_vote_or(bar_id, kTcThreads, stop || s_failed || over);
+      if (skip_pv) {
+        const bool raised = s_raised[c] == j;
+        skip_pv = named_vote_or(bar_id, kTcThreads, stop || s_failed);
+        if (raised && !skip_pv) {
+          // the new maxima over the reference and this item's logits; the run so far
+          // is rescaled and the probabilities written again
+          float v[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) v[h] = z[h];
+          const float wmax = warp_reduce_heads<G>(v, [](float x, float y) { return fmaxf(x, y); });
+          if (lane < G) red[cw * kTcNQ + lane] = wmax;
+          csync();
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float mn = fmaxf(fmaxf(m_ref[h], fmaxf(red[h], red[kTcNQ + h])),
+                                   fmaxf(red[2 * kTcNQ + h], red[3 * kTcNQ + h]));
+            const float f = (m_ref[h] == -INFINITY) ? 0.f : exp2f(m_ref[h] - mn);
+            o_run[h] *= f;
+            l_part[h] *= f;
+            m_ref[h] = mn;
+            p[h] = (z[h] == -INFINITY) ? 0.f : exp2f(z[h] - mn);
+          }
+          write_p(p);
+          csync();
+        }
+      }
       // ---- O^T = V^T P^T; its completion also hands the stage back to the producer
       if (ct == 0) {
         if (!skip_pv) {
@@ -1828,10 +1913,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           ptx::mbar_arrive(&empty[s]);
         }
       }
-      // the heads' sums while the product runs
+      // a single split's sums while the product runs
+      if (direct) {
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        psum[h] = red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
+        for (int h = 0; h < G; ++h)
+          psum[h] = red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
+      }
       if (!skip_pv && !ptx::mbar_wait(&bar_o[c], phase, abort_flag)) set_abort();
       ptx::tc_fence_after();
       // both barriers completed a phase when both products ran; after an abort the
@@ -1861,20 +1948,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         run_splits = n_splits;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          m_run[h] = m[h];
-          l_run[h] = psum[h];
+          l_part[h] = p[h];
           o_run[h] = o[h];
         }
         run_count = 1;
       } else {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float mn = fmaxf(m_run[h], m[h]);
-          const float f0 = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - mn);
-          const float f1 = (m[h] == -INFINITY) ? 0.f : exp2f(m[h] - mn);
-          l_run[h] = l_run[h] * f0 + psum[h] * f1;
-          o_run[h] = o_run[h] * f0 + o[h] * f1;
-          m_run[h] = mn;
+          l_part[h] += p[h];
+          o_run[h] += o[h];
         }
         ++run_count;
       }
@@ -2111,7 +2193,7 @@ cudaError_t launch_sparse_verify_fused(const SparseArgs& sa, int R, cudaStream_t
   p.v_store = nullptr;
   p.sel_rows = nullptr;
   p.rows_mode = 0;
-  p.early = 0;
+  p.early = sa.early;
   p.block_table = sa.block_table;
   p.idx = sa.idx;
   p.n_sel = sa.n_sel;

@@ -852,15 +852,17 @@ __device__ __forceinline__ void aggregate_scores(const VParams& a, int blk) {
 }
 
 // Combine the partial (m, l, o) of the CTAs that shared a pair: block (pair, verify
-// row c), thread = dim.  With B = 1 a pair is spread over ~C / Hkv CTAs, so each block
-// issues the loads of up to 32 partials at once and combines them in chunk order.
+// row c), thread = dim.  Each block issues the loads of up to kU partials at once and
+// combines them in chunk order: kU = 32 where a pair is spread over many CTAs (one
+// sequence: ~C / Hkv), kU = 8 where it meets at most 8 (a batch of sequences), which
+// keeps the kernel's registers low enough for ten blocks per SM instead of four (the
+// 36-layer decode loop's 1280 merge and aggregation blocks took 2.1 waves).
 // One flat grid: blocks [0, merge_pairs * NV) merge (pair, verify row); with kAgg the
 // rest are the fused-aggregation blocks (only that variant carries their 16 KB of
 // shared memory).
-template <int D, int NQ, int G, bool kAgg>
+template <int D, int NQ, int G, bool kAgg, int kU>
 __global__ void __launch_bounds__(D) verify_merge_kernel(const VParams a, int ctas,
                                                          int merge_pairs) {
-  constexpr int kU = 32;
   const int x = blockIdx.x;
   const int dim = threadIdx.x;
   pdl_launch_dependents();
@@ -945,9 +947,16 @@ cudaError_t launch_dng(const VerifyArgs& va, const VerifyPlan& plan, const VPara
   cfg.gridDim = dim3(merge_pairs * p.NV + agg, 1, 1);
   cfg.blockDim = dim3(D, 1, 1);
   cfg.dynamicSmemBytes = 0;
+  const bool few = plan.max_chunks <= 8;  // partials per pair: one round of 8 loads
   if (agg > 0)
-    return cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G, true>, p, plan.ctas, merge_pairs);
-  return cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G, false>, p, plan.ctas, merge_pairs);
+    return few ? cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G, true, 8>, p, plan.ctas,
+                                    merge_pairs)
+               : cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G, true, 32>, p, plan.ctas,
+                                    merge_pairs);
+  return few ? cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G, false, 8>, p, plan.ctas,
+                                  merge_pairs)
+             : cudaLaunchKernelEx(&cfg, verify_merge_kernel<D, NQ, G, false, 32>, p, plan.ctas,
+                                  merge_pairs);
 }
 
 inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {

@@ -368,10 +368,11 @@ vsd_status vsd_sparse_verify_attn(const vsd_geom* geom, int R, const void* q,
                                   const void* k_cache, const void* v_cache,
                                   const int32_t* block_table, const int32_t* prefix_len,
                                   const int32_t* idx, const int32_t* n_sel, int k_max,
-                                  float scale, void* out, void* workspace,
+                                  unsigned flags, float scale, void* out, void* workspace,
                                   size_t workspace_bytes, void* stream) {
   vsd_status st = sparse_verify_checks(geom, R, k_max);
   if (st != VSD_OK) return st;
+  if ((flags & ~VSD_SPARSE_VERIFY_EARLY_GATHER) != 0u) return VSD_ERR_INVALID_ARG;
   if (geom->B == 0) return VSD_OK;
   if (!q || !k_cache || !v_cache || !block_table || !prefix_len || !out || !workspace)
     return workspace ? VSD_ERR_INVALID_ARG : VSD_ERR_WORKSPACE;
@@ -414,6 +415,7 @@ vsd_status vsd_sparse_verify_attn(const vsd_geom* geom, int R, const void* q,
     sa.k_max = k_max;
     sa.max_tail = R;
     sa.scale = scale;
+    sa.early = (flags & VSD_SPARSE_VERIFY_EARLY_GATHER) ? 1 : 0;
     cudaError_t e = vsd::launch_sparse_verify_fused(sa, R, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return VSD_OK;

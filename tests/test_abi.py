@@ -160,3 +160,12 @@ def test_draft_step_rejects_bad_flags(lib):
     assert call(0x1 | 0x2) == -1      # record and reuse together
     assert call(0x2, rows=None) == -1  # reuse without the rows
     assert call(0x0, k_new=p) == -1   # k_new without v_new
+
+
+def test_sparse_verify_rejects_bad_flags(lib):
+    g = _geom()
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 255) & ~255)
+    rc = lib.vsd_sparse_verify_attn(ctypes.byref(g), 4, p, p, p, p, p, p, p, 16,
+                                    ctypes.c_uint(0x8), ctypes.c_float(0.088), p, p, 1024, None)
+    assert rc == -1

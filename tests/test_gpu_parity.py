@@ -553,6 +553,13 @@ def test_sparse_verify(d, Hq, Hkv, gamma, prefix, k):
                                h["prefix_len"], idx.cpu().numpy(), n_sel.cpu().numpy(),
                                scale=w.scale)
     assert_attn_close(out.float().cpu().numpy(), ref, "sparse verify output")
+    # the early-gather form: the same rows, gathered before the dependency wait
+    out_early = vsd.vsd_sparse_verify_attn(batch.q, batch.k_cache, batch.v_cache,
+                                           batch.block_table, batch.prefix_len, idx, n_sel,
+                                           scale=w.scale, flags=vsd.SPARSE_VERIFY_EARLY_GATHER)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    assert torch.equal(out_early, out)
     # every prefix position selected: the same as full verification
     full = torch.full((w.B, w.P_max), -1, dtype=torch.int32, device="cuda")
     for b, P in enumerate(prefix):
