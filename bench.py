@@ -368,7 +368,8 @@ def run_gpu(args, world, rank, local):
                     batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
                     P_max=P_max, scale=w.scale, row0=0, row1=R - 1, logits=logits,
                     partial=partial, score=score, score_hist=score_hist, n_sink=w.n_sink,
-                    n_recent=w.n_recent, out=out, workspace=workspace)
+                    n_recent=w.n_recent, flags=vsd.VERIFY_EARLY_PREFETCH, out=out,
+                    workspace=workspace)
             v1.record(stream)
             torch.cuda.synchronize()
             per["verify_scored_b2b"].append(v0.elapsed_time(v1) * 1e-3 / B2B_CALLS)
@@ -937,11 +938,15 @@ def layer_figures(w, dev, peak, peak_kind, reps=10, chain=20):
                             for i in range(gamma)], dtype=torch.int32, device=dev)
 
     def verify():
+        # (its predecessor in every graph below writes neither the cache below the
+        # prefix nor the lengths or block table: the first tiles are fetched before the
+        # dependency wait)
         vsd.vsd_verify_attn_collect_scored(batch.q, batch.k_cache, batch.v_cache,
                                            batch.block_table, batch.prefix_len, P_max=P_max,
                                            scale=w.scale, row0=0, row1=R - 1, logits=logits,
                                            partial=partial, score=score, score_hist=hist,
-                                           n_sink=w.n_sink, n_recent=w.n_recent, out=out,
+                                           n_sink=w.n_sink, n_recent=w.n_recent,
+                                           flags=vsd.VERIFY_EARLY_PREFETCH, out=out,
                                            workspace=ws)
 
     def select():

@@ -241,6 +241,16 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
  * over the selection's candidates C_b = [s, max(P_b - n_recent, s)), s = min(n_sink,
  * P_b): the selection's protected sinks and recent window are left out (n_sink =
  * n_recent = 0 counts every prefix position).
+ * flags: 0 or VSD_VERIFY_EARLY_PREFETCH (any other bit: VSD_ERR_INVALID_ARG): the
+ * kernel's K and V producers issue their first stages of cache tiles that lie wholly
+ * below P_b before the call waits for the preceding kernel on the stream (which hides
+ * the pipeline's start behind that kernel).  The caller promises that the preceding
+ * kernel writes none of block_table and prefix_len nor any cache row below P_b -- a
+ * decode loop's append of the verify block (rows P_b and beyond) qualifies -- and that
+ * it is a kernel of this library or one launched without programmatic dependent launch
+ * (every kernel of this library lets its dependents start only after its own wait, so
+ * what was written two launches earlier is complete).  q, the outputs, the workspace
+ * and score_hist are touched after the wait.
  * where key(x) maps the fp32 bits order-preservingly to uint32 (sign bit set for
  * x >= +0: bits | 0x80000000; else ~bits).  score fp32 [B][P_max] and score_hist
  * uint32 [B][4096] are caller-owned (4-byte aligned; the rows of several calls may
@@ -266,8 +276,11 @@ vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const voi
                                           int collect_row0, int collect_row1, int P_max,
                                           float scale, float* logits, float* partial_scores,
                                           float* score, uint32_t* score_hist, int n_sink,
-                                          int n_recent, void* out, void* workspace,
-                                          size_t workspace_bytes, void* stream);
+                                          int n_recent, unsigned flags, void* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* stream);
+
+#define VSD_VERIFY_EARLY_PREFETCH 0x4u
 
 vsd_status vsd_select_topk_scored(int n_rows, const float* score, const uint32_t* score_hist,
                                   const int32_t* prefix_len, int P_max, int k, int n_sink,
@@ -365,11 +378,10 @@ vsd_status vsd_sparse_decode_attn(const vsd_geom* geom, const void* q, const voi
  *                  gather behind that kernel's last microseconds).  The caller promises
  *                  that the preceding kernel writes none of idx, n_sel, tail_start,
  *                  seq_len, block_table and sel_rows, nor any cache row this call reads
- *                  except at seq_len[b] - 1, and that it is a draft-step,
- *                  sparse-verification, append or advance kernel of this library (these
- *                  let their dependents start only after their own wait for their
- *                  predecessor, so anything written two launches earlier is complete) or a
- *                  kernel launched without programmatic dependent launch.
+ *                  except at seq_len[b] - 1, and that it is a kernel of this library or a
+ *                  kernel launched without programmatic dependent launch.  (Every kernel
+ *                  of this library lets its dependents start only after its own wait for
+ *                  its predecessor, so anything written two launches earlier is complete.)
  *                  q, k_new / v_new, the workspace and out are always touched after the
  *                  wait.
  * Every other argument, result and rule as vsd_sparse_decode_attn (the workspace may be
@@ -412,11 +424,11 @@ vsd_status vsd_sparse_decode_attn_step(const vsd_geom* geom, const void* q, cons
  *              it waits for the preceding kernel on the stream, and the verify block's
  *              rows and q after the wait.  The caller promises that the preceding kernel
  *              writes none of idx, n_sel, prefix_len and block_table, nor the selected
- *              positions' cache rows, and that it is a draft-step, sparse-verification,
- *              append or advance kernel of this library (these let their dependents start
- *              only after their own wait, so what was written two launches earlier is
- *              complete) or a kernel launched without programmatic dependent launch.  The
- *              gathered path ignores the flag.
+ *              positions' cache rows, and that it is a kernel of this library or a
+ *              kernel launched without programmatic dependent launch (every kernel of
+ *              this library lets its dependents start only after its own wait, so what
+ *              was written two launches earlier is complete).  The gathered path
+ *              ignores the flag.
  *   prefix_len int32 [B]; P_b + R <= max_blocks_per_seq * page_size
  *   idx        int32 [B][k_max] selected prefix positions (< P_b), n_sel int32 [B]
  *              (0 <= n_sel[b] <= k_max); a position outside [0, P_b + R) is flagged

@@ -11,6 +11,7 @@ table (``workloads.py``) and the seeded input generators (``synth.py``).
 """
 from ._lib import (DEV_BAD_BLOCK, DEV_BAD_INDEX, DEV_BAD_LENGTH, DEV_TIMEOUT, Geom,  # noqa: F401
                    SPARSE_VERIFY_EARLY_GATHER, STEP_EARLY_GATHER, STEP_RECORD_ROWS,
+                   VERIFY_EARLY_PREFETCH,
                    STEP_REUSE_ROWS,
                    VsdError, geom_for, load, vsd_read_device_status, vsd_select_topk,
                    vsd_sparse_decode_attn, vsd_sparse_workspace_size, vsd_verify_attn_collect,

@@ -35,6 +35,7 @@ STEP_RECORD_ROWS = 0x1
 STEP_REUSE_ROWS = 0x2
 STEP_EARLY_GATHER = 0x4
 SPARSE_VERIFY_EARLY_GATHER = 0x4
+VERIFY_EARLY_PREFETCH = 0x4
 
 
 class VsdError(RuntimeError):
@@ -83,7 +84,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_sparse_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
         lib.vsd_sparse_decode_attn.argtypes = [GP, P, P, P, P, P, P, I, P, P, I, F, P, P, SZ, P]
         lib.vsd_verify_attn_collect_scored.argtypes = [GP, I, P, P, P, P, P, I, I, I, F, P, P,
-                                                       P, P, I, I, P, P, SZ, P]
+                                                       P, P, I, I, ctypes.c_uint, P, P, SZ, P]
         lib.vsd_select_topk_scored.argtypes = [I, P, P, P, I, I, I, I, P, P, P]
         lib.vsd_page_key_means.argtypes = [GP, P, P, P, P, I, P, P]
         lib.vsd_copy.argtypes = [P, P, SZ, P]
@@ -483,12 +484,13 @@ HIST_BINS = 4096
 def vsd_verify_attn_collect_scored(q, k_cache, v_cache, block_table, prefix_len, *, P_max: int,
                                    scale: float, row0: int = 0, row1: Optional[int] = None,
                                    logits=None, partial=None, score=None, score_hist=None,
-                                   n_sink: int = 0, n_recent: int = 0, out=None,
+                                   n_sink: int = 0, n_recent: int = 0, flags: int = 0, out=None,
                                    workspace=None, stream=None):
     """Verification with Collect-2-Query that also sums the partial scores over the KV
     groups (score fp32 [B, P_max]) and counts the level-0 histogram (uint32-valued int32
     [B, 4096]) of the selection's candidates (the n_sink first and n_recent last prefix
-    positions left out).  Returns (out, logits, partial, score, score_hist)."""
+    positions left out).  flags: 0 or VERIFY_EARLY_PREFETCH.  Returns (out, logits,
+    partial, score, score_hist)."""
     lib = load()
     B, R, Hq, d = q.shape
     _need(q, torch.bfloat16, "q")
@@ -512,7 +514,7 @@ def vsd_verify_attn_collect_scored(q, k_cache, v_cache, block_table, prefix_len,
                                             int(row0), int(row1), int(P_max), float(scale),
                                             _ptr(logits), _ptr(partial), _ptr(score),
                                             _ptr(score_hist), int(n_sink), int(n_recent),
-                                            _ptr(out), _ptr(workspace), ws_bytes,
+                                            int(flags), _ptr(out), _ptr(workspace), ws_bytes,
                                             _stream(stream))
     _check(rc, "vsd_verify_attn_collect_scored")
     return out, logits, partial, score, score_hist

@@ -52,8 +52,8 @@ __global__ void __launch_bounds__(kMeanWarps * 32) page_mean_kernel(const BlockT
   const int b = blockIdx.z, g = blockIdx.y;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int beta = blockIdx.x * kMeanWarps + w;
-  ptx::pdl_launch_dependents();
   ptx::pdl_wait_primary();  // the cache and the lengths may come from the preceding kernel
+  ptx::pdl_launch_dependents();
   const int P = __ldcg(a.prefix_len + b);
   const int nblk = (P + kPageB - 1) / kPageB;
   if (P < 0 || static_cast<long long>(P) > static_cast<long long>(a.max_blocks) * kPageB ||
@@ -166,8 +166,8 @@ __global__ void __launch_bounds__(kTcScoreThreads) block_score_tc_kernel(
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  ptx::pdl_launch_dependents();
   ptx::pdl_wait_primary();  // the page means come from the preceding kernel
+  ptx::pdl_launch_dependents();
 
   // tile id -> its (sequence, KV group) pair bg = b * Hkv + g and first page; a tile has
   // work when its sequence's length is valid and reaches the tile
@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 6 : 1) block_select_kernel(con
   const int b = row / (a.R * a.Hq);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   int32_t* out = a.blocks + static_cast<size_t>(row) * a.kb;
-  ptx::pdl_launch_dependents();
   ptx::pdl_wait_primary();  // the scores come from the preceding kernel
+  ptx::pdl_launch_dependents();
   const int P = __ldcg(a.prefix_len + b);
   int nblk = (P + kPageB - 1) / kPageB;
   if (P < 0 || nblk > a.nblk_max) nblk = 0;  // flagged by the score kernel

@@ -17,8 +17,8 @@ constexpr int kCopyThreads = 256;
 __global__ void __launch_bounds__(kCopyThreads) copy16_kernel(uint4* __restrict__ dst,
                                                               const uint4* __restrict__ src,
                                                               size_t n16) {
-  ptx::pdl_launch_dependents();
   ptx::pdl_wait_primary();  // the source may come from the preceding kernel
+  ptx::pdl_launch_dependents();
   for (size_t i = static_cast<size_t>(blockIdx.x) * kCopyThreads + threadIdx.x; i < n16;
        i += static_cast<size_t>(gridDim.x) * kCopyThreads)
     dst[i] = src[i];

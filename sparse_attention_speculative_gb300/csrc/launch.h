@@ -42,6 +42,7 @@ struct VerifyArgs {
   uint32_t* hist = nullptr;
   // the histogram counts positions [min(hist_sink, P), max(P - hist_recent, that)) only
   int hist_sink = 0, hist_recent = 0;
+  int early = 0;  // producers issue their first prefix tiles before the dependency wait
   float scale;
 };
 

@@ -326,7 +326,6 @@ __global__ void __launch_bounds__(kScThreads, (NG <= 4 ? 2 : 1))
   const int row = blockIdx.y;
   const int t = threadIdx.x;
 
-  ptx::pdl_launch_dependents();
   for (int i = t; i < 2 * kScBinsL; i += kScThreads) {
     (&sh.hl[0][0])[i] = 0u;
     (&sh.hs[0][0])[i] = 0u;
@@ -351,6 +350,7 @@ __global__ void __launch_bounds__(kScThreads, (NG <= 4 ? 2 : 1))
   bool done_arrived = false;  // list path: arrived after the last shared-memory exchange
   if (arrived) sc_cluster_arrive();
   ptx::pdl_wait_primary();  // the scores and the histogram come from the preceding kernels
+  ptx::pdl_launch_dependents();
 
   const int P_raw = __ldcg(a.prefix_len + row);
   const float* srow = a.score + static_cast<size_t>(row) * a.P_max;

@@ -296,7 +296,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   const int KPT = chunk / kSelThreads;  // 4, 8, 16 or 32 positions per thread
   const SelLayout L = sel_layout(sel_smem, chunk);
 
-  ptx::pdl_launch_dependents();
   // rank 0's cluster-wide arrays start at zero before anyone adds to them
   if (rank == 0)
     for (int i = t; i < kBins0 + 2 * kBinsL; i += kSelThreads) L.ghist[i] = 0u;
@@ -305,6 +304,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const SelPa
   __syncthreads();
   cluster_arrive();  // this CTA's shared memory is ready; waited on before remote use
   ptx::pdl_wait_primary();  // the partial scores come from the preceding kernels
+  ptx::pdl_launch_dependents();
 
   // Sums of 4 consecutive positions over the KV groups (fp32, groups in order).  Every
   // position below P_max is valid memory, so the first group of 4 is loaded before

@@ -104,6 +104,7 @@ struct VParams {
   float* score;              // fused aggregation outputs, or NULL (see VerifyArgs)
   uint32_t* hist;
   int hist_sink, hist_recent;  // the histogram skips the first / last positions
+  int early;  // the K / V producers issue their first stages before the dependency wait
   int pairs, t_max, max_chunks;
   float scale;
 };
@@ -239,11 +240,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_launch_dependents();  // the next kernel on the stream may become resident
-  pdl_wait_primary();       // inputs may come from the preceding kernel on the stream
-  if (a.hist != nullptr) {
-    // the aggregation in the merge kernel adds into a zeroed histogram
-    for (int i = blockIdx.x * kThreads + threadIdx.x; i < a.B * kHistBins; i += gridDim.x * kThreads)
+  // Inputs may come from the preceding kernel on the stream: every warp waits for it
+  // here, except in the early mode the two producers, which wait once they have issued
+  // their first stages of tiles wholly inside the prefix (below).
+  const bool producer = warp == 0 || warp == kVWarp;
+  if (!(producer && a.early)) {
+    pdl_wait_primary();
+    pdl_launch_dependents();
+  }
+  if (a.hist != nullptr && !producer) {
+    // the aggregation in the merge kernel adds into a zeroed histogram (zeroed by the
+    // warps between the producers, after their wait)
+    constexpr int kZeroThreads = kThreads - 64;
+    for (int i = blockIdx.x * kZeroThreads + threadIdx.x - 32; i < a.B * kHistBins;
+         i += gridDim.x * kZeroThreads)
       a.hist[i] = 0u;
   }
   const uint32_t tmem_s0 = tmem;       // S^T buffer b: columns [64 b, 64 b + NQ)
@@ -274,6 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol = l2_policy_evict_first();
     if (lane == 0) tma_prefetch_desc(map);
     uint32_t it = 0, issued = 0;
+    // In the early mode the first S tiles are issued before the dependency wait when
+    // they lie wholly inside the prefix (the preceding kernel may write the verify
+    // block's rows, at P and beyond; the block table, the prefix lengths and the rows
+    // below P are the caller's promise)
+    bool waited = a.early == 0;
     for (long long v = v0; v < v1;) {
       // Block-table entries come 4 tiles (32 pages, one per lane) per load round and
       // two rounds ahead; the first two rounds are issued together with the prefix
@@ -304,6 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool inside = lane < kPagesPerTile && lp * kPage < s.L;
         const bool bad = inside && (e < 0 || e >= a.num_blocks);
         const int blk = (inside && !bad) ? e : a.num_blocks;
+        if (!waited && (it >= static_cast<uint32_t>(S) || (tile + 1) * kTile > s.P)) {
+          pdl_wait_primary();
+          pdl_launch_dependents();
+          waited = true;
+        }
         const int stage = it % S;
         const uint32_t use = it / S;
         int ok = 1;
@@ -325,6 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issued = it + 1;
       }
+    }
+    if (!waited) {
+      pdl_wait_primary();
+      pdl_launch_dependents();
     }
     // Never leave a copy in flight: wait (with the drain limit) for the last stages.
     if (lane == 0) {
@@ -865,8 +889,8 @@ __global__ void __launch_bounds__(D) verify_merge_kernel(const VParams a, int ct
                                                          int merge_pairs) {
   const int x = blockIdx.x;
   const int dim = threadIdx.x;
-  pdl_launch_dependents();
   pdl_wait_primary();  // partials of the verification kernel are complete
+  pdl_launch_dependents();
   if (x >= merge_pairs * a.NV) {
     if constexpr (kAgg) aggregate_scores<D>(a, x - merge_pairs * a.NV);
     return;
@@ -984,6 +1008,7 @@ inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {
   p.score = va.score;
   p.hist = va.hist;
   p.hist_sink = va.hist_sink;
+  p.early = va.early;
   p.hist_recent = va.hist_recent;
   p.pairs = plan.pairs;
   p.t_max = plan.t_max;

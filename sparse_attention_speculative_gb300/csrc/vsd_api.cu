@@ -186,7 +186,8 @@ vsd_status verify_call(const vsd_geom* geom, int R, const void* q, const void* k
                        int collect_row1, const uint8_t* head_mask, int P_max, float scale,
                        float* logits, float* partial_scores, void* out, void* workspace,
                        size_t workspace_bytes, void* stream, float* score = nullptr,
-                       uint32_t* hist = nullptr, int hist_sink = 0, int hist_recent = 0) {
+                       uint32_t* hist = nullptr, int hist_sink = 0, int hist_recent = 0,
+                       int early = 0) {
   vsd_status st = verify_checks(geom, R, P_max);
   if (st != VSD_OK) return st;
   // all rows: the two halves of every key's columns meet in the part of the Q
@@ -242,6 +243,7 @@ vsd_status verify_call(const vsd_geom* geom, int R, const void* q, const void* k
   va.hist = hist;
   va.hist_sink = hist_sink;
   va.hist_recent = hist_recent;
+  va.early = early;
   va.scale = scale;
   cudaError_t e = vsd::launch_verify(va, plan, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -280,9 +282,11 @@ vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const voi
                                           int collect_row0, int collect_row1, int P_max,
                                           float scale, float* logits, float* partial_scores,
                                           float* score, uint32_t* score_hist, int n_sink,
-                                          int n_recent, void* out, void* workspace,
-                                          size_t workspace_bytes, void* stream) {
+                                          int n_recent, unsigned flags, void* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* stream) {
   if (n_sink < 0 || n_recent < 0) return VSD_ERR_INVALID_ARG;
+  if ((flags & ~VSD_VERIFY_EARLY_PREFETCH) != 0u) return VSD_ERR_INVALID_ARG;
   if (partial_scores == nullptr || score == nullptr || score_hist == nullptr)
     return geom != nullptr && geom->B == 0 ? VSD_OK : VSD_ERR_INVALID_ARG;
   // the aggregation writes the score one float at a time: 4-byte alignment suffices
@@ -290,7 +294,8 @@ vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const voi
   return verify_call(geom, R, q, k_cache, v_cache, block_table, prefix_len, false,
                      collect_row0, collect_row1, nullptr, P_max, scale, logits,
                      partial_scores, out, workspace, workspace_bytes, stream, score,
-                     score_hist, n_sink, n_recent);
+                     score_hist, n_sink, n_recent,
+                     (flags & VSD_VERIFY_EARLY_PREFETCH) ? 1 : 0);
 }
 
 vsd_status vsd_verify_attn_collect_all(const vsd_geom* geom, int R, const void* q,

@@ -161,11 +161,14 @@ class DecodeLoop:
             rows = slice(l * B, (l + 1) * B)
             _lib.vsd_append_kv(self.k_verify[l], self.v_verify[l], kc, vc, bt, self.prefix_len,
                                pos_offset=0, stream=s)
+            # the append writes the verify block's rows only (at the prefix length and
+            # beyond): the prefix's first tiles are fetched before waiting for it
             _lib.vsd_verify_attn_collect_scored(
                 self.q[l], kc, vc, bt, self.prefix_len, P_max=self.row_stride, scale=self.scale,
                 row0=0, row1=self.R - 1, logits=self.logits, partial=self.partial,
                 score=self.score[rows], score_hist=self.score_hist[rows], n_sink=self.n_sink,
-                n_recent=self.n_recent, out=self.out[l], workspace=self.verify_ws, stream=s)
+                n_recent=self.n_recent, flags=_lib.VERIFY_EARLY_PREFETCH, out=self.out[l],
+                workspace=self.verify_ws, stream=s)
         if marks and "verified" in marks:
             marks["verified"]()
         _lib.vsd_select_topk_scored(self.score, self.score_hist, self.rows_prefix, k=self.k,

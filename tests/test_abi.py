@@ -169,3 +169,13 @@ def test_sparse_verify_rejects_bad_flags(lib):
     rc = lib.vsd_sparse_verify_attn(ctypes.byref(g), 4, p, p, p, p, p, p, p, 16,
                                     ctypes.c_uint(0x8), ctypes.c_float(0.088), p, p, 1024, None)
     assert rc == -1
+
+
+def test_scored_verify_rejects_bad_flags(lib):
+    g = _geom()
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 255) & ~255)
+    rc = lib.vsd_verify_attn_collect_scored(ctypes.byref(g), 4, p, p, p, p, p, 0, 3, 1024,
+                                            ctypes.c_float(0.088), None, p, p, p, 0, 0,
+                                            ctypes.c_uint(0x1), p, p, 1024, None)
+    assert rc == -1

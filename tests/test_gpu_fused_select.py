@@ -70,6 +70,18 @@ def test_fused_score_and_histogram(d, Hq, Hkv, gamma, prefix):
         assert_rel_close(sc[b, :P], s_ref[b, :P], "aggregated score")
         np.testing.assert_array_equal(hs[b], np.bincount(_keys(sc[b, :P]) >> 20,
                                                          minlength=vsd.HIST_BINS))
+    # the early-prefetch form (first prefix tiles fetched before the dependency wait):
+    # the same results, bit for bit
+    out_e, _, pa_e, score_e, hist_e = vsd.vsd_verify_attn_collect_scored(
+        batch.q, batch.k_cache, batch.v_cache, batch.block_table, batch.prefix_len,
+        P_max=w.P_max, scale=w.scale, flags=vsd.VERIFY_EARLY_PREFETCH)
+    torch.cuda.synchronize()
+    assert vsd.vsd_read_device_status() == 0
+    assert torch.equal(out_e, out)
+    for b, P in enumerate(prefix):
+        assert torch.equal(pa_e[b, :, :P], pa[b, :, :P])
+        assert torch.equal(score_e[b, :P], score[b, :P])
+    assert torch.equal(hist_e, hist)
 
 
 def test_scored_select_matches_plain_select():
