@@ -687,10 +687,10 @@ def loop_run_bytes(w, accepted):
 
 def run_gpu_loop(args, world, rank, local):
     """Decode runs of a multi-layer model's attention (`DecodeLoop`): every iteration
-    appends the verify block's K/V of every layer, runs each layer's scored verification,
-    one selection over all layers x sequences, advances the prefixes by the accepted
-    counts, and runs gamma draft steps over every layer, each appending its input token's
-    K/V first.  One step = one run of `w.iterations` iterations from the initial prefix
+    runs each layer's scored verification, which first stores that layer's verify-block
+    K/V into its cache, one selection over all layers x sequences, advances the prefixes
+    by the accepted counts, and runs gamma draft steps over every layer, each storing its
+    input token's K/V first.  One step = one run of `w.iterations` iterations from the initial prefix
     (one CUDA-graph replay); the caches (tens of GB) exceed L2, so no flush is needed."""
     import sparse_attention_speculative_gb300 as vsd
     from sparse_attention_speculative_gb300 import build as pkg_build
@@ -779,8 +779,9 @@ def run_gpu_loop(args, world, rank, local):
     clk = clocks.summary()
 
     # per-phase breakdown: one run of iterations from a graph with external event
-    # records at the phase boundaries (verify = the layers' appends + verifications;
-    # select = the selection + the advance; draft = the draft steps with their appends)
+    # records at the phase boundaries (verify = the layers' verifications, each storing
+    # its verify block's K/V; select = the selection + the advance; draft = the draft
+    # steps, each storing its input token's K/V)
     marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
     g_marked = loop.record_marked({"verified": lambda: marks[1].record(stream),
                                    "selected": lambda: marks[2].record(stream),
@@ -811,7 +812,7 @@ def run_gpu_loop(args, world, rank, local):
                 "frac_of_nominal_8tbs": nbytes / t / 1e9 / nominal}
 
     # the dominant kernel: the layers' verification calls inside the iteration (their
-    # phase between two event records in the graph, the 36 small verify-block appends
+    # phase between two event records in the graph, the calls' verify-block stores
     # included), algorithmic bytes of the calls / phase time
     verify_call_bytes = statistics.mean(it["verify"] for it in ph_bytes) / NL
     achieved = statistics.mean(it["verify"] for it in ph_bytes) / t_v / 1e9
@@ -844,8 +845,8 @@ def run_gpu_loop(args, world, rank, local):
         "select_over_verify_call": t_s / (t_v / NL),
         "roofline": {"bound": "hbm", "kernel": "vsd_verify_attn_collect_scored",
                      "timing": "the %d layers' verification calls inside the iteration (their "
-                               "phase between event records in the iteration graph, the "
-                               "verify-block appends included), per call; bytes = "
+                               "phase between event records in the iteration graph, each call "
+                               "storing its verify block's K/V), per call; bytes = "
                                "algorithmic bytes of one call at the run's prefixes" % NL,
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak,

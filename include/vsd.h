@@ -251,6 +251,12 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
  * (every kernel of this library lets its dependents start only after its own wait, so
  * what was written two launches earlier is complete).  q, the outputs, the workspace
  * and score_hist are touched after the wait.
+ * k_new, v_new: bf16 [B][R][Hkv][head_dim] (16-byte aligned, both or neither) or NULL:
+ * the verify block's keys and values, stored into the caches at positions P_b .. P_b +
+ * R - 1 through the block table (what vsd_append_kv with pos_offset 0 stores) by the
+ * kernel itself, before it reads those rows; a block-table entry outside the cache is
+ * flagged VSD_DEV_BAD_BLOCK and its rows are not stored.  With them the caches are
+ * written (hence not const); without them they are only read.
  * where key(x) maps the fp32 bits order-preservingly to uint32 (sign bit set for
  * x >= +0: bits | 0x80000000; else ~bits).  score fp32 [B][P_max] and score_hist
  * uint32 [B][4096] are caller-owned (4-byte aligned; the rows of several calls may
@@ -271,14 +277,14 @@ vsd_status vsd_select_topk(int n_rows, int Hkv, const float* partial_scores,
  * (VSD_ERR_UNSUPPORTED otherwise).
  * ------------------------------------------------------------------------------ */
 vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const void* q,
-                                          const void* k_cache, const void* v_cache,
+                                          void* k_cache, void* v_cache,
                                           const int32_t* block_table, const int32_t* prefix_len,
                                           int collect_row0, int collect_row1, int P_max,
                                           float scale, float* logits, float* partial_scores,
                                           float* score, uint32_t* score_hist, int n_sink,
-                                          int n_recent, unsigned flags, void* out,
-                                          void* workspace, size_t workspace_bytes,
-                                          void* stream);
+                                          int n_recent, unsigned flags, const void* k_new,
+                                          const void* v_new, void* out, void* workspace,
+                                          size_t workspace_bytes, void* stream);
 
 #define VSD_VERIFY_EARLY_PREFETCH 0x4u
 

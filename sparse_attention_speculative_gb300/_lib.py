@@ -84,7 +84,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.vsd_sparse_workspace_size.argtypes = [GP, I, I, ctypes.POINTER(SZ)]
         lib.vsd_sparse_decode_attn.argtypes = [GP, P, P, P, P, P, P, I, P, P, I, F, P, P, SZ, P]
         lib.vsd_verify_attn_collect_scored.argtypes = [GP, I, P, P, P, P, P, I, I, I, F, P, P,
-                                                       P, P, I, I, ctypes.c_uint, P, P, SZ, P]
+                                                       P, P, I, I, ctypes.c_uint, P, P, P, P, SZ,
+                                                       P]
         lib.vsd_select_topk_scored.argtypes = [I, P, P, P, I, I, I, I, P, P, P]
         lib.vsd_page_key_means.argtypes = [GP, P, P, P, P, I, P, P]
         lib.vsd_copy.argtypes = [P, P, SZ, P]
@@ -484,16 +485,21 @@ HIST_BINS = 4096
 def vsd_verify_attn_collect_scored(q, k_cache, v_cache, block_table, prefix_len, *, P_max: int,
                                    scale: float, row0: int = 0, row1: Optional[int] = None,
                                    logits=None, partial=None, score=None, score_hist=None,
-                                   n_sink: int = 0, n_recent: int = 0, flags: int = 0, out=None,
-                                   workspace=None, stream=None):
+                                   n_sink: int = 0, n_recent: int = 0, flags: int = 0,
+                                   k_new=None, v_new=None, out=None, workspace=None, stream=None):
     """Verification with Collect-2-Query that also sums the partial scores over the KV
     groups (score fp32 [B, P_max]) and counts the level-0 histogram (uint32-valued int32
     [B, 4096]) of the selection's candidates (the n_sink first and n_recent last prefix
-    positions left out).  flags: 0 or VERIFY_EARLY_PREFETCH.  Returns (out, logits,
-    partial, score, score_hist)."""
+    positions left out).  flags: 0 or VERIFY_EARLY_PREFETCH.  k_new, v_new: bf16
+    [B, R, Hkv, d] or None: the verify block's keys and values, stored into the caches at
+    P_b .. P_b + R - 1 by the call itself.  Returns (out, logits, partial, score,
+    score_hist)."""
     lib = load()
     B, R, Hq, d = q.shape
     _need(q, torch.bfloat16, "q")
+    for name, x in (("k_new", k_new), ("v_new", v_new)):
+        if x is not None:
+            _need(x, torch.bfloat16, name)
     geom = geom_for(B, Hq, k_cache, block_table)
     if row1 is None:
         row1 = R - 1
@@ -514,8 +520,8 @@ def vsd_verify_attn_collect_scored(q, k_cache, v_cache, block_table, prefix_len,
                                             int(row0), int(row1), int(P_max), float(scale),
                                             _ptr(logits), _ptr(partial), _ptr(score),
                                             _ptr(score_hist), int(n_sink), int(n_recent),
-                                            int(flags), _ptr(out), _ptr(workspace), ws_bytes,
-                                            _stream(stream))
+                                            int(flags), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                            _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "vsd_verify_attn_collect_scored")
     return out, logits, partial, score, score_hist
 

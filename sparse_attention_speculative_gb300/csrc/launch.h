@@ -43,6 +43,13 @@ struct VerifyArgs {
   // the histogram counts positions [min(hist_sink, P), max(P - hist_recent, that)) only
   int hist_sink = 0, hist_recent = 0;
   int early = 0;  // producers issue their first prefix tiles before the dependency wait
+  // the verify block's keys / values ([B][R][Hkv][D]) stored into the caches (k_store,
+  // v_store: the same memory as the maps) at P_b .. P_b + R - 1 before those tiles are
+  // copied; null: nothing stored
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  void* k_store = nullptr;
+  void* v_store = nullptr;
   float scale;
 };
 

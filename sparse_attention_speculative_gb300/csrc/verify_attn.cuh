@@ -105,6 +105,12 @@ struct VParams {
   uint32_t* hist;
   int hist_sink, hist_recent;  // the histogram skips the first / last positions
   int early;  // the K / V producers issue their first stages before the dependency wait
+  // the verify block's keys / values ([B][R][Hkv][D]) stored into the cache at P_b ..
+  // P_b + R - 1 by the producers before they copy those tiles (or null)
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_store;
+  uint16_t* v_store;
   int pairs, t_max, max_chunks;
   float scale;
 };
@@ -331,6 +337,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok && lane == 0) set_abort();
         if (*abort_flag) continue;
+        if (a.k_new != nullptr) {
+          // the verify block's rows in this tile join the cache first (after the wait:
+          // the preceding kernel may write them), row u from lanes u * CPR .. on, then
+          // the stores are ordered before the tensor copies of this tile
+          const int r_lo = (s.P > tile * kTile ? s.P : tile * kTile) - s.P;
+          const int r_end = s.P + a.R < (tile + 1) * kTile ? s.P + a.R : (tile + 1) * kTile;
+          const int r_hi = r_end - s.P;
+          if (r_lo < r_hi) {
+            constexpr int CPR = D / 8;     // 16-byte chunks per row
+            constexpr int RPW = 32 / CPR;  // rows per warp pass
+            const uint16_t* src = is_k ? a.k_new : a.v_new;
+            uint16_t* dstc = is_k ? a.k_store : a.v_store;
+            for (int u0 = r_lo; u0 < r_hi; u0 += RPW) {
+              const int u = u0 + lane / CPR, c = lane % CPR;
+              const int pos = s.P + (u < r_hi ? u : r_lo);
+              const int eb = __shfl_sync(0xffffffffu, blk, (pos >> 4) - tile * kPagesPerTile);
+              if (u < r_hi && eb < a.num_blocks) {
+                const uint4 val = *reinterpret_cast<const uint4*>(
+                    src + ((static_cast<size_t>(s.b) * a.R + u) * a.Hkv + s.g) * D + c * 8);
+                *reinterpret_cast<uint4*>(
+                    dstc + ((static_cast<size_t>(eb) * a.Hkv + s.g) * kPage + (pos & (kPage - 1))) * D +
+                    c * 8) = val;
+              }
+            }
+            fence_proxy_async_all();
+            __syncwarp();
+          }
+        }
         const unsigned badbits = __ballot_sync(0xffffffffu, bad);
         if (lane == 0) {
           if (is_k && badbits) flag_status(a.status, VSD_DEV_BAD_BLOCK);
@@ -1009,6 +1043,10 @@ inline VParams make_params(const VerifyArgs& va, const VerifyPlan& plan) {
   p.hist = va.hist;
   p.hist_sink = va.hist_sink;
   p.early = va.early;
+  p.k_new = static_cast<const uint16_t*>(va.k_new);
+  p.v_new = static_cast<const uint16_t*>(va.v_new);
+  p.k_store = static_cast<uint16_t*>(va.k_store);
+  p.v_store = static_cast<uint16_t*>(va.v_store);
   p.hist_recent = va.hist_recent;
   p.pairs = plan.pairs;
   p.t_max = plan.t_max;

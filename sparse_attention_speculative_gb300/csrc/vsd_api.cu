@@ -187,7 +187,7 @@ vsd_status verify_call(const vsd_geom* geom, int R, const void* q, const void* k
                        float* logits, float* partial_scores, void* out, void* workspace,
                        size_t workspace_bytes, void* stream, float* score = nullptr,
                        uint32_t* hist = nullptr, int hist_sink = 0, int hist_recent = 0,
-                       int early = 0) {
+                       int early = 0, const void* k_new = nullptr, const void* v_new = nullptr) {
   vsd_status st = verify_checks(geom, R, P_max);
   if (st != VSD_OK) return st;
   // all rows: the two halves of every key's columns meet in the part of the Q
@@ -244,6 +244,10 @@ vsd_status verify_call(const vsd_geom* geom, int R, const void* q, const void* k
   va.hist_sink = hist_sink;
   va.hist_recent = hist_recent;
   va.early = early;
+  va.k_new = k_new;
+  va.v_new = v_new;
+  va.k_store = const_cast<void*>(k_cache);  // written only when k_new is given
+  va.v_store = const_cast<void*>(v_cache);
   va.scale = scale;
   cudaError_t e = vsd::launch_verify(va, plan, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -277,16 +281,18 @@ vsd_status vsd_verify_attn_collect_srh(const vsd_geom* geom, int R, const void* 
 }
 
 vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const void* q,
-                                          const void* k_cache, const void* v_cache,
+                                          void* k_cache, void* v_cache,
                                           const int32_t* block_table, const int32_t* prefix_len,
                                           int collect_row0, int collect_row1, int P_max,
                                           float scale, float* logits, float* partial_scores,
                                           float* score, uint32_t* score_hist, int n_sink,
-                                          int n_recent, unsigned flags, void* out,
-                                          void* workspace, size_t workspace_bytes,
-                                          void* stream) {
+                                          int n_recent, unsigned flags, const void* k_new,
+                                          const void* v_new, void* out, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
   if (n_sink < 0 || n_recent < 0) return VSD_ERR_INVALID_ARG;
   if ((flags & ~VSD_VERIFY_EARLY_PREFETCH) != 0u) return VSD_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr) || !aligned(k_new, 16) || !aligned(v_new, 16))
+    return VSD_ERR_INVALID_ARG;
   if (partial_scores == nullptr || score == nullptr || score_hist == nullptr)
     return geom != nullptr && geom->B == 0 ? VSD_OK : VSD_ERR_INVALID_ARG;
   // the aggregation writes the score one float at a time: 4-byte alignment suffices
@@ -295,7 +301,7 @@ vsd_status vsd_verify_attn_collect_scored(const vsd_geom* geom, int R, const voi
                      collect_row0, collect_row1, nullptr, P_max, scale, logits,
                      partial_scores, out, workspace, workspace_bytes, stream, score,
                      score_hist, n_sink, n_recent,
-                     (flags & VSD_VERIFY_EARLY_PREFETCH) ? 1 : 0);
+                     (flags & VSD_VERIFY_EARLY_PREFETCH) ? 1 : 0, k_new, v_new);
 }
 
 vsd_status vsd_verify_attn_collect_all(const vsd_geom* geom, int R, const void* q,

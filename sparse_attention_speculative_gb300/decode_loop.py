@@ -4,10 +4,10 @@ One iteration of verification-guided sparse self-speculative decoding (Vegas sum
 sec. 2 core mechanism: verification phase -> KV selection -> drafting phase) over L
 layers, every kernel libvsd's:
 
-  for every layer l:   the verify block's keys/values join layer l's cache at
-                       [P_b, P_b + R)                                 (vsd_append_kv)
-                       verification with Collect-2-Query and the fused aggregation
-                       -> this layer's score rows and histograms
+  for every layer l:   verification with Collect-2-Query and the fused aggregation
+                       -> this layer's score rows and histograms; the same call
+                       stores the verify block's keys/values into layer l's cache at
+                       [P_b, P_b + R) before it reads them
                                                      (vsd_verify_attn_collect_scored)
   once:                the protected top-k of every (layer, sequence) row
                                                              (vsd_select_topk_scored)
@@ -159,15 +159,17 @@ class DecodeLoop:
         for l in range(L):
             kc, vc, bt = self.k_caches[l], self.v_caches[l], self.block_tables[l]
             rows = slice(l * B, (l + 1) * B)
-            _lib.vsd_append_kv(self.k_verify[l], self.v_verify[l], kc, vc, bt, self.prefix_len,
-                               pos_offset=0, stream=s)
-            # the append writes the verify block's rows only (at the prefix length and
-            # beyond): the prefix's first tiles are fetched before waiting for it
+            # the call stores the verify block's rows itself (at the prefix length and
+            # beyond); its predecessor (the previous layer's verification, the previous
+            # iteration's last draft step or the input copy, which writes neither the
+            # lengths nor the cache below them) lets the prefix's first tiles be
+            # fetched before the wait for it
             _lib.vsd_verify_attn_collect_scored(
                 self.q[l], kc, vc, bt, self.prefix_len, P_max=self.row_stride, scale=self.scale,
                 row0=0, row1=self.R - 1, logits=self.logits, partial=self.partial,
                 score=self.score[rows], score_hist=self.score_hist[rows], n_sink=self.n_sink,
-                n_recent=self.n_recent, flags=_lib.VERIFY_EARLY_PREFETCH, out=self.out[l],
+                n_recent=self.n_recent, flags=_lib.VERIFY_EARLY_PREFETCH,
+                k_new=self.k_verify[l], v_new=self.v_verify[l], out=self.out[l],
                 workspace=self.verify_ws, stream=s)
         if marks and "verified" in marks:
             marks["verified"]()
@@ -209,11 +211,11 @@ class DecodeLoop:
     # ------------------------------------------------------------------ use
     @property
     def launches_per_iteration(self) -> int:
-        """libvsd kernel launches of one device iteration (no host copies): per layer an
-        append, the verification and its merge kernel; the selection and the advance;
-        per draft step and layer the draft kernel (it stores its input token's K/V
-        itself); the state copy."""
-        return self.L * 3 + 2 + self.gamma * self.L + 1
+        """libvsd kernel launches of one device iteration (no host copies): per layer the
+        verification (which stores the verify block's K/V itself) and its merge kernel;
+        the selection and the advance; per draft step and layer the draft kernel (it
+        stores its input token's K/V itself); the state copy."""
+        return self.L * 2 + 2 + self.gamma * self.L + 1
 
     @property
     def h2d_bytes(self) -> int:

@@ -175,7 +175,12 @@ def test_scored_verify_rejects_bad_flags(lib):
     g = _geom()
     buf = ctypes.create_string_buffer(4096)
     p = ctypes.c_void_p((ctypes.addressof(buf) + 255) & ~255)
-    rc = lib.vsd_verify_attn_collect_scored(ctypes.byref(g), 4, p, p, p, p, p, 0, 3, 1024,
-                                            ctypes.c_float(0.088), None, p, p, p, 0, 0,
-                                            ctypes.c_uint(0x1), p, p, 1024, None)
-    assert rc == -1
+
+    def call(flags, k_new=None, v_new=None):
+        return lib.vsd_verify_attn_collect_scored(ctypes.byref(g), 4, p, p, p, p, p, 0, 3, 1024,
+                                                  ctypes.c_float(0.088), None, p, p, p, 0, 0,
+                                                  ctypes.c_uint(flags), k_new, v_new, p, p, 1024,
+                                                  None)
+    assert call(0x1) == -1                # unknown flag
+    assert call(0x0, k_new=p) == -1       # keys to store without their values
+    assert call(0x0, v_new=p) == -1

@@ -261,3 +261,44 @@ def test_scored_select_boundary_bin_held_by_one_slice():
         want_i, want_n = oracle.select(s, pl, k=2048, n_sink=16, n_recent=256)
         np.testing.assert_array_equal(idx.cpu().numpy(), want_i)
         np.testing.assert_array_equal(n_sel.cpu().numpy(), want_n)
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,gamma,prefix", [
+    (128, 32, 8, 4, (6001, 0, 1, 511, 4096)),   # ragged; the block crosses a tile at 511
+    (64, 8, 2, 3, (127, 30)),                   # head_dim 64; the block ends a tile
+])
+def test_scored_verify_stores_the_verify_block(d, Hq, Hkv, gamma, prefix):
+    """The scored verification given the verify block's K/V stores them into the caches
+    itself: the same caches, outputs, scores and histogram, bit for bit, as the append
+    kernel followed by the call, in either dependency mode."""
+    from sparse_attention_speculative_gb300.synth import make_batch
+    from sparse_attention_speculative_gb300.workloads import Workload
+    vsd = _vsd()
+    w = Workload("vstore", B=len(prefix), P=max(prefix), Hq=Hq, Hkv=Hkv, d=d, gamma=gamma,
+                 k=64, n_sink=4, n_recent=16, planted_frac=0.01, seed=91, prefix_lens=prefix)
+    batch = make_batch(w, "cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    kn = torch.randn((w.B, w.R, Hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    vn = torch.randn((w.B, w.R, Hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    kc_a, vc_a = batch.k_cache.clone(), batch.v_cache.clone()
+    vsd.vsd_append_kv(kn, vn, kc_a, vc_a, batch.block_table, batch.prefix_len, pos_offset=0)
+    ref = vsd.vsd_verify_attn_collect_scored(batch.q, kc_a, vc_a, batch.block_table,
+                                             batch.prefix_len, P_max=w.P_max, scale=w.scale,
+                                             n_sink=w.n_sink, n_recent=w.n_recent)
+    torch.cuda.synchronize()
+    for flags in (0, vsd.VERIFY_EARLY_PREFETCH):
+        kc_b, vc_b = batch.k_cache.clone(), batch.v_cache.clone()
+        got = vsd.vsd_verify_attn_collect_scored(batch.q, kc_b, vc_b, batch.block_table,
+                                                 batch.prefix_len, P_max=w.P_max,
+                                                 scale=w.scale, n_sink=w.n_sink,
+                                                 n_recent=w.n_recent, flags=flags, k_new=kn,
+                                                 v_new=vn)
+        torch.cuda.synchronize()
+        assert vsd.vsd_read_device_status() == 0
+        assert torch.equal(kc_b, kc_a) and torch.equal(vc_b, vc_a)
+        assert torch.equal(got[0], ref[0])
+        for b, P in enumerate(prefix):
+            assert torch.equal(got[2][b, :, :P], ref[2][b, :, :P])
+            assert torch.equal(got[3][b, :P], ref[3][b, :P])
+        assert torch.equal(got[4], ref[4])
