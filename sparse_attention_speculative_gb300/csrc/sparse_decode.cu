@@ -87,6 +87,9 @@ struct SParams {
   float scale_log2;
   // fused sparse verification: R verify rows per sequence, log2 of the group size
   int vrows = 0, gshift = 0;
+  // warp-specialised step: the runs' partials are merged by a second kernel (pairs
+  // spread over many CTAs) instead of by each pair's last arrival
+  int ws_merge_kernel = 0;
 };
 
 // Thread layout of one warp's batch for head dimension D: a K / V row is read by
@@ -1384,7 +1387,11 @@ struct TcItem {
 // folds its items of one pair into one running (m, l, o) in registers and writes a
 // single partial per run (to the slot of the run's first split); the pair's last
 // arrival merges the runs' partials, whose slots follow from the launch geometry
-// (ws_slot), in a fixed order.
+// (ws_slot), in a fixed order -- or, where a pair spans more than eight CTAs (a 128K
+// list: ~17 CTAs, 34 partials), a second kernel does (one block per pair, a
+// programmatic dependent): there the last arrival's merge outlasts a kernel boundary
+// (128K step 13.4 -> 12.6 us), where a pair spans few CTAs it does not (the 36-layer
+// loop 17.9 -> 20.5 us, the 72B batch 14.0 -> 15.3 us with the second kernel).
 constexpr int kWsStages = 3;
 constexpr int kWsThreads = 3 * kTcThreads;
 constexpr float kDraftTau = 8.0f;  // slack of a run's reference maximum, log2 units
@@ -1725,6 +1732,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
               red[4 * kTcNQ + h] + red[5 * kTcNQ + h] + red[6 * kTcNQ + h] + red[7 * kTcNQ + h];
         }
       }
+      if (a.ws_merge_kernel) {  // merged by the next kernel
+        run_count = 0;
+        return;
+      }
       csync();
       if (ct == 0) {
         const unsigned old =
@@ -1977,6 +1988,27 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   }
 }
 
+// The runs' partials of one pair of the warp-specialised step when the step leaves
+// them to a second kernel: block = pair, thread = a float4 group of the G x D output
+// (in parts where the output has fewer than 128 groups), every partial's load of a
+// round in flight, the slots from the launch geometry.
+template <int D, int G>
+__global__ void __launch_bounds__(kTcThreads) ws_merge_kernel(const SParams a, const int items_per_cta) {
+  __shared__ float scratch[kTcThreads * 6];
+  ptx::pdl_wait_primary();  // every partial of the step is written
+  ptx::pdl_launch_dependents();
+  const int pair = blockIdx.x, b = pair / a.Hkv, g = pair - b * a.Hkv;
+  const SLen len = load_len(a, b);
+  const SList L = attended_list(len.ns, len.t0, len.t1, a, false);
+  const int n_splits = (L.total + a.split_len - 1) / a.split_len;
+  if (n_splits <= 1) return;  // one split wrote its output itself
+  const int i0 = pair * a.max_splits, ipc = items_per_cta, c0 = i0 / ipc;
+  merge_splits_by<D, G, kTcThreads, 16>(
+      a, scratch, pair, b, g, ws_partials(i0, n_splits, ipc), static_cast<int>(threadIdx.x),
+      [] { __syncthreads(); },
+      [i0, n_splits, c0, ipc](int k) { return ws_slot(k, i0, n_splits, c0, ipc); });
+}
+
 template <int D, int G>
 cudaError_t launch_ws(const SParams& p, long long items, int sm_count, cudaStream_t stream) {
   constexpr int smem = WsSmem<D>::kBytes;
@@ -1994,7 +2026,15 @@ cudaError_t launch_ws(const SParams& p, long long items, int sm_count, cudaStrea
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sparse_ws_kernel<D, G>, p, per_cta, static_cast<int>(items));
+  // a pair's splits spread over more than eight CTAs: the merge as a second kernel
+  SParams q = p;
+  q.ws_merge_kernel = p.max_splits > 1 && (p.max_splits + per_cta - 1) / per_cta + 1 > 8;
+  e = cudaLaunchKernelEx(&cfg, sparse_ws_kernel<D, G>, q, per_cta, static_cast<int>(items));
+  if (e != cudaSuccess || !q.ws_merge_kernel) return e;
+  cfg.gridDim = dim3(static_cast<unsigned>(items / p.max_splits), 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, ws_merge_kernel<D, G>, q, per_cta);
 }
 
 template <int D, int G>
