@@ -342,9 +342,10 @@ vsd_status vsd_select_topk_hybrid(int n_rows, int Hkv_target, const float* parti
  *              256-byte aligned.  It starts with per-(sequence, KV head) counters
  *              that must be zero before the first use; every call returns them to
  *              zero, so the buffer can be reused by later calls of this entry point
- *              of any geometry.  Zero it again after a call that raised
- *              VSD_DEV_TIMEOUT, and do not share it with other entry points or with
- *              calls that may run concurrently.
+ *              with the same B and Hkv (with others the counters sit where this call
+ *              wrote partials).  Zero it again before a call with other B or Hkv and
+ *              after a call that raised VSD_DEV_TIMEOUT, and do not share it with
+ *              other entry points or with calls that may run concurrently.
  * Supported: head_dim in {64, 128}, page_size 16, G <= 16.
  * ------------------------------------------------------------------------------ */
 vsd_status vsd_sparse_workspace_size(const vsd_geom* geom, int k_max, int max_tail,

@@ -148,7 +148,9 @@ _ws_cache = {}
 
 def _workspace(nbytes: int, device, tag: str) -> Optional[torch.Tensor]:
     """Cached device scratch, one buffer per (call kind, device, size), zero-filled
-    when allocated as the workspace contract asks (every call leaves it reusable)."""
+    when allocated as the workspace contract asks (every call leaves it reusable by
+    calls of the same kind; the kinds whose counters are laid out per (sequence, KV
+    head) carry B * Hkv in their tag)."""
     if nbytes == 0:
         return None
     key = (tag, str(device), nbytes)
@@ -312,7 +314,7 @@ def vsd_sparse_decode_attn(q, k_cache, v_cache, block_table, idx, n_sel, tail_st
         out = torch.empty_like(q)
     if workspace is None:
         workspace = _workspace(vsd_sparse_workspace_size(geom, k_max, max_tail), q.device,
-                               "sparse")
+                               "sparse:%d" % (geom.B * geom.Hkv))
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.vsd_sparse_decode_attn(ctypes.byref(geom), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(block_table), _ptr(idx), _ptr(n_sel), k_max,
@@ -620,7 +622,7 @@ def vsd_sparse_decode_attn_step(q, k_cache, v_cache, block_table, idx, n_sel, ta
         out = torch.empty_like(q)
     if workspace is None:
         workspace = _workspace(vsd_sparse_workspace_size(geom, k_max, max_tail), q.device,
-                               "sparse")
+                               "sparse:%d" % (geom.B * geom.Hkv))
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.vsd_sparse_decode_attn_step(ctypes.byref(geom), _ptr(q), _ptr(k_new), _ptr(v_new),
                                          _ptr(k_cache), _ptr(v_cache), _ptr(block_table),

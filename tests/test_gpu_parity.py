@@ -560,6 +560,18 @@ def test_sparse_verify(d, Hq, Hkv, gamma, prefix, k):
     torch.cuda.synchronize()
     assert vsd.vsd_read_device_status() == 0
     assert torch.equal(out_early, out)
+    # a workspace of the caller's, reused: calls repeat bit for bit
+    geom = vsd.geom_for(w.B, Hq, batch.k_cache, batch.block_table)
+    nb = vsd.vsd_sparse_verify_workspace_size(geom, w.R, k)
+    ws = torch.zeros(nb + 256, dtype=torch.uint8, device="cuda")
+    ws = ws[(-ws.data_ptr()) % 256:][:nb]
+    for flags in (0, vsd.SPARSE_VERIFY_EARLY_GATHER, 0):
+        again = vsd.vsd_sparse_verify_attn(batch.q, batch.k_cache, batch.v_cache,
+                                           batch.block_table, batch.prefix_len, idx, n_sel,
+                                           scale=w.scale, flags=flags, workspace=ws)
+        torch.cuda.synchronize()
+        assert vsd.vsd_read_device_status() == 0
+        assert torch.equal(again, out)
     # every prefix position selected: the same as full verification
     full = torch.full((w.B, w.P_max), -1, dtype=torch.int32, device="cuda")
     for b, P in enumerate(prefix):
