@@ -1007,23 +1007,27 @@ struct TcvSmem {
   static constexpr int kOffQ = kOffV + kBatch * D * 2;
   static constexpr int kOffRed = kOffQ + kQBytes;         // [2][4][NQ] floats
   static constexpr int kOffBar = kOffRed + 2 * 4 * NQ * 4;
+  static constexpr int kOffValid = kOffBar + 64;  // [kBatch] bytes: the key's row is present
   static constexpr int kOffP = kOffK;  // P^T in the K tile (after its QK product)
-  static constexpr int kUsed = kOffBar + 64 > kOffV + 2 * kHalf ? kOffBar + 64 : kOffV + 2 * kHalf;
+  static constexpr int kUsed =
+      kOffValid + kBatch > kOffV + 2 * kHalf ? kOffValid + kBatch : kOffV + 2 * kHalf;
   static constexpr int kBytes = kUsed + 1024;
   static_assert(kOffQ % 1024 == 0 && kQBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
   static_assert(NQ * 2 <= 128, "a P^T row holds the NQ probabilities of one key");
 };
 
-// Reduce v[0 .. NQ) (NQ = 16 or 32 columns) over the warp's 32 lanes with `op`, every
-// column at once: butterfly steps that halve the columns a lane keeps (lanes with the
-// step's bit set keep the upper half), NQ - 1 shuffles plus 16 for NQ = 16, all of a
-// step independent.  Afterwards lane L holds column L % NQ.
+// Reduce v[0 .. NQ) (NQ = 8, 16 or 32 columns) over the warp's 32 lanes with `op`,
+// every column at once: full exchanges at the lane distances of NQ and above, then
+// butterfly steps that halve the columns a lane keeps (lanes with the step's bit set
+// keep the upper half), all of a step independent.  Afterwards lane L holds column
+// L % NQ.
 template <int NQ, typename Op>
 __device__ __forceinline__ float warp_reduce_columns(float (&v)[NQ], Op op) {
   const int lane = threadIdx.x & 31;
-  if constexpr (NQ == 16) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = op(v[i], __shfl_xor_sync(0xffffffffu, v[i], 16));
+  for (int off = 16; off >= NQ; off >>= 1) {
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) v[i] = op(v[i], __shfl_xor_sync(0xffffffffu, v[i], off));
   }
 #pragma unroll
   for (int m = NQ / 2; m >= 1; m >>= 1) {
@@ -1038,21 +1042,33 @@ __device__ __forceinline__ float warp_reduce_columns(float (&v)[NQ], Op op) {
   return v[0];
 }
 
-// TMEM columns [c0, c0 + NQ) of this warp's lane quarter.
-template <int NQ>
-__device__ __forceinline__ void tmem_ld_nq(uint32_t taddr, float (&v)[NQ]) {
-  ptx::tmem_ld<16>(taddr, reinterpret_cast<uint32_t*>(v));
-  if constexpr (NQ == 32) ptx::tmem_ld<16>(taddr + 16, reinterpret_cast<uint32_t*>(v) + 16);
+// N consecutive TMEM columns of this warp's lane quarter (N = 8, 16 or 32).
+template <int N>
+__device__ __forceinline__ void tmem_ld_f32(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N == 32) {
+    ptx::tmem_ld<16>(taddr, reinterpret_cast<uint32_t*>(v));
+    ptx::tmem_ld<16>(taddr + 16, reinterpret_cast<uint32_t*>(v) + 16);
+  } else {
+    ptx::tmem_ld<N>(taddr, reinterpret_cast<uint32_t*>(v));
+  }
   ptx::tmem_wait_ld();
 }
 
-template <int D, int NQ>
-__global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SParams a) {
+// kParts warps per TMEM lane quarter: warp w holds the keys (and, for O^T, the
+// dimensions) of quarter w % 4 and the column part w / 4 of the NQ verify rows.  Only
+// the lower 128 threads resolve positions and gather rows (one per key, as in the draft
+// step); the others learn which keys are present through shared memory.  Two parts when
+// the launch is one wave at one CTA per SM (the softmax of a 32K call 2.3 -> 1.1 us,
+// the call 8.56 -> 8.22 us); one where several CTAs share an SM and hide one another's
+// softmax (the 128K call took 17.6 us with one part, 18.4 with two).
+template <int D, int NQ, int kParts>
+__global__ void __launch_bounds__(kParts * kTcThreads) sparse_verify_tc_kernel(const SParams a) {
   using Sm = TcvSmem<D, NQ>;
+  constexpr int kSvThreads = kParts * kTcThreads;
   constexpr int LPR = D / 8;                  // 16-byte chunks per row
   constexpr int RPI = 32 / LPR;               // rows per warp instruction
-  constexpr int QPT = NQ * LPR / kTcThreads;  // query chunks per thread
-  static_assert(NQ * LPR % kTcThreads == 0, "query staging");
+  constexpr int NH = NQ / kParts;             // verify columns per thread
+  static_assert(NH % 8 == 0, "P^T chunks of 8 columns");
   extern __shared__ uint8_t tcv_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tcv_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1065,9 +1081,15 @@ __global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SPar
   uint64_t* bar_o = bar_s + 1;
   uint64_t* bar_fin = bar_s + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 3);
+  uint8_t* valid_s = base + Sm::kOffValid;
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  // (one part: compile-time constants, every thread a gatherer)
+  const int quarter = warp & 3;
+  const int col0 = kParts == 1 ? 0 : (warp >> 2) * NH;
+  const int key = kParts == 1 ? t : quarter * 32 + lane;  // TMEM lane: key (S^T) / dim (O^T)
+  const bool gatherer = kParts == 1 || t < kBatch;        // key == t for these
   const int G = 1 << a.gshift;
   const int NR = a.vrows << a.gshift;  // real verify rows of the group (<= NQ)
   if (t == 0) {
@@ -1084,6 +1106,7 @@ __global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SPar
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // S^T: columns [0, NQ); O^T: [NQ, 2 NQ)
+  const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
   // idx / n_sel / the prefix lengths may come from the preceding kernel; in the early
   // mode they do not (nor the selected positions' cache rows): those rows are resolved
   // and gathered before the wait, the verify block's rows and the queries after it
@@ -1093,7 +1116,7 @@ __global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SPar
   }
 
   const int lo = split * a.split_len;
-  const int j_spec = (a.idx != nullptr && lo + t < a.k_max)
+  const int j_spec = (gatherer && a.idx != nullptr && lo + t < a.k_max)
                          ? __ldcg(a.idx + static_cast<size_t>(b) * a.k_max + lo + t)
                          : 0;
   const int ns_raw = a.n_sel != nullptr ? __ldcg(a.n_sel + b) : 0;
@@ -1112,14 +1135,15 @@ __global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SPar
   };
 
   if (work) {
-    // ---- this thread's position -> cache row (-1: absent, zero-filled and masked)
-    const int pos = lo + t;
+    // ---- the gatherer's position -> cache row (-1: absent, zero-filled and masked)
+    const int pos = lo + key;
     SRow rr{-1, false};
-    if (pos < L.total && pos < lo + kBatch) rr = resolve_position(a, L, b, g, pos, P + a.vrows, j_spec);
+    if (gatherer && pos < L.total && pos < lo + kBatch)
+      rr = resolve_position(a, L, b, g, pos, P + a.vrows, j_spec);
     const int crow = rr.row;
     const bool in_block = pos >= L.ns && pos < L.total;  // a verify-block row
     const int ch = lane % LPR;
-    // the selected (and absent) rows, or the verify block's rows
+    // the selected (and absent) rows, or the verify block's rows (gatherer warps)
     const auto gather = [&](bool block_rows) {
 #pragma unroll
       for (int u = 0; u < 32 / RPI; ++u) {
@@ -1135,17 +1159,24 @@ __global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SPar
         }
       }
     };
-    gather(false);
+    if (gatherer) gather(false);
     if (a.early) {
       ptx::pdl_wait_primary();
       ptx::pdl_launch_dependents();
     }
-    gather(true);
-    ptx::cp_async_commit();
-    // ---- the group's verify rows, padded with zeros to NQ, K-major and swizzled
+    if (gatherer) {
+      gather(true);
+      ptx::cp_async_commit();
+      if (kParts > 1) valid_s[t] = crow >= 0 ? 1 : 0;
+    }
+    // ---- the group's verify rows, padded with zeros to NQ, K-major and swizzled (all
+    // of a thread's loads in flight at once)
+    constexpr int QPT = (NQ * LPR + kSvThreads - 1) / kSvThreads;  // chunks per thread
 #pragma unroll
     for (int u = 0; u < QPT; ++u) {
-      const int i = t + u * kTcThreads, r = i / LPR, c = i % LPR;
+      const int i = t + u * kSvThreads;
+      if (NQ * LPR % kSvThreads != 0 && i >= NQ * LPR) break;
+      const int r = i / LPR, c = i % LPR;
       uint4 qv = make_uint4(0, 0, 0, 0);
       if (r < NR)
         qv = *reinterpret_cast<const uint4*>(
@@ -1154,7 +1185,7 @@ __global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SPar
       *reinterpret_cast<uint4*>(q_s + (c >> 3) * (NQ * 128) + r * 128 +
                                 (((c & 7) ^ (r & 7)) << 4)) = qv;
     }
-    ptx::cp_async_wait_all();
+    if (gatherer) ptx::cp_async_wait_all();
     ptx::fence_proxy_async_smem();
     __syncthreads();
 
@@ -1177,51 +1208,53 @@ __global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SPar
       drain_s = true;
     }
     ptx::tc_fence_after();
-    float z[NQ];  // this key's logits for the NQ rows
-    tmem_ld_nq<NQ>(tmem + (static_cast<uint32_t>(warp * 32) << 16), z);
+    float z[NH];  // this key's logits for the thread's NH rows
+    tmem_ld_f32<NH>(tmem + lane_addr + col0, z);
     // ---- softmax per row over the CTA's keys (log2 units), the verify block masked
     // causally: a block key at u = pos - n_sel is seen by the rows of verify row >= u
-    const bool valid = crow >= 0;
+    const bool valid = kParts == 1 ? crow >= 0 : valid_s[key] != 0;
     const int u_blk = pos - L.ns;  // < 0: a selected position, seen by every row
 #pragma unroll
-    for (int c = 0; c < NQ; ++c) {
-      const bool seen = valid && c < NR && (u_blk < 0 || u_blk <= (c >> a.gshift));
+    for (int c = 0; c < NH; ++c) {
+      const int cc = col0 + c;
+      const bool seen = valid && cc < NR && (u_blk < 0 || u_blk <= (cc >> a.gshift));
       z[c] = seen ? z[c] * a.scale_log2 : -INFINITY;
     }
-    // per-row maxima: one column-wise reduction over the warp's keys, the warps meet in
-    // shared memory, lane c of every warp then holds row c's maximum
+    // per-row maxima: one column-wise reduction over the warp's keys, the quarters meet
+    // in shared memory, lane c of every warp then holds row col0 + c's maximum
     {
-      float v[NQ];
+      float v[NH];
 #pragma unroll
-      for (int c = 0; c < NQ; ++c) v[c] = z[c];
-      const float wm = warp_reduce_columns<NQ>(v, [](float x, float y) { return fmaxf(x, y); });
-      if (lane < NQ) red[warp * NQ + lane] = wm;
+      for (int c = 0; c < NH; ++c) v[c] = z[c];
+      const float wm = warp_reduce_columns<NH>(v, [](float x, float y) { return fmaxf(x, y); });
+      if (lane < NH) red[quarter * NQ + col0 + lane] = wm;
     }
     __syncthreads();
-    const int cl = lane % NQ;
+    const int cl = col0 + lane % NH;
     const float m_lane =
         fmaxf(fmaxf(red[cl], red[NQ + cl]), fmaxf(red[2 * NQ + cl], red[3 * NQ + cl]));
     {
-      float v[NQ];
+      float v[NH];
 #pragma unroll
-      for (int c = 0; c < NQ; ++c) {
+      for (int c = 0; c < NH; ++c) {
         const float m = __shfl_sync(0xffffffffu, m_lane, c);
         const float p = (z[c] == -INFINITY) ? 0.f : exp2f(z[c] - m);
         z[c] = p;
         v[c] = p;
       }
-      const float ws = warp_reduce_columns<NQ>(v, [](float x, float y) { return x + y; });
-      if (lane < NQ) red[4 * NQ + warp * NQ + lane] = ws;
+      const float ws = warp_reduce_columns<NH>(v, [](float x, float y) { return x + y; });
+      if (lane < NH) red[4 * NQ + quarter * NQ + col0 + lane] = ws;
     }
-    // row t of P^T: NQ bf16 in NQ / 8 swizzled 16-byte chunks
+    // row `key` of P^T: this thread's NH bf16 in NH / 8 swizzled 16-byte chunks
 #pragma unroll
-    for (int k = 0; k < NQ / 8; ++k) {
+    for (int k = 0; k < NH / 8; ++k) {
       uint4 pk;
       pk.x = pack_bf16x2(z[k * 8 + 0], z[k * 8 + 1]);
       pk.y = pack_bf16x2(z[k * 8 + 2], z[k * 8 + 3]);
       pk.z = pack_bf16x2(z[k * 8 + 4], z[k * 8 + 5]);
       pk.w = pack_bf16x2(z[k * 8 + 6], z[k * 8 + 7]);
-      *reinterpret_cast<uint4*>(p_s + t * 128 + ((k ^ (t & 7)) << 4)) = pk;
+      const int chunk = col0 / 8 + k;
+      *reinterpret_cast<uint4*>(p_s + key * 128 + ((chunk ^ (key & 7)) << 4)) = pk;
     }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
@@ -1249,24 +1282,25 @@ __global__ void __launch_bounds__(kTcThreads) sparse_verify_tc_kernel(const SPar
       drain_o = true;
     }
     ptx::tc_fence_after();
-    if (warp < D / 32) {  // TMEM lanes 0 .. D-1 hold the output dimensions
-      float o[NQ];
-      tmem_ld_nq<NQ>(tmem + (static_cast<uint32_t>(warp * 32) << 16) + NQ, o);
-      const int dim = t;
+    if (quarter < D / 32) {  // TMEM lanes 0 .. D-1 hold the output dimensions
+      float o[NH];
+      tmem_ld_f32<NH>(tmem + lane_addr + NQ + col0, o);
+      const int dim = key;
       if (direct) {
 #pragma unroll
-        for (int r = 0; r < NQ; ++r) {
+        for (int c = 0; c < NH; ++c) {
+          const int r = col0 + c;
           uint16_t* row = out_row(r);
           if (row == nullptr) continue;
           const float l = red[4 * NQ + r] + red[5 * NQ + r] + red[6 * NQ + r] + red[7 * NQ + r];
-          const __nv_bfloat16 bv = __float2bfloat16_rn(l > 0.f ? o[r] / l : 0.f);
+          const __nv_bfloat16 bv = __float2bfloat16_rn(l > 0.f ? o[c] / l : 0.f);
           row[dim] = *reinterpret_cast<const uint16_t*>(&bv);
         }
       } else {
         float* wsl = a.ws + (static_cast<size_t>(pair) * a.max_splits + split) * SSlot<D, NQ>::kFloats;
 #pragma unroll
-        for (int r = 0; r < NQ; ++r) wsl[SSlot<D, NQ>::kO + r * D + dim] = o[r];
-        if (dim < NQ) {  // m and l of row `dim`
+        for (int c = 0; c < NH; ++c) wsl[SSlot<D, NQ>::kO + (col0 + c) * D + dim] = o[c];
+        if (col0 == 0 && dim < NQ) {  // m and l of row `dim`
           wsl[dim] = fmaxf(fmaxf(red[dim], red[NQ + dim]), fmaxf(red[2 * NQ + dim], red[3 * NQ + dim]));
           wsl[NQ + dim] = red[4 * NQ + dim] + red[5 * NQ + dim] + red[6 * NQ + dim] + red[7 * NQ + dim];
         }
@@ -2082,18 +2116,19 @@ cudaError_t launch_tcv(const SParams& p, int B, int Hkv, cudaStream_t stream) {
   const long long ctas = static_cast<long long>(p.max_splits) * Hkv * B;
   constexpr int kSpreadSmem = 120 * 1024;
   static_assert(TcvSmem<D, NQ>::kBytes <= kSpreadSmem, "spread reservation");
-  const int smem = ctas <= sm_count ? kSpreadSmem : TcvSmem<D, NQ>::kBytes;
-  e = cudaFuncSetAttribute(sparse_verify_tc_kernel<D, NQ>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const bool one_wave = ctas <= sm_count;
+  const int smem = one_wave ? kSpreadSmem : TcvSmem<D, NQ>::kBytes;
+  const auto kern = one_wave ? sparse_verify_tc_kernel<D, NQ, 2> : sparse_verify_tc_kernel<D, NQ, 1>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.max_splits, Hkv, B);
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.blockDim = dim3((one_wave ? 2 : 1) * kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, sparse_verify_tc_kernel<D, NQ>, p);
+  e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess || p.max_splits <= 1) return e;
   cfg.gridDim = dim3(p.vrows << p.gshift, Hkv, B);
   cfg.dynamicSmemBytes = 0;
