@@ -526,6 +526,8 @@ def test_results_do_not_depend_on_the_split():
 @pytest.mark.parametrize("d,Hq,Hkv,gamma,prefix,k", [
     (128, 32, 8, 4, (6000, 1500, 300), 512),   # Qwen3-8B geometry, ragged: fused, 20 rows
     (128, 64, 8, 5, (4096, 2049), 256),        # Qwen2.5-72B geometry (48 rows): gathered
+    (128, 64, 8, 5, (3000, 2000, 2500, 1800), 512),  # the same, four sequences: gathered
+    (64, 8, 1, 3, (132000,), 131500),          # a list beyond 1024 batches (32 rows): gathered
     (64, 8, 2, 3, (777, 31), 64),              # head_dim 64, a prefix shorter than k: fused
     (128, 16, 16, 7, (3000, 5000), 2048),      # one head per group, 8 rows, 17 splits
     (128, 32, 4, 3, (9000,), 4096),            # 8 heads per group, 32 rows, 33 splits
